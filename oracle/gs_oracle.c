@@ -1,0 +1,541 @@
+/*
+ * gs_oracle.c -- the CPU oracle for graph-based 3pCF and parity-4pCF counts.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the library's product path links,
+ * loads or calls this file; only the tests, the smoke check and the timed CPU
+ * baseline of the benchmark do. It shares no code, header, table or constant
+ * with the CUDA library.
+ *
+ * It is a plain, slow, obviously correct restatement of what the GRAMSCI v2
+ * paper ("Fast Graph-based Higher-Order Clustering Statistics on the GPU")
+ * computes, in exact integer arithmetic on lattice coordinates:
+ *
+ *   - graph: brute force over all pairs (the definition that the kd-tree
+ *     search of §II.1 reaches faster), rows sorted by index as Eq.(1)
+ *     requires, each neighbour stored with its radial-bin byte (§II.1);
+ *   - 3pCF: the hub-and-spoke loop of §II.2, counting each unordered
+ *     triangle once (at its lowest-index vertex), with the closing side
+ *     re-tested from coordinates instead of a graph lookup;
+ *   - parity 4pCF: the signed volume of Eq.(3) over every hub and spoke
+ *     triple whose three spoke-spoke pairs are also neighbours (§III.2),
+ *     with zero volume given zero odd weight (§III.2, degenerate rule);
+ *   - brute force over all triples / quadruples, with no graph at all.
+ *
+ * Conventions (readings where the paper is silent):
+ *   - lattice coordinates in [0, box); periodic boxes use the minimum image
+ *     (delta -= box if 2*delta >= box, delta += box if 2*delta < -box);
+ *   - a pair (i != j) is an edge iff e_0^2 <= d^2 < e_nb^2, with bin b the one
+ *     for which e_b^2 <= d^2 < e_{b+1}^2 (half-open bins on squared integers);
+ *   - 3pCF bins are sorted b1 <= b2 <= b3 and packed lexicographically;
+ *     4pCF spokes are ordered by hub bin b1 < b2 < b3 (distinct bins only),
+ *     packed lexicographically, and the volume uses r_is = x_s - x_i with
+ *     the spokes in that bin order; odd += sign(V), sign(0) = 0.
+ *
+ * Parallelism: hubs are shared among pthreads through an atomic cursor; each
+ * thread owns a private histogram and the integer histograms are summed at
+ * the end, so the result does not depend on the thread count.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+#include <stdatomic.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------ */
+/* threads                                                                   */
+
+static int g_threads = 0;
+
+int oracle_set_threads(int t) { g_threads = t; return g_threads; }
+
+int oracle_threads(void)
+{
+    if (g_threads > 0) return g_threads;
+    long c = sysconf(_SC_NPROCESSORS_ONLN);
+    return c > 0 ? (int)c : 1;
+}
+
+typedef void (*hub_fn)(void *ctx, int tid, int64_t i);
+
+typedef struct {
+    void *ctx;
+    hub_fn fn;
+    int64_t n;
+    int64_t chunk;
+    _Atomic int64_t next;
+} pool_t;
+
+typedef struct { pool_t *p; int tid; } worker_arg_t;
+
+static void *worker(void *arg)
+{
+    worker_arg_t *w = (worker_arg_t *)arg;
+    pool_t *p = w->p;
+    for (;;) {
+        int64_t s = atomic_fetch_add(&p->next, p->chunk);
+        if (s >= p->n) break;
+        int64_t e = s + p->chunk < p->n ? s + p->chunk : p->n;
+        for (int64_t i = s; i < e; ++i) p->fn(p->ctx, w->tid, i);
+    }
+    return NULL;
+}
+
+/* Run fn(ctx, tid, i) for every i in [begin, end) on nt threads. */
+static void parallel_for(int64_t begin, int64_t end, int nt, hub_fn fn, void *ctx)
+{
+    pool_t p;
+    p.ctx = ctx; p.fn = fn; p.n = end; p.chunk = 4;
+    atomic_init(&p.next, begin);
+    if (nt <= 1) {
+        worker_arg_t w = { &p, 0 };
+        worker(&w);
+        return;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    worker_arg_t *wa = (worker_arg_t *)malloc(sizeof(worker_arg_t) * (size_t)nt);
+    for (int t = 0; t < nt; ++t) {
+        wa[t].p = &p; wa[t].tid = t;
+        pthread_create(&th[t], NULL, worker, &wa[t]);
+    }
+    for (int t = 0; t < nt; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(wa);
+}
+
+/* ------------------------------------------------------------------------ */
+/* the pair rule                                                             */
+
+typedef struct {
+    const int32_t *xyz;   /* [n][3] */
+    int64_t n;
+    int64_t box;
+    int periodic;
+    const int64_t *edges; /* [nb+1] lattice units */
+    int nb;
+} cat_t;
+
+/* Component of the displacement x_b - x_a along one axis. */
+static int64_t axis_delta(int64_t a, int64_t b, int64_t box, int periodic)
+{
+    int64_t d = b - a;
+    if (periodic) {
+        if (2 * d >= box) d -= box;
+        else if (2 * d < -box) d += box;
+    }
+    return d;
+}
+
+static void displacement(const cat_t *c, int64_t a, int64_t b, int64_t r[3])
+{
+    for (int ax = 0; ax < 3; ++ax)
+        r[ax] = axis_delta(c->xyz[3 * a + ax], c->xyz[3 * b + ax], c->box, c->periodic);
+}
+
+static int64_t dist2(const cat_t *c, int64_t a, int64_t b)
+{
+    int64_t r[3];
+    displacement(c, a, b, r);
+    return r[0] * r[0] + r[1] * r[1] + r[2] * r[2];
+}
+
+/* Radial bin of the pair (a, b), or -1 when it is not an edge. */
+static int pair_bin(const cat_t *c, int64_t a, int64_t b)
+{
+    if (a == b) return -1;
+    int64_t d2 = dist2(c, a, b);
+    for (int k = 0; k < c->nb; ++k) {
+        int64_t lo = c->edges[k], hi = c->edges[k + 1];
+        if (lo * lo <= d2 && d2 < hi * hi) return k;
+    }
+    return -1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* configuration indices by enumeration                                      */
+
+/* Lexicographic rank of every sorted triple b1 <= b2 <= b3, as a dense nb^3 table. */
+static int32_t *table3(int nb)
+{
+    int32_t *t = (int32_t *)malloc(sizeof(int32_t) * (size_t)nb * nb * nb);
+    int32_t c = 0;
+    for (int a = 0; a < nb; ++a)
+        for (int b = a; b < nb; ++b)
+            for (int d = b; d < nb; ++d)
+                t[((size_t)a * nb + b) * nb + d] = c++;
+    return t;
+}
+
+/* Lexicographic rank of every strictly increasing triple b1 < b2 < b3. */
+static int32_t *table4(int nb)
+{
+    int32_t *t = (int32_t *)malloc(sizeof(int32_t) * (size_t)nb * nb * nb);
+    int32_t c = 0;
+    for (int a = 0; a < nb; ++a)
+        for (int b = a + 1; b < nb; ++b)
+            for (int d = b + 1; d < nb; ++d)
+                t[((size_t)a * nb + b) * nb + d] = c++;
+    return t;
+}
+
+int64_t oracle_nconfig3(int nb) { return (int64_t)nb * (nb + 1) * (nb + 2) / 6; }
+int64_t oracle_nconfig4(int nb) { return (int64_t)nb * (nb - 1) * (nb - 2) / 6; }
+
+static void sort3(int v[3])
+{
+    int t;
+    if (v[0] > v[1]) { t = v[0]; v[0] = v[1]; v[1] = t; }
+    if (v[1] > v[2]) { t = v[1]; v[1] = v[2]; v[2] = t; }
+    if (v[0] > v[1]) { t = v[0]; v[0] = v[1]; v[1] = t; }
+}
+
+/* ------------------------------------------------------------------------ */
+/* graph by brute force over all pairs                                       */
+
+typedef struct {
+    cat_t c;
+    int64_t *deg;
+    const int64_t *row_ptr;
+    int32_t *nbr;
+    uint8_t *bin;
+} graph_ctx_t;
+
+static void degree_hub(void *vctx, int tid, int64_t i)
+{
+    (void)tid;
+    graph_ctx_t *g = (graph_ctx_t *)vctx;
+    int64_t d = 0;
+    for (int64_t j = 0; j < g->c.n; ++j)
+        if (pair_bin(&g->c, i, j) >= 0) ++d;
+    g->deg[i] = d;
+}
+
+static void fill_hub(void *vctx, int tid, int64_t i)
+{
+    (void)tid;
+    graph_ctx_t *g = (graph_ctx_t *)vctx;
+    int64_t p = g->row_ptr[i];
+    for (int64_t j = 0; j < g->c.n; ++j) {          /* j ascending: rows come out sorted */
+        int b = pair_bin(&g->c, i, j);
+        if (b >= 0) { g->nbr[p] = (int32_t)j; g->bin[p] = (uint8_t)b; ++p; }
+    }
+}
+
+/* deg[i] = |N(i)|; returns the directed edge total sum(deg). */
+int64_t oracle_graph_degrees(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                             const int64_t *edges, int nb, int64_t *deg)
+{
+    graph_ctx_t g = { { xyz, n, box, periodic, edges, nb }, deg, NULL, NULL, NULL };
+    parallel_for(0, n, oracle_threads(), degree_hub, &g);
+    int64_t e = 0;
+    for (int64_t i = 0; i < n; ++i) e += deg[i];
+    return e;
+}
+
+/* Fill rows [row_ptr[i], row_ptr[i+1]) with sorted neighbour ids and bins. */
+void oracle_graph_fill(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                       const int64_t *edges, int nb, const int64_t *row_ptr,
+                       int32_t *nbr, uint8_t *bin)
+{
+    graph_ctx_t g = { { xyz, n, box, periodic, edges, nb }, NULL, row_ptr, nbr, bin };
+    parallel_for(0, n, oracle_threads(), fill_hub, &g);
+}
+
+/* One row N(i) by brute force; returns its length. nbr/bin hold up to n entries. */
+int64_t oracle_row(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                   const int64_t *edges, int nb, int64_t i, int32_t *nbr, uint8_t *bin)
+{
+    cat_t c = { xyz, n, box, periodic, edges, nb };
+    int64_t p = 0;
+    for (int64_t j = 0; j < n; ++j) {
+        int b = pair_bin(&c, i, j);
+        if (b >= 0) { nbr[p] = (int32_t)j; bin[p] = (uint8_t)b; ++p; }
+    }
+    return p;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 3pCF: hub-and-spoke loop over the graph                                   */
+
+typedef struct {
+    cat_t c;
+    const int64_t *row_ptr;
+    const int32_t *nbr;
+    const uint8_t *bin;
+    const int32_t *t3;
+    int64_t ncfg;
+    uint64_t *hist;        /* [threads][ncfg] */
+} tri_ctx_t;
+
+static void tri_hub(void *vctx, int tid, int64_t i)
+{
+    tri_ctx_t *t = (tri_ctx_t *)vctx;
+    uint64_t *h = t->hist + (size_t)tid * (size_t)t->ncfg;
+    int nb = t->c.nb;
+    for (int64_t a = t->row_ptr[i]; a < t->row_ptr[i + 1]; ++a) {
+        int64_t j = t->nbr[a];
+        if (j <= i) continue;                      /* spoke j > hub i */
+        for (int64_t b = a + 1; b < t->row_ptr[i + 1]; ++b) {
+            int64_t k = t->nbr[b];                 /* k > j since the row is sorted */
+            int bjk = pair_bin(&t->c, j, k);       /* closing side, from coordinates */
+            if (bjk < 0) continue;
+            int v[3] = { t->bin[a], t->bin[b], bjk };
+            sort3(v);
+            h[t->t3[((size_t)v[0] * nb + v[1]) * nb + v[2]]] += 1;
+        }
+    }
+}
+
+static void reduce_u64(uint64_t *out, const uint64_t *parts, int nt, int64_t m)
+{
+    memset(out, 0, sizeof(uint64_t) * (size_t)m);
+    for (int t = 0; t < nt; ++t)
+        for (int64_t x = 0; x < m; ++x) out[x] += parts[(size_t)t * m + x];
+}
+
+static void reduce_i64(int64_t *out, const int64_t *parts, int nt, int64_t m)
+{
+    memset(out, 0, sizeof(int64_t) * (size_t)m);
+    for (int t = 0; t < nt; ++t)
+        for (int64_t x = 0; x < m; ++x) out[x] += parts[(size_t)t * m + x];
+}
+
+/* hist[C(nb+2,3)]: triangles per sorted bin triple, hubs i in [hub_begin, hub_end). */
+void oracle_3pcf_range(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                       const int64_t *edges, int nb, const int64_t *row_ptr,
+                       const int32_t *nbr, const uint8_t *bin,
+                       int64_t hub_begin, int64_t hub_end, uint64_t *hist)
+{
+    int nt = oracle_threads();
+    tri_ctx_t t;
+    t.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    t.row_ptr = row_ptr; t.nbr = nbr; t.bin = bin;
+    t.t3 = table3(nb);
+    t.ncfg = oracle_nconfig3(nb);
+    t.hist = (uint64_t *)calloc((size_t)nt * (size_t)t.ncfg, sizeof(uint64_t));
+    if (hub_end > hub_begin) parallel_for(hub_begin, hub_end, nt, tri_hub, &t);
+    reduce_u64(hist, t.hist, nt, t.ncfg);
+    free(t.hist);
+    free((void *)t.t3);
+}
+
+void oracle_3pcf(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                 const int64_t *edges, int nb, const int64_t *row_ptr,
+                 const int32_t *nbr, const uint8_t *bin, uint64_t *hist)
+{
+    oracle_3pcf_range(xyz, n, box, periodic, edges, nb, row_ptr, nbr, bin, 0, n, hist);
+}
+
+/* ------------------------------------------------------------------------ */
+/* parity 4pCF: every hub, every spoke triple forming a clique               */
+
+typedef struct {
+    cat_t c;
+    const int64_t *row_ptr;
+    const int32_t *nbr;
+    const uint8_t *bin;
+    const int32_t *t4;
+    int64_t ncfg;
+    uint64_t *even;       /* [threads][ncfg] */
+    int64_t *odd;         /* [threads][ncfg] */
+} quad_ctx_t;
+
+/* Signed volume (r1 x r2) . r3, Eq.(3). */
+static int64_t triple_product(const int64_t r1[3], const int64_t r2[3], const int64_t r3[3])
+{
+    int64_t cx = r1[1] * r2[2] - r1[2] * r2[1];
+    int64_t cy = r1[2] * r2[0] - r1[0] * r2[2];
+    int64_t cz = r1[0] * r2[1] - r1[1] * r2[0];
+    return cx * r3[0] + cy * r3[1] + cz * r3[2];
+}
+
+/* Add one (hub, spoke triple) to the even and odd channels. The spokes are
+ * put in hub-bin order before the volume is taken. */
+static void add_clique(const cat_t *c, const int32_t *t4, uint64_t *even, int64_t *odd,
+                       int64_t hub, const int64_t s[3], const int b[3])
+{
+    if (b[0] == b[1] || b[0] == b[2] || b[1] == b[2]) return;
+    int order[3] = { 0, 1, 2 };
+    for (int x = 0; x < 3; ++x)
+        for (int y = x + 1; y < 3; ++y)
+            if (b[order[y]] < b[order[x]]) { int tmp = order[x]; order[x] = order[y]; order[y] = tmp; }
+    int64_t r[3][3];
+    for (int q = 0; q < 3; ++q) displacement(c, hub, s[order[q]], r[q]);
+    int64_t v = triple_product(r[0], r[1], r[2]);
+    int nb = c->nb;
+    int idx = t4[((size_t)b[order[0]] * nb + b[order[1]]) * nb + b[order[2]]];
+    even[idx] += 1;
+    odd[idx] += (v > 0) - (v < 0);
+}
+
+static void quad_hub(void *vctx, int tid, int64_t i)
+{
+    quad_ctx_t *q = (quad_ctx_t *)vctx;
+    uint64_t *ev = q->even + (size_t)tid * (size_t)q->ncfg;
+    int64_t *od = q->odd + (size_t)tid * (size_t)q->ncfg;
+    int64_t r0 = q->row_ptr[i], r1 = q->row_ptr[i + 1];
+    for (int64_t a = r0; a < r1; ++a)
+        for (int64_t b = a + 1; b < r1; ++b) {
+            if (pair_bin(&q->c, q->nbr[a], q->nbr[b]) < 0) continue;
+            for (int64_t d = b + 1; d < r1; ++d) {
+                if (pair_bin(&q->c, q->nbr[a], q->nbr[d]) < 0) continue;
+                if (pair_bin(&q->c, q->nbr[b], q->nbr[d]) < 0) continue;
+                int64_t s[3] = { q->nbr[a], q->nbr[b], q->nbr[d] };
+                int bb[3] = { q->bin[a], q->bin[b], q->bin[d] };
+                add_clique(&q->c, q->t4, ev, od, i, s, bb);
+            }
+        }
+}
+
+/* even/odd[C(nb,3)] over hubs i in [hub_begin, hub_end). */
+void oracle_4pcf_parity_range(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                              const int64_t *edges, int nb, const int64_t *row_ptr,
+                              const int32_t *nbr, const uint8_t *bin,
+                              int64_t hub_begin, int64_t hub_end,
+                              uint64_t *even, int64_t *odd)
+{
+    int nt = oracle_threads();
+    quad_ctx_t q;
+    q.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    q.row_ptr = row_ptr; q.nbr = nbr; q.bin = bin;
+    q.t4 = table4(nb < 3 ? 3 : nb);
+    q.ncfg = oracle_nconfig4(nb);
+    size_t m = q.ncfg > 0 ? (size_t)q.ncfg : 1;
+    q.even = (uint64_t *)calloc((size_t)nt * m, sizeof(uint64_t));
+    q.odd = (int64_t *)calloc((size_t)nt * m, sizeof(int64_t));
+    if (q.ncfg > 0) {
+        if (hub_end > hub_begin) parallel_for(hub_begin, hub_end, nt, quad_hub, &q);
+        reduce_u64(even, q.even, nt, q.ncfg);
+        reduce_i64(odd, q.odd, nt, q.ncfg);
+    }
+    free(q.even); free(q.odd);
+    free((void *)q.t4);
+}
+
+void oracle_4pcf_parity(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                        const int64_t *edges, int nb, const int64_t *row_ptr,
+                        const int32_t *nbr, const uint8_t *bin, uint64_t *even, int64_t *odd)
+{
+    oracle_4pcf_parity_range(xyz, n, box, periodic, edges, nb, row_ptr, nbr, bin, 0, n, even, odd);
+}
+
+/* Parity-4pCF contribution of the listed hubs only, each row found by brute
+ * force over all points (no graph needed: for sampled checks at full size). */
+void oracle_4pcf_parity_hubs(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                             const int64_t *edges, int nb, const int64_t *hubs, int64_t nh,
+                             uint64_t *even, int64_t *odd)
+{
+    cat_t c = { xyz, n, box, periodic, edges, nb };
+    int32_t *t4 = table4(nb < 3 ? 3 : nb);
+    int64_t ncfg = oracle_nconfig4(nb);
+    memset(even, 0, sizeof(uint64_t) * (size_t)(ncfg > 0 ? ncfg : 0));
+    memset(odd, 0, sizeof(int64_t) * (size_t)(ncfg > 0 ? ncfg : 0));
+    int32_t *row = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    uint8_t *rb = (uint8_t *)malloc((size_t)(n > 0 ? n : 1));
+    for (int64_t h = 0; h < nh && ncfg > 0; ++h) {
+        int64_t i = hubs[h];
+        int64_t m = oracle_row(xyz, n, box, periodic, edges, nb, i, row, rb);
+        for (int64_t a = 0; a < m; ++a)
+            for (int64_t b = a + 1; b < m; ++b) {
+                if (pair_bin(&c, row[a], row[b]) < 0) continue;
+                for (int64_t d = b + 1; d < m; ++d) {
+                    if (pair_bin(&c, row[a], row[d]) < 0) continue;
+                    if (pair_bin(&c, row[b], row[d]) < 0) continue;
+                    int64_t s[3] = { row[a], row[b], row[d] };
+                    int bb[3] = { rb[a], rb[b], rb[d] };
+                    add_clique(&c, t4, even, odd, i, s, bb);
+                }
+            }
+    }
+    free(row); free(rb); free(t4);
+}
+
+/* ------------------------------------------------------------------------ */
+/* brute force with no graph                                                 */
+
+typedef struct {
+    cat_t c;
+    const int32_t *t;
+    int64_t ncfg;
+    uint64_t *hist;
+    int64_t *odd;
+} brute_ctx_t;
+
+static void brute3_i(void *vctx, int tid, int64_t i)
+{
+    brute_ctx_t *b = (brute_ctx_t *)vctx;
+    uint64_t *h = b->hist + (size_t)tid * (size_t)b->ncfg;
+    int nb = b->c.nb;
+    for (int64_t j = i + 1; j < b->c.n; ++j) {
+        int bij = pair_bin(&b->c, i, j);
+        if (bij < 0) continue;
+        for (int64_t k = j + 1; k < b->c.n; ++k) {
+            int bik = pair_bin(&b->c, i, k);
+            if (bik < 0) continue;
+            int bjk = pair_bin(&b->c, j, k);
+            if (bjk < 0) continue;
+            int v[3] = { bij, bik, bjk };
+            sort3(v);
+            h[b->t[((size_t)v[0] * nb + v[1]) * nb + v[2]]] += 1;
+        }
+    }
+}
+
+/* O(N^3) over all unordered triples i < j < k. */
+void oracle_brute3(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                   const int64_t *edges, int nb, uint64_t *hist)
+{
+    int nt = oracle_threads();
+    brute_ctx_t b;
+    b.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    b.t = table3(nb);
+    b.ncfg = oracle_nconfig3(nb);
+    b.hist = (uint64_t *)calloc((size_t)nt * (size_t)b.ncfg, sizeof(uint64_t));
+    b.odd = NULL;
+    parallel_for(0, n, nt, brute3_i, &b);
+    reduce_u64(hist, b.hist, nt, b.ncfg);
+    free(b.hist);
+    free((void *)b.t);
+}
+
+static void brute4_i(void *vctx, int tid, int64_t i)
+{
+    brute_ctx_t *b = (brute_ctx_t *)vctx;
+    uint64_t *ev = b->hist + (size_t)tid * (size_t)b->ncfg;
+    int64_t *od = b->odd + (size_t)tid * (size_t)b->ncfg;
+    int64_t n = b->c.n;
+    for (int64_t j = 0; j < n; ++j) {
+        int bij = pair_bin(&b->c, i, j);
+        if (bij < 0) continue;
+        for (int64_t k = j + 1; k < n; ++k) {
+            int bik = pair_bin(&b->c, i, k);
+            if (bik < 0 || pair_bin(&b->c, j, k) < 0) continue;
+            for (int64_t l = k + 1; l < n; ++l) {
+                int bil = pair_bin(&b->c, i, l);
+                if (bil < 0 || pair_bin(&b->c, j, l) < 0 || pair_bin(&b->c, k, l) < 0) continue;
+                int64_t s[3] = { j, k, l };
+                int bb[3] = { bij, bik, bil };
+                add_clique(&b->c, b->t, ev, od, i, s, bb);
+            }
+        }
+    }
+}
+
+/* O(N^4): every hub i and every triple j < k < l of other points. */
+void oracle_brute4(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                   const int64_t *edges, int nb, uint64_t *even, int64_t *odd)
+{
+    int nt = oracle_threads();
+    brute_ctx_t b;
+    b.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    b.t = table4(nb < 3 ? 3 : nb);
+    b.ncfg = oracle_nconfig4(nb);
+    if (b.ncfg <= 0) { free((void *)b.t); return; }
+    b.hist = (uint64_t *)calloc((size_t)nt * (size_t)b.ncfg, sizeof(uint64_t));
+    b.odd = (int64_t *)calloc((size_t)nt * (size_t)b.ncfg, sizeof(int64_t));
+    parallel_for(0, n, nt, brute4_i, &b);
+    reduce_u64(even, b.hist, nt, b.ncfg);
+    reduce_i64(odd, b.odd, nt, b.ncfg);
+    free(b.hist); free(b.odd);
+    free((void *)b.t);
+}
