@@ -1,1 +1,206 @@
-"""GB300-native graph-based 3pCF / parity-4pCF counting (placeholder, filled in below)."""
+"""GB300-native graph-based 3pCF and parity-4pCF counting.
+
+A thin Python layer over libgramsci_gb.so (C ABI: include/gramsci_gb.h). It
+only marshals arguments: every step of the computation (cell sort, neighbour
+graph, triangle and clique enumeration, histograms) runs in the library's
+sm_103a CUDA kernels. PyTorch supplies device memory and CUDA streams.
+
+Counting follows the GRAMSCI v2 paper ("Fast Graph-based Higher-Order
+Clustering Statistics on the GPU"): the fixed-radius neighbour graph of §II.1,
+the triangle (3pCF) enumeration of §II.2 / §III.1, and the parity-decomposed
+4pCF of §III.2 (Eq.(3)).
+
+Histograms come back as int64 tensors whose bits are the library's uint64
+counts (torch has no general uint64 arithmetic); use ``as_uint64`` to read
+them as unsigned NumPy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _lib
+from ._lib import GramsciError
+
+__all__ = ["Graph", "GramsciError", "build_graph", "count_3pcf_from_host",
+           "count_4pcf_parity_from_host", "config_count_3pcf", "config_count_4pcf",
+           "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path"]
+
+
+def library_path() -> str:
+    return _lib.lib_path()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _edges(edges_lu):
+    e = np.ascontiguousarray(np.asarray(edges_lu, dtype=np.int64))
+    if e.ndim != 1 or len(e) < 2:
+        raise ValueError("edges_lu needs at least two entries")
+    return e
+
+
+def as_uint64(t) -> np.ndarray:
+    """Host NumPy uint64 view of a histogram tensor."""
+    return t.detach().cpu().numpy().view(np.uint64)
+
+
+def config_count_3pcf(nbins: int) -> int:
+    return _lib.load().gs_config_count_3pcf(nbins)
+
+
+def config_count_4pcf(nbins: int) -> int:
+    return _lib.load().gs_config_count_4pcf(nbins)
+
+
+def config_index_3pcf(nbins: int, b1: int, b2: int, b3: int) -> int:
+    return _lib.load().gs_config_index_3pcf(nbins, b1, b2, b3)
+
+
+def config_index_4pcf(nbins: int, b1: int, b2: int, b3: int) -> int:
+    return _lib.load().gs_config_index_4pcf(nbins, b1, b2, b3)
+
+
+class Graph:
+    """A neighbour graph resident in device memory (handle of the C library)."""
+
+    def __init__(self, handle: ctypes.c_void_p, nbins: int, device):
+        self._h = handle
+        self.nbins = nbins
+        self.device = device
+
+    # -- sizes
+    def info(self):
+        n, e, m = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+        _lib.check(_lib.load().gs_graph_info(self._h, ctypes.byref(n), ctypes.byref(e), ctypes.byref(m)))
+        return n.value, e.value, m.value
+
+    @property
+    def n(self) -> int:
+        return self.info()[0]
+
+    @property
+    def n_edges(self) -> int:
+        return self.info()[1]
+
+    @property
+    def max_degree(self) -> int:
+        return self.info()[2]
+
+    # -- counts
+    def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
+        """uint64 triangle histogram over sorted bin triples (int64 tensor on the device)."""
+        torch = _torch()
+        hub_end = self.n if hub_end is None else hub_end
+        m = config_count_3pcf(self.nbins)
+        if out is None:
+            out = torch.empty(m, dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_count_3pcf(self._h, ctypes.c_void_p(out.data_ptr()),
+                                             int(hub_begin), int(hub_end), _stream(stream)))
+        return out
+
+    def count_4pcf_parity(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
+        """(even uint64, odd int64) histograms over strictly increasing hub-bin triples."""
+        torch = _torch()
+        hub_end = self.n if hub_end is None else hub_end
+        m = max(config_count_4pcf(self.nbins), 0)
+        if out is None:
+            out = (torch.zeros(m, dtype=torch.int64, device=self.device),
+                   torch.zeros(m, dtype=torch.int64, device=self.device))
+        even, odd = out
+        _lib.check(_lib.load().gs_count_4pcf_parity(self._h, ctypes.c_void_p(even.data_ptr()),
+                                                    ctypes.c_void_p(odd.data_ptr()),
+                                                    int(hub_begin), int(hub_end), _stream(stream)))
+        return even, odd
+
+    # -- exports
+    def export_csr(self, stream=None):
+        """(row_ptr int64 [n+1], nbr int32 [E], bin uint8 [E]) in input numbering, rows sorted."""
+        torch = _torch()
+        n, e, _ = self.info()
+        row_ptr = torch.empty(n + 1, dtype=torch.int64, device=self.device)
+        nbr = torch.empty(max(e, 1), dtype=torch.int32, device=self.device)
+        bins = torch.empty(max(e, 1), dtype=torch.uint8, device=self.device)
+        _lib.check(_lib.load().gs_graph_export_csr(self._h, ctypes.c_void_p(row_ptr.data_ptr()),
+                                                   ctypes.c_void_p(nbr.data_ptr()),
+                                                   ctypes.c_void_p(bins.data_ptr()), _stream(stream)))
+        return row_ptr, nbr[:e], bins[:e]
+
+    def export_perm(self, stream=None):
+        """int32 [n]: input index of each point in the graph's internal (hub) order."""
+        torch = _torch()
+        perm = torch.empty(max(self.n, 1), dtype=torch.int32, device=self.device)
+        _lib.check(_lib.load().gs_graph_export_perm(self._h, ctypes.c_void_p(perm.data_ptr()),
+                                                    _stream(stream)))
+        return perm[:self.n]
+
+    def free(self):
+        if self._h:
+            _lib.load().gs_graph_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+
+
+def build_graph(coords, box_lu: int, periodic: bool, edges_lu, stream=None) -> Graph:
+    """Neighbour graph of int32 lattice coordinates (a CUDA tensor [n, 3])."""
+    torch = _torch()
+    if not (isinstance(coords, torch.Tensor) and coords.is_cuda and coords.dtype == torch.int32):
+        raise TypeError("coords must be an int32 CUDA tensor of shape [n, 3]")
+    coords = coords.contiguous().reshape(-1, 3)
+    e = _edges(edges_lu)
+    h = ctypes.c_void_p()
+    _lib.check(_lib.load().gs_build_graph(ctypes.c_void_p(coords.data_ptr()), coords.shape[0], int(box_lu),
+                                          int(bool(periodic)), int(e[-1]),
+                                          e.ctypes.data_as(ctypes.c_void_p), len(e) - 1,
+                                          _stream(stream), ctypes.byref(h)))
+    return Graph(h, len(e) - 1, coords.device)
+
+
+def count_3pcf_from_host(coords: np.ndarray, box_lu: int, periodic: bool, edges_lu, out=None,
+                         stream=None) -> np.ndarray:
+    """Host coordinates in, host uint64 histogram out, in one library call."""
+    xyz = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 3))
+    e = _edges(edges_lu)
+    m = config_count_3pcf(len(e) - 1)
+    if out is None:
+        out = np.zeros(m, dtype=np.uint64)
+    _lib.check(_lib.load().gs_3pcf_from_host(xyz.ctypes.data_as(ctypes.c_void_p), len(xyz), int(box_lu),
+                                             int(bool(periodic)), int(e[-1]), e.ctypes.data_as(ctypes.c_void_p),
+                                             len(e) - 1, out.ctypes.data_as(ctypes.c_void_p), _stream(stream)))
+    return out
+
+
+def count_4pcf_parity_from_host(coords: np.ndarray, box_lu: int, periodic: bool, edges_lu, out=None,
+                                stream=None):
+    xyz = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 3))
+    e = _edges(edges_lu)
+    m = max(config_count_4pcf(len(e) - 1), 0)
+    if out is None:
+        out = (np.zeros(max(m, 1), dtype=np.uint64), np.zeros(max(m, 1), dtype=np.int64))
+    even, odd = out
+    _lib.check(_lib.load().gs_4pcf_parity_from_host(
+        xyz.ctypes.data_as(ctypes.c_void_p), len(xyz), int(box_lu), int(bool(periodic)), int(e[-1]),
+        e.ctypes.data_as(ctypes.c_void_p), len(e) - 1, even.ctypes.data_as(ctypes.c_void_p),
+        odd.ctypes.data_as(ctypes.c_void_p), _stream(stream)))
+    return even[:m], odd[:m]

@@ -1,0 +1,77 @@
+"""ctypes declarations of the C ABI in include/gramsci_gb.h.
+
+Loading fails loudly when libgramsci_gb.so is missing: there is no fallback
+implementation of any step.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_int = ctypes.c_int
+_p = ctypes.c_void_p
+
+GS_OK, GS_ERR_ARG, GS_ERR_NOMEM, GS_ERR_CUDA, GS_ERR_CAPACITY, GS_ERR_INTERNAL = range(6)
+STATUS_NAMES = {0: "GS_OK", 1: "GS_ERR_ARG", 2: "GS_ERR_NOMEM", 3: "GS_ERR_CUDA",
+                4: "GS_ERR_CAPACITY", 5: "GS_ERR_INTERNAL"}
+
+# name -> (restype, argtypes); every function the header declares
+SIGNATURES = {
+    "gs_build_graph": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _p, ctypes.POINTER(_p)]),
+    "gs_count_3pcf": (_int, [_p, _p, _i64, _i64, _p]),
+    "gs_count_4pcf_parity": (_int, [_p, _p, _p, _i64, _i64, _p]),
+    "gs_graph_info": (_int, [_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i32)]),
+    "gs_graph_export_csr": (_int, [_p, _p, _p, _p, _p]),
+    "gs_graph_export_perm": (_int, [_p, _p, _p]),
+    "gs_config_count_3pcf": (_i64, [_int]),
+    "gs_config_count_4pcf": (_i64, [_int]),
+    "gs_config_index_3pcf": (_i64, [_int, _int, _int, _int]),
+    "gs_config_index_4pcf": (_i64, [_int, _int, _int, _int]),
+    "gs_3pcf_from_host": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _p, _p]),
+    "gs_4pcf_parity_from_host": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _p, _p, _p]),
+    "gs_graph_free": (None, [_p]),
+    "gs_last_error": (ctypes.c_char_p, []),
+    "gs_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+class GramsciError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    from . import build as _build
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """The loaded library. Raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            if build_if_missing:
+                from . import build as _build
+                _build.build()
+            else:
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m cosmology_point_correlation_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def check(status: int):
+    if status != GS_OK:
+        raise GramsciError(status, load().gs_last_error().decode())

@@ -1,0 +1,693 @@
+// gs_build.cu -- fixed-radius neighbour graph on the GPU (GRAMSCI v2, §II.1 and
+// §III.5.1): cell list, counting sort by cell, two-pass (count, fill) neighbour
+// search writing index-sorted CSR rows with a radial-bin byte per edge.
+//
+// The paper builds the graph on the CPU with a kd-tree; here a uniform cell
+// grid with cell side >= r_max makes the search a scan of <= 27 neighbour
+// cells, which the GPU does with coalesced, shared-memory-staged candidate
+// tiles. Rows come out sorted (Eq.(1)) with no sort pass: points are numbered
+// in cell order and the neighbour cells of a point are visited in increasing
+// cell id, so the candidates are met in increasing index order.
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "gs_internal.cuh"
+
+// ---------------------------------------------------------------- errors
+
+static thread_local char g_msg[512] = "";
+
+gs_status gs_set_error(gs_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+void gs_clear_error() { g_msg[0] = 0; }
+
+extern "C" const char *gs_last_error(void) { return g_msg; }
+
+int gs_sm_count()
+{
+    static int cache[64] = { 0 };
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 1;
+    if (!cache[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = v > 0 ? v : 1;
+    }
+    return cache[dev];
+}
+
+// ---------------------------------------------------------------- exclusive scan
+//
+// Three phases over tiles of SCAN_TILE elements: per-tile scan writing tile
+// totals, a one-block scan of the totals, then a uniform add.
+
+constexpr int SCAN_THREADS = 256;
+constexpr int SCAN_ITEMS = 8;
+constexpr int SCAN_TILE = SCAN_THREADS * SCAN_ITEMS;
+
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T *total)
+{
+    __shared__ T warp_sums[SCAN_THREADS / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        T y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        T w = lane < SCAN_THREADS / 32 ? warp_sums[lane] : T(0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            T y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < SCAN_THREADS / 32) warp_sums[lane] = w;
+    }
+    __syncthreads();
+    T prefix = (warp > 0 ? warp_sums[warp - 1] : T(0)) + x - v;
+    *total = warp_sums[SCAN_THREADS / 32 - 1];
+    __syncthreads();
+    return prefix;
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(SCAN_THREADS)
+k_scan_tiles(const int32_t *__restrict__ in, Tout *__restrict__ out, Tout *__restrict__ tile_sums,
+             int64_t n)
+{
+    const int64_t base = (int64_t)blockIdx.x * SCAN_TILE + (int64_t)threadIdx.x * SCAN_ITEMS;
+    Tout v[SCAN_ITEMS];
+    Tout s = 0;
+#pragma unroll
+    for (int k = 0; k < SCAN_ITEMS; ++k) {
+        v[k] = (base + k < n) ? (Tout)in[base + k] : Tout(0);
+        s += v[k];
+    }
+    Tout total;
+    Tout run = block_exclusive_scan<Tout>(s, &total);
+#pragma unroll
+    for (int k = 0; k < SCAN_ITEMS; ++k) {
+        if (base + k < n) out[base + k] = run;
+        run += v[k];
+    }
+    if (threadIdx.x == 0) tile_sums[blockIdx.x] = total;
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(SCAN_THREADS)
+k_scan_sums(Tout *__restrict__ sums, int64_t ntiles, Tout *__restrict__ grand_total)
+{
+    Tout carry = 0;
+    for (int64_t b = 0; b < ntiles; b += SCAN_TILE) {
+        const int64_t base = b + (int64_t)threadIdx.x * SCAN_ITEMS;
+        Tout v[SCAN_ITEMS];
+        Tout s = 0;
+#pragma unroll
+        for (int k = 0; k < SCAN_ITEMS; ++k) {
+            v[k] = (base + k < ntiles) ? sums[base + k] : Tout(0);
+            s += v[k];
+        }
+        Tout total;
+        Tout run = block_exclusive_scan<Tout>(s, &total) + carry;
+#pragma unroll
+        for (int k = 0; k < SCAN_ITEMS; ++k) {
+            if (base + k < ntiles) sums[base + k] = run;
+            run += v[k];
+        }
+        carry += total;
+    }
+    if (threadIdx.x == 0) *grand_total = carry;
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(SCAN_THREADS)
+k_scan_add(Tout *__restrict__ out, const Tout *__restrict__ tile_sums, int64_t n)
+{
+    const int64_t base = (int64_t)blockIdx.x * SCAN_TILE + (int64_t)threadIdx.x * SCAN_ITEMS;
+    const Tout add = tile_sums[blockIdx.x];
+#pragma unroll
+    for (int k = 0; k < SCAN_ITEMS; ++k)
+        if (base + k < n) out[base + k] += add;
+}
+
+template <typename Tout>
+static gs_status scan_impl(const int32_t *in, Tout *out, int64_t n, cudaStream_t st)
+{
+    if (n == 0) {
+        GS_TRY_CUDA(cudaMemsetAsync(out, 0, sizeof(Tout), st));
+        return GS_OK;
+    }
+    const int64_t ntiles = (n + SCAN_TILE - 1) / SCAN_TILE;
+    Tout *sums = nullptr;
+    GS_TRY_CUDA(cudaMallocAsync(&sums, sizeof(Tout) * ntiles, st));
+    k_scan_tiles<Tout><<<(unsigned)ntiles, SCAN_THREADS, 0, st>>>(in, out, sums, n);
+    k_scan_sums<Tout><<<1, SCAN_THREADS, 0, st>>>(sums, ntiles, out + n);
+    k_scan_add<Tout><<<(unsigned)ntiles, SCAN_THREADS, 0, st>>>(out, sums, n);
+    cudaError_t e = cudaGetLastError();
+    cudaFreeAsync(sums, st);
+    if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "scan launch failed: %s", cudaGetErrorString(e));
+    return GS_OK;
+}
+
+gs_status gs_scan_i32_to_i64(const int32_t *in, int64_t *out, int64_t n, cudaStream_t st)
+{
+    return scan_impl<int64_t>(in, out, n, st);
+}
+
+gs_status gs_scan_i32_to_i32(const int32_t *in, int32_t *out, int64_t n, cudaStream_t st)
+{
+    return scan_impl<int32_t>(in, out, n, st);
+}
+
+// ---------------------------------------------------------------- cell sort
+
+// Cell of each point and its arrival slot in that cell; flags coordinates
+// outside [0, box).
+__global__ void k_cell_assign(const int32_t *__restrict__ xyz, int64_t n, int box, int ncell,
+                              int32_t *__restrict__ cell, int32_t *__restrict__ slot,
+                              int32_t *__restrict__ cell_count, int32_t *__restrict__ err)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        int x = xyz[3 * i], y = xyz[3 * i + 1], z = xyz[3 * i + 2];
+        bool ok = x >= 0 && x < box && y >= 0 && y < box && z >= 0 && z < box;
+        if (!ok) {
+            atomicOr(err, 1);
+            x = y = z = 0;
+        }
+        int cx = (int)((long long)x * ncell / box);
+        int cy = (int)((long long)y * ncell / box);
+        int cz = (int)((long long)z * ncell / box);
+        int c = (cx * ncell + cy) * ncell + cz;
+        cell[i] = c;
+        slot[i] = atomicAdd(&cell_count[c], 1);
+    }
+}
+
+__global__ void k_cell_scatter(const int32_t *__restrict__ cell, const int32_t *__restrict__ slot,
+                               const int32_t *__restrict__ cell_start, int64_t n,
+                               int32_t *__restrict__ tmp)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        tmp[cell_start[cell[i]] + slot[i]] = (int32_t)i;
+}
+
+// Put each cell's points in increasing input index (the atomic slots above
+// arrive in arbitrary order). One warp per cell, rank sort: each element's
+// new position is the number of smaller ids in its cell.
+__global__ void k_cell_order(const int32_t *__restrict__ cell_start, int ncells,
+                             const int32_t *__restrict__ tmp, int32_t *__restrict__ perm)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t c = w0; c < ncells; c += nw) {
+        const int s0 = cell_start[c], s1 = cell_start[c + 1];
+        for (int a = s0 + lane; a < s1; a += 32) {
+            const int e = tmp[a];
+            int r = 0;
+            for (int b = s0; b < s1; ++b) r += tmp[b] < e;
+            perm[s0 + r] = e;
+        }
+    }
+}
+
+__global__ void k_gather_points(const int32_t *__restrict__ xyz, const int32_t *__restrict__ perm,
+                                int64_t n, int4 *__restrict__ pts, int32_t *__restrict__ inv)
+{
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < n;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const int i = perm[p];
+        pts[p] = make_int4(xyz[3 * (int64_t)i], xyz[3 * (int64_t)i + 1], xyz[3 * (int64_t)i + 2], i);
+        inv[i] = (int32_t)p;
+    }
+}
+
+// ---------------------------------------------------------------- neighbour search
+//
+// One block per home cell. The block stages up to NB_HOME home points and,
+// range by range, up to NB_CAND candidate points in shared memory; each warp
+// tests its home points against the staged tile, 32 candidates per step, and
+// (FILL pass) writes hits in candidate order with a ballot prefix count.
+// Neighbour cells are visited in increasing id, merged into contiguous index
+// ranges (a z-run of three cells is one range unless it wraps).
+
+constexpr int NB_THREADS = 256;
+constexpr int NB_HOME = 512;
+constexpr int NB_CAND = 1024;
+
+template <bool FILL>
+__global__ void __launch_bounds__(NB_THREADS)
+k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start, int ncell,
+            int box, int periodic, long long e0sq, long long rsq,
+            const long long *__restrict__ esq, int nb,
+            int32_t *__restrict__ deg, int32_t *__restrict__ fwd,
+            const int64_t *__restrict__ row_ptr, int32_t *__restrict__ nbr,
+            uint8_t *__restrict__ bin, unsigned *__restrict__ max_deg)
+{
+    __shared__ int4 s_home[NB_HOME];
+    __shared__ int s_cnt[NB_HOME];
+    __shared__ int s_lo[NB_HOME];
+    __shared__ int4 s_cand[NB_CAND];
+    __shared__ long long s_esq[256];
+    __shared__ int s_r0[27], s_r1[27];
+    __shared__ int s_nr;
+
+    const int c = blockIdx.x;
+    const int h0 = cell_start[c], h1 = cell_start[c + 1];
+    if (h0 >= h1) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = NB_THREADS / 32;
+
+    if (FILL)
+        for (int t = threadIdx.x; t <= nb; t += NB_THREADS) s_esq[t] = esq[t];
+    if (threadIdx.x == 0) {
+        const int cx = c / (ncell * ncell), cy = (c / ncell) % ncell, cz = c % ncell;
+        int ids[27];
+        int m = 0;
+        for (int dx = -1; dx <= 1; ++dx)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dz = -1; dz <= 1; ++dz) {
+                    int x = cx + dx, y = cy + dy, z = cz + dz;
+                    if (periodic) {
+                        x = (x + ncell) % ncell;
+                        y = (y + ncell) % ncell;
+                        z = (z + ncell) % ncell;
+                    } else if (x < 0 || x >= ncell || y < 0 || y >= ncell || z < 0 || z >= ncell) {
+                        continue;
+                    }
+                    ids[m++] = (x * ncell + y) * ncell + z;
+                }
+        for (int a = 1; a < m; ++a)        // insertion sort, m <= 27
+            for (int b = a; b > 0 && ids[b - 1] > ids[b]; --b) {
+                int t = ids[b];
+                ids[b] = ids[b - 1];
+                ids[b - 1] = t;
+            }
+        int nr = 0, prev = -2;
+        for (int a = 0; a < m; ++a) {
+            if (ids[a] == prev) continue;  // duplicate cell (fewer than 3 cells per axis)
+            if (ids[a] == prev + 1) {
+                s_r1[nr - 1] = cell_start[ids[a] + 1];
+            } else {
+                s_r0[nr] = cell_start[ids[a]];
+                s_r1[nr] = cell_start[ids[a] + 1];
+                ++nr;
+            }
+            prev = ids[a];
+        }
+        s_nr = nr;
+    }
+    __syncthreads();
+    const int nr = s_nr;
+
+    for (int hb = h0; hb < h1; hb += NB_HOME) {
+        const int hn = min(NB_HOME, h1 - hb);
+        for (int t = threadIdx.x; t < hn; t += NB_THREADS) {
+            s_home[t] = pts[hb + t];
+            s_cnt[t] = 0;
+            s_lo[t] = 0;
+        }
+        __syncthreads();
+        for (int r = 0; r < nr; ++r) {
+            for (int cb = s_r0[r]; cb < s_r1[r]; cb += NB_CAND) {
+                const int cn = min(NB_CAND, s_r1[r] - cb);
+                for (int t = threadIdx.x; t < cn; t += NB_THREADS) s_cand[t] = pts[cb + t];
+                __syncthreads();
+                for (int hp = warp; hp < hn; hp += nwarps) {
+                    const int p = hb + hp;
+                    const int4 P = s_home[hp];
+                    int cnt = s_cnt[hp];
+                    int lo = s_lo[hp];
+                    const int64_t rowp = FILL ? row_ptr[p] : 0;
+                    for (int t0 = 0; t0 < cn; t0 += 32) {
+                        const int t = t0 + lane;
+                        bool hit = false;
+                        long long d2 = 0;
+                        if (t < cn) {
+                            const int4 Q = s_cand[t];
+                            const int dx = gs_delta(P.x, Q.x, box, periodic);
+                            const int dy = gs_delta(P.y, Q.y, box, periodic);
+                            const int dz = gs_delta(P.z, Q.z, box, periodic);
+                            d2 = gs_norm2(dx, dy, dz);
+                            hit = (cb + t != p) && d2 >= e0sq && d2 < rsq;
+                        }
+                        const unsigned m = __ballot_sync(0xffffffffu, hit);
+                        if (FILL && hit) {
+                            const int64_t pos = rowp + cnt + __popc(m & gs_lanemask_lt());
+                            int lo_b = 0, hi_b = nb;       // e_lo^2 <= d2 < e_hi^2
+                            while (hi_b - lo_b > 1) {
+                                const int mid = (lo_b + hi_b) >> 1;
+                                if (s_esq[mid] <= d2) lo_b = mid; else hi_b = mid;
+                            }
+                            nbr[pos] = cb + t;
+                            bin[pos] = (uint8_t)lo_b;
+                        }
+                        cnt += __popc(m);
+                        if (!FILL) lo += __popc(__ballot_sync(0xffffffffu, hit && cb + t < p));
+                    }
+                    if (lane == 0) {
+                        s_cnt[hp] = cnt;
+                        s_lo[hp] = lo;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        if (!FILL) {
+            for (int t = threadIdx.x; t < hn; t += NB_THREADS) {
+                deg[hb + t] = s_cnt[t];
+                fwd[hb + t] = s_lo[t];
+                atomicMax(max_deg, (unsigned)s_cnt[t]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- build
+
+static int choose_ncell(int64_t box, int64_t rmax, int64_t n)
+{
+    int64_t nc = rmax > 0 ? box / rmax : 1;
+    if (nc < 1) nc = 1;
+    // keep the cell table no larger than the point count (and within 2^24 cells)
+    while (nc > 1 && (nc * nc * nc > std::max<int64_t>(n, 1) || nc * nc * nc > (1ll << 24))) --nc;
+    return (int)nc;
+}
+
+static void free_graph_arrays(gs_graph *g)
+{
+    if (!g) return;
+    cudaFree(g->pts);
+    cudaFree(g->inv);
+    cudaFree(g->row_ptr);
+    cudaFree(g->fwd);
+    cudaFree(g->nbr);
+    cudaFree(g->bin);
+    cudaFree(g->work);
+    cudaFree(g->err);
+}
+
+extern "C" void gs_graph_free(gs_graph_t g)
+{
+    if (!g) return;
+    cudaDeviceSynchronize();
+    free_graph_arrays(g);
+    delete g;
+}
+
+static gs_status validate_build(const int32_t *coords, int64_t n, int64_t box, int periodic,
+                                int64_t rmax, const int64_t *edges, int nb, gs_graph_t *out)
+{
+    if (!out) return gs_set_error(GS_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (n < 0 || n >= 2147483647ll) return gs_set_error(GS_ERR_ARG, "n = %lld outside [0, 2^31-1)", (long long)n);
+    if (n > 0 && !coords) return gs_set_error(GS_ERR_ARG, "coords_dev is NULL");
+    if (box < 1 || box > (1ll << 30)) return gs_set_error(GS_ERR_ARG, "box_lu = %lld outside [1, 2^30]", (long long)box);
+    if (nb < 1 || nb > 255) return gs_set_error(GS_ERR_ARG, "nbins = %d outside [1, 255]", nb);
+    if (!edges) return gs_set_error(GS_ERR_ARG, "edges_lu is NULL");
+    if (edges[0] < 0) return gs_set_error(GS_ERR_ARG, "edges_lu[0] < 0");
+    for (int k = 0; k < nb; ++k)
+        if (edges[k + 1] <= edges[k]) return gs_set_error(GS_ERR_ARG, "edges_lu not strictly increasing at %d", k);
+    if (edges[nb] != rmax) return gs_set_error(GS_ERR_ARG, "r_max_lu != edges_lu[nbins]");
+    if (rmax > (1ll << 31)) return gs_set_error(GS_ERR_ARG, "r_max_lu too large");
+    if (periodic && 2 * rmax > box) return gs_set_error(GS_ERR_ARG, "periodic box needs 2*r_max_lu <= box_lu");
+    return GS_OK;
+}
+
+extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
+                                    int64_t r_max_lu, const int64_t *edges_lu, int nbins,
+                                    void *cuda_stream, gs_graph_t *out)
+{
+    gs_clear_error();
+    gs_status s = validate_build(coords_dev, n, box_lu, periodic, r_max_lu, edges_lu, nbins, out);
+    if (s != GS_OK) return s;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+
+    gs_graph *g = new gs_graph();
+    memset(g, 0, sizeof(*g));
+    cudaGetDevice(&g->device);
+    g->n = n;
+    g->box_lu = box_lu;
+    g->periodic = periodic ? 1 : 0;
+    g->nb = nbins;
+    for (int k = 0; k <= nbins; ++k) g->edges[k] = edges_lu[k];
+    g->ncell = choose_ncell(box_lu, r_max_lu, n);
+    const int ncells = g->ncell * g->ncell * g->ncell;
+
+    int32_t *cell = nullptr, *slot = nullptr, *cell_count = nullptr, *cell_start = nullptr;
+    int32_t *tmp = nullptr, *perm = nullptr, *deg = nullptr;
+    long long *esq = nullptr;
+    unsigned *maxd = nullptr;
+    const int sms = gs_sm_count();
+    const int grid1 = (int)std::min<int64_t>(std::max<int64_t>((n + 255) / 256, 1), (int64_t)sms * 16);
+
+#define GS_BUILD_CUDA(call)                                                                  \
+    do {                                                                                     \
+        cudaError_t e_ = (call);                                                             \
+        if (e_ != cudaSuccess) {                                                             \
+            s = gs_set_error(e_ == cudaErrorMemoryAllocation ? GS_ERR_NOMEM : GS_ERR_CUDA,   \
+                             "%s failed: %s", #call, cudaGetErrorString(e_));                \
+            goto fail;                                                                       \
+        }                                                                                    \
+    } while (0)
+
+    {
+        const size_t nn = (size_t)std::max<int64_t>(n, 1);
+        GS_BUILD_CUDA(cudaMalloc(&g->pts, sizeof(int4) * nn));
+        GS_BUILD_CUDA(cudaMalloc(&g->inv, sizeof(int32_t) * nn));
+        GS_BUILD_CUDA(cudaMalloc(&g->row_ptr, sizeof(int64_t) * (nn + 1)));
+        GS_BUILD_CUDA(cudaMalloc(&g->fwd, sizeof(int32_t) * nn));
+        GS_BUILD_CUDA(cudaMalloc(&g->work, sizeof(unsigned long long) * 4));
+        GS_BUILD_CUDA(cudaMalloc(&g->err, sizeof(int32_t)));
+        GS_BUILD_CUDA(cudaMallocAsync(&cell, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&slot, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&tmp, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&perm, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&deg, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&cell_count, sizeof(int32_t) * ncells, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&cell_start, sizeof(int32_t) * (ncells + 1), st));
+        GS_BUILD_CUDA(cudaMallocAsync(&esq, sizeof(long long) * 256, st));
+        GS_BUILD_CUDA(cudaMallocAsync(&maxd, sizeof(unsigned), st));
+
+        long long hesq[256];
+        for (int k = 0; k <= nbins; ++k) hesq[k] = (long long)edges_lu[k] * edges_lu[k];
+        GS_BUILD_CUDA(cudaMemcpyAsync(esq, hesq, sizeof(long long) * (nbins + 1), cudaMemcpyHostToDevice, st));
+        GS_BUILD_CUDA(cudaMemsetAsync(cell_count, 0, sizeof(int32_t) * ncells, st));
+        GS_BUILD_CUDA(cudaMemsetAsync(g->err, 0, sizeof(int32_t), st));
+        GS_BUILD_CUDA(cudaMemsetAsync(maxd, 0, sizeof(unsigned), st));
+
+        if (n > 0) {
+            k_cell_assign<<<grid1, 256, 0, st>>>(coords_dev, n, (int)box_lu, g->ncell, cell, slot,
+                                                 cell_count, g->err);
+            GS_BUILD_CUDA(cudaGetLastError());
+        }
+        s = gs_scan_i32_to_i32(cell_count, cell_start, ncells, st);
+        if (s != GS_OK) goto fail;
+        if (n > 0) {
+            k_cell_scatter<<<grid1, 256, 0, st>>>(cell, slot, cell_start, n, tmp);
+            const int gw = (int)std::min<int64_t>(((int64_t)ncells * 32 + 255) / 256, (int64_t)sms * 32);
+            k_cell_order<<<gw, 256, 0, st>>>(cell_start, ncells, tmp, perm);
+            k_gather_points<<<grid1, 256, 0, st>>>(coords_dev, perm, n, g->pts, g->inv);
+            k_neighbors<false><<<ncells, NB_THREADS, 0, st>>>(
+                g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
+                (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
+                deg, g->fwd, nullptr, nullptr, nullptr, maxd);
+            GS_BUILD_CUDA(cudaGetLastError());
+        }
+        s = gs_scan_i32_to_i64(deg, g->row_ptr, n, st);
+        if (s != GS_OK) goto fail;
+
+        int32_t herr = 0;
+        unsigned hmax = 0;
+        GS_BUILD_CUDA(cudaMemcpyAsync(&g->n_edges, g->row_ptr + n, sizeof(int64_t), cudaMemcpyDeviceToHost, st));
+        GS_BUILD_CUDA(cudaMemcpyAsync(&herr, g->err, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+        GS_BUILD_CUDA(cudaMemcpyAsync(&hmax, maxd, sizeof(unsigned), cudaMemcpyDeviceToHost, st));
+        GS_BUILD_CUDA(cudaStreamSynchronize(st));
+        if (herr) {
+            s = gs_set_error(GS_ERR_ARG, "a coordinate lies outside [0, box_lu)");
+            goto fail;
+        }
+        g->max_degree = (int32_t)hmax;
+
+        const size_t ne = (size_t)std::max<int64_t>(g->n_edges, 1);
+        GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));
+        GS_BUILD_CUDA(cudaMalloc(&g->bin, ne));
+        if (n > 0 && g->n_edges > 0) {
+            k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
+                g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
+                (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
+                nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr);
+            GS_BUILD_CUDA(cudaGetLastError());
+        }
+    }
+    cudaFreeAsync(cell, st);
+    cudaFreeAsync(slot, st);
+    cudaFreeAsync(tmp, st);
+    cudaFreeAsync(perm, st);
+    cudaFreeAsync(deg, st);
+    cudaFreeAsync(cell_count, st);
+    cudaFreeAsync(cell_start, st);
+    cudaFreeAsync(esq, st);
+    cudaFreeAsync(maxd, st);
+    *out = g;
+    return GS_OK;
+
+fail:
+    cudaStreamSynchronize(st);
+    cudaFree(cell);
+    cudaFree(slot);
+    cudaFree(tmp);
+    cudaFree(perm);
+    cudaFree(deg);
+    cudaFree(cell_count);
+    cudaFree(cell_start);
+    cudaFree(esq);
+    cudaFree(maxd);
+    free_graph_arrays(g);
+    delete g;
+    return s;
+#undef GS_BUILD_CUDA
+}
+
+// ---------------------------------------------------------------- export
+
+__global__ void k_input_degrees(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ inv,
+                                int64_t n, int32_t *__restrict__ deg_in)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int p = inv[i];
+        deg_in[i] = (int32_t)(row_ptr[p + 1] - row_ptr[p]);
+    }
+}
+
+constexpr int EX_THREADS = 256;
+constexpr int EX_SMEM = 4096;   // rows up to this length are sorted in shared memory
+
+// One block per input row: map neighbour ids to input numbering and sort the
+// row by them (bitonic in shared memory, rank sort for longer rows).
+__global__ void __launch_bounds__(EX_THREADS)
+k_export_rows(const int4 *__restrict__ pts, const int32_t *__restrict__ inv,
+              const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ nbr,
+              const uint8_t *__restrict__ bin, int64_t n, const int64_t *__restrict__ out_ptr,
+              int32_t *__restrict__ out_nbr, uint8_t *__restrict__ out_bin)
+{
+    __shared__ unsigned long long s_kv[EX_SMEM];
+    for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+        const int p = inv[i];
+        const int64_t r0 = row_ptr[p];
+        const int len = (int)(row_ptr[p + 1] - r0);
+        const int64_t o0 = out_ptr[i];
+        if (len <= EX_SMEM) {
+            int pw = 1;
+            while (pw < len) pw <<= 1;
+            for (int t = threadIdx.x; t < pw; t += EX_THREADS)
+                s_kv[t] = t < len ? (((unsigned long long)(unsigned)pts[nbr[r0 + t]].w << 8) | bin[r0 + t])
+                                  : ~0ull;
+            __syncthreads();
+            for (int k = 2; k <= pw; k <<= 1)
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    for (int t = threadIdx.x; t < pw; t += EX_THREADS) {
+                        const int u = t ^ j;
+                        if (u > t) {
+                            const bool up = (t & k) == 0;
+                            const unsigned long long a = s_kv[t], b = s_kv[u];
+                            if ((a > b) == up) {
+                                s_kv[t] = b;
+                                s_kv[u] = a;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            for (int t = threadIdx.x; t < len; t += EX_THREADS) {
+                out_nbr[o0 + t] = (int32_t)(s_kv[t] >> 8);
+                out_bin[o0 + t] = (uint8_t)(s_kv[t] & 0xff);
+            }
+            __syncthreads();
+        } else {
+            for (int t = threadIdx.x; t < len; t += EX_THREADS) {
+                const int e = pts[nbr[r0 + t]].w;
+                int r = 0;
+                for (int u = 0; u < len; ++u) r += pts[nbr[r0 + u]].w < e;
+                out_nbr[o0 + r] = e;
+                out_bin[o0 + r] = bin[r0 + t];
+            }
+        }
+    }
+}
+
+extern "C" gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int32_t *nbr_dev,
+                                         uint8_t *bin_dev, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !row_ptr_dev || (g->n_edges > 0 && (!nbr_dev || !bin_dev)))
+        return gs_set_error(GS_ERR_ARG, "NULL argument");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const int64_t n = g->n;
+    if (n == 0) {
+        GS_TRY_CUDA(cudaMemsetAsync(row_ptr_dev, 0, sizeof(int64_t), st));
+        return GS_OK;
+    }
+    int32_t *deg_in = nullptr;
+    GS_TRY_CUDA(cudaMallocAsync(&deg_in, sizeof(int32_t) * n, st));
+    const int sms = gs_sm_count();
+    const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sms * 16);
+    k_input_degrees<<<grid, 256, 0, st>>>(g->row_ptr, g->inv, n, deg_in);
+    gs_status s = gs_scan_i32_to_i64(deg_in, row_ptr_dev, n, st);
+    cudaFreeAsync(deg_in, st);
+    if (s != GS_OK) return s;
+    if (g->n_edges > 0) {
+        const int gridr = (int)std::min<int64_t>(n, (int64_t)sms * 8);
+        k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, g->row_ptr, g->nbr, g->bin, n,
+                                                    row_ptr_dev, nbr_dev, bin_dev);
+    }
+    GS_TRY_CUDA(cudaGetLastError());
+    return GS_OK;
+}
+
+__global__ void k_perm(const int4 *__restrict__ pts, int64_t n, int32_t *__restrict__ perm)
+{
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < n;
+         p += (int64_t)gridDim.x * blockDim.x)
+        perm[p] = pts[p].w;
+}
+
+extern "C" gs_status gs_graph_export_perm(gs_graph_t g, int32_t *perm_dev, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || (g->n > 0 && !perm_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (g->n == 0) return GS_OK;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const int grid = (int)std::min<int64_t>((g->n + 255) / 256, (int64_t)gs_sm_count() * 16);
+    k_perm<<<grid, 256, 0, st>>>(g->pts, g->n, perm_dev);
+    GS_TRY_CUDA(cudaGetLastError());
+    return GS_OK;
+}
+
+extern "C" gs_status gs_graph_info(gs_graph_t g, int64_t *n, int64_t *n_edges, int32_t *max_degree)
+{
+    gs_clear_error();
+    if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    if (n) *n = g->n;
+    if (n_edges) *n_edges = g->n_edges;
+    if (max_degree) *max_degree = g->max_degree;
+    return GS_OK;
+}

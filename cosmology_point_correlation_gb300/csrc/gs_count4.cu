@@ -1,0 +1,349 @@
+// gs_count4.cu -- parity-decomposed 4pCF (GRAMSCI v2, §III.1.1 and §III.2).
+//
+// For every hub i and every triple of spokes j1 < j2 < j3 in N(i) that are
+// pairwise adjacent, the paper's three-way merge (§III.1.1, Eq.(2)) finds j3
+// in hub tail ∩ N(j1) ∩ N(j2). Here the same triples come from one adjacency
+// bit-matrix per hub: row s of the matrix holds, as bits, the positions t > s
+// of the hub row whose node is also a neighbour of spoke s. The three-way
+// intersection for (s1, s2) is then the AND of rows s1 and s2 above s2 --
+// m/32 word operations instead of a pointer walk.
+//
+// Per hub, one thread block:
+//   1. stages the hub row (ids, hub bins, minimum-image spoke vectors x_s - x_i)
+//      and a hash table id -> row position in shared memory;
+//   2. builds the bit-matrix: each warp walks the forward part of N(j) for one
+//      spoke j (coalesced), probing the table;
+//   3. a warp per s1, its lanes over s2: for each pair with bit (s1, s2) set and
+//      distinct hub bins it ANDs the two rows, and for every s3 with a third distinct bin
+//      orders the spokes by hub bin, takes V = det[r_1; r_2; r_3] (Eq.(3)) in
+//      exact int64, and adds 1 to even and sign(V) to odd (V == 0 adds 0, the
+//      degenerate rule of §III.2).
+// Hubs of degree <= C4_M run entirely in shared memory with uint32 / int32
+// shared histograms; rarer hubs of higher degree run in a second kernel whose
+// per-block matrix lives in a global scratch slice and which adds straight
+// into the global histograms.
+
+#include <algorithm>
+
+#include "gs_internal.cuh"
+
+constexpr int C4_THREADS = 256;
+constexpr int C4_WARPS = C4_THREADS / 32;
+constexpr int C4_M = 512;                   // largest hub degree kept in shared memory
+constexpr int C4_WORDS = C4_M / 32;
+constexpr int C4_TABLE = 2 * C4_M;
+constexpr int C4_SMEM_HIST_MAX = 8192;
+constexpr int C4_EMPTY = -1;
+
+struct C4Args {
+    const int4 *pts;
+    const int64_t *row_ptr;
+    const int32_t *fwd;
+    const int32_t *nbr;
+    const uint8_t *bin;
+    int64_t hub_begin, hub_end;
+    int box, periodic;
+    int nb, ncfg;
+    unsigned long long *even;
+    long long *odd;
+    unsigned long long *cursor;
+    // large-hub path
+    int big_m;                    // largest degree the scratch slices hold
+    char *scratch;                // gridDim.x slices of scratch_stride bytes
+    size_t scratch_stride;
+};
+
+// Workspace of one hub: either shared memory or a global scratch slice.
+struct HubSpace {
+    int32_t *key;      // hash table (tsize slots)
+    int32_t *pos;      // row position of each table slot
+    int32_t *row;      // [m] neighbour ids
+    uint8_t *hb;       // [m] hub bins
+    int *vx, *vy, *vz; // [m] spoke vectors
+    unsigned *bits;    // [m][W] adjacency bits
+};
+
+template <bool SMEM_HIST>
+__device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long long i, int m,
+                                       int tlog, unsigned *s_even, int *s_odd,
+                                       const int *lex_a, const int *lex_b)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t r0 = a.row_ptr[i];
+    const int W = (m + 31) >> 5;
+    const int tsize = 1 << tlog, shift = 32 - tlog, mask = tsize - 1;
+    const int4 P = a.pts[i];
+
+    // 1. stage the row and the table
+    for (int t = threadIdx.x; t < m; t += C4_THREADS) {
+        const int32_t k = a.nbr[r0 + t];
+        w.row[t] = k;
+        w.hb[t] = a.bin[r0 + t];
+        const int4 Q = a.pts[k];
+        w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
+        w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
+        w.vz[t] = gs_delta(P.z, Q.z, a.box, a.periodic);
+        uint32_t h = gs_hash(k, shift);
+        while (atomicCAS(&w.key[h], C4_EMPTY, k) != C4_EMPTY) h = (h + 1) & mask;
+        w.pos[h] = t;
+    }
+    for (int t = threadIdx.x; t < m * W; t += C4_THREADS) w.bits[t] = 0u;
+    __syncthreads();
+
+    // 2. adjacency among the spokes: bit (s, t) for t > s
+    const int32_t kmax = w.row[m - 1];
+    for (int s = warp; s < m - 1; s += C4_WARPS) {
+        const int32_t j = w.row[s];
+        const int64_t pe = a.row_ptr[j + 1];
+        for (int64_t p = a.row_ptr[j] + a.fwd[j]; p < pe; p += 32) {
+            const int64_t q = p + lane;
+            const int32_t k = q < pe ? a.nbr[q] : 0x7fffffff;
+            if (k <= kmax) {
+                uint32_t h = gs_hash(k, shift);
+                int32_t key;
+                while ((key = w.key[h]) != k && key != C4_EMPTY) h = (h + 1) & mask;
+                if (key == k) {
+                    const int t = w.pos[h];
+                    atomicOr(&w.bits[(size_t)s * W + (t >> 5)], 1u << (t & 31));
+                }
+            }
+            if (__shfl_sync(0xffffffffu, k, 31) > kmax) break;
+        }
+    }
+    __syncthreads();
+
+    // 3. cliques (s1 < s2 < s3), distinct hub bins: a warp per s1, lanes over s2
+    for (int s1 = warp; s1 < m - 2; s1 += C4_WARPS) {
+        const int b1 = w.hb[s1];
+        const unsigned *row1 = w.bits + (size_t)s1 * W;
+        for (int s2 = s1 + 1 + lane; s2 < m - 1; s2 += 32) {
+            if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
+            const int b2 = w.hb[s2];
+            if (b1 == b2) continue;
+            const unsigned *row2 = w.bits + (size_t)s2 * W;
+            for (int wd = s2 >> 5; wd < W; ++wd) {
+                unsigned common = row1[wd] & row2[wd];
+                if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);     // keep s3 > s2
+                while (common) {
+                    const int s3 = (wd << 5) + __ffs(common) - 1;
+                    common &= common - 1;
+                    const int b3 = w.hb[s3];
+                    if (b3 == b1 || b3 == b2) continue;
+                    // order the three spokes by hub bin
+                    int sa = s1, sb = s2, sc = s3, ba = b1, bb = b2, bc = b3, tt;
+                    if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
+                    if (bb > bc) { tt = bb; bb = bc; bc = tt; tt = sb; sb = sc; sc = tt; }
+                    if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
+                    const long long ax = w.vx[sa], ay = w.vy[sa], az = w.vz[sa];
+                    const long long bx = w.vx[sb], by = w.vy[sb], bz = w.vz[sb];
+                    const long long cx = w.vx[sc], cy = w.vy[sc], cz = w.vz[sc];
+                    const long long v = (ay * bz - az * by) * cx + (az * bx - ax * bz) * cy +
+                                        (ax * by - ay * bx) * cz;
+                    const int sg = (v > 0) - (v < 0);
+                    const int idx = lex_a[ba] + lex_b[bb] + bc;
+                    if (SMEM_HIST) {
+                        atomicAdd(&s_even[idx], 1u);
+                        if (sg) atomicAdd(&s_odd[idx], sg);
+                    } else {
+                        atomicAdd(a.even + idx, 1ull);
+                        if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < tsize; t += C4_THREADS) w.key[t] = C4_EMPTY;
+}
+
+// gs_idx4(a, b, c) = F4(a) - H(a + 1) + H(b) + c - b - 1 with
+// H(t) = t (nb - 1) - t (t - 1) / 2 and F4(a) = gs_idx4(a, a + 1, a + 2),
+// split into two per-bin tables: idx4 = lex_a[a] + lex_b[b] + c.
+__device__ __forceinline__ void c4_lex_tables(int nb, int *lex_a, int *lex_b)
+{
+    for (int t = threadIdx.x; t < nb; t += C4_THREADS) {
+        const int64_t h1 = (int64_t)(t + 1) * (nb - 1) - (int64_t)(t + 1) * t / 2;
+        const int64_t h0 = (int64_t)t * (nb - 1) - (int64_t)t * (t - 1) / 2;
+        lex_a[t] = (int)(gs_idx4(nb, t, t + 1, t + 2) - h1);
+        lex_b[t] = (int)(h0 - t - 1);
+    }
+}
+
+__device__ __forceinline__ void c4_flush(unsigned *se, int *so, int ncfg, unsigned long long *ge, long long *go)
+{
+    for (int t = threadIdx.x; t < ncfg; t += C4_THREADS) {
+        const unsigned e = se[t];
+        const int o = so[t];
+        if (e) atomicAdd(ge + t, (unsigned long long)e);
+        if (o) atomicAdd((unsigned long long *)(go + t), (unsigned long long)(long long)o);
+        se[t] = 0;
+        so[t] = 0;
+    }
+}
+
+// Hubs of degree 3..C4_M, workspace in shared memory; histograms in shared
+// memory too unless there are too many configurations.
+template <bool SMEM_HIST>
+__global__ void __launch_bounds__(C4_THREADS)
+k_count4_small(C4Args a)
+{
+    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], even [ncfg], odd [ncfg]
+    __shared__ int32_t s_key[C4_TABLE];
+    __shared__ int32_t s_pos[C4_TABLE];
+    __shared__ int32_t s_row[C4_M];
+    __shared__ uint8_t s_hb[C4_M];
+    __shared__ int s_vx[C4_M], s_vy[C4_M], s_vz[C4_M];
+    __shared__ int s_lex_a[256], s_lex_b[256];
+    __shared__ long long s_hub;
+    __shared__ unsigned long long s_pending;
+
+    unsigned *s_bits = s_dyn;
+    unsigned *s_even = s_dyn + C4_M * C4_WORDS;
+    int *s_odd = (int *)(s_even + a.ncfg);
+    c4_lex_tables(a.nb, s_lex_a, s_lex_b);
+    if (SMEM_HIST)
+        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) {
+            s_even[t] = 0;
+            s_odd[t] = 0;
+        }
+    for (int t = threadIdx.x; t < C4_TABLE; t += C4_THREADS) s_key[t] = C4_EMPTY;
+    if (threadIdx.x == 0) s_pending = 0;
+    HubSpace w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits };
+
+    for (;;) {
+        __syncthreads();
+        if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
+        __syncthreads();
+        const long long i = s_hub;
+        if (i >= a.hub_end) break;
+        const int m = (int)(a.row_ptr[i + 1] - a.row_ptr[i]);
+        if (m < 3 || m > C4_M) continue;
+        if (SMEM_HIST) {
+            // C(m, 3) bounds the cliques of this hub
+            const unsigned long long bound = (unsigned long long)m * (m - 1) * (m - 2) / 6;
+            if (s_pending + bound > 0x7fffffffull) {
+                c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+                __syncthreads();
+                if (threadIdx.x == 0) s_pending = 0;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) s_pending += bound;
+        }
+        int tlog = 4;
+        while ((1 << tlog) < 2 * m) ++tlog;
+        c4_hub<SMEM_HIST>(a, w, i, m, tlog, s_even, s_odd, s_lex_a, s_lex_b);
+    }
+    if (SMEM_HIST) {
+        __syncthreads();
+        c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+    }
+}
+
+// Hubs of degree > C4_M: workspace in a global scratch slice per block,
+// histograms added straight to global memory.
+__global__ void __launch_bounds__(C4_THREADS)
+k_count4_large(C4Args a)
+{
+    __shared__ int s_lex_a[256], s_lex_b[256];
+    __shared__ long long s_hub;
+    c4_lex_tables(a.nb, s_lex_a, s_lex_b);
+
+    const int M = a.big_m;
+    int tlog = 4;
+    while ((1 << tlog) < 2 * M) ++tlog;
+    const int WM = (M + 31) >> 5;
+    char *base = a.scratch + (size_t)blockIdx.x * a.scratch_stride;
+    HubSpace w;
+    w.key = (int32_t *)base;
+    w.pos = w.key + (1 << tlog);
+    w.row = w.pos + (1 << tlog);
+    w.vx = w.row + M;
+    w.vy = w.vx + M;
+    w.vz = w.vy + M;
+    w.bits = (unsigned *)(w.vz + M);
+    w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
+    for (int t = threadIdx.x; t < (1 << tlog); t += C4_THREADS) w.key[t] = C4_EMPTY;
+
+    for (;;) {
+        __syncthreads();
+        if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
+        __syncthreads();
+        const long long i = s_hub;
+        if (i >= a.hub_end) break;
+        const int m = (int)(a.row_ptr[i + 1] - a.row_ptr[i]);
+        if (m <= C4_M) continue;
+        int tl = 4;
+        while ((1 << tl) < 2 * m) ++tl;
+        c4_hub<false>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
+    }
+}
+
+extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
+                                          int64_t hub_begin, int64_t hub_end, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
+        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
+                            (long long)hub_end, (long long)g->n);
+    if (g->edges[g->nb] >= (1ll << 20))
+        return gs_set_error(GS_ERR_ARG, "parity 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
+    const int64_t ncfg = gs_ncfg4(g->nb);
+    if (ncfg <= 0) return GS_OK;
+    if (!even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL histogram");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
+    GS_TRY_CUDA(cudaMemsetAsync(g->work + 1, 0, 2 * sizeof(unsigned long long), st));
+
+    C4Args a{};
+    a.pts = g->pts;
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.hub_begin = hub_begin;
+    a.hub_end = hub_end;
+    a.box = (int)g->box_lu;
+    a.periodic = g->periodic;
+    a.nb = g->nb;
+    a.ncfg = (int)ncfg;
+    a.even = (unsigned long long *)even_dev;
+    a.odd = (long long *)odd_dev;
+
+    const int64_t hubs = hub_end - hub_begin;
+    const int sms = gs_sm_count();
+    const bool smem = ncfg <= C4_SMEM_HIST_MAX;
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
+    auto kern = smem ? k_count4_small<true> : k_count4_small<false>;
+    int per_sm = 0;
+    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
+    per_sm = std::max(per_sm, 1);
+    a.cursor = g->work + 1;
+    const int grid = (int)std::min<int64_t>((int64_t)sms * per_sm, hubs);
+    kern<<<grid, C4_THREADS, dyn, st>>>(a);
+    GS_TRY_CUDA(cudaGetLastError());
+
+    if (g->max_degree > C4_M) {
+        const int M = g->max_degree;
+        int tlog = 4;
+        while ((1 << tlog) < 2 * M) ++tlog;
+        const size_t WM = (size_t)(M + 31) / 32;
+        size_t stride = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM + M;
+        stride = (stride + 255) & ~(size_t)255;
+        const int gl = (int)std::min<int64_t>((int64_t)sms * 2, hubs);
+        char *scratch = nullptr;
+        GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
+        a.cursor = g->work + 2;
+        a.big_m = M;
+        a.scratch = scratch;
+        a.scratch_stride = stride;
+        k_count4_large<<<gl, C4_THREADS, 0, st>>>(a);
+        cudaError_t e = cudaGetLastError();
+        cudaFreeAsync(scratch, st);
+        if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    return GS_OK;
+}

@@ -1,0 +1,113 @@
+// gs_internal.cuh -- shared definitions of the sm_103a library (not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gramsci_gb.h"
+
+// ---------------------------------------------------------------- the graph
+//
+// HBM layout of one graph (N points, E directed edges):
+//   pts      int4   [N]    x, y, z and the input index, points sorted by cell
+//                          (16-byte rows: one aligned vector load per point)
+//   inv      int32  [N]    input index -> internal index
+//   row_ptr  int64  [N+1]  CSR offsets (E may exceed 2^31, GRAMSCI §III.5.1)
+//   fwd      int32  [N]    offset in row i of the first neighbour > i
+//   nbr      int32  [E]    neighbour ids (internal), strictly increasing per row
+//   bin      uint8  [E]    radial bin of each edge
+// Internal index = position in cell order, so a hub's neighbours are a few
+// contiguous index ranges and consecutive hubs share most of their spokes
+// (L2 reuse in the counting kernels).
+struct gs_graph {
+    int device;
+    int64_t n;
+    int64_t box_lu;
+    int periodic;
+    int nb;
+    int64_t edges[256];
+    int64_t n_edges;
+    int32_t max_degree;
+    int ncell;                 // cells per axis
+    int4 *pts;
+    int32_t *inv;
+    int64_t *row_ptr;
+    int32_t *fwd;
+    int32_t *nbr;
+    uint8_t *bin;
+    unsigned long long *work;  // 4 device counters used by the count kernels
+    int32_t *err;              // device error word of the build kernels
+};
+
+// ---------------------------------------------------------------- errors
+
+gs_status gs_set_error(gs_status s, const char *fmt, ...);
+void gs_clear_error();
+
+#define GS_TRY_CUDA(call)                                                              \
+    do {                                                                               \
+        cudaError_t e_ = (call);                                                       \
+        if (e_ != cudaSuccess) {                                                       \
+            return gs_set_error(e_ == cudaErrorMemoryAllocation ? GS_ERR_NOMEM : GS_ERR_CUDA, \
+                                "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                                __FILE__, __LINE__);                                   \
+        }                                                                              \
+    } while (0)
+
+// Number of SMs of the current device (cached per device).
+int gs_sm_count();
+
+// Exclusive scan of n int32 values; out has n+1 entries (out[n] = total).
+gs_status gs_scan_i32_to_i64(const int32_t *in, int64_t *out, int64_t n, cudaStream_t st);
+gs_status gs_scan_i32_to_i32(const int32_t *in, int32_t *out, int64_t n, cudaStream_t st);
+
+// ---------------------------------------------------------------- device helpers
+
+// Minimum-image (periodic) or raw displacement component b - a; |b - a| < 2^30.
+__device__ __forceinline__ int gs_delta(int a, int b, int box, int periodic)
+{
+    int d = b - a;
+    if (periodic) {
+        d -= (2 * d >= box) ? box : 0;
+        d += (2 * d < -box) ? box : 0;
+    }
+    return d;
+}
+
+__device__ __forceinline__ long long gs_norm2(int dx, int dy, int dz)
+{
+    return (long long)dx * dx + (long long)dy * dy + (long long)dz * dz;
+}
+
+// Packed lexicographic index of a sorted bin triple a <= b <= c over nb bins:
+// (#triples with first bin < a) + (#with first bin a and second bin < b) + (c - b).
+__host__ __device__ __forceinline__ int64_t gs_idx3(int nb, int a, int b, int c)
+{
+    auto tet = [](int64_t m) { return m * (m + 1) * (m + 2) / 6; };
+    auto g = [nb](int64_t t) { return t * nb - t * (t - 1) / 2; };
+    return tet(nb) - tet(nb - a) + g(b) - g(a) + (c - b);
+}
+
+// Packed lexicographic index of a strictly increasing triple a < b < c.
+__host__ __device__ __forceinline__ int64_t gs_idx4(int nb, int a, int b, int c)
+{
+    auto c3 = [](int64_t m) { return m * (m - 1) * (m - 2) / 6; };
+    auto h = [nb](int64_t t) { return t * (nb - 1) - t * (t - 1) / 2; };
+    return c3(nb) - c3(nb - a) + h(b) - h(a + 1) + (c - b - 1);
+}
+
+__host__ __device__ __forceinline__ int64_t gs_ncfg3(int nb) { return (int64_t)nb * (nb + 1) * (nb + 2) / 6; }
+__host__ __device__ __forceinline__ int64_t gs_ncfg4(int nb) { return (int64_t)nb * (nb - 1) * (nb - 2) / 6; }
+
+// Multiplicative hash of a node id into a table of 2^(32 - shift) slots.
+__device__ __forceinline__ uint32_t gs_hash(int32_t key, int shift)
+{
+    return ((uint32_t)key * 0x9E3779B1u) >> shift;
+}
+
+__device__ __forceinline__ unsigned gs_lanemask_lt()
+{
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}

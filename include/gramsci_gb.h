@@ -1,0 +1,169 @@
+/*
+ * gramsci_gb.h -- C ABI of libgramsci_gb.so: graph-based 3pCF and
+ * parity-decomposed 4pCF counting on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the GRAMSCI v2 paper, "Fast Graph-based Higher-Order
+ * Clustering Statistics on the GPU":
+ *   - gs_build_graph: the fixed-radius neighbour graph of §II.1 (all j with
+ *     |x_i - x_j| < r_max), stored as sorted adjacency lists (Eq.(1)) with a
+ *     radial-bin byte per neighbour, flattened to CSR (§III.5.1: 64-bit row
+ *     offsets, 32-bit neighbour ids, 8-bit bins).
+ *   - gs_count_3pcf: the triangle count of §II.2 / §III.1 (hub, spoke and a
+ *     third point adjacent to both), binned by the sorted side bins
+ *     b1 <= b2 <= b3 and packed lexicographically (§V.1, Fig.8 key).
+ *   - gs_count_4pcf_parity: the parity-decomposed 4pCF of §III.2: per hub and
+ *     triple of mutually adjacent spokes, an even count and an odd sum of the
+ *     sign of V = (r_ij1 x r_ij2) . r_ij3 (Eq.(3)), V == 0 adding 0 to odd.
+ *
+ * Data model (all integer, all exact):
+ *   - Coordinates are int32 lattice positions (1 lattice unit = 1/1024
+ *     h^-1 Mpc in the intended use) in [0, box_lu) on each axis, row-major
+ *     [n][3] (x, y, z).
+ *   - periodic != 0: separations use the minimum image in a cube of side
+ *     box_lu (delta -= box if 2*delta >= box, delta += box if 2*delta < -box).
+ *   - Bin edges e_0 < e_1 < ... < e_nb in lattice units; a pair i != j is an
+ *     edge iff e_0^2 <= d^2 < e_nb^2, its bin the b with e_b^2 <= d^2 <
+ *     e_{b+1}^2. d^2 is computed in int64.
+ *   - 3pCF: every unordered triangle {i, j, k} whose three sides are edges
+ *     adds 1 at index idx3(sort(b_ij, b_ik, b_jk)), the rank of the sorted
+ *     triple among all b1 <= b2 <= b3 in lexicographic order
+ *     (gs_config_count_3pcf(nb) = C(nb+2, 3) entries).
+ *   - parity 4pCF: for each hub i and each set of three spokes {j, k, l} in
+ *     N(i) that are pairwise adjacent and whose hub bins are pairwise
+ *     distinct, the spokes are ordered by hub bin (b1 < b2 < b3),
+ *     V = det[r_is1; r_is2; r_is3] with r_is = x_s - x_i (minimum image), and
+ *     even[idx4] += 1, odd[idx4] += sign(V) where idx4 ranks b1 < b2 < b3 in
+ *     lexicographic order (gs_config_count_4pcf(nb) = C(nb, 3) entries).
+ *
+ * Conventions:
+ *   - "_dev" pointers are CUDA device pointers on the current device; the
+ *     caller owns and allocates them. Host pointers are marked "_host".
+ *   - Every call runs on `cuda_stream` (a cudaStream_t; NULL = the legacy
+ *     default stream). gs_build_graph synchronises that stream once (to read
+ *     the edge total); the count and export calls are asynchronous.
+ *   - Outputs are overwritten, never accumulated.
+ *   - On any non-OK status no output has been written by this call (except
+ *     where noted), everything the call allocated is freed, and
+ *     gs_last_error() returns a message for the calling thread.
+ *   - Limits: 0 <= n < 2^31 - 1; 1 <= box_lu <= 2^30; 1 <= nbins <= 255;
+ *     periodic boxes need 2 * r_max_lu <= box_lu; the parity 4pCF needs
+ *     r_max_lu < 2^20 (so that the int64 volume is exact).
+ */
+#ifndef GRAMSCI_GB_H
+#define GRAMSCI_GB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gs_graph *gs_graph_t;   /* opaque; owns all device memory of one graph */
+
+typedef enum {
+    GS_OK = 0,
+    GS_ERR_ARG = 1,        /* invalid argument (sizes, edges, coordinates out of range, ...) */
+    GS_ERR_NOMEM = 2,      /* a device allocation failed */
+    GS_ERR_CUDA = 3,       /* a CUDA runtime call or kernel launch failed */
+    GS_ERR_CAPACITY = 4,   /* the graph exceeds a documented size limit */
+    GS_ERR_INTERNAL = 5    /* a device-side consistency check failed */
+} gs_status;
+
+/* Build the neighbour graph of n points (§II.1, Eq.(1); CSR layout §III.5.1).
+ *   coords_dev  int32 [n][3], device, caller-owned; values in [0, box_lu)
+ *   n           number of points (0 allowed: empty graph)
+ *   box_lu      cube side in lattice units
+ *   periodic    1 = minimum-image separations, 0 = open box
+ *   r_max_lu    must equal edges_lu[nbins]
+ *   edges_lu    int64 [nbins+1], HOST, strictly increasing, edges_lu[0] >= 0
+ *   nbins       1..255
+ *   out         receives the new graph handle (free with gs_graph_free)
+ * The coordinates are copied; coords_dev may be freed after the call returns.
+ * Errors: GS_ERR_ARG for bad arguments or a coordinate outside [0, box_lu)
+ * (checked on the device, reported at the call's one synchronisation),
+ * GS_ERR_NOMEM, GS_ERR_CUDA. On error *out is set to NULL. */
+gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
+                         int64_t r_max_lu, const int64_t *edges_lu, int nbins,
+                         void *cuda_stream, gs_graph_t *out);
+
+/* Triangle histogram of the 3pCF (§II.2 hub-and-spoke enumeration, §III.1
+ * set intersection of the hub's and the spoke's sorted lists).
+ *   hist_dev    uint64 [gs_config_count_3pcf(nbins)], device, overwritten
+ *   hub_begin, hub_end  half-open range of hubs in the graph's internal order
+ *               (points sorted by cell); [0, n) gives the full histogram.
+ *               Each triangle is counted at its lowest internal index, so the
+ *               histograms of disjoint ranges that cover [0, n) sum exactly
+ *               to the full one.
+ * Errors: GS_ERR_ARG (NULL pointers, range outside [0, n]), GS_ERR_CUDA. */
+gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int64_t hub_end,
+                        void *cuda_stream);
+
+/* Parity-decomposed 4pCF histograms (§III.1.1 three-way intersection,
+ * §III.2 Eq.(3), degenerate volumes add 0 to odd).
+ *   even_dev    uint64 [gs_config_count_4pcf(nbins)], device, overwritten
+ *   odd_dev     int64  [gs_config_count_4pcf(nbins)], device, overwritten
+ *   hub_begin, hub_end  half-open hub range in internal order, as above;
+ *               every hub's contribution is independent of the others.
+ * For nbins < 3 there are no configurations and nothing is written.
+ * Errors: GS_ERR_ARG (NULL pointers, bad range, r_max_lu >= 2^20),
+ * GS_ERR_NOMEM (scratch for hubs of very high degree), GS_ERR_CUDA. */
+gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
+                               int64_t hub_begin, int64_t hub_end, void *cuda_stream);
+
+/* Sizes of a built graph (host outputs; any pointer may be NULL).
+ *   n           number of points
+ *   n_edges     directed edges, sum of degrees (= 2 x pairs)
+ *   max_degree  largest |N(i)| */
+gs_status gs_graph_info(gs_graph_t g, int64_t *n, int64_t *n_edges, int32_t *max_degree);
+
+/* The graph as CSR in INPUT numbering, rows sorted by neighbour id (Eq.(1)).
+ *   row_ptr_dev int64 [n+1], device
+ *   nbr_dev     int32 [n_edges], device
+ *   bin_dev     uint8 [n_edges], device
+ * Asynchronous on cuda_stream. Errors: GS_ERR_ARG, GS_ERR_NOMEM, GS_ERR_CUDA. */
+gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int32_t *nbr_dev,
+                              uint8_t *bin_dev, void *cuda_stream);
+
+/* Internal order: perm_dev int32 [n], device; perm_dev[p] = input index of
+ * the point the graph numbers p (the hub order of the count calls). */
+gs_status gs_graph_export_perm(gs_graph_t g, int32_t *perm_dev, void *cuda_stream);
+
+/* Number of histogram entries: C(nbins+2, 3) and C(nbins, 3); -1 if nbins is
+ * outside 1..255. */
+int64_t gs_config_count_3pcf(int nbins);
+int64_t gs_config_count_4pcf(int nbins);
+
+/* Packed index of a configuration (host-side, same formula as the device):
+ * idx3 of b1 <= b2 <= b3, idx4 of b1 < b2 < b3; -1 if the triple is not in
+ * that form or out of range. */
+int64_t gs_config_index_3pcf(int nbins, int b1, int b2, int b3);
+int64_t gs_config_index_4pcf(int nbins, int b1, int b2, int b3);
+
+/* One call from host arrays to a host histogram: copies coords_host to the
+ * device, builds the graph, counts, copies the result back and frees
+ * everything, all on cuda_stream; returns once the result is in host memory.
+ * Arguments as for gs_build_graph; hist_host / even_host / odd_host are host
+ * arrays of the sizes above (pinned memory makes the copies faster). */
+gs_status gs_3pcf_from_host(const int32_t *coords_host, int64_t n, int64_t box_lu, int periodic,
+                            int64_t r_max_lu, const int64_t *edges_lu, int nbins,
+                            uint64_t *hist_host, void *cuda_stream);
+gs_status gs_4pcf_parity_from_host(const int32_t *coords_host, int64_t n, int64_t box_lu,
+                                   int periodic, int64_t r_max_lu, const int64_t *edges_lu,
+                                   int nbins, uint64_t *even_host, int64_t *odd_host,
+                                   void *cuda_stream);
+
+/* Release a graph and its device memory (NULL is a no-op). Synchronises the
+ * device before freeing. */
+void gs_graph_free(gs_graph_t g);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char *gs_last_error(void);
+
+/* Library version string. */
+const char *gs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRAMSCI_GB_H */

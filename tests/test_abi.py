@@ -1,0 +1,65 @@
+"""The C ABI loads and exports every function include/*.h declares; the
+host-only entry points work without a GPU. CPU only: no compute call here
+touches a device."""
+import glob
+import os
+import re
+
+import pytest
+
+from cosmology_point_correlation_gb300 import _lib, build
+from tests import fixtures as fx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(gs_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"gs_build_graph", "gs_count_3pcf", "gs_count_4pcf_parity"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_config_counts(lib):
+    assert lib.gs_config_count_3pcf(10) == 220      # GRAMSCI v2 §V.1: 220 configurations, 10 bins
+    for nb in range(1, 40):
+        assert lib.gs_config_count_3pcf(nb) == len(fx.configs3(nb))
+        assert lib.gs_config_count_4pcf(nb) == len(fx.configs4(nb))
+    assert lib.gs_config_count_3pcf(0) == -1 and lib.gs_config_count_3pcf(256) == -1
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 5, 8, 15, 30, 41])
+def test_config_index_matches_enumeration(lib, nb):
+    for k, c in enumerate(fx.configs3(nb)):
+        assert lib.gs_config_index_3pcf(nb, *c) == k
+    for k, c in enumerate(fx.configs4(nb)):
+        assert lib.gs_config_index_4pcf(nb, *c) == k
+    assert lib.gs_config_index_3pcf(nb, 1, 0, 0) == -1
+    assert lib.gs_config_index_4pcf(nb, 0, 0, 1) == -1
+
+
+def test_version_and_error_string(lib):
+    assert b"sm_103a" in lib.gs_version()
+    assert isinstance(lib.gs_last_error(), bytes)
+
+
+def test_null_graph_is_rejected_without_device_work(lib):
+    assert lib.gs_graph_info(None, None, None, None) == _lib.GS_ERR_ARG
+    assert b"NULL" in lib.gs_last_error()
+    lib.gs_graph_free(None)

@@ -1,0 +1,115 @@
+"""3pCF triangle histograms on the GPU equal the oracle bit for bit
+(GRAMSCI v2 §II.2, §III.1; configurations as in §V.1 Fig.8)."""
+import numpy as np
+import pytest
+
+import oracle
+from cosmology_point_correlation_gb300 import as_uint64, catalogues, configs, count_3pcf_from_host
+from tests import fixtures as fx
+from tests.gpu_util import gpu_3pcf, gpu_graph, mirror
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_config():
+    w = configs.TINY_3PCF
+    xyz = w.points()
+    ref = oracle.count_3pcf(xyz, w.box_lu, 1, w.edges_lu)
+    assert ref.sum() > 600_000
+    assert np.array_equal(gpu_3pcf(xyz, w.box_lu, 1, w.edges_lu), ref)
+
+
+@pytest.mark.parametrize("fixture", list(fx.triangle_fixtures()), ids=lambda f: f["name"])
+def test_fixtures(fixture):
+    f = fixture
+    nb = len(f["edges"]) - 1
+    hist = gpu_3pcf(f["points"], f["box"], f["periodic"], f["edges"])
+    cfg = fx.configs3(nb)
+    assert {cfg[k]: int(v) for k, v in enumerate(hist) if v} == f["expect"]
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+@pytest.mark.parametrize("n", [5_000, 20_011])
+def test_clustered(periodic, n):
+    box = catalogues.box_lattice(120.0)
+    xyz = catalogues.neyman_scott(n, 120.0, n // 50, 50.0, 3.0, n + periodic)
+    edges = catalogues.linear_edges_lu(10.0, 15)
+    ref = oracle.count_3pcf(xyz, box, periodic, edges)
+    assert np.array_equal(gpu_3pcf(xyz, box, periodic, edges), ref)
+
+
+def test_clustered_config_scaled_down():
+    # the clustered workload's process and binning at 1/10 of its points in 1/10 of its volume
+    w = configs.CLUSTERED_3PCF_D
+    L = 500.0 / 10 ** (1 / 3)
+    box = catalogues.box_lattice(L)
+    xyz = catalogues.neyman_scott(20_000, L, 400, 50.0, 3.0, w.seed)
+    ref = oracle.count_3pcf(xyz, box, 1, w.edges_lu)
+    assert np.array_equal(gpu_3pcf(xyz, box, 1, w.edges_lu), ref)
+
+
+def test_hub_rows_longer_than_the_table():
+    # 2300 points within 0.45 r_max of each other: every pair is an edge, the
+    # first hubs have > 2048 forward neighbours, so their rows run in chunks
+    rng = np.random.default_rng(3)
+    R = 40000
+    v = rng.normal(size=(2300, 3))
+    v *= (0.45 * R * rng.uniform(0, 1, size=(2300, 1)) ** (1 / 3)) / np.linalg.norm(v, axis=1, keepdims=True)
+    xyz = (v + 100000).astype(np.int32)
+    edges = [0, 9000, 21000, 33000, R]
+    ref = oracle.count_3pcf(xyz, 300000, 0, edges)
+    assert ref.sum() == 2300 * 2299 * 2298 // 6
+    with gpu_graph(xyz, 300000, 0, edges) as g:
+        assert g.max_degree == 2299
+        assert np.array_equal(as_uint64(g.count_3pcf()), ref)
+
+
+def test_many_bins_global_histogram():
+    # C(62,3) = 37820 configurations: histogram too large for shared memory
+    box = catalogues.box_lattice(60.0)
+    xyz = catalogues.uniform(2500, 60.0, 8)
+    edges = catalogues.linear_edges_lu(12.0, 60)
+    ref = oracle.count_3pcf(xyz, box, 1, edges)
+    assert np.array_equal(gpu_3pcf(xyz, box, 1, edges), ref)
+
+
+def test_hub_ranges_sum_to_full():
+    w = configs.TINY_3PCF
+    xyz = w.points()
+    full = oracle.count_3pcf(xyz, w.box_lu, 1, w.edges_lu)
+    cuts = [0, 1, 2, 777, 1500, 1999, 2000]
+    parts = gpu_3pcf(xyz, w.box_lu, 1, w.edges_lu, ranges=list(zip(cuts, cuts[1:])))
+    assert np.array_equal(np.sum(parts, axis=0, dtype=np.uint64), full)
+    assert gpu_3pcf(xyz, w.box_lu, 1, w.edges_lu, ranges=[(5, 5)])[0].sum() == 0
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+def test_invariances_on_the_gpu(periodic):
+    box = catalogues.box_lattice(100.0)
+    xyz = catalogues.neyman_scott(30_000, 100.0, 600, 50.0, 3.0, 123)
+    edges = catalogues.linear_edges_lu(8.0, 10)
+    base = gpu_3pcf(xyz, box, periodic, edges)
+    assert base.sum() > 1e6
+    perm = np.random.default_rng(2).permutation(len(xyz))
+    assert np.array_equal(gpu_3pcf(xyz[perm], box, periodic, edges), base)
+    assert np.array_equal(gpu_3pcf(mirror(xyz, box, periodic), box, periodic, edges), base)
+    assert np.array_equal(gpu_3pcf(np.ascontiguousarray(xyz[:, [2, 0, 1]]), box, periodic, edges), base)
+    if periodic:
+        moved = ((xyz.astype(np.int64) + [51234, 7, 99999]) % box).astype(np.int32)
+        assert np.array_equal(gpu_3pcf(moved, box, periodic, edges), base)
+
+
+def test_host_buffer_entry_point():
+    w = configs.TINY_3PCF
+    xyz = w.points()
+    ref = oracle.count_3pcf(xyz, w.box_lu, 1, w.edges_lu)
+    assert np.array_equal(count_3pcf_from_host(xyz, w.box_lu, True, w.edges_lu), ref)
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3])
+def test_tiny_inputs(n):
+    xyz = np.full((n, 3), 500, dtype=np.int32)
+    h = gpu_3pcf(xyz, 10000, 1, [0, 100, 200])
+    assert int(h.sum()) == (1 if n == 3 else 0)
+    if n == 3:
+        assert h[0] == 1
