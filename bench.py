@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Throughput of the graph-based 3pCF path on GB300, printed as one JSON line.
+
+One step = the whole hot path on one synthetic catalogue already resident in
+device memory: cell sort, neighbour graph (count + fill), 3pCF merge-walk
+count with its histogram. The default workload is the BAO-scale 3pCF
+(2,000,000 Neyman-Scott points in an open 2000 h^-1 Mpc box, r_max 150,
+30 bins, ~6.7e9 directed edges). The parity-4pCF path is timed the same way
+on its own workload and reported in the "parity_4pcf" object.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (oracle/, plain C) on a bounded
+sub-cube sample of the same workload. Under torchrun every rank counts its
+own realisation of the workload (weak scaling, no collective on the data
+path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from cosmology_point_correlation_gb300 import catalogues, configs  # noqa: E402
+
+METRIC = "3pCF triangles/s and edges/s on 1 GB300; achieved HBM GB/s vs peak"
+FALLBACK_HBM_GBS = 6800.0
+BYTES_PER_EDGE = 5                      # int32 neighbour id + uint8 bin
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "k_count3_bao_3pcf.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "cosmology_point_correlation_gb300", "csrc", f)
+                  for f in ("gs_count3.cu", "gs_internal.cuh")]
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="bao_3pcf", choices=sorted(configs.ALL))
+    p.add_argument("--parity-workload", default="parity_4pcf")
+    p.add_argument("--scale", type=float, default=1.0,
+                   help="fraction of the workload's points, box shrunk to keep the density")
+    p.add_argument("--no-parity", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sample-points", type=int, default=10_000,
+                   help="points in the sub-cube the CPU oracle counts")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ workloads
+
+def catalogue(w: configs.Workload, scale: float, rank: int):
+    """(xyz, box_lu, description) of one realisation; rank r uses seed + 1000 r."""
+    n = max(1, int(round(w.n * scale)))
+    box_mpc = w.box_mpc * (n / w.n) ** (1.0 / 3.0)
+    seed = w.seed + 1000 * rank
+    if w.process == "uniform":
+        xyz = catalogues.uniform(n, box_mpc, seed)
+    else:
+        xyz = catalogues.neyman_scott(n, box_mpc, max(1, int(round(w.ns["n_parents"] * n / w.n))),
+                                      w.ns["mu"], w.ns["sigma"], seed)
+    desc = {"workload": w.name, "n": n, "box_mpc": round(box_mpc, 3), "periodic": w.periodic,
+            "r_max_mpc": w.r_max_mpc, "nbins": w.nbins, "process": w.process, "seed": seed}
+    if w.ns:
+        desc["neyman_scott"] = w.ns
+    return xyz, catalogues.box_lattice(box_mpc), desc
+
+
+def sub_cube(xyz: np.ndarray, box_lu: int, n_target: int):
+    """Points of the corner sub-cube holding about n_target points, as an open box."""
+    n = len(xyz)
+    side = int(box_lu * min(1.0, (n_target / n) ** (1.0 / 3.0)))
+    keep = np.all(xyz < side, axis=1)
+    return np.ascontiguousarray(xyz[keep]), side
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu_index)],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for r in csv.reader(io.StringIO(f.read())):
+                    if len(r) >= 9:
+                        rows.append([c.strip() for c in r])
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_index_of(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(parts) and parts[local_rank].isdigit():
+            return int(parts[local_rank])
+    return local_rank
+
+
+# ------------------------------------------------------------------ peaks / profiles
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per full launch of the 3pCF kernel from the committed ncu
+    summary, or None when it was taken on other kernel source or workload."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    kv = {}
+    for line in text.splitlines():
+        if ":" in line and line.lstrip().startswith("- "):
+            k, v = line.lstrip()[2:].split(":", 1)
+            kv[k.strip()] = v.strip().strip("`")
+    if kv.get("kernel_source_sha256") != kernel_source_hash() or kv.get("workload") != workload:
+        return None
+    try:
+        return float(kv["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and not (world == 1 and n_gpus == 1):
+        if world == 1:
+            raise SystemExit(f"--gpus {n_gpus} needs torchrun with {n_gpus} processes")
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max_sum(world, values_max, values_sum):
+    if world == 1:
+        return values_max, values_sum
+    import torch
+    import torch.distributed as dist
+    a = torch.tensor(values_max, dtype=torch.float64, device="cuda")
+    b = torch.tensor(values_sum, dtype=torch.float64, device="cuda")
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return a.tolist(), b.tolist()
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline only)
+
+def oracle_rate(xyz, box_lu, w):
+    """Oracle triangles/s on a sub-cube sample: graph by brute force + hub loop."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    g = oracle.graph(xyz, box_lu, 0, w.edges_lu)
+    hist = oracle.count_3pcf(xyz, box_lu, 0, w.edges_lu, g)
+    dt = time.perf_counter() - t0
+    return int(hist.sum()), g.n_edges, dt, oracle.threads()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    xyz, box_lu, desc = catalogue(w, args.scale, 0)
+    sample, side = sub_cube(xyz, box_lu, min(args.sample_points, 6_000))
+    for _ in range(args.warmup):
+        oracle_rate(sample, side, w)
+    tris, edges, times, cores = 0, 0, [], 1
+    for _ in range(args.steps):
+        t, e, dt, cores = oracle_rate(sample, side, w)
+        tris, edges = t, e
+        times.append(dt)
+    sec = statistics.mean(times)
+    value = tris / sec
+    sample_desc = (f"open corner sub-cube of side {side / 1024:.1f} h^-1 Mpc of the {w.name} catalogue: "
+                   f"{len(sample)} points, {edges} directed edges, {tris} triangles per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "triangles/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+            "config": desc, "edges_per_s": edges / sec,
+            "cpu_baseline": {"value": value, "unit": "triangles/s", "cores": cores, "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": value, "unit": "triangles/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def time_path(coords, box_lu, w, steps, kind, hist_out=None):
+    """Run `steps` passes; returns per-step (step_ms, count_ms, result) lists."""
+    import torch
+    from cosmology_point_correlation_gb300 import build_graph
+    stream = torch.cuda.current_stream()
+    res = []
+    for _ in range(steps):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        g = build_graph(coords, box_lu, w.periodic, w.edges_lu, stream=stream)
+        e1.record(stream)
+        if kind == "3pcf":
+            out = g.count_3pcf(out=hist_out, stream=stream)
+        else:
+            out = g.count_4pcf_parity(out=hist_out, stream=stream)
+        e2.record(stream)
+        stream.synchronize()
+        n_edges = g.n_edges
+        g.free()
+        res.append((e0.elapsed_time(e2), e1.elapsed_time(e2), e0.elapsed_time(e1), n_edges, out))
+    return res
+
+
+def run_ours(args, w):
+    import torch
+    from cosmology_point_correlation_gb300 import (as_uint64, build_graph, count_3pcf_from_host,
+                                                    kernel_launches)
+    rank, world, local = dist_init(args.gpus)
+    dev = torch.device("cuda", local)
+    xyz, box_lu, desc = catalogue(w, args.scale, rank)
+    coords = torch.from_numpy(xyz).to(dev)
+    ncfg = w.nbins * (w.nbins + 1) * (w.nbins + 2) // 6
+    hist = torch.empty(ncfg, dtype=torch.int64, device=dev)
+
+    # work statistics of this catalogue's graph (untimed)
+    with build_graph(coords, box_lu, w.periodic, w.edges_lu) as g:
+        st = g.stats()
+    alg_bytes = BYTES_PER_EDGE * (st["n_edges"] // 2 + st["spoke_walk"])
+
+    time_path(coords, box_lu, w, args.warmup, "3pcf", hist)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = kernel_launches()
+    with ClockSampler(gpu_index_of(local)) as clk:
+        t_wall0 = time.perf_counter()
+        res = time_path(coords, box_lu, w, args.steps, "3pcf", hist)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    launches = kernel_launches() - launches0
+    clocks = clk.summary()
+    if any(r in BAD_REASONS for r in clocks["reasons"]):
+        # throttled: measure once more
+        launches0 = kernel_launches()
+        with ClockSampler(gpu_index_of(local)) as clk:
+            res = time_path(coords, box_lu, w, args.steps, "3pcf", hist)
+            torch.cuda.synchronize()
+        launches = kernel_launches() - launches0
+        clocks = clk.summary()
+        clocks["remeasured"] = True
+
+    step_ms = statistics.mean(r[0] for r in res)
+    count_ms = statistics.mean(r[1] for r in res)
+    build_ms = statistics.mean(r[2] for r in res)
+    n_edges = res[-1][3]
+    tris = int(as_uint64(res[-1][4]).sum())
+    (step_ms_max, count_ms_max), (tris_all, edges_all) = reduce_max_sum(world, [step_ms, count_ms],
+                                                                        [float(tris), float(n_edges)])
+
+    # end to end: host coordinates in, host histogram out, through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        pinned = torch.from_numpy(xyz).pin_memory()
+        out = torch.zeros(ncfg, dtype=torch.int64).pin_memory()
+        host_xyz = pinned.numpy()
+        host_out = out.numpy().view(np.uint64)
+        count_3pcf_from_host(host_xyz, box_lu, w.periodic, w.edges_lu, out=host_out)
+        times = []
+        for _ in range(max(1, min(args.steps, 2))):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            count_3pcf_from_host(host_xyz, box_lu, w.periodic, w.edges_lu, out=host_out)
+            times.append(time.perf_counter() - t0)
+        e2e_s = statistics.mean(times)
+        [e2e_s_max], _ = reduce_max_sum(world, [e2e_s], [0.0])
+        e2e = {"value": tris_all / e2e_s_max, "unit": "triangles/s",
+               "h2d_bytes_per_step": int(xyz.nbytes), "d2h_bytes_per_step": int(ncfg * 8),
+               "ms_per_step": e2e_s_max * 1e3}
+
+    # parity 4pCF on its own workload
+    parity = None
+    if not args.no_parity:
+        pw = configs.ALL[args.parity_workload]
+        pxyz, pbox, pdesc = catalogue(pw, args.scale, rank)
+        pcoords = torch.from_numpy(pxyz).to(dev)
+        time_path(pcoords, pbox, pw, max(1, args.warmup), "4pcf")
+        torch.cuda.synchronize()
+        pres = time_path(pcoords, pbox, pw, args.steps, "4pcf")
+        p_step = statistics.mean(r[0] for r in pres)
+        p_count = statistics.mean(r[1] for r in pres)
+        even, odd = pres[-1][4]
+        cliques = int(as_uint64(even).sum())
+        (p_step, p_count), (cl_all, pe_all) = reduce_max_sum(world, [p_step, p_count],
+                                                             [float(cliques), float(pres[-1][3])])
+        parity = {"config": pdesc, "ms_per_step": p_step, "count_ms": p_count,
+                  "cliques_per_s": cl_all / (p_step / 1e3), "edges_per_s": pe_all / (p_step / 1e3),
+                  "cliques": cliques, "odd_sum": int(odd.sum().item()), "n_edges": pres[-1][3]}
+
+    # CPU oracle on a bounded sample (rank 0 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample, side = sub_cube(xyz, box_lu, args.sample_points)
+        t, e, dt, cores = oracle_rate(sample, side, w)
+        cpu = {"value": t / dt, "unit": "triangles/s", "cores": cores, "kind": "oracle",
+               "sample": (f"open corner sub-cube of side {side / 1024:.1f} h^-1 Mpc of the workload "
+                          f"catalogue: {len(sample)} points, {e} directed edges, {t} triangles, "
+                          f"graph + count in {dt:.1f} s")}
+
+    peak, peak_kind = hbm_peak()
+    achieved = alg_bytes / (count_ms / 1e3) / 1e9
+    traffic = profiled_traffic(w.name) if args.scale == 1.0 else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_kind": peak_kind, "kernel": "k_count3",
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "per_unit": "5 B per spoke-row entry walked (sum over forward edges (i,j) of |N+(j)|) "
+                            "+ 5 B per forward edge for the hub rows"}
+
+    if rank == 0:
+        value = tris_all / (step_ms_max / 1e3)
+        desc["l2"] = (f"inputs larger than L2: the CSR graph ({BYTES_PER_EDGE * n_edges / 1e9:.1f} GB) "
+                      "is rebuilt and re-read every step")
+        line = {"metric": METRIC, "value": value, "unit": "triangles/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int64", "data": "synthetic", "config": desc,
+                "edges_per_s": edges_all / (step_ms_max / 1e3),
+                "count_edges_per_s": edges_all / 2 / (count_ms_max / 1e3),
+                "triangles_per_step": tris_all, "n_edges": n_edges, "build_ms": build_ms,
+                "count_ms": count_ms_max, "wall_s_timed": t_wall,
+                "graph_stats": st, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clocks, "parity_4pcf": parity}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = configs.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

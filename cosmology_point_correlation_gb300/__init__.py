@@ -25,11 +25,16 @@ from ._lib import GramsciError
 
 __all__ = ["Graph", "GramsciError", "build_graph", "count_3pcf_from_host",
            "count_4pcf_parity_from_host", "config_count_3pcf", "config_count_4pcf",
-           "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path"]
+           "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path", "kernel_launches"]
 
 
 def library_path() -> str:
     return _lib.lib_path()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process."""
+    return int(_lib.load().gs_kernel_launches())
 
 
 def _torch():
@@ -96,6 +101,12 @@ class Graph:
     @property
     def max_degree(self) -> int:
         return self.info()[2]
+
+    def stats(self, stream=None) -> dict:
+        """Work statistics (sum C(f,2), sum b*f, max forward degree, ...); synchronises."""
+        st = _lib.GraphStats()
+        _lib.check(_lib.load().gs_graph_stats(self._h, ctypes.byref(st), _stream(stream)))
+        return {name: getattr(st, name) for name, _ in _lib.GraphStats._fields_ if name != "reserved"}
 
     # -- counts
     def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):

@@ -37,6 +37,17 @@ SIGNATURES = {
     "gs_version": (ctypes.c_char_p, []),
 }
 
+
+
+class GraphStats(ctypes.Structure):
+    _fields_ = [("n", _i64), ("n_edges", _i64), ("max_degree", _i32), ("max_forward", _i32),
+                ("cells_per_axis", _i32), ("reserved", _i32), ("hub_tail", _i64),
+                ("spoke_walk", _i64)]
+
+
+SIGNATURES["gs_graph_stats"] = (_int, [_p, ctypes.POINTER(GraphStats), _p])
+SIGNATURES["gs_kernel_launches"] = (ctypes.c_uint64, [])
+
 _lib = None
 
 

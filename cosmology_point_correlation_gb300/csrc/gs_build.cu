@@ -10,9 +10,11 @@
 // cell id, so the candidates are met in increasing index order.
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "gs_internal.cuh"
 
@@ -32,6 +34,12 @@ gs_status gs_set_error(gs_status s, const char *fmt, ...)
 void gs_clear_error() { g_msg[0] = 0; }
 
 extern "C" const char *gs_last_error(void) { return g_msg; }
+
+static std::atomic<uint64_t> g_launches{ 0 };
+
+void gs_note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+extern "C" uint64_t gs_kernel_launches(void) { return g_launches.load(); }
 
 int gs_sm_count()
 {
@@ -156,8 +164,11 @@ static gs_status scan_impl(const int32_t *in, Tout *out, int64_t n, cudaStream_t
     Tout *sums = nullptr;
     GS_TRY_CUDA(cudaMallocAsync(&sums, sizeof(Tout) * ntiles, st));
     k_scan_tiles<Tout><<<(unsigned)ntiles, SCAN_THREADS, 0, st>>>(in, out, sums, n);
+    gs_note_launch();
     k_scan_sums<Tout><<<1, SCAN_THREADS, 0, st>>>(sums, ntiles, out + n);
+    gs_note_launch();
     k_scan_add<Tout><<<(unsigned)ntiles, SCAN_THREADS, 0, st>>>(out, sums, n);
+    gs_note_launch();
     cudaError_t e = cudaGetLastError();
     cudaFreeAsync(sums, st);
     if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "scan launch failed: %s", cudaGetErrorString(e));
@@ -402,6 +413,7 @@ static void free_graph_arrays(gs_graph *g)
     cudaFree(g->bin);
     cudaFree(g->work);
     cudaFree(g->err);
+    cudaFree(g->cfg3);
 }
 
 extern "C" void gs_graph_free(gs_graph_t g)
@@ -476,6 +488,19 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         GS_BUILD_CUDA(cudaMalloc(&g->fwd, sizeof(int32_t) * nn));
         GS_BUILD_CUDA(cudaMalloc(&g->work, sizeof(unsigned long long) * 4));
         GS_BUILD_CUDA(cudaMalloc(&g->err, sizeof(int32_t)));
+        if (nbins <= 40) {
+            // configuration index of every (z, x, y) bin triple, for the 3pCF kernel
+            std::vector<uint16_t> h((size_t)nbins * nbins * nbins);
+            for (int z = 0; z < nbins; ++z)
+                for (int x = 0; x < nbins; ++x)
+                    for (int y = 0; y < nbins; ++y) {
+                        int v[3] = { x, y, z };
+                        std::sort(v, v + 3);
+                        h[((size_t)z * nbins + x) * nbins + y] = (uint16_t)gs_idx3(nbins, v[0], v[1], v[2]);
+                    }
+            GS_BUILD_CUDA(cudaMalloc(&g->cfg3, sizeof(uint16_t) * h.size()));
+            GS_BUILD_CUDA(cudaMemcpy(g->cfg3, h.data(), sizeof(uint16_t) * h.size(), cudaMemcpyHostToDevice));
+        }
         GS_BUILD_CUDA(cudaMallocAsync(&cell, sizeof(int32_t) * nn, st));
         GS_BUILD_CUDA(cudaMallocAsync(&slot, sizeof(int32_t) * nn, st));
         GS_BUILD_CUDA(cudaMallocAsync(&tmp, sizeof(int32_t) * nn, st));
@@ -496,19 +521,24 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         if (n > 0) {
             k_cell_assign<<<grid1, 256, 0, st>>>(coords_dev, n, (int)box_lu, g->ncell, cell, slot,
                                                  cell_count, g->err);
+            gs_note_launch();
             GS_BUILD_CUDA(cudaGetLastError());
         }
         s = gs_scan_i32_to_i32(cell_count, cell_start, ncells, st);
         if (s != GS_OK) goto fail;
         if (n > 0) {
             k_cell_scatter<<<grid1, 256, 0, st>>>(cell, slot, cell_start, n, tmp);
+            gs_note_launch();
             const int gw = (int)std::min<int64_t>(((int64_t)ncells * 32 + 255) / 256, (int64_t)sms * 32);
             k_cell_order<<<gw, 256, 0, st>>>(cell_start, ncells, tmp, perm);
+            gs_note_launch();
             k_gather_points<<<grid1, 256, 0, st>>>(coords_dev, perm, n, g->pts, g->inv);
+            gs_note_launch();
             k_neighbors<false><<<ncells, NB_THREADS, 0, st>>>(
                 g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                 (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
                 deg, g->fwd, nullptr, nullptr, nullptr, maxd);
+            gs_note_launch();
             GS_BUILD_CUDA(cudaGetLastError());
         }
         s = gs_scan_i32_to_i64(deg, g->row_ptr, n, st);
@@ -526,14 +556,16 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         }
         g->max_degree = (int32_t)hmax;
 
-        const size_t ne = (size_t)std::max<int64_t>(g->n_edges, 1);
+        const size_t ne = (size_t)(g->n_edges + GS_EDGE_PAD);
         GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));
         GS_BUILD_CUDA(cudaMalloc(&g->bin, ne));
+        GS_BUILD_CUDA(cudaMemsetAsync(g->nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD, st));
         if (n > 0 && g->n_edges > 0) {
             k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
                 g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                 (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
                 nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr);
+            gs_note_launch();
             GS_BUILD_CUDA(cudaGetLastError());
         }
     }
@@ -651,6 +683,7 @@ extern "C" gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int
     const int sms = gs_sm_count();
     const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sms * 16);
     k_input_degrees<<<grid, 256, 0, st>>>(g->row_ptr, g->inv, n, deg_in);
+    gs_note_launch();
     gs_status s = gs_scan_i32_to_i64(deg_in, row_ptr_dev, n, st);
     cudaFreeAsync(deg_in, st);
     if (s != GS_OK) return s;
@@ -658,6 +691,7 @@ extern "C" gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int
         const int gridr = (int)std::min<int64_t>(n, (int64_t)sms * 8);
         k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, g->row_ptr, g->nbr, g->bin, n,
                                                     row_ptr_dev, nbr_dev, bin_dev);
+        gs_note_launch();
     }
     GS_TRY_CUDA(cudaGetLastError());
     return GS_OK;
@@ -678,7 +712,63 @@ extern "C" gs_status gs_graph_export_perm(gs_graph_t g, int32_t *perm_dev, void 
     cudaStream_t st = (cudaStream_t)cuda_stream;
     const int grid = (int)std::min<int64_t>((g->n + 255) / 256, (int64_t)gs_sm_count() * 16);
     k_perm<<<grid, 256, 0, st>>>(g->pts, g->n, perm_dev);
+    gs_note_launch();
     GS_TRY_CUDA(cudaGetLastError());
+    return GS_OK;
+}
+
+// Per-graph work statistics: sum C(f,2), sum b*f, max f (see gramsci_gb.h).
+__global__ void k_graph_stats(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd,
+                              int64_t n, unsigned long long *__restrict__ acc)
+{
+    unsigned long long tail = 0, walk = 0;
+    unsigned fmax = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const unsigned long long d = (unsigned long long)(row_ptr[i + 1] - row_ptr[i]);
+        const unsigned long long b = (unsigned long long)fwd[i], f = d - b;
+        tail += f * (f - (f > 0)) / 2;
+        walk += b * f;
+        fmax = max(fmax, (unsigned)f);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        tail += __shfl_down_sync(0xffffffffu, tail, o);
+        walk += __shfl_down_sync(0xffffffffu, walk, o);
+        fmax = max(fmax, __shfl_down_sync(0xffffffffu, fmax, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(acc, tail);
+        atomicAdd(acc + 1, walk);
+        atomicMax(acc + 2, (unsigned long long)fmax);
+    }
+}
+
+extern "C" gs_status gs_graph_stats(gs_graph_t g, gs_graph_stats_t *out, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !out) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    unsigned long long *acc = nullptr, h[3] = { 0, 0, 0 };
+    GS_TRY_CUDA(cudaMallocAsync(&acc, sizeof(h), st));
+    cudaError_t e = cudaMemsetAsync(acc, 0, sizeof(h), st);
+    if (e == cudaSuccess && g->n > 0) {
+        const int grid = (int)std::min<int64_t>((g->n + 255) / 256, (int64_t)gs_sm_count() * 8);
+        k_graph_stats<<<grid, 256, 0, st>>>(g->row_ptr, g->fwd, g->n, acc);
+        gs_note_launch();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h, acc, sizeof(h), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFreeAsync(acc, st);
+    if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "graph stats failed: %s", cudaGetErrorString(e));
+    out->n = g->n;
+    out->n_edges = g->n_edges;
+    out->max_degree = g->max_degree;
+    out->max_forward = (int32_t)h[2];
+    out->cells_per_axis = g->ncell;
+    out->reserved = 0;
+    out->hub_tail = (int64_t)h[0];
+    out->spoke_walk = (int64_t)h[1];
     return GS_OK;
 }
 

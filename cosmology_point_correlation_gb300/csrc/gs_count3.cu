@@ -30,12 +30,13 @@
 
 #include "gs_internal.cuh"
 
-constexpr int C3_THREADS = 256;
+constexpr int C3_THREADS = 512;
 constexpr int C3_WARPS = C3_THREADS / 32;
-constexpr int C3_TABLE_LOG = 12;                 // 4096 slots
+constexpr int C3_TABLE_LOG = 13;                 // 8192 slots
 constexpr int C3_TABLE = 1 << C3_TABLE_LOG;
-constexpr int C3_CHUNK = C3_TABLE / 2;           // load factor <= 1/2
-constexpr int C3_SMEM_HIST_MAX = 12288;          // configurations kept in shared memory
+constexpr int C3_CHUNK = C3_TABLE / 4;           // load factor <= 1/4: short probe chains
+constexpr int C3_SPOKES = 4096;                  // spokes grouped per pass
+constexpr int C3_SMEM_HIST_MAX = 12288;          // configurations kept in shared memory (nbins <= 40)
 constexpr int C3_EMPTY = -1;
 
 struct C3Args {
@@ -48,6 +49,7 @@ struct C3Args {
     int ncfg;
     unsigned long long *ghist;
     unsigned long long *cursor;   // next hub to hand out
+    const uint16_t *cfg3;         // [nb][nb][nb] configuration index of (z, x, y) (SMEM_HIST)
 };
 
 // Flush the shared histogram into the global one and clear it.
@@ -62,21 +64,51 @@ __device__ __forceinline__ void c3_flush(unsigned *sh, int ncfg, unsigned long l
     }
 }
 
+// Configuration index of the sorted triple of (x, y, z), from the per-bin tables
+// lex_a / lex_b: idx3(lo, mid, hi) = lex_a[lo] + lex_b[mid] + hi.
+__device__ __forceinline__ int c3_index(int x, int y, int z, const int *lex_a, const int *lex_b)
+{
+    const int lo = min(x, min(y, z));
+    const int hi = max(x, max(y, z));
+    const int mid = x + y + z - lo - hi;
+    return lex_a[lo] + lex_b[mid] + hi;
+}
+
+// Copy the z-slice of the configuration table (nb x nb u16) into this warp's
+// shared-memory table.
+__device__ __forceinline__ void c3_fill_tab(uint16_t *tab, const uint16_t *cfg3, int nb, int z)
+{
+    const int lane = threadIdx.x & 31;
+    const uint16_t *src = cfg3 + (size_t)z * nb * nb;
+    __syncwarp();
+    for (int t = lane; t < nb * nb; t += 32) tab[t] = __ldg(src + t);
+    __syncwarp();
+}
+
 template <bool SMEM_HIST>
-__global__ void __launch_bounds__(C3_THREADS)
+__global__ void __launch_bounds__(C3_THREADS, 2)
 k_count3(C3Args a)
 {
-    extern __shared__ unsigned s_hist[];            // [ncfg] when SMEM_HIST
-    __shared__ int32_t s_key[C3_TABLE];
-    __shared__ uint8_t s_bin[C3_TABLE];
-    __shared__ int s_lex_a[256];                    // idx3 = s_lex_a[lo] + s_lex_b[mid] + hi
+    // dynamic: hash keys [C3_TABLE] i32, their bins [C3_TABLE] u8, then (SMEM_HIST
+    // only) the histogram [ncfg] u32 and one nb x nb u16 table per warp
+    extern __shared__ unsigned s_dyn[];
+    __shared__ uint16_t s_order[C3_SPOKES];         // spoke positions grouped by b_ij
+    __shared__ int s_next;                          // next entry of s_order to hand out
+    __shared__ int s_bucket[257];
+    __shared__ int s_lex_a[256];
     __shared__ int s_lex_b[256];
     __shared__ long long s_hub;
-    __shared__ unsigned long long s_pending;        // hits bound since the last flush
+    __shared__ unsigned long long s_pending;        // bound on hits since the last flush
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nb = a.nb;
-    // gs_idx3(a, b, c) = F(a) - G(a) + G(b) - b + c with F(a) = gs_idx3(a, a, a) and
+    int32_t *s_key = (int32_t *)s_dyn;
+    uint8_t *s_bin = (uint8_t *)(s_key + C3_TABLE);
+    unsigned *s_hist = (unsigned *)(s_bin + C3_TABLE);
+    uint16_t *tab = (uint16_t *)(s_hist + ((a.ncfg + 3) & ~3)) + warp * nb * nb;
+    int tab_z = -1;
+
+    // idx3(a, b, c) = F(a) - G(a) + G(b) - b + c with F(a) = idx3(a, a, a) and
     // G(t) = t nb - t (t - 1) / 2, split into two per-bin tables.
     for (int t = threadIdx.x; t < nb; t += C3_THREADS) {
         const int64_t Gt = (int64_t)t * nb - (int64_t)t * (t - 1) / 2;
@@ -96,18 +128,19 @@ k_count3(C3Args a)
         const long long i = s_hub;
         if (i >= a.hub_end) break;
 
-        const int64_t f0 = a.row_ptr[i] + a.fwd[i];          // forward row F = nbr[f0, f1)
+        const int64_t f0 = a.row_ptr[i] + a.fwd[i];          // forward row F = nbr[f0, f0 + f)
         const int f = (int)(a.row_ptr[i + 1] - f0);
         for (int c0 = 0; c0 < f; c0 += C3_CHUNK) {           // chunks of candidate keys
             const int c1 = min(f, c0 + C3_CHUNK);
             const int cn = c1 - c0;
-            int lg = 6;                                      // table of 2^lg >= 2 cn slots
-            while ((1 << lg) < 2 * cn) ++lg;
+            if (c1 < 2) break;                               // a lone key closes nothing
+            int lg = 6;                                      // table of 2^lg >= 4 cn slots
+            while ((1 << lg) < 4 * cn) ++lg;
             const int tsize = 1 << lg, shift = 32 - lg, mask = tsize - 1;
 
             if (SMEM_HIST) {
-                // bound on the hits of this chunk: every spoke before c1 can close
-                // at most cn triangles
+                // bound on the hits of this chunk: every spoke before c1 closes at
+                // most cn triangles
                 const unsigned long long bound = (unsigned long long)c1 * cn;
                 if (s_pending + bound > 0xffffffffull) {     // block-uniform
                     __syncthreads();
@@ -124,53 +157,132 @@ k_count3(C3Args a)
                 while (atomicCAS(&s_key[h], C3_EMPTY, k) != C3_EMPTY) h = (h + 1) & mask;
                 s_bin[h] = a.bin[f0 + c0 + t];
             }
-            __syncthreads();
-
             const int32_t kmax = a.nbr[f0 + c1 - 1];
             const int32_t kfirst = a.nbr[f0 + c0];
-            for (int s = warp; s < c1 - 1; s += C3_WARPS) {
-                const int32_t j = a.nbr[f0 + s];
-                const int bij = a.bin[f0 + s];
-                const int64_t rj1 = a.row_ptr[j + 1];
-                int64_t p;
-                if (s + 1 >= c0) {
-                    p = a.row_ptr[j] + a.fwd[j];                   // first entry > j
-                } else {
-                    // first entry >= kfirst in N(j) (lower bound; only for later chunks)
-                    int64_t lo = a.row_ptr[j] + a.fwd[j], hi = rj1;
-                    while (lo < hi) {
-                        const int64_t mid = (lo + hi) >> 1;
-                        if (a.nbr[mid] < kfirst) lo = mid + 1; else hi = mid;
-                    }
-                    p = lo;
-                }
-                for (; p < rj1; p += 32) {
-                    const int64_t q = p + lane;
-                    int32_t k = 0x7fffffff;
-                    int bjk = 0;
-                    if (q < rj1) {
-                        k = a.nbr[q];
-                        bjk = a.bin[q];
-                    }
-                    if (k <= kmax) {
-                        uint32_t h = gs_hash(k, shift);
-                        int32_t key;
-                        while ((key = s_key[h]) != k && key != C3_EMPTY) h = (h + 1) & mask;
-                        if (key == k) {
-                            const int bik = s_bin[h];
-                            const int lo = min(bij, min(bik, bjk));
-                            const int hi = max(bij, max(bik, bjk));
-                            const int mid = bij + bik + bjk - lo - hi;
-                            const int idx = s_lex_a[lo] + s_lex_b[mid] + hi;
-                            if (SMEM_HIST) atomicAdd(&s_hist[idx], 1u);
-                            else atomicAdd(a.ghist + idx, 1ull);
+
+            // spokes s in [sb, se) of [0, c1 - 1), at most C3_SPOKES at a time
+            for (int sb = 0; sb < c1 - 1; sb += C3_SPOKES) {
+                const int se = min(c1 - 1, sb + C3_SPOKES);
+                const int ns = se - sb;
+                // counting sort of the spokes by b_ij, so that each warp's run of
+                // the list needs few rebuilds of its configuration table
+                for (int t = threadIdx.x; t <= nb; t += C3_THREADS) s_bucket[t] = 0;
+                __syncthreads();
+                for (int t = threadIdx.x; t < ns; t += C3_THREADS) atomicAdd(&s_bucket[a.bin[f0 + sb + t] + 1], 1);
+                __syncthreads();
+                if (warp == 0) {
+                    int carry = 0;
+                    for (int b0 = 0; b0 <= nb; b0 += 32) {
+                        const int v = b0 + lane <= nb ? s_bucket[b0 + lane] : 0;
+                        int x = v;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int y = __shfl_up_sync(0xffffffffu, x, o);
+                            if (lane >= o) x += y;
                         }
+                        if (b0 + lane <= nb) s_bucket[b0 + lane] = carry + x;   // inclusive: bucket b starts at s_bucket[b]
+                        carry += __shfl_sync(0xffffffffu, x, 31);
                     }
-                    // the row is sorted: stop once the last lane's key passes kmax
-                    if (__shfl_sync(0xffffffffu, k, 31) > kmax) break;
                 }
+                __syncthreads();
+                for (int t = threadIdx.x; t < ns; t += C3_THREADS) {
+                    const int b = a.bin[f0 + sb + t];
+                    s_order[atomicAdd(&s_bucket[b], 1)] = (uint16_t)t;
+                }
+                __syncthreads();
+
+                if (threadIdx.x == 0) s_next = 0;
+                __syncthreads();
+                for (;;) {
+                    int li = 0;
+                    if (lane == 0) li = atomicAdd(&s_next, 1);
+                    li = __shfl_sync(0xffffffffu, li, 0);
+                    if (li >= ns) break;
+                    const int s = sb + s_order[li];
+                    const int32_t j = a.nbr[f0 + s];
+                    const int bij = a.bin[f0 + s];
+                    if (SMEM_HIST && bij != tab_z) {
+                        c3_fill_tab(tab, a.cfg3, nb, bij);
+                        tab_z = bij;
+                    }
+                    const int64_t pe = a.row_ptr[j + 1];
+                    int64_t p0;
+                    if (s + 1 >= c0) {
+                        p0 = a.row_ptr[j] + a.fwd[j];                  // first entry > j
+                    } else {
+                        // first entry >= kfirst in N(j) (lower bound; only for later chunks)
+                        int64_t lo = a.row_ptr[j] + a.fwd[j], hi = pe;
+                        while (lo < hi) {
+                            const int64_t mid = (lo + hi) >> 1;
+                            if (a.nbr[mid] < kfirst) lo = mid + 1; else hi = mid;
+                        }
+                        p0 = lo;
+                    }
+                    if (p0 >= pe) continue;
+                    // Walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
+                    // 4l .. 4l+3 of the step as one int4 and their bins as one word.
+                    const int64_t pa = p0 & ~(int64_t)3;
+                    const int head = (int)(p0 - pa);
+                    const int total = head + (int)(pe - p0);
+                    const int4 *vk = reinterpret_cast<const int4 *>(a.nbr + pa) + lane;
+                    const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.bin + pa) + lane;
+                    int4 kk = __ldg(vk);                            // step 0, then prefetch
+                    uint32_t bb = __ldg(vb);
+                    for (int base = 0; base < total; base += 128) {
+                        vk += 32;
+                        vb += 32;
+                        int4 kn = kk;
+                        uint32_t bn = bb;
+                        if (base + 128 < total) {                  // next step in flight
+                            kn = __ldg(vk);
+                            bn = __ldg(vb);
+                        }
+                        unsigned vmask = 0xfu;
+                        if (base == 0 || base + 128 > total) {     // first / last step only
+                            const int r0 = base + 4 * lane;
+                            if (head > r0) vmask &= (0xfu << min(head - r0, 4)) & 0xfu;
+                            if (total - r0 < 4) vmask &= (1u << max(total - r0, 0)) - 1u;
+                        }
+                        const int k[4] = { kk.x, kk.y, kk.z, kk.w };
+                        uint32_t h[4];
+                        int32_t key[4];
+                        unsigned pend = 0;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {              // first probes, all in flight
+                            h[e] = gs_hash(k[e], shift);
+                            key[e] = s_key[h[e]];
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pend |= (unsigned)(key[e] != k[e] && key[e] != C3_EMPTY) << e;
+                        while (pend) {                             // collisions (rare at load <= 1/4)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if ((pend >> e) & 1u) {
+                                    h[e] = (h[e] + 1) & mask;
+                                    key[e] = s_key[h[e]];
+                                    if (key[e] == k[e] || key[e] == C3_EMPTY) pend &= ~(1u << e);
+                                }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (((vmask >> e) & 1u) && key[e] == k[e]) {
+                                const int bik = s_bin[h[e]];
+                                const int bjk = (bb >> (8 * e)) & 0xffu;
+                                if (SMEM_HIST) {
+                                    atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
+                                } else {
+                                    atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
+                                }
+                            }
+                        }
+                        // rows are sorted: stop once the step's last key passes kmax
+                        if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
+                        kk = kn;
+                        bb = bn;
+                    }
+                }
+                __syncthreads();
             }
-            __syncthreads();
             for (int t = threadIdx.x; t < tsize; t += C3_THREADS) s_key[t] = C3_EMPTY;
             __syncthreads();
         }
@@ -206,23 +318,22 @@ extern "C" gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub
     a.ncfg = ncfg;
     a.ghist = (unsigned long long *)hist_dev;
     a.cursor = g->work;
+    a.cfg3 = g->cfg3;
 
     // shared-memory histogram unless it is too large or a chunk's hit bound
     // (spokes x chunk) could overflow a 32-bit counter
-    const bool smem = ncfg <= C3_SMEM_HIST_MAX && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
-    const size_t dyn = smem ? sizeof(unsigned) * ncfg : 0;
+    const bool smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
+    const size_t dyn = (sizeof(int32_t) + 1) * C3_TABLE +
+                       (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * g->nb * g->nb : 0);
+    auto kern = smem ? k_count3<true> : k_count3<false>;
     int per_sm = 0;
-    if (smem) {
-        GS_TRY_CUDA(cudaFuncSetAttribute(k_count3<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
-        GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_count3<true>, C3_THREADS, dyn));
-    } else {
-        GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_count3<false>, C3_THREADS, 0));
-    }
+    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C3_THREADS, dyn));
     per_sm = std::max(per_sm, 1);
     const int64_t hubs = hub_end - hub_begin;
     const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * per_sm, hubs);
-    if (smem) k_count3<true><<<grid, C3_THREADS, dyn, st>>>(a);
-    else k_count3<false><<<grid, C3_THREADS, 0, st>>>(a);
+    kern<<<grid, C3_THREADS, dyn, st>>>(a);
+    gs_note_launch();
     GS_TRY_CUDA(cudaGetLastError());
     return GS_OK;
 }

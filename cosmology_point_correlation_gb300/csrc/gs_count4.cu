@@ -324,6 +324,7 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
     a.cursor = g->work + 1;
     const int grid = (int)std::min<int64_t>((int64_t)sms * per_sm, hubs);
     kern<<<grid, C4_THREADS, dyn, st>>>(a);
+    gs_note_launch();
     GS_TRY_CUDA(cudaGetLastError());
 
     if (g->max_degree > C4_M) {
@@ -341,6 +342,7 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
         a.scratch = scratch;
         a.scratch_stride = stride;
         k_count4_large<<<gl, C4_THREADS, 0, st>>>(a);
+        gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
         if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));

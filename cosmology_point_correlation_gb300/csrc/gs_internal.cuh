@@ -37,6 +37,7 @@ struct gs_graph {
     uint8_t *bin;
     unsigned long long *work;  // 4 device counters used by the count kernels
     int32_t *err;              // device error word of the build kernels
+    uint16_t *cfg3;            // [nb][nb][nb] idx3(sort(x, y, z)) at (z, x, y), nb <= 40; or NULL
 };
 
 // ---------------------------------------------------------------- errors
@@ -53,6 +54,14 @@ void gs_clear_error();
                                 __FILE__, __LINE__);                                   \
         }                                                                              \
     } while (0)
+
+// Count one kernel launch (reported by gs_kernel_launches).
+void gs_note_launch();
+
+// Entries of padding after the last edge of nbr / bin: a warp may read whole
+// 16-byte vectors up to 128 entries past a row's end without leaving the
+// allocation.
+constexpr int64_t GS_EDGE_PAD = 128;
 
 // Number of SMs of the current device (cached per device).
 int gs_sm_count();

@@ -42,6 +42,9 @@
  *     default stream). gs_build_graph synchronises that stream once (to read
  *     the edge total); the count and export calls are asynchronous.
  *   - Outputs are overwritten, never accumulated.
+ *   - A graph keeps one work cursor per count kind, so count calls on the
+ *     same graph must not overlap in time (issue them on one stream);
+ *     different graphs are independent.
  *   - On any non-OK status no output has been written by this call (except
  *     where noted), everything the call allocated is freed, and
  *     gs_last_error() returns a message for the calling thread.
@@ -115,6 +118,32 @@ gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_de
  *   n_edges     directed edges, sum of degrees (= 2 x pairs)
  *   max_degree  largest |N(i)| */
 gs_status gs_graph_info(gs_graph_t g, int64_t *n, int64_t *n_edges, int32_t *max_degree);
+
+/* Work statistics of a built graph, in the graph's internal order, where
+ * f_i = |{j in N(i): j > i}| (forward degree) and b_i = deg_i - f_i:
+ *   hub_tail    sum_i C(f_i, 2): hub-tail entries the merge-walk of §III.1
+ *               reads over all forward spokes (also the number of candidate
+ *               third vertices)
+ *   spoke_walk  sum over forward edges (i, j) of f_j = sum_j b_j f_j: spoke-row
+ *               entries the merge-walk reads
+ *   max_forward largest f_i
+ * Computed on the device; the call synchronises cuda_stream. */
+typedef struct {
+    int64_t n;
+    int64_t n_edges;
+    int32_t max_degree;
+    int32_t max_forward;
+    int32_t cells_per_axis;
+    int32_t reserved;
+    int64_t hub_tail;
+    int64_t spoke_walk;
+} gs_graph_stats_t;
+
+gs_status gs_graph_stats(gs_graph_t g, gs_graph_stats_t *out, void *cuda_stream);
+
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all threads, all devices). */
+uint64_t gs_kernel_launches(void);
 
 /* The graph as CSR in INPUT numbering, rows sorted by neighbour id (Eq.(1)).
  *   row_ptr_dev int64 [n+1], device
