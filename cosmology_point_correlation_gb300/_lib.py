@@ -23,6 +23,7 @@ SIGNATURES = {
     "gs_build_graph": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _p, ctypes.POINTER(_p)]),
     "gs_count_3pcf": (_int, [_p, _p, _i64, _i64, _p]),
     "gs_count_4pcf_parity": (_int, [_p, _p, _p, _i64, _i64, _p]),
+    "gs_count_4pcf_parity_static": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_graph_info": (_int, [_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i32)]),
     "gs_graph_export_csr": (_int, [_p, _p, _p, _p, _p]),
     "gs_graph_export_perm": (_int, [_p, _p, _p]),

@@ -24,6 +24,7 @@
 // into the global histograms.
 
 #include <algorithm>
+#include <mutex>
 
 #include "gs_internal.cuh"
 
@@ -346,6 +347,127 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
         if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    return GS_OK;
+}
+
+// ---------------------------------------------------------------- fixed-workspace variant
+//
+// gs_count_4pcf_parity_static runs the same two kernels as gs_count_4pcf_parity
+// but takes every piece of scratch memory it needs -- the two work cursors and
+// the per-block workspace of hubs with more than C4_M neighbours -- from the
+// file-scope device array below instead of cudaMallocAsync / graph memory.
+// The array is part of the library image: every GPU that loads the library
+// holds GS_C4_STATIC_BYTES of device memory for it until the process exits.
+
+constexpr size_t GS_C4_STATIC_BYTES = (size_t)16 << 20;     // 16 MiB
+constexpr size_t GS_C4_STATIC_HEAD = 256;                     // two cursors, padded
+
+static __device__ __align__(256) unsigned char g_c4_static[GS_C4_STATIC_BYTES];
+
+static std::mutex g_c4_static_mu;
+static char *g_c4_static_base[64];                            // per device
+
+// Device address of g_c4_static on the current device. Host code may not use
+// the symbol itself (it names a host-side stand-in), so the address is looked
+// up once per device with that device current and cached.
+static gs_status c4_static_base(char **out)
+{
+    int dev = 0;
+    GS_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return gs_set_error(GS_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_c4_static_mu);
+    if (!g_c4_static_base[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_c4_static);
+        if (e != cudaSuccess || !p)
+            return gs_set_error(GS_ERR_CUDA, "cudaGetSymbolAddress of the static workspace failed: %s",
+                                cudaGetErrorString(e));
+        g_c4_static_base[dev] = (char *)p;
+    }
+    *out = g_c4_static_base[dev];
+    return GS_OK;
+}
+
+extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
+                                                 int64_t hub_begin, int64_t hub_end, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
+        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
+                            (long long)hub_end, (long long)g->n);
+    if (g->edges[g->nb] >= (1ll << 20))
+        return gs_set_error(GS_ERR_ARG, "parity 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
+    const int64_t ncfg = gs_ncfg4(g->nb);
+    if (ncfg <= 0) return GS_OK;
+    if (!even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL histogram");
+
+    // workspace of one block for the largest hub; refuse before writing anything
+    const int M = g->max_degree;
+    size_t stride = 0;
+    if (M > C4_M) {
+        int tlog = 4;
+        while ((1 << tlog) < 2 * M) ++tlog;
+        const size_t WM = (size_t)(M + 31) / 32;
+        stride = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM + M;
+        stride = (stride + 255) & ~(size_t)255;
+        if (stride > GS_C4_STATIC_BYTES - GS_C4_STATIC_HEAD)
+            return gs_set_error(GS_ERR_CAPACITY,
+                                "a hub of degree %d needs %zu bytes of workspace; the static workspace holds %zu "
+                                "(use gs_count_4pcf_parity)", M, stride, GS_C4_STATIC_BYTES - GS_C4_STATIC_HEAD);
+    }
+    char *base = nullptr;
+    gs_status s = c4_static_base(&base);
+    if (s != GS_OK) return s;
+
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
+    unsigned long long *cursors = (unsigned long long *)base;
+    GS_TRY_CUDA(cudaMemsetAsync(cursors, 0, 2 * sizeof(unsigned long long), st));   // left over from the last call
+
+    C4Args a{};
+    a.pts = g->pts;
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.hub_begin = hub_begin;
+    a.hub_end = hub_end;
+    a.box = (int)g->box_lu;
+    a.periodic = g->periodic;
+    a.nb = g->nb;
+    a.ncfg = (int)ncfg;
+    a.even = (unsigned long long *)even_dev;
+    a.odd = (long long *)odd_dev;
+
+    const int64_t hubs = hub_end - hub_begin;
+    const int sms = gs_sm_count();
+    const bool smem = ncfg <= C4_SMEM_HIST_MAX;
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
+    auto kern = smem ? k_count4_small<true> : k_count4_small<false>;
+    int per_sm = 0;
+    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
+    per_sm = std::max(per_sm, 1);
+    a.cursor = cursors;
+    const int grid = (int)std::min<int64_t>((int64_t)sms * per_sm, hubs);
+    kern<<<grid, C4_THREADS, dyn, st>>>(a);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
+
+    if (M > C4_M) {
+        const int64_t slices = (int64_t)((GS_C4_STATIC_BYTES - GS_C4_STATIC_HEAD) / stride);
+        const int gl = (int)std::min<int64_t>(std::min<int64_t>((int64_t)sms * 2, hubs), slices);
+        a.cursor = cursors + 1;
+        a.big_m = M;
+        a.scratch = base + GS_C4_STATIC_HEAD;
+        a.scratch_stride = stride;
+        k_count4_large<<<gl, C4_THREADS, 0, st>>>(a);
+        gs_note_launch();
+        GS_TRY_CUDA(cudaGetLastError());
     }
     return GS_OK;
 }

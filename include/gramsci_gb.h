@@ -113,6 +113,30 @@ gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int
 gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
                                int64_t hub_begin, int64_t hub_end, void *cuda_stream);
 
+/* The parity-4pCF count of gs_count_4pcf_parity, without any device memory
+ * allocation inside the call. The paper has no counterpart: this entry point
+ * is for callers that cannot call cudaMalloc / cudaMallocAsync -- for example
+ * a latency-critical pipeline where cudaMalloc and cudaFree would synchronise
+ * the whole device and stall other streams, or a service that reserves all of
+ * its device memory once at start-up and forbids later allocations.
+ * gs_count_4pcf_parity allocates a per-block workspace for hubs of more than
+ * 512 neighbours; this variant instead uses a fixed 16 MiB workspace that is
+ * compiled into the library (a static device array: every GPU that loads the
+ * library holds those 16 MiB until the process exits), plus its own two work
+ * cursors kept in the same array.
+ *   Arguments, outputs and results are those of gs_count_4pcf_parity.
+ *   Limit: one workspace slice must fit a hub of the graph's largest degree
+ *   (about 16 MiB at degree ~11,800); otherwise GS_ERR_CAPACITY is returned
+ *   before anything is written.
+ *   Set-up: the first call on each device looks up the workspace's device
+ *   address (cudaGetSymbolAddress) with that device current and caches it;
+ *   make that first call before any stream capture.
+ *   Sharing: all calls share the one workspace. The call clears what must
+ *   start at zero, but calls whose kernels overlap on the GPU (different
+ *   streams, different threads) race on it: serialise them. */
+gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
+                                      int64_t hub_begin, int64_t hub_end, void *cuda_stream);
+
 /* Sizes of a built graph (host outputs; any pointer may be NULL).
  *   n           number of points
  *   n_edges     directed edges, sum of degrees (= 2 x pairs)
