@@ -57,6 +57,8 @@ def parse_args():
     p.add_argument("--scale", type=float, default=1.0,
                    help="fraction of the workload's points, box shrunk to keep the density")
     p.add_argument("--no-parity", action="store_true")
+    p.add_argument("--only-parity", action="store_true",
+                   help="time only the parity-4pCF path and print its own line")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sample-points", type=int, default=10_000,
@@ -425,9 +427,43 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_parity_only(args):
+    """One JSON line for the parity-4pCF path alone (build + count per step)."""
+    import torch
+    from cosmology_point_correlation_gb300 import as_uint64, kernel_launches
+    rank, world, local = dist_init(args.gpus)
+    pw = configs.ALL[args.parity_workload]
+    pxyz, pbox, pdesc = catalogue(pw, args.scale, rank)
+    pcoords = torch.from_numpy(pxyz).to(torch.device("cuda", local))
+    time_path(pcoords, pbox, pw, args.warmup, "4pcf")
+    torch.cuda.synchronize()
+    barrier(world)
+    l0 = kernel_launches()
+    pres = time_path(pcoords, pbox, pw, args.steps, "4pcf")
+    launches = kernel_launches() - l0
+    step = statistics.mean(r[0] for r in pres)
+    count = statistics.mean(r[1] for r in pres)
+    even, odd = pres[-1][4]
+    cliques = int(as_uint64(even).sum())
+    (step, count), (cl_all, e_all) = reduce_max_sum(world, [step, count], [float(cliques), float(pres[-1][3])])
+    if rank == 0:
+        print(json.dumps({"metric": "parity 4pCF (hub, clique) counts/s", "value": cl_all / (step / 1e3),
+                          "unit": "cliques/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": step, "count_ms": count, "higher_is_better": True, "scaling": "weak",
+                          "dtype": "int64", "data": "synthetic", "config": pdesc,
+                          "edges_per_s": e_all / (step / 1e3), "odd_sum": int(odd.sum().item()),
+                          "gpu_launches": launches}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     w = configs.ALL[args.workload]
+    if args.only_parity and args.impl == "ours":
+        run_parity_only(args)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:
