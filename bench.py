@@ -226,12 +226,14 @@ def barrier(world):
 
 
 def reduce_max_sum(world, values_max, values_sum):
+    """Element-wise max of values_max and sum of values_sum over ranks."""
     if world == 1:
         return values_max, values_sum
     import torch
     import torch.distributed as dist
-    a = torch.tensor(values_max, dtype=torch.float64, device="cuda")
-    b = torch.tensor(values_sum, dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    a = torch.tensor(values_max, dtype=torch.float64, device=dev)
+    b = torch.tensor(values_sum, dtype=torch.float64, device=dev)
     dist.all_reduce(a, op=dist.ReduceOp.MAX)
     dist.all_reduce(b, op=dist.ReduceOp.SUM)
     return a.tolist(), b.tolist()

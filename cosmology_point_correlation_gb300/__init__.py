@@ -134,6 +134,47 @@ class Graph:
                                                     int(hub_begin), int(hub_end), _stream(stream)))
         return even, odd
 
+    def count_3pcf_hubs(self, hubs, out=None, stream=None):
+        """Triangles incident to each listed hub (input indices), summed; uint64 bits in int64."""
+        torch = _torch()
+        h = _ids(hubs, self.device)
+        m = config_count_3pcf(self.nbins)
+        if out is None:
+            out = torch.empty(m, dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_count_3pcf_hubs(self._h, ctypes.c_void_p(h.data_ptr()), h.numel(),
+                                                  ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+        return out
+
+    def count_4pcf_parity_hubs(self, hubs, out=None, stream=None):
+        """(even, odd) parity-4pCF contribution of the listed hubs (input indices)."""
+        torch = _torch()
+        h = _ids(hubs, self.device)
+        m = max(config_count_4pcf(self.nbins), 0)
+        if out is None:
+            out = (torch.zeros(m, dtype=torch.int64, device=self.device),
+                   torch.zeros(m, dtype=torch.int64, device=self.device))
+        even, odd = out
+        _lib.check(_lib.load().gs_count_4pcf_parity_hubs(self._h, ctypes.c_void_p(h.data_ptr()), h.numel(),
+                                                         ctypes.c_void_p(even.data_ptr()),
+                                                         ctypes.c_void_p(odd.data_ptr()), _stream(stream)))
+        return even, odd
+
+    def export_rows(self, ids, stream=None):
+        """(row_ptr int64 [count+1], nbr int32, bin uint8) of the listed input points, sorted rows."""
+        torch = _torch()
+        h = _ids(ids, self.device)
+        row_ptr = torch.empty(h.numel() + 1, dtype=torch.int64, device=self.device)
+        lib = _lib.load()
+        _lib.check(lib.gs_graph_export_rows(self._h, ctypes.c_void_p(h.data_ptr()), h.numel(),
+                                            ctypes.c_void_p(row_ptr.data_ptr()), None, None, _stream(stream)))
+        total = int(row_ptr[-1].item())
+        nbr = torch.empty(max(total, 1), dtype=torch.int32, device=self.device)
+        bins = torch.empty(max(total, 1), dtype=torch.uint8, device=self.device)
+        _lib.check(lib.gs_graph_export_rows(self._h, ctypes.c_void_p(h.data_ptr()), h.numel(),
+                                            ctypes.c_void_p(row_ptr.data_ptr()), ctypes.c_void_p(nbr.data_ptr()),
+                                            ctypes.c_void_p(bins.data_ptr()), _stream(stream)))
+        return row_ptr, nbr[:total], bins[:total]
+
     # -- exports
     def export_csr(self, stream=None):
         """(row_ptr int64 [n+1], nbr int32 [E], bin uint8 [E]) in input numbering, rows sorted."""
@@ -171,6 +212,12 @@ class Graph:
 
     def __exit__(self, *exc):
         self.free()
+
+
+def _ids(ids, device):
+    torch = _torch()
+    t = torch.as_tensor(np.asarray(ids, dtype=np.int32) if not isinstance(ids, torch.Tensor) else ids)
+    return t.to(device=device, dtype=torch.int32).contiguous().reshape(-1)
 
 
 def build_graph(coords, box_lu: int, periodic: bool, edges_lu, stream=None) -> Graph:

@@ -600,12 +600,13 @@ fail:
 
 // ---------------------------------------------------------------- export
 
+// Degree of output row t: input point ids[t] (or t when ids is NULL).
 __global__ void k_input_degrees(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ inv,
-                                int64_t n, int32_t *__restrict__ deg_in)
+                                const int32_t *__restrict__ ids, int64_t n, int32_t *__restrict__ deg_in)
 {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int p = inv[i];
+        const int p = inv[ids ? ids[i] : i];
         deg_in[i] = (int32_t)(row_ptr[p + 1] - row_ptr[p]);
     }
 }
@@ -616,14 +617,14 @@ constexpr int EX_SMEM = 4096;   // rows up to this length are sorted in shared m
 // One block per input row: map neighbour ids to input numbering and sort the
 // row by them (bitonic in shared memory, rank sort for longer rows).
 __global__ void __launch_bounds__(EX_THREADS)
-k_export_rows(const int4 *__restrict__ pts, const int32_t *__restrict__ inv,
+k_export_rows(const int4 *__restrict__ pts, const int32_t *__restrict__ inv, const int32_t *__restrict__ ids,
               const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ nbr,
               const uint8_t *__restrict__ bin, int64_t n, const int64_t *__restrict__ out_ptr,
               int32_t *__restrict__ out_nbr, uint8_t *__restrict__ out_bin)
 {
     __shared__ unsigned long long s_kv[EX_SMEM];
     for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
-        const int p = inv[i];
+        const int p = inv[ids ? ids[i] : i];
         const int64_t r0 = row_ptr[p];
         const int len = (int)(row_ptr[p + 1] - r0);
         const int64_t o0 = out_ptr[i];
@@ -666,35 +667,55 @@ k_export_rows(const int4 *__restrict__ pts, const int32_t *__restrict__ inv,
     }
 }
 
+// Rows of the input points ids[0..count) (all points in input order when ids is
+// NULL), neighbour ids in input numbering, each row sorted.
+static gs_status export_rows(gs_graph_t g, const int32_t *ids, int64_t count, int64_t *row_ptr_dev,
+                             int32_t *nbr_dev, uint8_t *bin_dev, cudaStream_t st)
+{
+    if (count == 0) {
+        GS_TRY_CUDA(cudaMemsetAsync(row_ptr_dev, 0, sizeof(int64_t), st));
+        return GS_OK;
+    }
+    int32_t *deg_in = nullptr;
+    GS_TRY_CUDA(cudaMallocAsync(&deg_in, sizeof(int32_t) * count, st));
+    const int sms = gs_sm_count();
+    const int grid = (int)std::min<int64_t>((count + 255) / 256, (int64_t)sms * 16);
+    k_input_degrees<<<grid, 256, 0, st>>>(g->row_ptr, g->inv, ids, count, deg_in);
+    gs_note_launch();
+    gs_status s = gs_scan_i32_to_i64(deg_in, row_ptr_dev, count, st);
+    cudaFreeAsync(deg_in, st);
+    if (s != GS_OK) return s;
+    if (nbr_dev && g->n_edges > 0) {
+        const int gridr = (int)std::min<int64_t>(count, (int64_t)sms * 8);
+        k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, ids, g->row_ptr, g->nbr, g->bin, count,
+                                                    row_ptr_dev, nbr_dev, bin_dev);
+        gs_note_launch();
+    }
+    GS_TRY_CUDA(cudaGetLastError());
+    return GS_OK;
+}
+
 extern "C" gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int32_t *nbr_dev,
                                          uint8_t *bin_dev, void *cuda_stream)
 {
     gs_clear_error();
     if (!g || !row_ptr_dev || (g->n_edges > 0 && (!nbr_dev || !bin_dev)))
         return gs_set_error(GS_ERR_ARG, "NULL argument");
+    return export_rows(g, nullptr, g->n, row_ptr_dev, nbr_dev, bin_dev, (cudaStream_t)cuda_stream);
+}
+
+extern "C" gs_status gs_graph_export_rows(gs_graph_t g, const int32_t *ids_dev, int64_t count,
+                                          int64_t *row_ptr_dev, int32_t *nbr_dev, uint8_t *bin_dev,
+                                          void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !row_ptr_dev || (count > 0 && !ids_dev) || (nbr_dev && !bin_dev))
+        return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (count < 0) return gs_set_error(GS_ERR_ARG, "negative row count");
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    const int64_t n = g->n;
-    if (n == 0) {
-        GS_TRY_CUDA(cudaMemsetAsync(row_ptr_dev, 0, sizeof(int64_t), st));
-        return GS_OK;
-    }
-    int32_t *deg_in = nullptr;
-    GS_TRY_CUDA(cudaMallocAsync(&deg_in, sizeof(int32_t) * n, st));
-    const int sms = gs_sm_count();
-    const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sms * 16);
-    k_input_degrees<<<grid, 256, 0, st>>>(g->row_ptr, g->inv, n, deg_in);
-    gs_note_launch();
-    gs_status s = gs_scan_i32_to_i64(deg_in, row_ptr_dev, n, st);
-    cudaFreeAsync(deg_in, st);
+    gs_status s = gs_check_ids(g, ids_dev, count, st);
     if (s != GS_OK) return s;
-    if (g->n_edges > 0) {
-        const int gridr = (int)std::min<int64_t>(n, (int64_t)sms * 8);
-        k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, g->row_ptr, g->nbr, g->bin, n,
-                                                    row_ptr_dev, nbr_dev, bin_dev);
-        gs_note_launch();
-    }
-    GS_TRY_CUDA(cudaGetLastError());
-    return GS_OK;
+    return export_rows(g, ids_dev, count, row_ptr_dev, nbr_dev, bin_dev, st);
 }
 
 __global__ void k_perm(const int4 *__restrict__ pts, int64_t n, int32_t *__restrict__ perm)

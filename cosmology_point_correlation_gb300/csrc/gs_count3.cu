@@ -50,6 +50,10 @@ struct C3Args {
     unsigned long long *ghist;
     unsigned long long *cursor;   // next hub to hand out
     const uint16_t *cfg3;         // [nb][nb][nb] configuration index of (z, x, y) (SMEM_HIST)
+    // hub-list mode: hubs given by input index; every triangle incident to a
+    // listed hub is counted for it (the whole row is staged, not its forward part)
+    const int32_t *hubs;          // [nhubs] input indices, or NULL
+    const int32_t *inv;           // input -> internal index
 };
 
 // Flush the shared histogram into the global one and clear it.
@@ -85,7 +89,7 @@ __device__ __forceinline__ void c3_fill_tab(uint16_t *tab, const uint16_t *cfg3,
     __syncwarp();
 }
 
-template <bool SMEM_HIST>
+template <bool SMEM_HIST, bool HUB_LIST>
 __global__ void __launch_bounds__(C3_THREADS, 2)
 k_count3(C3Args a)
 {
@@ -125,10 +129,10 @@ k_count3(C3Args a)
         __syncthreads();                                     // everyone has read the last s_hub
         if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
         __syncthreads();
-        const long long i = s_hub;
-        if (i >= a.hub_end) break;
-
-        const int64_t f0 = a.row_ptr[i] + a.fwd[i];          // forward row F = nbr[f0, f0 + f)
+        if (s_hub >= a.hub_end) break;
+        // forward row F = nbr[f0, f0 + f); in hub-list mode the whole row
+        const long long i = HUB_LIST ? (long long)a.inv[a.hubs[s_hub]] : s_hub;
+        const int64_t f0 = HUB_LIST ? a.row_ptr[i] : a.row_ptr[i] + a.fwd[i];
         const int f = (int)(a.row_ptr[i + 1] - f0);
         for (int c0 = 0; c0 < f; c0 += C3_CHUNK) {           // chunks of candidate keys
             const int c1 = min(f, c0 + C3_CHUNK);
@@ -293,6 +297,44 @@ k_count3(C3Args a)
     }
 }
 
+static gs_status launch_count3(gs_graph_t g, C3Args &a, int64_t hubs, cudaStream_t st)
+{
+    const int ncfg = a.ncfg;
+    // shared-memory histogram unless it is too large or a chunk's hit bound
+    // (spokes x chunk) could overflow a 32-bit counter
+    const bool smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
+    const size_t dyn = (sizeof(int32_t) + 1) * C3_TABLE +
+                       (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * g->nb * g->nb : 0);
+    const bool list = a.hubs != nullptr;
+    auto kern = smem ? (list ? k_count3<true, true> : k_count3<true, false>)
+                     : (list ? k_count3<false, true> : k_count3<false, false>);
+    int per_sm = 0;
+    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C3_THREADS, dyn));
+    per_sm = std::max(per_sm, 1);
+    const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * per_sm, hubs);
+    kern<<<grid, C3_THREADS, dyn, st>>>(a);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
+    return GS_OK;
+}
+
+static C3Args count3_args(gs_graph_t g, uint64_t *hist_dev)
+{
+    C3Args a{};
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.nb = g->nb;
+    a.ncfg = (int)gs_ncfg3(g->nb);
+    a.ghist = (unsigned long long *)hist_dev;
+    a.cursor = g->work;
+    a.cfg3 = g->cfg3;
+    a.inv = g->inv;
+    return a;
+}
+
 extern "C" gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int64_t hub_end,
                                    void *cuda_stream)
 {
@@ -306,34 +348,50 @@ extern "C" gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub
     GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * ncfg, st));
     if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
     GS_TRY_CUDA(cudaMemsetAsync(g->work, 0, sizeof(unsigned long long), st));
-
-    C3Args a;
-    a.row_ptr = g->row_ptr;
-    a.fwd = g->fwd;
-    a.nbr = g->nbr;
-    a.bin = g->bin;
+    C3Args a = count3_args(g, hist_dev);
     a.hub_begin = hub_begin;
     a.hub_end = hub_end;
-    a.nb = g->nb;
-    a.ncfg = ncfg;
-    a.ghist = (unsigned long long *)hist_dev;
-    a.cursor = g->work;
-    a.cfg3 = g->cfg3;
+    return launch_count3(g, a, hub_end - hub_begin, st);
+}
 
-    // shared-memory histogram unless it is too large or a chunk's hit bound
-    // (spokes x chunk) could overflow a 32-bit counter
-    const bool smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
-    const size_t dyn = (sizeof(int32_t) + 1) * C3_TABLE +
-                       (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * g->nb * g->nb : 0);
-    auto kern = smem ? k_count3<true> : k_count3<false>;
-    int per_sm = 0;
-    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
-    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C3_THREADS, dyn));
-    per_sm = std::max(per_sm, 1);
-    const int64_t hubs = hub_end - hub_begin;
-    const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * per_sm, hubs);
-    kern<<<grid, C3_THREADS, dyn, st>>>(a);
+// Range check of a device list of input indices, one flag word for the host.
+__global__ void k_check_ids(const int32_t *__restrict__ ids, int64_t count, int64_t n, int32_t *__restrict__ err)
+{
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < count;
+         t += (int64_t)gridDim.x * blockDim.x)
+        if (ids[t] < 0 || ids[t] >= n) atomicOr(err, 1);
+}
+
+gs_status gs_check_ids(gs_graph_t g, const int32_t *ids, int64_t count, cudaStream_t st)
+{
+    if (count == 0) return GS_OK;
+    GS_TRY_CUDA(cudaMemsetAsync(g->err, 0, sizeof(int32_t), st));
+    const int grid = (int)std::min<int64_t>((count + 255) / 256, (int64_t)gs_sm_count() * 4);
+    k_check_ids<<<grid, 256, 0, st>>>(ids, count, g->n, g->err);
     gs_note_launch();
-    GS_TRY_CUDA(cudaGetLastError());
+    int32_t h = 0;
+    GS_TRY_CUDA(cudaMemcpyAsync(&h, g->err, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    GS_TRY_CUDA(cudaStreamSynchronize(st));
+    if (h) return gs_set_error(GS_ERR_ARG, "a hub index lies outside [0, n)");
     return GS_OK;
+}
+
+extern "C" gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
+                                        uint64_t *hist_dev, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !hist_dev || (count > 0 && !hubs_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (count < 0) return gs_set_error(GS_ERR_ARG, "negative hub count");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    gs_status s = gs_check_ids(g, hubs_dev, count, st);
+    if (s != GS_OK) return s;
+    const int ncfg = (int)gs_ncfg3(g->nb);
+    GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * ncfg, st));
+    if (count == 0 || g->n_edges == 0) return GS_OK;
+    GS_TRY_CUDA(cudaMemsetAsync(g->work, 0, sizeof(unsigned long long), st));
+    C3Args a = count3_args(g, hist_dev);
+    a.hub_begin = 0;
+    a.hub_end = count;
+    a.hubs = hubs_dev;
+    return launch_count3(g, a, count, st);
 }

@@ -48,6 +48,9 @@ struct C4Args {
     unsigned long long *even;
     long long *odd;
     unsigned long long *cursor;
+    // hub-list mode: hubs [0, hub_end) of this list, given by input index
+    const int32_t *hubs;
+    const int32_t *inv;
     // large-hub path
     int big_m;                    // largest degree the scratch slices hold
     char *scratch;                // gridDim.x slices of scratch_stride bytes
@@ -184,7 +187,7 @@ __device__ __forceinline__ void c4_flush(unsigned *se, int *so, int ncfg, unsign
 
 // Hubs of degree 3..C4_M, workspace in shared memory; histograms in shared
 // memory too unless there are too many configurations.
-template <bool SMEM_HIST>
+template <bool SMEM_HIST, bool HUB_LIST>
 __global__ void __launch_bounds__(C4_THREADS)
 k_count4_small(C4Args a)
 {
@@ -215,8 +218,8 @@ k_count4_small(C4Args a)
         __syncthreads();
         if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
         __syncthreads();
-        const long long i = s_hub;
-        if (i >= a.hub_end) break;
+        if (s_hub >= a.hub_end) break;
+        const long long i = HUB_LIST ? (long long)a.inv[a.hubs[s_hub]] : s_hub;
         const int m = (int)(a.row_ptr[i + 1] - a.row_ptr[i]);
         if (m < 3 || m > C4_M) continue;
         if (SMEM_HIST) {
@@ -242,6 +245,7 @@ k_count4_small(C4Args a)
 
 // Hubs of degree > C4_M: workspace in a global scratch slice per block,
 // histograms added straight to global memory.
+template <bool HUB_LIST>
 __global__ void __launch_bounds__(C4_THREADS)
 k_count4_large(C4Args a)
 {
@@ -269,8 +273,8 @@ k_count4_large(C4Args a)
         __syncthreads();
         if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
         __syncthreads();
-        const long long i = s_hub;
-        if (i >= a.hub_end) break;
+        if (s_hub >= a.hub_end) break;
+        const long long i = HUB_LIST ? (long long)a.inv[a.hubs[s_hub]] : s_hub;
         const int m = (int)(a.row_ptr[i + 1] - a.row_ptr[i]);
         if (m <= C4_M) continue;
         int tl = 4;
@@ -317,7 +321,7 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true> : k_count4_small<false>;
+    auto kern = smem ? k_count4_small<true, false> : k_count4_small<false, false>;
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -342,7 +346,78 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        k_count4_large<<<gl, C4_THREADS, 0, st>>>(a);
+        k_count4_large<false><<<gl, C4_THREADS, 0, st>>>(a);
+        gs_note_launch();
+        cudaError_t e = cudaGetLastError();
+        cudaFreeAsync(scratch, st);
+        if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    return GS_OK;
+}
+
+extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
+                                               uint64_t *even_dev, int64_t *odd_dev, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || (count > 0 && !hubs_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (count < 0) return gs_set_error(GS_ERR_ARG, "negative hub count");
+    if (g->edges[g->nb] >= (1ll << 20))
+        return gs_set_error(GS_ERR_ARG, "parity 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
+    const int64_t ncfg = gs_ncfg4(g->nb);
+    if (ncfg <= 0) return GS_OK;
+    if (!even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL histogram");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    gs_status s = gs_check_ids(g, hubs_dev, count, st);
+    if (s != GS_OK) return s;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
+    if (count == 0 || g->n_edges == 0) return GS_OK;
+    GS_TRY_CUDA(cudaMemsetAsync(g->work + 1, 0, 2 * sizeof(unsigned long long), st));
+
+    C4Args a{};
+    a.pts = g->pts;
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.hub_begin = 0;
+    a.hub_end = count;
+    a.hubs = hubs_dev;
+    a.inv = g->inv;
+    a.box = (int)g->box_lu;
+    a.periodic = g->periodic;
+    a.nb = g->nb;
+    a.ncfg = (int)ncfg;
+    a.even = (unsigned long long *)even_dev;
+    a.odd = (long long *)odd_dev;
+
+    const int sms = gs_sm_count();
+    const bool smem = ncfg <= C4_SMEM_HIST_MAX;
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
+    auto kern = smem ? k_count4_small<true, true> : k_count4_small<false, true>;
+    int per_sm = 0;
+    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
+    per_sm = std::max(per_sm, 1);
+    a.cursor = g->work + 1;
+    kern<<<(int)std::min<int64_t>((int64_t)sms * per_sm, count), C4_THREADS, dyn, st>>>(a);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
+    if (g->max_degree > C4_M) {
+        const int M = g->max_degree;
+        int tlog = 4;
+        while ((1 << tlog) < 2 * M) ++tlog;
+        const size_t WM = (size_t)(M + 31) / 32;
+        size_t stride = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM + M;
+        stride = (stride + 255) & ~(size_t)255;
+        const int gl = (int)std::min<int64_t>((int64_t)sms * 2, count);
+        char *scratch = nullptr;
+        GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
+        a.cursor = g->work + 2;
+        a.big_m = M;
+        a.scratch = scratch;
+        a.scratch_stride = stride;
+        k_count4_large<true><<<gl, C4_THREADS, 0, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
@@ -447,7 +522,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true> : k_count4_small<false>;
+    auto kern = smem ? k_count4_small<true, false> : k_count4_small<false, false>;
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -465,7 +540,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
         a.big_m = M;
         a.scratch = base + GS_C4_STATIC_HEAD;
         a.scratch_stride = stride;
-        k_count4_large<<<gl, C4_THREADS, 0, st>>>(a);
+        k_count4_large<false><<<gl, C4_THREADS, 0, st>>>(a);
         gs_note_launch();
         GS_TRY_CUDA(cudaGetLastError());
     }

@@ -63,6 +63,10 @@ void gs_note_launch();
 // allocation.
 constexpr int64_t GS_EDGE_PAD = 128;
 
+// GS_ERR_ARG unless every one of `count` device input indices lies in [0, n);
+// synchronises st.
+gs_status gs_check_ids(gs_graph_t g, const int32_t *ids, int64_t count, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int gs_sm_count();
 

@@ -137,6 +137,27 @@ gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_de
 gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
                                       int64_t hub_begin, int64_t hub_end, void *cuda_stream);
 
+/* Hub-and-spoke triangle counts of selected hubs (§II.2 literally: for hub
+ * i, every pair of neighbours j < k of i that are neighbours of each other).
+ * Each triangle incident to a listed hub is counted once for that hub, so a
+ * triangle is seen from each of its listed vertices (over all n hubs the
+ * result is 3 x gs_count_3pcf). Same kernel as gs_count_3pcf, with the
+ * whole hub row staged instead of its forward part.
+ *   hubs_dev   int32 [count], device, INPUT indices in [0, n); repeats count
+ *              again
+ *   hist_dev   uint64 [gs_config_count_3pcf(nbins)], device, overwritten
+ * Synchronises cuda_stream once (index check). Errors: GS_ERR_ARG (NULL,
+ * negative count, an index outside [0, n)), GS_ERR_CUDA. */
+gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
+                             uint64_t *hist_dev, void *cuda_stream);
+
+/* Parity-4pCF contribution of selected hubs (INPUT indices), as
+ * gs_count_4pcf_parity restricted to those hubs; the same kernels.
+ * Synchronises cuda_stream once (index check). Errors as gs_count_3pcf_hubs
+ * plus those of gs_count_4pcf_parity. */
+gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
+                                    uint64_t *even_dev, int64_t *odd_dev, void *cuda_stream);
+
 /* Sizes of a built graph (host outputs; any pointer may be NULL).
  *   n           number of points
  *   n_edges     directed edges, sum of degrees (= 2 x pairs)
@@ -176,6 +197,17 @@ uint64_t gs_kernel_launches(void);
  * Asynchronous on cuda_stream. Errors: GS_ERR_ARG, GS_ERR_NOMEM, GS_ERR_CUDA. */
 gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int32_t *nbr_dev,
                               uint8_t *bin_dev, void *cuda_stream);
+
+/* Selected rows in INPUT numbering, each sorted (Eq.(1)).
+ *   ids_dev     int32 [count], device, input indices in [0, n)
+ *   row_ptr_dev int64 [count+1], device: offsets of the output rows
+ *   nbr_dev     int32 [row_ptr_dev[count]] or NULL, device
+ *   bin_dev     uint8 [row_ptr_dev[count]], device (needed when nbr_dev is set)
+ * With nbr_dev NULL only row_ptr_dev is written, so a caller can size the
+ * row arrays first. Synchronises cuda_stream once (index check). */
+gs_status gs_graph_export_rows(gs_graph_t g, const int32_t *ids_dev, int64_t count,
+                               int64_t *row_ptr_dev, int32_t *nbr_dev, uint8_t *bin_dev,
+                               void *cuda_stream);
 
 /* Internal order: perm_dev int32 [n], device; perm_dev[p] = input index of
  * the point the graph numbers p (the hub order of the count calls). */

@@ -11,6 +11,8 @@ code with the CUDA library. Every function follows the GRAMSCI v2 paper
 - ``count_4pcf_parity``: even count and odd sum of sign(V), V from Eq.(3),
   with V == 0 giving odd weight 0 (§III.2).
 - ``brute3`` / ``brute4``: all triples / quadruples with no graph.
+- ``row``, ``count_3pcf_hubs``, ``count_4pcf_parity_hubs``: per point / per hub
+  results from brute-force rows, for sampled checks at full size.
 
 Parity pins: every function here is checked in ``tests/test_oracle_*.py``
 against hand-derived fixtures, closed forms, invariants and an independent
@@ -57,6 +59,7 @@ def _load():
         lib.oracle_3pcf_range.argtypes = cat + [_p, _p, _p, _i64, _i64, _p]
         lib.oracle_4pcf_parity_range.argtypes = cat + [_p, _p, _p, _i64, _i64, _p, _p]
         lib.oracle_4pcf_parity_hubs.argtypes = cat + [_p, _i64, _p, _p]
+        lib.oracle_3pcf_hubs.argtypes = cat + [_p, _i64, _p]
         lib.oracle_brute3.argtypes = cat + [_p]
         lib.oracle_brute4.argtypes = cat + [_p, _p]
         lib.oracle_nconfig3.argtypes = [_int]
@@ -168,6 +171,16 @@ def count_4pcf_parity(xyz, box_lu, periodic, edges_lu, g: Graph | None = None,
     lib.oracle_4pcf_parity_range(*cat, *gargs, int(hub_begin), int(hub_end),
                                  _ptr(even), _ptr(odd))
     return even[:m], odd[:m]
+
+
+def count_3pcf_hubs(xyz, box_lu, periodic, edges_lu, hubs) -> np.ndarray:
+    """Triangles incident to each listed hub (input numbering), summed; no graph."""
+    lib = _load()
+    xyz, edges, nb, cat = _cat(xyz, box_lu, periodic, edges_lu)
+    hubs = np.ascontiguousarray(np.asarray(hubs, dtype=np.int64))
+    hist = np.zeros(nconfig3(nb), dtype=np.uint64)
+    lib.oracle_3pcf_hubs(*cat, _ptr(hubs), len(hubs), _ptr(hist))
+    return hist
 
 
 def count_4pcf_parity_hubs(xyz, box_lu, periodic, edges_lu, hubs):

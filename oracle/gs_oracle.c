@@ -419,35 +419,118 @@ void oracle_4pcf_parity(const int32_t *xyz, int64_t n, int64_t box, int periodic
     oracle_4pcf_parity_range(xyz, n, box, periodic, edges, nb, row_ptr, nbr, bin, 0, n, even, odd);
 }
 
+/* Per-hub work with rows found by brute force over all points (no graph):
+ * for sampled checks at full size. Each thread keeps its own row buffer. */
+typedef struct {
+    cat_t c;
+    const int64_t *hubs;
+    const int32_t *t;       /* configuration table (3pCF: table3, 4pCF: table4) */
+    int64_t ncfg;
+    uint64_t *even;         /* [threads][ncfg] (3pCF: the histogram) */
+    int64_t *odd;           /* [threads][ncfg] (4pCF only) */
+    int32_t **row;          /* [threads][n] */
+    uint8_t **rb;           /* [threads][n] */
+} hubs_ctx_t;
+
+/* Every triangle {i, j, k} with j, k in N(i), j < k, (j, k) an edge: the
+ * hub-and-spoke loop of §II.2 without the forward restriction. */
+static void tri_listed_hub(void *vctx, int tid, int64_t h)
+{
+    hubs_ctx_t *x = (hubs_ctx_t *)vctx;
+    const cat_t *c = &x->c;
+    int64_t i = x->hubs[h];
+    int32_t *row = x->row[tid];
+    uint8_t *rb = x->rb[tid];
+    uint64_t *hist = x->even + (size_t)tid * (size_t)x->ncfg;
+    int nb = c->nb;
+    int64_t m = oracle_row(c->xyz, c->n, c->box, c->periodic, c->edges, nb, i, row, rb);
+    for (int64_t a = 0; a < m; ++a)
+        for (int64_t b = a + 1; b < m; ++b) {
+            int bjk = pair_bin(c, row[a], row[b]);
+            if (bjk < 0) continue;
+            int v[3] = { rb[a], rb[b], bjk };
+            sort3(v);
+            hist[x->t[((size_t)v[0] * nb + v[1]) * nb + v[2]]] += 1;
+        }
+}
+
+static void quad_listed_hub(void *vctx, int tid, int64_t h)
+{
+    hubs_ctx_t *x = (hubs_ctx_t *)vctx;
+    const cat_t *c = &x->c;
+    int64_t i = x->hubs[h];
+    int32_t *row = x->row[tid];
+    uint8_t *rb = x->rb[tid];
+    uint64_t *ev = x->even + (size_t)tid * (size_t)x->ncfg;
+    int64_t *od = x->odd + (size_t)tid * (size_t)x->ncfg;
+    int64_t m = oracle_row(c->xyz, c->n, c->box, c->periodic, c->edges, c->nb, i, row, rb);
+    for (int64_t a = 0; a < m; ++a)
+        for (int64_t b = a + 1; b < m; ++b) {
+            if (pair_bin(c, row[a], row[b]) < 0) continue;
+            for (int64_t d = b + 1; d < m; ++d) {
+                if (pair_bin(c, row[a], row[d]) < 0) continue;
+                if (pair_bin(c, row[b], row[d]) < 0) continue;
+                int64_t sp[3] = { row[a], row[b], row[d] };
+                int bb[3] = { rb[a], rb[b], rb[d] };
+                add_clique(c, x->t, ev, od, i, sp, bb);
+            }
+        }
+}
+
+static void run_listed(hubs_ctx_t *x, int64_t nh, hub_fn fn, int nt)
+{
+    size_t nn = (size_t)(x->c.n > 0 ? x->c.n : 1);
+    x->row = (int32_t **)malloc(sizeof(int32_t *) * (size_t)nt);
+    x->rb = (uint8_t **)malloc(sizeof(uint8_t *) * (size_t)nt);
+    for (int t = 0; t < nt; ++t) {
+        x->row[t] = (int32_t *)malloc(sizeof(int32_t) * nn);
+        x->rb[t] = (uint8_t *)malloc(nn);
+    }
+    parallel_for(0, nh, nt, fn, x);
+    for (int t = 0; t < nt; ++t) { free(x->row[t]); free(x->rb[t]); }
+    free(x->row); free(x->rb);
+}
+
+/* 3pCF triangles incident to each listed hub (input indices), summed. */
+void oracle_3pcf_hubs(const int32_t *xyz, int64_t n, int64_t box, int periodic,
+                      const int64_t *edges, int nb, const int64_t *hubs, int64_t nh, uint64_t *hist)
+{
+    int nt = oracle_threads();
+    hubs_ctx_t x;
+    memset(&x, 0, sizeof(x));
+    x.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    x.hubs = hubs;
+    x.t = table3(nb);
+    x.ncfg = oracle_nconfig3(nb);
+    x.even = (uint64_t *)calloc((size_t)nt * (size_t)x.ncfg, sizeof(uint64_t));
+    run_listed(&x, nh, tri_listed_hub, nt);
+    reduce_u64(hist, x.even, nt, x.ncfg);
+    free(x.even);
+    free((void *)x.t);
+}
+
 /* Parity-4pCF contribution of the listed hubs only, each row found by brute
  * force over all points (no graph needed: for sampled checks at full size). */
 void oracle_4pcf_parity_hubs(const int32_t *xyz, int64_t n, int64_t box, int periodic,
                              const int64_t *edges, int nb, const int64_t *hubs, int64_t nh,
                              uint64_t *even, int64_t *odd)
 {
-    cat_t c = { xyz, n, box, periodic, edges, nb };
-    int32_t *t4 = table4(nb < 3 ? 3 : nb);
     int64_t ncfg = oracle_nconfig4(nb);
-    memset(even, 0, sizeof(uint64_t) * (size_t)(ncfg > 0 ? ncfg : 0));
-    memset(odd, 0, sizeof(int64_t) * (size_t)(ncfg > 0 ? ncfg : 0));
-    int32_t *row = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
-    uint8_t *rb = (uint8_t *)malloc((size_t)(n > 0 ? n : 1));
-    for (int64_t h = 0; h < nh && ncfg > 0; ++h) {
-        int64_t i = hubs[h];
-        int64_t m = oracle_row(xyz, n, box, periodic, edges, nb, i, row, rb);
-        for (int64_t a = 0; a < m; ++a)
-            for (int64_t b = a + 1; b < m; ++b) {
-                if (pair_bin(&c, row[a], row[b]) < 0) continue;
-                for (int64_t d = b + 1; d < m; ++d) {
-                    if (pair_bin(&c, row[a], row[d]) < 0) continue;
-                    if (pair_bin(&c, row[b], row[d]) < 0) continue;
-                    int64_t s[3] = { row[a], row[b], row[d] };
-                    int bb[3] = { rb[a], rb[b], rb[d] };
-                    add_clique(&c, t4, even, odd, i, s, bb);
-                }
-            }
-    }
-    free(row); free(rb); free(t4);
+    if (ncfg <= 0) return;
+    int nt = oracle_threads();
+    hubs_ctx_t x;
+    memset(&x, 0, sizeof(x));
+    x.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    x.hubs = hubs;
+    x.t = table4(nb);
+    x.ncfg = ncfg;
+    x.even = (uint64_t *)calloc((size_t)nt * (size_t)ncfg, sizeof(uint64_t));
+    x.odd = (int64_t *)calloc((size_t)nt * (size_t)ncfg, sizeof(int64_t));
+    run_listed(&x, nh, quad_listed_hub, nt);
+    reduce_u64(even, x.even, nt, ncfg);
+    reduce_i64(odd, x.odd, nt, ncfg);
+    free(x.even); free(x.odd);
+    free((void *)x.t);
 }
 
 /* ------------------------------------------------------------------------ */

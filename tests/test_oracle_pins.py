@@ -302,3 +302,53 @@ def test_degenerate_inputs():
     h = oracle.count_3pcf(xyz, 1000, 0, [0, 50])
     assert h.tolist() == [1]
     assert oracle.nconfig4(1) == 0 and oracle.nconfig4(2) == 0
+
+
+# ---------------------------------------------------------------- per-hub (sampled) forms
+
+def _np_hub_triangles(xyz, box, periodic, edges, hubs):
+    nb = len(edges) - 1
+    B, _ = fx.np_bins(xyz, box, periodic, edges)
+    index = {c: n for n, c in enumerate(fx.configs3(nb))}
+    hist = np.zeros(len(index), dtype=np.uint64)
+    for h in hubs:
+        spokes = np.nonzero(B[h] >= 0)[0]
+        for j, k in itertools.combinations(spokes, 2):
+            if B[j, k] >= 0:
+                hist[index[tuple(sorted((int(B[h, j]), int(B[h, k]), int(B[j, k]))))]] += 1
+    return hist
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+def test_3pcf_hubs_against_numpy_and_trace(periodic):
+    box = 16000
+    xyz = catalogues.neyman_scott(120, box / 1024, 6, 20.0, 1.5, 71 + periodic)
+    edges = [0, 700, 1500, 2600, 4000]
+    hubs = [0, 5, 5, 17, 119, 64]
+    assert np.array_equal(oracle.count_3pcf_hubs(xyz, box, periodic, edges, hubs),
+                          _np_hub_triangles(xyz, box, periodic, edges, hubs))
+    # over all hubs every triangle is seen from each of its three vertices
+    allh = oracle.count_3pcf_hubs(xyz, box, periodic, edges, np.arange(len(xyz)))
+    assert np.array_equal(allh, 3 * oracle.count_3pcf(xyz, box, periodic, edges))
+
+
+def test_3pcf_hubs_fixture():
+    f = next(x for x in fx.triangle_fixtures() if x["name"] == "A")
+    nb = len(f["edges"]) - 1
+    h = oracle.count_3pcf_hubs(f["points"], f["box"], f["periodic"], f["edges"], np.arange(len(f["points"])))
+    cfg = fx.configs3(nb)
+    assert {cfg[k]: int(v) for k, v in enumerate(h) if v} == {c: 3 * n for c, n in f["expect"].items()}
+
+
+def test_rows_and_parity_hubs_match_graph():
+    box = 30000
+    xyz = catalogues.neyman_scott(400, box / 1024, 8, 50.0, 1.5, 91)
+    edges = catalogues.linear_edges_lu(5.0, 6)
+    g = oracle.graph(xyz, box, 1, edges)
+    for i in (0, 3, 399, 200):
+        nbr, b = oracle.row(xyz, box, 1, edges, i)
+        assert np.array_equal(nbr, g.nbr[g.row_ptr[i]:g.row_ptr[i + 1]])
+        assert np.array_equal(b, g.bin[g.row_ptr[i]:g.row_ptr[i + 1]])
+    e1, o1 = oracle.count_4pcf_parity_hubs(xyz, box, 1, edges, [7, 8, 9])
+    e2, o2 = oracle.count_4pcf_parity(xyz, box, 1, edges, g, 7, 10)
+    assert np.array_equal(e1, e2) and np.array_equal(o1, o2)
