@@ -62,8 +62,10 @@ class GramsciError(RuntimeError):
 
 
 def lib_path() -> str:
+    """The in-tree build, or the file named by GRAMSCI_GB_LIBRARY (another build
+    of the same sources, e.g. a debug build)."""
     from . import build as _build
-    return _build.LIB
+    return os.environ.get("GRAMSCI_GB_LIBRARY") or _build.LIB
 
 
 def load(build_if_missing: bool = False):

@@ -560,6 +560,7 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));
         GS_BUILD_CUDA(cudaMalloc(&g->bin, ne));
         GS_BUILD_CUDA(cudaMemsetAsync(g->nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD, st));
+        GS_BUILD_CUDA(cudaMemsetAsync(g->bin + g->n_edges, 0, GS_EDGE_PAD, st));
         if (n > 0 && g->n_edges > 0) {
             k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
                 g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,

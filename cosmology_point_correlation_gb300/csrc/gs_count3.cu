@@ -36,6 +36,12 @@ constexpr int C3_TABLE_LOG = 13;                 // 8192 slots
 constexpr int C3_TABLE = 1 << C3_TABLE_LOG;
 constexpr int C3_CHUNK = C3_TABLE / 4;           // load factor <= 1/4: short probe chains
 constexpr int C3_SPOKES = 4096;                  // spokes grouped per pass
+constexpr int C3_SPAN_BITS = 1 << 18;            // bitmap mode: key span of a chunk
+constexpr int C3_SPAN_PAIRS = C3_SPAN_BITS / 64;
+// bytes of the candidate-key region: the larger of the two modes
+constexpr int C3_REGION_BITMAP = C3_SPAN_PAIRS * (8 + 2) + C3_TABLE / 4;
+constexpr int C3_REGION_HASH = C3_TABLE * 5;
+constexpr int C3_REGION = ((C3_REGION_BITMAP > C3_REGION_HASH ? C3_REGION_BITMAP : C3_REGION_HASH) + 15) & ~15;
 constexpr int C3_SMEM_HIST_MAX = 12288;          // configurations kept in shared memory (nbins <= 40)
 constexpr int C3_EMPTY = -1;
 
@@ -89,26 +95,60 @@ __device__ __forceinline__ void c3_fill_tab(uint16_t *tab, const uint16_t *cfg3,
     __syncwarp();
 }
 
+// Exclusive block-wide scan of one int per thread (C3_THREADS threads).
+__device__ __forceinline__ int c3_block_scan(int v, int *s_warp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < C3_WARPS ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < C3_WARPS) s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int r = (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
+    __syncthreads();
+    return r;
+}
+
 template <bool SMEM_HIST, bool HUB_LIST>
 __global__ void __launch_bounds__(C3_THREADS, 2)
 k_count3(C3Args a)
 {
-    // dynamic: hash keys [C3_TABLE] i32, their bins [C3_TABLE] u8, then (SMEM_HIST
-    // only) the histogram [ncfg] u32 and one nb x nb u16 table per warp
+    // dynamic: the candidate-key region [C3_REGION bytes] (bitmap mode: bitmap,
+    // per-pair ranks, chunk bins; hash mode: keys, bins), then (SMEM_HIST only)
+    // the histogram [ncfg] u32 and one nb x nb u16 table per warp
     extern __shared__ unsigned s_dyn[];
     __shared__ uint16_t s_order[C3_SPOKES];         // spoke positions grouped by b_ij
     __shared__ int s_next;                          // next entry of s_order to hand out
     __shared__ int s_bucket[257];
     __shared__ int s_lex_a[256];
     __shared__ int s_lex_b[256];
+    __shared__ int s_warp[C3_WARPS];
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;        // bound on hits since the last flush
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nb = a.nb;
+    // bitmap mode
+    uint2 *s_bm = (uint2 *)s_dyn;                                     // [C3_SPAN_PAIRS] bits
+    uint16_t *s_rank = (uint16_t *)(s_bm + C3_SPAN_PAIRS);            // [C3_SPAN_PAIRS] bits before the pair
+    uint8_t *s_cbin = (uint8_t *)(s_rank + C3_SPAN_PAIRS);            // [C3_CHUNK] bins in key order
+    // hash mode
     int32_t *s_key = (int32_t *)s_dyn;
     uint8_t *s_bin = (uint8_t *)(s_key + C3_TABLE);
-    unsigned *s_hist = (unsigned *)(s_bin + C3_TABLE);
+    unsigned *s_hist = (unsigned *)((char *)s_dyn + C3_REGION);
     uint16_t *tab = (uint16_t *)(s_hist + ((a.ncfg + 3) & ~3)) + warp * nb * nb;
     int tab_z = -1;
 
@@ -121,7 +161,6 @@ k_count3(C3Args a)
     }
     if (SMEM_HIST)
         for (int t = threadIdx.x; t < a.ncfg; t += C3_THREADS) s_hist[t] = 0;
-    for (int t = threadIdx.x; t < C3_TABLE; t += C3_THREADS) s_key[t] = C3_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
     __syncthreads();
 
@@ -138,7 +177,12 @@ k_count3(C3Args a)
             const int c1 = min(f, c0 + C3_CHUNK);
             const int cn = c1 - c0;
             if (c1 < 2) break;                               // a lone key closes nothing
-            int lg = 6;                                      // table of 2^lg >= 4 cn slots
+            const int32_t kmax = a.nbr[f0 + c1 - 1];
+            const int32_t kfirst = a.nbr[f0 + c0];
+            const int64_t span64 = (int64_t)kmax - kfirst + 1;
+            const bool bmode = span64 <= C3_SPAN_BITS;       // block-uniform
+            const int span = (int)(span64 < C3_SPAN_BITS ? span64 : C3_SPAN_BITS);
+            int lg = 6;                                      // hash mode: 2^lg >= 4 cn slots
             while ((1 << lg) < 4 * cn) ++lg;
             const int tsize = 1 << lg, shift = 32 - lg, mask = tsize - 1;
 
@@ -155,21 +199,44 @@ k_count3(C3Args a)
                 __syncthreads();
                 if (threadIdx.x == 0) s_pending += bound;
             }
-            for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
-                const int32_t k = a.nbr[f0 + c0 + t];
-                uint32_t h = gs_hash(k, shift);
-                while (atomicCAS(&s_key[h], C3_EMPTY, k) != C3_EMPTY) h = (h + 1) & mask;
-                s_bin[h] = a.bin[f0 + c0 + t];
+            if (bmode) {
+                // exact bitmap of the chunk's keys over [kfirst, kmax], the rank of
+                // every 64-bit pair, and the chunk's bins in key order
+                const int npairs = (span + 63) >> 6;
+                for (int t = threadIdx.x; t < npairs; t += C3_THREADS) s_bm[t] = make_uint2(0u, 0u);
+                __syncthreads();
+                for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
+                    const int off = a.nbr[f0 + c0 + t] - kfirst;
+                    atomicOr(reinterpret_cast<unsigned *>(s_bm) + (off >> 5), 1u << (off & 31));
+                    s_cbin[t] = a.bin[f0 + c0 + t];
+                }
+                __syncthreads();
+                const int per = (npairs + C3_THREADS - 1) / C3_THREADS;
+                const int q0 = threadIdx.x * per;
+                int cnt = 0;
+                for (int q = q0; q < min(npairs, q0 + per); ++q) cnt += __popc(s_bm[q].x) + __popc(s_bm[q].y);
+                int run = c3_block_scan(cnt, s_warp);
+                for (int q = q0; q < min(npairs, q0 + per); ++q) {
+                    s_rank[q] = (uint16_t)run;
+                    run += __popc(s_bm[q].x) + __popc(s_bm[q].y);
+                }
+            } else {
+                for (int t = threadIdx.x; t < tsize; t += C3_THREADS) s_key[t] = C3_EMPTY;
+                __syncthreads();
+                for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
+                    const int32_t k = a.nbr[f0 + c0 + t];
+                    uint32_t h = gs_hash(k, shift);
+                    while (atomicCAS(&s_key[h], C3_EMPTY, k) != C3_EMPTY) h = (h + 1) & mask;
+                    s_bin[h] = a.bin[f0 + c0 + t];
+                }
             }
-            const int32_t kmax = a.nbr[f0 + c1 - 1];
-            const int32_t kfirst = a.nbr[f0 + c0];
 
             // spokes s in [sb, se) of [0, c1 - 1), at most C3_SPOKES at a time
             for (int sb = 0; sb < c1 - 1; sb += C3_SPOKES) {
                 const int se = min(c1 - 1, sb + C3_SPOKES);
                 const int ns = se - sb;
-                // counting sort of the spokes by b_ij, so that each warp's run of
-                // the list needs few rebuilds of its configuration table
+                // counting sort of the spokes by b_ij, so that a warp's spokes
+                // share their bin and its configuration table changes rarely
                 for (int t = threadIdx.x; t <= nb; t += C3_THREADS) s_bucket[t] = 0;
                 __syncthreads();
                 for (int t = threadIdx.x; t < ns; t += C3_THREADS) atomicAdd(&s_bucket[a.bin[f0 + sb + t] + 1], 1);
@@ -193,10 +260,9 @@ k_count3(C3Args a)
                     const int b = a.bin[f0 + sb + t];
                     s_order[atomicAdd(&s_bucket[b], 1)] = (uint16_t)t;
                 }
-                __syncthreads();
-
                 if (threadIdx.x == 0) s_next = 0;
                 __syncthreads();
+
                 for (;;) {
                     int li = 0;
                     if (lane == 0) li = atomicAdd(&s_next, 1);
@@ -223,6 +289,11 @@ k_count3(C3Args a)
                         p0 = lo;
                     }
                     if (p0 >= pe) continue;
+                    // one triangle with sides (b_ij, b_ik, b_jk)
+                    auto hit = [&](int bik, int bjk) {
+                        if (SMEM_HIST) atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
+                        else atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
+                    };
                     // Walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
                     // 4l .. 4l+3 of the step as one int4 and their bins as one word.
                     const int64_t pa = p0 & ~(int64_t)3;
@@ -248,36 +319,43 @@ k_count3(C3Args a)
                             if (total - r0 < 4) vmask &= (1u << max(total - r0, 0)) - 1u;
                         }
                         const int k[4] = { kk.x, kk.y, kk.z, kk.w };
-                        uint32_t h[4];
-                        int32_t key[4];
-                        unsigned pend = 0;
+                        if (bmode) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {              // first probes, all in flight
-                            h[e] = gs_hash(k[e], shift);
-                            key[e] = s_key[h[e]];
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) pend |= (unsigned)(key[e] != k[e] && key[e] != C3_EMPTY) << e;
-                        while (pend) {                             // collisions (rare at load <= 1/4)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if ((pend >> e) & 1u) {
-                                    h[e] = (h[e] + 1) & mask;
-                                    key[e] = s_key[h[e]];
-                                    if (key[e] == k[e] || key[e] == C3_EMPTY) pend &= ~(1u << e);
-                                }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (((vmask >> e) & 1u) && key[e] == k[e]) {
-                                const int bik = s_bin[h[e]];
-                                const int bjk = (bb >> (8 * e)) & 0xffu;
-                                if (SMEM_HIST) {
-                                    atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
-                                } else {
-                                    atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
+                            for (int e = 0; e < 4; ++e) {
+                                const unsigned off = (unsigned)(k[e] - kfirst);
+                                const bool in = off < (unsigned)span;
+                                const unsigned o = in ? off : 0u;
+                                const uint2 pr = s_bm[o >> 6];
+                                const unsigned w = (o & 32u) ? pr.y : pr.x;
+                                if (in && ((vmask >> e) & 1u) && ((w >> (o & 31u)) & 1u)) {
+                                    const int rank = s_rank[o >> 6] + ((o & 32u) ? __popc(pr.x) : 0) +
+                                                     __popc(w & ((1u << (o & 31u)) - 1u));
+                                    hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu);
                                 }
                             }
+                        } else {
+                            uint32_t h[4];
+                            int32_t key[4];
+                            unsigned pend = 0;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {          // first probes, all in flight
+                                h[e] = gs_hash(k[e], shift);
+                                key[e] = s_key[h[e]];
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) pend |= (unsigned)(key[e] != k[e] && key[e] != C3_EMPTY) << e;
+                            while (pend) {                         // collisions
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if ((pend >> e) & 1u) {
+                                        h[e] = (h[e] + 1) & mask;
+                                        key[e] = s_key[h[e]];
+                                        if (key[e] == k[e] || key[e] == C3_EMPTY) pend &= ~(1u << e);
+                                    }
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (((vmask >> e) & 1u) && key[e] == k[e]) hit(s_bin[h[e]], (bb >> (8 * e)) & 0xffu);
                         }
                         // rows are sorted: stop once the step's last key passes kmax
                         if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
@@ -287,8 +365,6 @@ k_count3(C3Args a)
                 }
                 __syncthreads();
             }
-            for (int t = threadIdx.x; t < tsize; t += C3_THREADS) s_key[t] = C3_EMPTY;
-            __syncthreads();
         }
     }
     if (SMEM_HIST) {
@@ -303,7 +379,7 @@ static gs_status launch_count3(gs_graph_t g, C3Args &a, int64_t hubs, cudaStream
     // shared-memory histogram unless it is too large or a chunk's hit bound
     // (spokes x chunk) could overflow a 32-bit counter
     const bool smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
-    const size_t dyn = (sizeof(int32_t) + 1) * C3_TABLE +
+    const size_t dyn = C3_REGION +
                        (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * g->nb * g->nb : 0);
     const bool list = a.hubs != nullptr;
     auto kern = smem ? (list ? k_count3<true, true> : k_count3<true, false>)
