@@ -25,7 +25,8 @@ from ._lib import GramsciError
 
 __all__ = ["Graph", "GramsciError", "build_graph", "count_3pcf_from_host",
            "count_4pcf_parity_from_host", "config_count_3pcf", "config_count_4pcf",
-           "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path", "kernel_launches"]
+           "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path", "kernel_launches",
+           "equilateral", "isosceles", "xi_natural"]
 
 
 def library_path() -> str:
@@ -109,6 +110,14 @@ class Graph:
         return {name: getattr(st, name) for name, _ in _lib.GraphStats._fields_ if name != "reserved"}
 
     # -- counts
+    def count_2pcf(self, out=None, stream=None):
+        """Unordered pairs per radial bin (uint64 bits in an int64 tensor)."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty(self.nbins, dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_count_2pcf(self._h, ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+        return out
+
     def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
         """uint64 triangle histogram over sorted bin triples (int64 tensor on the device)."""
         torch = _torch()
@@ -212,6 +221,29 @@ class Graph:
 
     def __exit__(self, *exc):
         self.free()
+
+
+def equilateral(hist, nbins: int):
+    """The equilateral slice of a 3pCF histogram: configurations (b, b, b), b = 0..nbins-1."""
+    h = np.asarray(hist)
+    return h[[config_index_3pcf(nbins, b, b, b) for b in range(nbins)]]
+
+
+def isosceles(hist, nbins: int, b: int):
+    """Configurations with two sides in bin b: entry c is the sorted triple of (b, b, c)."""
+    h = np.asarray(hist)
+    return h[[config_index_3pcf(nbins, *sorted((b, b, c))) for c in range(nbins)]]
+
+
+def xi_natural(dd, rr, n_data: int, n_random: int):
+    """Natural-estimator 2pCF per bin from data and random pair counts:
+    xi = (DD / C(n_data, 2)) / (RR / C(n_random, 2)) - 1."""
+    dd = np.asarray(dd, dtype=np.float64)
+    rr = np.asarray(rr, dtype=np.float64)
+    nd = n_data * (n_data - 1) / 2.0
+    nr = n_random * (n_random - 1) / 2.0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return (dd / nd) / (rr / nr) - 1.0
 
 
 def _ids(ids, device):

@@ -158,6 +158,13 @@ gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t coun
 gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
                                     uint64_t *even_dev, int64_t *odd_dev, void *cuda_stream);
 
+/* Internal 2pCF pair counts: the number of unordered pairs {i, j} in each
+ * radial bin, from one sweep of the graph's bin bytes (§III.3: the two-point
+ * function on the same graph and binning as the higher-order counts).
+ *   hist_dev   uint64 [nbins], device, overwritten
+ * Asynchronous. Errors: GS_ERR_ARG (NULL), GS_ERR_CUDA. */
+gs_status gs_count_2pcf(gs_graph_t g, uint64_t *hist_dev, void *cuda_stream);
+
 /* Sizes of a built graph (host outputs; any pointer may be NULL).
  *   n           number of points
  *   n_edges     directed edges, sum of degrees (= 2 x pairs)

@@ -11,6 +11,10 @@ code with the CUDA library. Every function follows the GRAMSCI v2 paper
 - ``count_4pcf_parity``: even count and odd sum of sign(V), V from Eq.(3),
   with V == 0 giving odd weight 0 (§III.2).
 - ``brute3`` / ``brute4``: all triples / quadruples with no graph.
+- ``count_4pcf6`` / ``brute4six``: six-edge-bin 4pCF (each tetrahedron once, its
+  configuration the smallest bin tuple over vertex orderings, odd channel the
+  sign of V for a minimal ordering of a chiral configuration; §II.2, §III.2,
+  276 configurations for 4 bins as in §V.2).
 - ``row``, ``count_3pcf_hubs``, ``count_4pcf_parity_hubs``: per point / per hub
   results from brute-force rows, for sampled checks at full size.
 
@@ -60,6 +64,12 @@ def _load():
         lib.oracle_4pcf_parity_range.argtypes = cat + [_p, _p, _p, _i64, _i64, _p, _p]
         lib.oracle_4pcf_parity_hubs.argtypes = cat + [_p, _i64, _p, _p]
         lib.oracle_3pcf_hubs.argtypes = cat + [_p, _i64, _p]
+        lib.oracle_4pcf6.argtypes = cat + [_p, _p, _i64, _i64, _p, _p]
+        lib.oracle_brute4six.argtypes = cat + [_p, _p]
+        lib.oracle_nconfig6.argtypes = [_int]
+        lib.oracle_nconfig6.restype = _i64
+        lib.oracle_config_index6.argtypes = [_int, _p]
+        lib.oracle_config_index6.restype = _i64
         lib.oracle_brute3.argtypes = cat + [_p]
         lib.oracle_brute4.argtypes = cat + [_p, _p]
         lib.oracle_nconfig3.argtypes = [_int]
@@ -171,6 +181,52 @@ def count_4pcf_parity(xyz, box_lu, periodic, edges_lu, g: Graph | None = None,
     lib.oracle_4pcf_parity_range(*cat, *gargs, int(hub_begin), int(hub_end),
                                  _ptr(even), _ptr(odd))
     return even[:m], odd[:m]
+
+
+def count_2pcf(xyz, box_lu, periodic, edges_lu, g: Graph | None = None) -> np.ndarray:
+    """Unordered pairs per radial bin: each pair sits in two rows of the graph."""
+    xyz, edges, nb, _ = _cat(xyz, box_lu, periodic, edges_lu)
+    if g is None:
+        g = graph(xyz, box_lu, periodic, edges)
+    return (np.bincount(g.bin, minlength=nb) // 2).astype(np.uint64)
+
+
+def nconfig6(nb: int) -> int:
+    """Six-edge-bin tetrahedron configurations for nb bins (by enumeration)."""
+    return _load().oracle_nconfig6(nb)
+
+
+def config_index6(nb: int, t) -> int:
+    """Index of a canonical tuple (b01, b02, b03, b12, b13, b23); -1 if not canonical."""
+    a = np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+    return _load().oracle_config_index6(nb, _ptr(a))
+
+
+def count_4pcf6(xyz, box_lu, periodic, edges_lu, g: Graph | None = None,
+                hub_begin: int = 0, hub_end: int | None = None):
+    """Six-edge-bin 4pCF: (even, odd) per configuration, each tetrahedron once
+    (at its lowest-index vertex; hub range in input numbering)."""
+    lib = _load()
+    xyz, edges, nb, cat = _cat(xyz, box_lu, periodic, edges_lu)
+    if g is None:
+        g = graph(xyz, box_lu, periodic, edges)
+    hub_end = len(xyz) if hub_end is None else hub_end
+    m = nconfig6(nb)
+    even = np.zeros(m, dtype=np.uint64)
+    odd = np.zeros(m, dtype=np.int64)
+    nbr = g.nbr if len(g.nbr) else np.zeros(1, dtype=np.int32)
+    lib.oracle_4pcf6(*cat, _ptr(g.row_ptr), _ptr(nbr), int(hub_begin), int(hub_end), _ptr(even), _ptr(odd))
+    return even, odd
+
+
+def brute4six(xyz, box_lu, periodic, edges_lu):
+    lib = _load()
+    xyz, edges, nb, cat = _cat(xyz, box_lu, periodic, edges_lu)
+    m = nconfig6(nb)
+    even = np.zeros(m, dtype=np.uint64)
+    odd = np.zeros(m, dtype=np.int64)
+    lib.oracle_brute4six(*cat, _ptr(even), _ptr(odd))
+    return even, odd
 
 
 def count_3pcf_hubs(xyz, box_lu, periodic, edges_lu, hubs) -> np.ndarray:

@@ -622,3 +622,241 @@ void oracle_brute4(const int32_t *xyz, int64_t n, int64_t box, int periodic,
     free(b.hist); free(b.odd);
     free((void *)b.t);
 }
+
+/* ------------------------------------------------------------------------ */
+/* six-edge-bin 4pCF with parity channels                                    */
+/*
+ * A tetrahedron is four points whose six pairs are all edges; each counts
+ * once. Its configuration is the lexicographically smallest tuple
+ * (b01, b02, b03, b12, b13, b23) over the 24 orderings (v0, v1, v2, v3) of its
+ * vertices, where b_ab is the bin of the pair (v_a, v_b); configurations are
+ * numbered in lexicographic order of their smallest tuples. The odd channel
+ * adds sign(V) with V = det[x_v1 - x_v0; x_v2 - x_v0; x_v3 - x_v0] for an
+ * ordering that reaches the smallest tuple -- and 0 when orderings of both
+ * permutation parities reach it (an achiral configuration: the sign would
+ * depend on labels) or when V = 0. (GRAMSCI v2 §II.2 tetrahedra, §III.2
+ * Eq.(3); 276 configurations for 4 bins, §V.2.)
+ */
+
+/* the 24 orderings of (0,1,2,3) and their parities, generated by swaps */
+static int g_perm[24][4];
+static int g_perm_par[24];
+static int g_perm_ready = 0;
+
+static void make_perms(void)
+{
+    if (g_perm_ready) return;
+    int c = 0;
+    for (int a = 0; a < 4; ++a)
+        for (int b = 0; b < 4; ++b)
+            for (int d = 0; d < 4; ++d)
+                for (int e = 0; e < 4; ++e) {
+                    if (a == b || a == d || a == e || b == d || b == e || d == e) continue;
+                    int p[4] = { a, b, d, e };
+                    int inv = 0;
+                    for (int x = 0; x < 4; ++x)
+                        for (int y = x + 1; y < 4; ++y) inv += p[x] > p[y];
+                    for (int x = 0; x < 4; ++x) g_perm[c][x] = p[x];
+                    g_perm_par[c] = inv & 1;
+                    ++c;
+                }
+    g_perm_ready = 1;
+}
+
+/* bins of the six pairs of an ordered 4-tuple of points */
+static int tuple_of(const int bm[4][4], const int *o, int t[6])
+{
+    t[0] = bm[o[0]][o[1]]; t[1] = bm[o[0]][o[2]]; t[2] = bm[o[0]][o[3]];
+    t[3] = bm[o[1]][o[2]]; t[4] = bm[o[1]][o[3]]; t[5] = bm[o[2]][o[3]];
+    return 0;
+}
+
+static int cmp6(const int *a, const int *b)
+{
+    for (int k = 0; k < 6; ++k) {
+        if (a[k] < b[k]) return -1;
+        if (a[k] > b[k]) return 1;
+    }
+    return 0;
+}
+
+/* smallest tuple over all orderings; *par = parity of a minimal ordering
+ * relative to (0,1,2,3), *chiral = 0 if minimal orderings of both parities
+ * exist; best_order receives one minimal ordering */
+static void canonical(const int bm[4][4], int best[6], int *chiral, int best_order[4])
+{
+    make_perms();
+    int seen_even = 0, seen_odd = 0;
+    int have = 0;
+    for (int q = 0; q < 24; ++q) {
+        int t[6];
+        tuple_of(bm, g_perm[q], t);
+        int c = have ? cmp6(t, best) : -1;
+        if (c < 0) {
+            memcpy(best, t, sizeof(t));
+            for (int x = 0; x < 4; ++x) best_order[x] = g_perm[q][x];
+            seen_even = !g_perm_par[q];
+            seen_odd = g_perm_par[q];
+            have = 1;
+        } else if (c == 0) {
+            if (g_perm_par[q]) seen_odd = 1; else seen_even = 1;
+        }
+    }
+    *chiral = !(seen_even && seen_odd);
+}
+
+/* number of configurations for nb bins, and the index of a canonical tuple:
+ * rank among all canonical tuples in lexicographic order (by enumeration) */
+static int64_t six_count_and_index(int nb, const int *want)
+{
+    int64_t rank = 0;
+    int t[6];
+    for (t[0] = 0; t[0] < nb; ++t[0])
+    for (t[1] = 0; t[1] < nb; ++t[1])
+    for (t[2] = 0; t[2] < nb; ++t[2])
+    for (t[3] = 0; t[3] < nb; ++t[3])
+    for (t[4] = 0; t[4] < nb; ++t[4])
+    for (t[5] = 0; t[5] < nb; ++t[5]) {
+        /* is t its own smallest relabelling? rebuild the pair matrix */
+        int bm[4][4];
+        bm[0][1] = bm[1][0] = t[0]; bm[0][2] = bm[2][0] = t[1]; bm[0][3] = bm[3][0] = t[2];
+        bm[1][2] = bm[2][1] = t[3]; bm[1][3] = bm[3][1] = t[4]; bm[2][3] = bm[3][2] = t[5];
+        int best[6], ch, ord[4];
+        canonical(bm, best, &ch, ord);
+        if (cmp6(best, t) != 0) continue;
+        if (want && cmp6(want, t) == 0) return rank;
+        ++rank;
+    }
+    return want ? -1 : rank;
+}
+
+int64_t oracle_nconfig6(int nb) { return six_count_and_index(nb, NULL); }
+
+/* Dense table: configuration index of every canonical tuple, by packed tuple. */
+static int32_t *six_index_table(int nb)
+{
+    size_t nt = 1;
+    for (int k = 0; k < 6; ++k) nt *= (size_t)nb;
+    int32_t *tab = (int32_t *)malloc(sizeof(int32_t) * nt);
+    for (size_t x = 0; x < nt; ++x) tab[x] = -1;
+    int32_t rank = 0;
+    int t[6];
+    for (t[0] = 0; t[0] < nb; ++t[0])
+    for (t[1] = 0; t[1] < nb; ++t[1])
+    for (t[2] = 0; t[2] < nb; ++t[2])
+    for (t[3] = 0; t[3] < nb; ++t[3])
+    for (t[4] = 0; t[4] < nb; ++t[4])
+    for (t[5] = 0; t[5] < nb; ++t[5]) {
+        int bm[4][4];
+        bm[0][1] = bm[1][0] = t[0]; bm[0][2] = bm[2][0] = t[1]; bm[0][3] = bm[3][0] = t[2];
+        bm[1][2] = bm[2][1] = t[3]; bm[1][3] = bm[3][1] = t[4]; bm[2][3] = bm[3][2] = t[5];
+        int best[6], ch, ord[4];
+        canonical(bm, best, &ch, ord);
+        if (cmp6(best, t) != 0) continue;
+        size_t p = 0;
+        for (int k = 0; k < 6; ++k) p = p * (size_t)nb + (size_t)t[k];
+        tab[p] = rank++;
+    }
+    return tab;
+}
+
+/* One tetrahedron of points q[0..3] (catalogue indices). */
+static void add_tetra(const cat_t *c, const int32_t *tab, const int64_t q[4], uint64_t *even, int64_t *odd)
+{
+    int bm[4][4];
+    for (int a = 0; a < 4; ++a)
+        for (int b = a + 1; b < 4; ++b) bm[a][b] = bm[b][a] = pair_bin(c, q[a], q[b]);
+    int best[6], chiral, ord[4];
+    canonical(bm, best, &chiral, ord);
+    size_t p = 0;
+    for (int k = 0; k < 6; ++k) p = p * (size_t)c->nb + (size_t)best[k];
+    int idx = tab[p];
+    even[idx] += 1;
+    if (!chiral) return;
+    int64_t r[3][3];
+    for (int k = 0; k < 3; ++k) displacement(c, q[ord[0]], q[ord[k + 1]], r[k]);
+    int64_t v = triple_product(r[0], r[1], r[2]);
+    odd[idx] += (v > 0) - (v < 0);
+}
+
+typedef struct {
+    cat_t c;
+    const int64_t *row_ptr;
+    const int32_t *nbr;
+    const int32_t *tab;
+    int64_t ncfg;
+    uint64_t *even;
+    int64_t *odd;
+} six_ctx_t;
+
+/* hub i = the lowest-index vertex; j < k < l forward neighbours, pairwise adjacent */
+static void six_hub(void *vctx, int tid, int64_t i)
+{
+    six_ctx_t *x = (six_ctx_t *)vctx;
+    uint64_t *ev = x->even + (size_t)tid * (size_t)x->ncfg;
+    int64_t *od = x->odd + (size_t)tid * (size_t)x->ncfg;
+    int64_t r0 = x->row_ptr[i], r1 = x->row_ptr[i + 1];
+    for (int64_t a = r0; a < r1; ++a) {
+        if (x->nbr[a] <= i) continue;
+        for (int64_t b = a + 1; b < r1; ++b) {
+            if (pair_bin(&x->c, x->nbr[a], x->nbr[b]) < 0) continue;
+            for (int64_t d = b + 1; d < r1; ++d) {
+                if (pair_bin(&x->c, x->nbr[a], x->nbr[d]) < 0) continue;
+                if (pair_bin(&x->c, x->nbr[b], x->nbr[d]) < 0) continue;
+                int64_t q[4] = { i, x->nbr[a], x->nbr[b], x->nbr[d] };
+                add_tetra(&x->c, x->tab, q, ev, od);
+            }
+        }
+    }
+}
+
+void oracle_4pcf6(const int32_t *xyz, int64_t n, int64_t box, int periodic, const int64_t *edges, int nb,
+                  const int64_t *row_ptr, const int32_t *nbr, int64_t hub_begin, int64_t hub_end,
+                  uint64_t *even, int64_t *odd)
+{
+    int nt = oracle_threads();
+    six_ctx_t x;
+    x.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    x.row_ptr = row_ptr; x.nbr = nbr;
+    x.tab = six_index_table(nb);
+    x.ncfg = oracle_nconfig6(nb);
+    x.even = (uint64_t *)calloc((size_t)nt * (size_t)x.ncfg, sizeof(uint64_t));
+    x.odd = (int64_t *)calloc((size_t)nt * (size_t)x.ncfg, sizeof(int64_t));
+    if (hub_end > hub_begin) parallel_for(hub_begin, hub_end, nt, six_hub, &x);
+    reduce_u64(even, x.even, nt, x.ncfg);
+    reduce_i64(odd, x.odd, nt, x.ncfg);
+    free(x.even); free(x.odd);
+    free((void *)x.tab);
+}
+
+/* O(N^4 / 24): every set of four points whose six pairs are edges. */
+void oracle_brute4six(const int32_t *xyz, int64_t n, int64_t box, int periodic, const int64_t *edges, int nb,
+                      uint64_t *even, int64_t *odd)
+{
+    cat_t c = { xyz, n, box, periodic, edges, nb };
+    int32_t *tab = six_index_table(nb);
+    int64_t ncfg = oracle_nconfig6(nb);
+    memset(even, 0, sizeof(uint64_t) * (size_t)ncfg);
+    memset(odd, 0, sizeof(int64_t) * (size_t)ncfg);
+    for (int64_t a = 0; a < n; ++a)
+        for (int64_t b = a + 1; b < n; ++b) {
+            if (pair_bin(&c, a, b) < 0) continue;
+            for (int64_t d = b + 1; d < n; ++d) {
+                if (pair_bin(&c, a, d) < 0 || pair_bin(&c, b, d) < 0) continue;
+                for (int64_t e = d + 1; e < n; ++e) {
+                    if (pair_bin(&c, a, e) < 0 || pair_bin(&c, b, e) < 0 || pair_bin(&c, d, e) < 0) continue;
+                    int64_t q[4] = { a, b, d, e };
+                    add_tetra(&c, tab, q, even, odd);
+                }
+            }
+        }
+    free(tab);
+}
+
+/* The configuration index of one canonical tuple, -1 if it is not canonical. */
+int64_t oracle_config_index6(int nb, const int32_t *t)
+{
+    int w[6];
+    for (int k = 0; k < 6; ++k) w[k] = t[k];
+    return six_count_and_index(nb, w);
+}

@@ -5,6 +5,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 
 from cosmology_point_correlation_gb300 import _lib, build
@@ -63,3 +64,14 @@ def test_null_graph_is_rejected_without_device_work(lib):
     assert lib.gs_graph_info(None, None, None, None) == _lib.GS_ERR_ARG
     assert b"NULL" in lib.gs_last_error()
     lib.gs_graph_free(None)
+
+
+def test_3pcf_slices_follow_the_configuration_order(lib):
+    from cosmology_point_correlation_gb300 import equilateral, isosceles, xi_natural
+    nb = 7
+    cfg = fx.configs3(nb)
+    hist = np.arange(len(cfg))              # entry k holds k
+    assert equilateral(hist, nb).tolist() == [cfg.index((b, b, b)) for b in range(nb)]
+    assert isosceles(hist, nb, 3).tolist() == [cfg.index(tuple(sorted((3, 3, c)))) for c in range(nb)]
+    xi = xi_natural([10, 0], [10, 5], 101, 101)
+    assert xi[0] == 0.0 and xi[1] == -1.0

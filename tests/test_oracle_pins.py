@@ -352,3 +352,18 @@ def test_rows_and_parity_hubs_match_graph():
     e1, o1 = oracle.count_4pcf_parity_hubs(xyz, box, 1, edges, [7, 8, 9])
     e2, o2 = oracle.count_4pcf_parity(xyz, box, 1, edges, g, 7, 10)
     assert np.array_equal(e1, e2) and np.array_equal(o1, o2)
+
+
+# ---------------------------------------------------------------- internal 2pCF
+
+@pytest.mark.parametrize("periodic", [0, 1])
+def test_2pcf_matches_numpy_pairs(periodic):
+    box = 20000
+    xyz = catalogues.neyman_scott(300, box / 1024, 10, 20.0, 1.5, 5 + periodic)
+    edges = [0, 700, 1500, 2600, 4000, 6000]
+    B, _ = fx.np_bins(xyz, box, periodic, edges)
+    iu = np.triu_indices(len(xyz), 1)
+    b = B[iu]
+    ref = np.bincount(b[b >= 0], minlength=len(edges) - 1).astype(np.uint64)
+    assert np.array_equal(oracle.count_2pcf(xyz, box, periodic, edges), ref)
+    assert ref.sum() > 100

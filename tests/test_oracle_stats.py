@@ -71,7 +71,7 @@ def tiny_ensemble():
     for seed in range(2000, 2032):
         xyz = w.points(seed=seed)
         g = oracle.graph(xyz, w.box_lu, 1, w.edges_lu)
-        pairs.append(np.bincount(g.bin, minlength=w.nbins) // 2)
+        pairs.append(oracle.count_2pcf(xyz, w.box_lu, 1, w.edges_lu, g))
         tris.append(oracle.count_3pcf(xyz, w.box_lu, 1, w.edges_lu, g))
     return np.array(pairs, dtype=np.float64), np.array(tris, dtype=np.float64)
 
