@@ -143,6 +143,22 @@ class Graph:
                                                     int(hub_begin), int(hub_end), _stream(stream)))
         return even, odd
 
+    def count_4pcf6(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
+        """(even, odd) six-edge-bin 4pCF per tetrahedron configuration (each tetrahedron once)."""
+        torch = _torch()
+        hub_end = self.n if hub_end is None else hub_end
+        m = _lib.load().gs_config_count_4pcf6(self.nbins)
+        if m < 0:
+            raise GramsciError(_lib.GS_ERR_ARG, "the six-bin 4pCF supports at most 10 bins")
+        if out is None:
+            out = (torch.zeros(m, dtype=torch.int64, device=self.device),
+                   torch.zeros(m, dtype=torch.int64, device=self.device))
+        even, odd = out
+        _lib.check(_lib.load().gs_count_4pcf6(self._h, ctypes.c_void_p(even.data_ptr()),
+                                              ctypes.c_void_p(odd.data_ptr()), int(hub_begin), int(hub_end),
+                                              _stream(stream)))
+        return even, odd
+
     def count_3pcf_hubs(self, hubs, out=None, stream=None):
         """Triangles incident to each listed hub (input indices), summed; uint64 bits in int64."""
         torch = _torch()

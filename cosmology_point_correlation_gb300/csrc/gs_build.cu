@@ -385,6 +385,7 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
                 deg[hb + t] = s_cnt[t];
                 fwd[hb + t] = s_lo[t];
                 atomicMax(max_deg, (unsigned)s_cnt[t]);
+                atomicMax(max_deg + 1, (unsigned)(s_cnt[t] - s_lo[t]));
             }
         }
         __syncthreads();
@@ -414,6 +415,7 @@ static void free_graph_arrays(gs_graph *g)
     cudaFree(g->work);
     cudaFree(g->err);
     cudaFree(g->cfg3);
+    cudaFree(g->cfg6);
 }
 
 extern "C" void gs_graph_free(gs_graph_t g)
@@ -509,14 +511,14 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         GS_BUILD_CUDA(cudaMallocAsync(&cell_count, sizeof(int32_t) * ncells, st));
         GS_BUILD_CUDA(cudaMallocAsync(&cell_start, sizeof(int32_t) * (ncells + 1), st));
         GS_BUILD_CUDA(cudaMallocAsync(&esq, sizeof(long long) * 256, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&maxd, sizeof(unsigned), st));
+        GS_BUILD_CUDA(cudaMallocAsync(&maxd, 2 * sizeof(unsigned), st));
 
         long long hesq[256];
         for (int k = 0; k <= nbins; ++k) hesq[k] = (long long)edges_lu[k] * edges_lu[k];
         GS_BUILD_CUDA(cudaMemcpyAsync(esq, hesq, sizeof(long long) * (nbins + 1), cudaMemcpyHostToDevice, st));
         GS_BUILD_CUDA(cudaMemsetAsync(cell_count, 0, sizeof(int32_t) * ncells, st));
         GS_BUILD_CUDA(cudaMemsetAsync(g->err, 0, sizeof(int32_t), st));
-        GS_BUILD_CUDA(cudaMemsetAsync(maxd, 0, sizeof(unsigned), st));
+        GS_BUILD_CUDA(cudaMemsetAsync(maxd, 0, 2 * sizeof(unsigned), st));
 
         if (n > 0) {
             k_cell_assign<<<grid1, 256, 0, st>>>(coords_dev, n, (int)box_lu, g->ncell, cell, slot,
@@ -545,16 +547,17 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         if (s != GS_OK) goto fail;
 
         int32_t herr = 0;
-        unsigned hmax = 0;
+        unsigned hmax[2] = { 0, 0 };
         GS_BUILD_CUDA(cudaMemcpyAsync(&g->n_edges, g->row_ptr + n, sizeof(int64_t), cudaMemcpyDeviceToHost, st));
         GS_BUILD_CUDA(cudaMemcpyAsync(&herr, g->err, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
-        GS_BUILD_CUDA(cudaMemcpyAsync(&hmax, maxd, sizeof(unsigned), cudaMemcpyDeviceToHost, st));
+        GS_BUILD_CUDA(cudaMemcpyAsync(hmax, maxd, 2 * sizeof(unsigned), cudaMemcpyDeviceToHost, st));
         GS_BUILD_CUDA(cudaStreamSynchronize(st));
         if (herr) {
             s = gs_set_error(GS_ERR_ARG, "a coordinate lies outside [0, box_lu)");
             goto fail;
         }
-        g->max_degree = (int32_t)hmax;
+        g->max_degree = (int32_t)hmax[0];
+        g->max_forward = (int32_t)hmax[1];
 
         const size_t ne = (size_t)(g->n_edges + GS_EDGE_PAD);
         GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));

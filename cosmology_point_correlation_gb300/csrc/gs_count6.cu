@@ -1,0 +1,424 @@
+// gs_count6.cu -- six-edge-bin 4pCF with parity channels (GRAMSCI v2, §II.2:
+// tetrahedra whose six pairs are all neighbours; §III.2, Eq.(3): handedness;
+// §V.2: tetrahedron configurations, 276 of them for 4 radial bins).
+//
+// Every tetrahedron {i, j1, j2, j3} with i < j1 < j2 < j3 (internal order) is
+// found once, at hub i, from its forward row F = {j in N(i) : j > i}:
+//   1. F is staged in shared memory (ids, hub bins, spoke vectors x_j - x_i)
+//      with a hash table id -> position;
+//   2. warps walk the forward part of each spoke's row N(j) and, for every
+//      entry that is also in F, set bit (s, t) of an adjacency bit-matrix and
+//      store the spoke-spoke bin in a byte matrix;
+//   3. cliques (s1 < s2 < s3) come from the AND of two bit rows; the six bins
+//      (b_ij1, b_ij2, b_ij3, b_j1j2, b_j1j3, b_j2j3) index a per-graph table
+//      holding the configuration and the parity of a vertex ordering that
+//      turns this labelling into the configuration's smallest tuple (0 when
+//      orderings of both parities do: an achiral configuration); the odd
+//      channel adds that parity times sign(det[r_j1; r_j2; r_j3]).
+// Hubs with more than C6_M forward neighbours use a global scratch slice per
+// block instead of shared memory.
+
+#include <algorithm>
+#include <array>
+#include <vector>
+
+#include "gs_internal.cuh"
+
+constexpr int C6_THREADS = 256;
+constexpr int C6_WARPS = C6_THREADS / 32;
+constexpr int C6_M = 256;                   // forward degree kept in shared memory
+constexpr int C6_WORDS = C6_M / 32;
+constexpr int C6_SMEM_HIST_MAX = 4096;
+constexpr int C6_EMPTY = -1;
+constexpr int C6_MAX_BINS = 10;             // the tuple table holds nb^6 entries
+
+struct C6Args {
+    const int4 *pts;
+    const int64_t *row_ptr;
+    const int32_t *fwd;
+    const int32_t *nbr;
+    const uint8_t *bin;
+    const int32_t *cfg6;          // [nb^6] (configuration << 2) | (orientation parity + 1)
+    int64_t hub_begin, hub_end;
+    int box, periodic, nb, ncfg;
+    unsigned long long *even;
+    long long *odd;
+    unsigned long long *cursor;
+    int big_m;                    // large path: forward degree the slices hold
+    char *scratch;
+    size_t scratch_stride;
+};
+
+struct C6Space {
+    int32_t *key;      // hash table
+    int32_t *pos;
+    int32_t *row;      // [f] ids
+    uint8_t *hb;       // [f] hub bins
+    int *vx, *vy, *vz; // [f] spoke vectors
+    unsigned *bits;    // [f][W]
+    uint8_t *sbin;     // [f][f] spoke-spoke bins (valid where the bit is set)
+};
+
+template <bool SMEM_HIST>
+__device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long long i, int64_t f0, int f,
+                                       int tlog, unsigned *s_even, int *s_odd)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = (f + 31) >> 5;
+    const int tsize = 1 << tlog, shift = 32 - tlog, mask = tsize - 1;
+    const int4 P = a.pts[i];
+    const int nb = a.nb;
+
+    for (int t = threadIdx.x; t < f; t += C6_THREADS) {
+        const int32_t k = a.nbr[f0 + t];
+        w.row[t] = k;
+        w.hb[t] = a.bin[f0 + t];
+        const int4 Q = a.pts[k];
+        w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
+        w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
+        w.vz[t] = gs_delta(P.z, Q.z, a.box, a.periodic);
+        uint32_t h = gs_hash(k, shift);
+        while (atomicCAS(&w.key[h], C6_EMPTY, k) != C6_EMPTY) h = (h + 1) & mask;
+        w.pos[h] = t;
+    }
+    for (int t = threadIdx.x; t < f * W; t += C6_THREADS) w.bits[t] = 0u;
+    __syncthreads();
+
+    const int32_t kmax = w.row[f - 1];
+    for (int s = warp; s < f - 1; s += C6_WARPS) {
+        const int32_t j = w.row[s];
+        const int64_t pe = a.row_ptr[j + 1];
+        for (int64_t p = a.row_ptr[j] + a.fwd[j]; p < pe; p += 32) {
+            const int64_t q = p + lane;
+            const int32_t k = q < pe ? a.nbr[q] : 0x7fffffff;
+            if (k <= kmax) {
+                uint32_t h = gs_hash(k, shift);
+                int32_t key;
+                while ((key = w.key[h]) != k && key != C6_EMPTY) h = (h + 1) & mask;
+                if (key == k) {
+                    const int t = w.pos[h];
+                    atomicOr(&w.bits[(size_t)s * W + (t >> 5)], 1u << (t & 31));
+                    w.sbin[(size_t)s * f + t] = a.bin[q];
+                }
+            }
+            if (__shfl_sync(0xffffffffu, k, 31) > kmax) break;
+        }
+    }
+    __syncthreads();
+
+    for (int s1 = warp; s1 < f - 2; s1 += C6_WARPS) {
+        const unsigned *row1 = w.bits + (size_t)s1 * W;
+        const int b01 = w.hb[s1];
+        const long long x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
+        for (int s2 = s1 + 1 + lane; s2 < f - 1; s2 += 32) {
+            if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
+            const unsigned *row2 = w.bits + (size_t)s2 * W;
+            const int b02 = w.hb[s2], b12 = w.sbin[(size_t)s1 * f + s2];
+            const long long x2 = w.vx[s2], y2 = w.vy[s2], z2 = w.vz[s2];
+            const long long cx = y1 * z2 - z1 * y2, cy = z1 * x2 - x1 * z2, cz = x1 * y2 - y1 * x2;
+            const int base = ((b01 * nb + b02) * nb) * nb * nb * nb;          // b03, b12, b13, b23 follow
+            for (int wd = s2 >> 5; wd < W; ++wd) {
+                unsigned common = row1[wd] & row2[wd];
+                if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
+                while (common) {
+                    const int s3 = (wd << 5) + __ffs(common) - 1;
+                    common &= common - 1;
+                    const int b03 = w.hb[s3];
+                    const int b13 = w.sbin[(size_t)s1 * f + s3], b23 = w.sbin[(size_t)s2 * f + s3];
+                    const int pk = base + ((b03 * nb + b12) * nb + b13) * nb + b23;
+                    const int v = __ldg(a.cfg6 + pk);
+                    const int ci = v >> 2, par = (v & 3) - 1;
+                    const long long d = cx * w.vx[s3] + cy * w.vy[s3] + cz * w.vz[s3];
+                    const int sg = par * ((d > 0) - (d < 0));
+                    if (SMEM_HIST) {
+                        atomicAdd(&s_even[ci], 1u);
+                        if (sg) atomicAdd(&s_odd[ci], sg);
+                    } else {
+                        atomicAdd(a.even + ci, 1ull);
+                        if (sg) atomicAdd((unsigned long long *)(a.odd + ci), (unsigned long long)(long long)sg);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < tsize; t += C6_THREADS) w.key[t] = C6_EMPTY;
+}
+
+__device__ __forceinline__ void c6_flush(unsigned *se, int *so, int ncfg, unsigned long long *ge, long long *go)
+{
+    for (int t = threadIdx.x; t < ncfg; t += C6_THREADS) {
+        if (se[t]) atomicAdd(ge + t, (unsigned long long)se[t]);
+        if (so[t]) atomicAdd((unsigned long long *)(go + t), (unsigned long long)(long long)so[t]);
+        se[t] = 0;
+        so[t] = 0;
+    }
+}
+
+// Hubs with 3..C6_M forward neighbours, workspace in shared memory.
+template <bool SMEM_HIST>
+__global__ void __launch_bounds__(C6_THREADS)
+k_count6_small(C6Args a)
+{
+    extern __shared__ unsigned s_dyn[];         // bits [C6_M*C6_WORDS], sbin [C6_M*C6_M], even, odd
+    __shared__ int32_t s_key[2 * C6_M];
+    __shared__ int32_t s_pos[2 * C6_M];
+    __shared__ int32_t s_row[C6_M];
+    __shared__ uint8_t s_hb[C6_M];
+    __shared__ int s_vx[C6_M], s_vy[C6_M], s_vz[C6_M];
+    __shared__ long long s_hub;
+    __shared__ unsigned long long s_pending;
+
+    unsigned *s_bits = s_dyn;
+    uint8_t *s_sbin = (uint8_t *)(s_bits + C6_M * C6_WORDS);
+    unsigned *s_even = (unsigned *)(s_sbin + C6_M * C6_M);
+    int *s_odd = (int *)(s_even + a.ncfg);
+    if (SMEM_HIST)
+        for (int t = threadIdx.x; t < a.ncfg; t += C6_THREADS) {
+            s_even[t] = 0;
+            s_odd[t] = 0;
+        }
+    for (int t = threadIdx.x; t < 2 * C6_M; t += C6_THREADS) s_key[t] = C6_EMPTY;
+    if (threadIdx.x == 0) s_pending = 0;
+    C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin };
+
+    for (;;) {
+        __syncthreads();
+        if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
+        __syncthreads();
+        const long long i = s_hub;
+        if (i >= a.hub_end) break;
+        const int64_t f0 = a.row_ptr[i] + a.fwd[i];
+        const int f = (int)(a.row_ptr[i + 1] - f0);
+        if (f < 3 || f > C6_M) continue;
+        if (SMEM_HIST) {
+            const unsigned long long bound = (unsigned long long)f * (f - 1) * (f - 2) / 6;
+            if (s_pending + bound > 0x7fffffffull) {
+                c6_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+                __syncthreads();
+                if (threadIdx.x == 0) s_pending = 0;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) s_pending += bound;
+        }
+        int tlog = 4;
+        while ((1 << tlog) < 2 * f) ++tlog;
+        c6_hub<SMEM_HIST>(a, w, i, f0, f, tlog, s_even, s_odd);
+    }
+    if (SMEM_HIST) {
+        __syncthreads();
+        c6_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+    }
+}
+
+// Hubs with more than C6_M forward neighbours: workspace in a global slice.
+__global__ void __launch_bounds__(C6_THREADS)
+k_count6_large(C6Args a)
+{
+    __shared__ long long s_hub;
+    const int M = a.big_m;
+    int tlog = 4;
+    while ((1 << tlog) < 2 * M) ++tlog;
+    const int WM = (M + 31) >> 5;
+    char *base = a.scratch + (size_t)blockIdx.x * a.scratch_stride;
+    C6Space w;
+    w.key = (int32_t *)base;
+    w.pos = w.key + (1 << tlog);
+    w.row = w.pos + (1 << tlog);
+    w.vx = w.row + M;
+    w.vy = w.vx + M;
+    w.vz = w.vy + M;
+    w.bits = (unsigned *)(w.vz + M);
+    w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
+    w.sbin = w.hb + M;
+    for (int t = threadIdx.x; t < (1 << tlog); t += C6_THREADS) w.key[t] = C6_EMPTY;
+
+    for (;;) {
+        __syncthreads();
+        if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
+        __syncthreads();
+        const long long i = s_hub;
+        if (i >= a.hub_end) break;
+        const int64_t f0 = a.row_ptr[i] + a.fwd[i];
+        const int f = (int)(a.row_ptr[i + 1] - f0);
+        if (f <= C6_M) continue;
+        int tl = 4;
+        while ((1 << tl) < 2 * f) ++tl;
+        c6_hub<false>(a, w, i, f0, f, tl, nullptr, nullptr);
+    }
+}
+
+static size_t c6_large_stride(int M)
+{
+    int tlog = 4;
+    while ((1 << tlog) < 2 * M) ++tlog;
+    const size_t WM = (size_t)(M + 31) / 32;
+    const size_t bytes = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM +
+                         M + (size_t)M * M;
+    return (bytes + 255) & ~(size_t)255;
+}
+
+// Host table over all nb^6 bin tuples t = (b01, b02, b03, b12, b13, b23) of a
+// labelled tetrahedron: the configuration (rank of the smallest relabelling
+// among all smallest tuples, in lexicographic order) and the parity of a
+// relabelling reaching it, 0 if relabellings of both parities do.
+static std::vector<int32_t> c6_table(int nb, int *ncfg_out)
+{
+    // vertex permutations and the edge permutation each induces: relabelled
+    // tuple u[e] = t[edge(perm[a], perm[b])] for edge e = (a, b)
+    static const int ea[6] = { 0, 0, 0, 1, 1, 2 }, eb[6] = { 1, 2, 3, 2, 3, 3 };
+    int eid[4][4];
+    for (int e = 0; e < 6; ++e) eid[ea[e]][eb[e]] = eid[eb[e]][ea[e]] = e;
+    std::vector<std::array<int, 6>> emap;
+    std::vector<int> par;
+    int p[4] = { 0, 1, 2, 3 };
+    std::sort(p, p + 4);
+    do {
+        std::array<int, 6> m;
+        for (int e = 0; e < 6; ++e) m[e] = eid[p[ea[e]]][p[eb[e]]];
+        emap.push_back(m);
+        int inv = 0;
+        for (int x = 0; x < 4; ++x)
+            for (int y = x + 1; y < 4; ++y) inv += p[x] > p[y];
+        par.push_back(inv & 1);
+    } while (std::next_permutation(p, p + 4));
+
+    size_t nt = 1;
+    for (int k = 0; k < 6; ++k) nt *= (size_t)nb;
+    std::vector<int32_t> canon(nt), orient(nt);
+    auto pack = [nb](const int *u) {
+        size_t q = 0;
+        for (int k = 0; k < 6; ++k) q = q * (size_t)nb + (size_t)u[k];
+        return q;
+    };
+    int t[6];
+    for (size_t q = 0; q < nt; ++q) {
+        size_t r = q;
+        for (int k = 5; k >= 0; --k) {
+            t[k] = (int)(r % (size_t)nb);
+            r /= (size_t)nb;
+        }
+        size_t best = (size_t)-1;
+        bool ev = false, od = false;
+        for (size_t g = 0; g < emap.size(); ++g) {
+            int u[6];
+            for (int e = 0; e < 6; ++e) u[e] = t[emap[g][e]];
+            const size_t pu = pack(u);           // packed order = lexicographic order
+            if (pu < best) {
+                best = pu;
+                ev = !par[g];
+                od = par[g];
+            } else if (pu == best) {
+                (par[g] ? od : ev) = true;
+            }
+        }
+        canon[q] = (int32_t)best;
+        orient[q] = (ev && od) ? 0 : (ev ? 1 : -1);
+    }
+    // configuration numbers: canonical tuples in increasing packed order
+    std::vector<int32_t> rank(nt, -1);
+    int n = 0;
+    for (size_t q = 0; q < nt; ++q)
+        if ((size_t)canon[q] == q) rank[q] = n++;
+    std::vector<int32_t> out(nt);
+    for (size_t q = 0; q < nt; ++q) out[q] = (rank[canon[q]] << 2) | (orient[q] + 1);
+    *ncfg_out = n;
+    return out;
+}
+
+static gs_status c6_prepare(gs_graph_t g)
+{
+    if (g->cfg6) return GS_OK;
+    int n = 0;
+    std::vector<int32_t> t = c6_table(g->nb, &n);
+    int32_t *d = nullptr;
+    GS_TRY_CUDA(cudaMalloc(&d, sizeof(int32_t) * t.size()));
+    cudaError_t e = cudaMemcpy(d, t.data(), sizeof(int32_t) * t.size(), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(d);
+        return gs_set_error(GS_ERR_CUDA, "copy of the configuration table failed: %s", cudaGetErrorString(e));
+    }
+    g->cfg6 = d;
+    g->ncfg6 = n;
+    return GS_OK;
+}
+
+extern "C" int64_t gs_config_count_4pcf6(int nbins)
+{
+    if (nbins < 1 || nbins > C6_MAX_BINS) return -1;
+    const int64_t b = nbins;
+    return (b * b * b * b * b * b + 9 * b * b * b * b + 14 * b * b) / 24;
+}
+
+extern "C" gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
+                                    int64_t hub_end, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (g->nb > C6_MAX_BINS)
+        return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF supports at most %d bins", C6_MAX_BINS);
+    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
+        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
+                            (long long)hub_end, (long long)g->n);
+    if (g->edges[g->nb] >= (1ll << 20))
+        return gs_set_error(GS_ERR_ARG, "the 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
+    gs_status s = c6_prepare(g);
+    if (s != GS_OK) return s;
+    const int ncfg = g->ncfg6;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
+    GS_TRY_CUDA(cudaMemsetAsync(g->work + 3, 0, sizeof(unsigned long long), st));
+
+    C6Args a{};
+    a.pts = g->pts;
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.cfg6 = g->cfg6;
+    a.hub_begin = hub_begin;
+    a.hub_end = hub_end;
+    a.box = (int)g->box_lu;
+    a.periodic = g->periodic;
+    a.nb = g->nb;
+    a.ncfg = ncfg;
+    a.even = (unsigned long long *)even_dev;
+    a.odd = (long long *)odd_dev;
+    a.cursor = g->work + 3;
+
+    const int64_t hubs = hub_end - hub_begin;
+    const int sms = gs_sm_count();
+    const bool smem = ncfg <= C6_SMEM_HIST_MAX;
+    const size_t dyn = sizeof(unsigned) * C6_M * C6_WORDS + (size_t)C6_M * C6_M + (smem ? 8 * (size_t)ncfg : 0);
+    auto kern = smem ? k_count6_small<true> : k_count6_small<false>;
+    int per_sm = 0;
+    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C6_THREADS, dyn));
+    per_sm = std::max(per_sm, 1);
+    kern<<<(int)std::min<int64_t>((int64_t)sms * per_sm, hubs), C6_THREADS, dyn, st>>>(a);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
+
+    const int M = g->max_forward;              // bounds the large path's slices
+    if (M > C6_M) {
+        const size_t stride = c6_large_stride(M);
+        const size_t budget = (size_t)2 << 30;
+        const int gl = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>((int64_t)sms * 2, hubs),
+                                                                   (int64_t)(budget / stride)));
+        char *scratch = nullptr;
+        GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
+        GS_TRY_CUDA(cudaMemsetAsync(g->work + 3, 0, sizeof(unsigned long long), st));
+        a.cursor = g->work + 3;
+        a.big_m = M;
+        a.scratch = scratch;
+        a.scratch_stride = stride;
+        k_count6_large<<<gl, C6_THREADS, 0, st>>>(a);
+        gs_note_launch();
+        cudaError_t e = cudaGetLastError();
+        cudaFreeAsync(scratch, st);
+        if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    return GS_OK;
+}

@@ -28,6 +28,7 @@ struct gs_graph {
     int64_t edges[256];
     int64_t n_edges;
     int32_t max_degree;
+    int32_t max_forward;       // largest |{j in N(i) : j > i}|
     int ncell;                 // cells per axis
     int4 *pts;
     int32_t *inv;
@@ -38,6 +39,8 @@ struct gs_graph {
     unsigned long long *work;  // 4 device counters used by the count kernels
     int32_t *err;              // device error word of the build kernels
     uint16_t *cfg3;            // [nb][nb][nb] idx3(sort(x, y, z)) at (z, x, y), nb <= 40; or NULL
+    int32_t *cfg6;             // [nb^6] six-bin 4pCF configuration and orientation (built on first use)
+    int ncfg6;
 };
 
 // ---------------------------------------------------------------- errors

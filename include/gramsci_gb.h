@@ -158,6 +158,28 @@ gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t coun
 gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
                                     uint64_t *even_dev, int64_t *odd_dev, void *cuda_stream);
 
+/* Six-edge-bin 4pCF with parity channels (§II.2 tetrahedra: four points whose
+ * six pairs are all neighbours; §III.2 Eq.(3) handedness; §V.2
+ * configurations). Every tetrahedron counts once. Its configuration is the
+ * lexicographically smallest bin tuple (b01, b02, b03, b12, b13, b23) over the
+ * 24 orderings (v0, v1, v2, v3) of its vertices (b_ab: bin of the pair
+ * v_a v_b); configurations are numbered in lexicographic order of those
+ * tuples (gs_config_count_4pcf6(nb) = (nb^6 + 9 nb^4 + 14 nb^2) / 24 of them,
+ * 276 for 4 bins). even[c] counts the tetrahedra of configuration c; odd[c]
+ * sums sign(det[x_v1 - x_v0; x_v2 - x_v0; x_v3 - x_v0]) for an ordering that
+ * reaches the smallest tuple, with 0 when orderings of both permutation
+ * parities reach it (an achiral configuration) or when the volume is 0.
+ *   even_dev  uint64 [gs_config_count_4pcf6(nbins)], device, overwritten
+ *   odd_dev   int64  [gs_config_count_4pcf6(nbins)], device, overwritten
+ *   hub_begin, hub_end  internal-order hub range; a tetrahedron belongs to
+ *             its lowest internal index, so disjoint ranges add exactly.
+ * The first call on a graph builds a table of nb^6 entries (synchronously).
+ * Limits: nbins <= 10, r_max_lu < 2^20. Errors: GS_ERR_ARG, GS_ERR_NOMEM,
+ * GS_ERR_CUDA. */
+gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
+                         int64_t hub_begin, int64_t hub_end, void *cuda_stream);
+int64_t gs_config_count_4pcf6(int nbins);
+
 /* Internal 2pCF pair counts: the number of unordered pairs {i, j} in each
  * radial bin, from one sweep of the graph's bin bytes (§III.3: the two-point
  * function on the same graph and binning as the higher-order counts).

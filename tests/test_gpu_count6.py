@@ -1,0 +1,75 @@
+"""Six-edge-bin 4pCF with parity channels on the GPU against the oracle
+(GRAMSCI v2 §II.2 tetrahedra, §III.2 Eq.(3), §V.2 configurations)."""
+import numpy as np
+import pytest
+
+import oracle
+from cosmology_point_correlation_gb300 import as_uint64, catalogues, configs
+from tests import fixtures as fx
+from tests.gpu_util import gpu_graph, mirror
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu6(xyz, box, periodic, edges, ranges=None):
+    with gpu_graph(xyz, box, periodic, edges) as g:
+        if ranges is None:
+            e, o = g.count_4pcf6()
+            return as_uint64(e), o.cpu().numpy()
+        out = [g.count_4pcf6(a, b) for a, b in ranges]
+        return (np.sum([as_uint64(e) for e, _ in out], axis=0, dtype=np.uint64),
+                np.sum([o.cpu().numpy() for _, o in out], axis=0))
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+@pytest.mark.parametrize("n,nb", [(3000, 4), (8000, 5)])
+def test_matches_oracle(periodic, n, nb):
+    L = 500.0 * (n / 200_000) ** (1 / 3)
+    box = catalogues.box_lattice(L)
+    xyz = catalogues.neyman_scott(n, L, max(1, n // 50), 50.0, 3.0, 21 + n + periodic)
+    edges = catalogues.linear_edges_lu(20.0, nb)
+    ref_e, ref_o = oracle.count_4pcf6(xyz, box, periodic, edges)
+    assert ref_e.sum() > 10_000 and np.abs(ref_o).sum() > 0
+    e, o = _gpu6(xyz, box, periodic, edges)
+    assert np.array_equal(e, ref_e) and np.array_equal(o, ref_o)
+
+
+def test_fixture_shapes():
+    shapes = {s["name"]: s for s in fx.tetrahedron_shapes()}
+    box = 1_000_000
+    for name in ("T", "T_mirror", "T_relabel", "R", "P"):
+        xyz = (shapes[name]["vertices"] + 500_000).astype(np.int32)
+        ref_e, ref_o = oracle.count_4pcf6(xyz, box, 0, fx.TETRA_EDGES)
+        e, o = _gpu6(xyz, box, 0, fx.TETRA_EDGES)
+        assert np.array_equal(e, ref_e) and np.array_equal(o, ref_o), name
+    k = oracle.config_index6(4, (0, 1, 2, 2, 2, 3))
+    e, o = _gpu6((shapes["T"]["vertices"] + 500_000).astype(np.int32), box, 0, fx.TETRA_EDGES)
+    assert e[k] == 1 and o[k] == 1
+
+
+def test_hub_with_more_forward_neighbours_than_shared_memory_holds():
+    # one hub (input index 0, all points in one cell) with 300 forward
+    # neighbours on a shell of radius 0.9 r_max: the global-scratch path
+    rng = np.random.default_rng(8)
+    R = 20000
+    v = rng.normal(size=(300, 3))
+    v *= (0.9 * R * (0.5 + 0.5 * rng.uniform(size=(300, 1)))) / np.linalg.norm(v, axis=1, keepdims=True)
+    xyz = (np.vstack([[[0, 0, 0]], np.rint(v)]) + 25000).astype(np.int32)
+    edges = [0, 8000, 12000, 16000, R]
+    ref_e, ref_o = oracle.count_4pcf6(xyz, 50000, 0, edges)
+    assert ref_e.sum() > 1000
+    e, o = _gpu6(xyz, 50000, 0, edges)
+    assert np.array_equal(e, ref_e) and np.array_equal(o, ref_o)
+
+
+def test_parity_catalogue_four_bins_full_size():
+    w = configs.PARITY_4PCF
+    xyz = w.points()
+    edges = catalogues.linear_edges_lu(w.r_max_mpc, 4)
+    e, o = _gpu6(xyz, w.box_lu, True, edges)
+    assert len(e) == 276 and e.sum() > 0
+    n = len(xyz)
+    e2, o2 = _gpu6(xyz, w.box_lu, True, edges, ranges=[(0, n // 3), (n // 3, n)])
+    assert np.array_equal(e2, e) and np.array_equal(o2, o)
+    e3, o3 = _gpu6(mirror(xyz, w.box_lu, True), w.box_lu, True, edges)
+    assert np.array_equal(e3, e) and np.array_equal(o3, -o)
