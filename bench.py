@@ -315,10 +315,28 @@ def run_ours(args, w):
     ncfg = w.nbins * (w.nbins + 1) * (w.nbins + 2) // 6
     hist = torch.empty(ncfg, dtype=torch.int64, device=dev)
 
-    # work statistics of this catalogue's graph (untimed)
+    # work statistics of this catalogue's graph (untimed), and the internal
+    # 2pCF pass on the same graph (one sweep of the bin bytes)
     with build_graph(coords, box_lu, w.periodic, w.edges_lu) as g:
         st = g.stats()
+        dd = g.count_2pcf()
+        torch.cuda.synchronize()
+        t2 = []
+        for _ in range(max(args.steps, 3)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.count_2pcf(out=dd)
+            e1.record()
+            torch.cuda.synchronize()
+            t2.append(e0.elapsed_time(e1))
+        pairs = int(as_uint64(dd).sum())
     alg_bytes = BYTES_PER_EDGE * (st["n_edges"] // 2 + st["spoke_walk"])
+    peak, peak_kind = hbm_peak()
+    t2_ms = statistics.mean(t2)
+    twopcf = {"ms": t2_ms, "pairs": pairs, "pairs_per_s": pairs / (t2_ms / 1e3),
+              "roofline": {"bound": "hbm", "achieved": st["n_edges"] / (t2_ms / 1e3) / 1e9, "peak": peak,
+                           "unit": "GB/s", "frac": st["n_edges"] / (t2_ms / 1e3) / 1e9 / peak,
+                           "per_unit": "1 B per directed edge (the bin byte)"}}
 
     time_path(coords, box_lu, w, args.warmup, "3pcf", hist)
     torch.cuda.synchronize()
@@ -391,6 +409,33 @@ def run_ours(args, w):
                   "cliques_per_s": cl_all / (p_step / 1e3), "edges_per_s": pe_all / (p_step / 1e3),
                   "cliques": cliques, "odd_sum": int(odd.sum().item()), "n_edges": pres[-1][3]}
 
+    # six-edge-bin 4pCF (276 configurations) on the parity catalogue with 4 bins
+    fourpcf6 = None
+    if not args.no_parity:
+        import dataclasses
+        pw = configs.ALL[args.parity_workload]
+        w6 = dataclasses.replace(pw, name=pw.name + "_4bins", nbins=4)
+        xyz6, box6, desc6 = catalogue(w6, args.scale, rank)
+        c6 = torch.from_numpy(xyz6).to(dev)
+        res6 = []
+        for k in range(max(1, args.warmup) + args.steps):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record()
+            g6 = build_graph(c6, box6, w6.periodic, w6.edges_lu)
+            e1.record()
+            ev6, od6 = g6.count_4pcf6()
+            e2.record()
+            torch.cuda.synchronize()
+            if k >= max(1, args.warmup):
+                res6.append((e0.elapsed_time(e2), e1.elapsed_time(e2), int(as_uint64(ev6).sum()),
+                             int(od6.sum().item())))
+            g6.free()
+        s6 = statistics.mean(r[0] for r in res6)
+        k6 = statistics.mean(r[1] for r in res6)
+        fourpcf6 = {"config": desc6, "ms_per_step": s6, "count_ms": k6, "configurations": int(len(ev6)),
+                    "tetrahedra": res6[-1][2], "odd_sum": res6[-1][3],
+                    "tetrahedra_per_s": res6[-1][2] / (s6 / 1e3)}
+
     # CPU oracle on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -401,7 +446,6 @@ def run_ours(args, w):
                           f"catalogue: {len(sample)} points, {e} directed edges, {t} triangles, "
                           f"graph + count in {dt:.1f} s")}
 
-    peak, peak_kind = hbm_peak()
     achieved = alg_bytes / (count_ms / 1e3) / 1e9
     traffic = profiled_traffic(w.name) if args.scale == 1.0 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -422,7 +466,8 @@ def run_ours(args, w):
                 "triangles_per_step": tris_all, "n_edges": n_edges, "build_ms": build_ms,
                 "count_ms": count_ms_max, "wall_s_timed": t_wall,
                 "graph_stats": st, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clocks, "parity_4pcf": parity}
+                "gpu_launches": launches, "clocks": clocks, "parity_4pcf": parity,
+                "fourpcf6": fourpcf6, "twopcf": twopcf}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

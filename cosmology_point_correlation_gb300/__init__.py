@@ -26,7 +26,7 @@ from ._lib import GramsciError
 __all__ = ["Graph", "GramsciError", "build_graph", "count_3pcf_from_host",
            "count_4pcf_parity_from_host", "config_count_3pcf", "config_count_4pcf",
            "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path", "kernel_launches",
-           "equilateral", "isosceles", "xi_natural"]
+           "equilateral", "isosceles", "xi_natural", "config_tuples_4pcf6", "zeta4_disconnected"]
 
 
 def library_path() -> str:
@@ -260,6 +260,29 @@ def xi_natural(dd, rr, n_data: int, n_random: int):
     nr = n_random * (n_random - 1) / 2.0
     with np.errstate(divide="ignore", invalid="ignore"):
         return (dd / nd) / (rr / nr) - 1.0
+
+
+def config_tuples_4pcf6(nbins: int) -> np.ndarray:
+    """int32 [n_configs, 6]: the smallest bin tuple (b01, b02, b03, b12, b13, b23)
+    of every six-bin 4pCF configuration, in index order."""
+    lib = _lib.load()
+    n = lib.gs_config_count_4pcf6(nbins)
+    if n < 0:
+        raise GramsciError(_lib.GS_ERR_ARG, "nbins outside 1..10")
+    out = np.zeros((n, 6), dtype=np.int32)
+    for c in range(n):
+        _lib.check(lib.gs_config_tuple_4pcf6(nbins, c, out[c].ctypes.data_as(ctypes.c_void_p)))
+    return out
+
+
+def zeta4_disconnected(xi, nbins: int) -> np.ndarray:
+    """Disconnected 4pCF of every six-bin configuration (GRAMSCI v2 §III.3,
+    Eq.(4)): xi(r01) xi(r23) + xi(r02) xi(r13) + xi(r03) xi(r12), the sum over
+    the three ways of splitting the four points into two pairs, evaluated on
+    the configuration's bins; xi is the binned 2pCF (length nbins)."""
+    x = np.asarray(xi, dtype=np.float64)
+    t = config_tuples_4pcf6(nbins)
+    return x[t[:, 0]] * x[t[:, 5]] + x[t[:, 1]] * x[t[:, 4]] + x[t[:, 2]] * x[t[:, 3]]
 
 
 def _ids(ids, device):

@@ -28,6 +28,7 @@ SIGNATURES = {
     "gs_count_2pcf": (_int, [_p, _p, _p]),
     "gs_count_4pcf6": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_config_count_4pcf6": (_i64, [_int]),
+    "gs_config_tuple_4pcf6": (_int, [_int, _i64, _p]),
     "gs_count_4pcf_parity_hubs": (_int, [_p, _p, _i64, _p, _p, _p]),
     "gs_graph_export_rows": (_int, [_p, _p, _i64, _p, _p, _p, _p]),
     "gs_graph_info": (_int, [_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i32)]),

@@ -343,6 +343,37 @@ static gs_status c6_prepare(gs_graph_t g)
     return GS_OK;
 }
 
+extern "C" gs_status gs_config_tuple_4pcf6(int nbins, int64_t config, int32_t *tuple_host)
+{
+    gs_clear_error();
+    if (nbins < 1 || nbins > C6_MAX_BINS || !tuple_host) return gs_set_error(GS_ERR_ARG, "bad argument");
+    int n = 0;
+    static thread_local int cached_nb = 0;
+    static thread_local std::vector<int64_t> canon_packed;
+    if (cached_nb != nbins) {
+        std::vector<int32_t> t = c6_table(nbins, &n);
+        canon_packed.assign((size_t)n, 0);
+        size_t nt = t.size();
+        std::vector<int32_t> first(n, -1);
+        // the smallest packed tuple of each configuration is the canonical one
+        for (size_t q = 0; q < nt; ++q) {
+            const int c = t[q] >> 2;
+            if (first[c] < 0) {
+                first[c] = (int32_t)q;
+                canon_packed[c] = (int64_t)q;
+            }
+        }
+        cached_nb = nbins;
+    }
+    if (config < 0 || config >= (int64_t)canon_packed.size()) return gs_set_error(GS_ERR_ARG, "configuration out of range");
+    int64_t q = canon_packed[config];
+    for (int k = 5; k >= 0; --k) {
+        tuple_host[k] = (int32_t)(q % nbins);
+        q /= nbins;
+    }
+    return GS_OK;
+}
+
 extern "C" int64_t gs_config_count_4pcf6(int nbins)
 {
     if (nbins < 1 || nbins > C6_MAX_BINS) return -1;

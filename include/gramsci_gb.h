@@ -180,6 +180,11 @@ gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
                          int64_t hub_begin, int64_t hub_end, void *cuda_stream);
 int64_t gs_config_count_4pcf6(int nbins);
 
+/* The smallest bin tuple (b01, b02, b03, b12, b13, b23) of six-bin 4pCF
+ * configuration `config` (host call, no device work): tuple_host int32 [6].
+ * Errors: GS_ERR_ARG (nbins outside 1..10, config out of range). */
+gs_status gs_config_tuple_4pcf6(int nbins, int64_t config, int32_t *tuple_host);
+
 /* Internal 2pCF pair counts: the number of unordered pairs {i, j} in each
  * radial bin, from one sweep of the graph's bin bytes (§III.3: the two-point
  * function on the same graph and binning as the higher-order counts).

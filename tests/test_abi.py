@@ -75,3 +75,21 @@ def test_3pcf_slices_follow_the_configuration_order(lib):
     assert isosceles(hist, nb, 3).tolist() == [cfg.index(tuple(sorted((3, 3, c)))) for c in range(nb)]
     xi = xi_natural([10, 0], [10, 5], 101, 101)
     assert xi[0] == 0.0 and xi[1] == -1.0
+
+
+def test_six_bin_configuration_tuples_and_disconnected_term(lib):
+    import oracle
+    from cosmology_point_correlation_gb300 import config_tuples_4pcf6, zeta4_disconnected
+    assert lib.gs_config_count_4pcf6(4) == 276 and lib.gs_config_count_4pcf6(11) == -1
+    t = config_tuples_4pcf6(4)
+    assert t.shape == (276, 6)
+    for k in range(0, 276, 7):              # the oracle's own enumeration agrees
+        assert oracle.config_index6(4, t[k]) == k
+    xi = np.array([0.5, 0.25, 0.125, 0.0625])
+    z = zeta4_disconnected(xi, 4)
+    k = oracle.config_index6(4, (0, 1, 2, 2, 2, 3))
+    # pairings (01,23), (02,13), (03,12): xi0*xi3 + xi1*xi2 + xi2*xi2
+    assert z[k] == xi[0] * xi[3] + xi[1] * xi[2] + xi[2] * xi[2]
+    # Eq.(4) is the same for every labelling of a tetrahedron
+    k0 = oracle.config_index6(4, (0, 0, 0, 0, 0, 0))
+    assert z[k0] == 3 * xi[0] ** 2
