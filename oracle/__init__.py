@@ -15,6 +15,9 @@ code with the CUDA library. Every function follows the GRAMSCI v2 paper
   configuration the smallest bin tuple over vertex orderings, odd channel the
   sign of V for a minimal ordering of a chiral configuration; §II.2, §III.2,
   276 configurations for 4 bins as in §V.2).
+- ``count_2pcf_weighted`` / ``count_3pcf_weighted``: exact sums of products of
+  signed integer weights (§II.1, §III.3: the Landy-Szalay / Szapudi-Szalay
+  numerators), in 128-bit integers.
 - ``row``, ``count_3pcf_hubs``, ``count_4pcf_parity_hubs``: per point / per hub
   results from brute-force rows, for sampled checks at full size.
 
@@ -65,6 +68,8 @@ def _load():
         lib.oracle_4pcf_parity_hubs.argtypes = cat + [_p, _i64, _p, _p]
         lib.oracle_3pcf_hubs.argtypes = cat + [_p, _i64, _p]
         lib.oracle_4pcf6.argtypes = cat + [_p, _p, _i64, _i64, _p, _p]
+        lib.oracle_2pcf_weighted.argtypes = cat + [_p, _p]
+        lib.oracle_3pcf_weighted.argtypes = cat + [_p, _p, _p, _p, _p]
         lib.oracle_brute4six.argtypes = cat + [_p, _p]
         lib.oracle_nconfig6.argtypes = [_int]
         lib.oracle_nconfig6.restype = _i64
@@ -227,6 +232,35 @@ def brute4six(xyz, box_lu, periodic, edges_lu):
     odd = np.zeros(m, dtype=np.int64)
     lib.oracle_brute4six(*cat, _ptr(even), _ptr(odd))
     return even, odd
+
+
+def from_words128(words) -> list:
+    """Python ints from (low, high) int64 word pairs."""
+    a = np.asarray(words, dtype=np.int64).reshape(-1, 2)
+    return [int(lo) % (1 << 64) + (int(hi) << 64) for lo, hi in a]
+
+
+def count_2pcf_weighted(xyz, box_lu, periodic, edges_lu, w) -> list:
+    """Exact sum of w_i w_j over the pairs of each bin (Python ints); brute force."""
+    lib = _load()
+    xyz, edges, nb, cat = _cat(xyz, box_lu, periodic, edges_lu)
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.int16))
+    out = np.zeros(2 * nb, dtype=np.int64)
+    lib.oracle_2pcf_weighted(*cat, _ptr(w), _ptr(out))
+    return from_words128(out)
+
+
+def count_3pcf_weighted(xyz, box_lu, periodic, edges_lu, w, g: Graph | None = None) -> list:
+    """Exact sum of w_i w_j w_k over the triangles of each configuration (Python ints)."""
+    lib = _load()
+    xyz, edges, nb, cat = _cat(xyz, box_lu, periodic, edges_lu)
+    if g is None:
+        g = graph(xyz, box_lu, periodic, edges)
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.int16))
+    out = np.zeros(2 * nconfig3(nb), dtype=np.int64)
+    gargs, keep = _graph_args(g)
+    lib.oracle_3pcf_weighted(*cat, *gargs, _ptr(w), _ptr(out))
+    return from_words128(out)
 
 
 def count_3pcf_hubs(xyz, box_lu, periodic, edges_lu, hubs) -> np.ndarray:

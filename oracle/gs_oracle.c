@@ -860,3 +860,86 @@ int64_t oracle_config_index6(int nb, const int32_t *t)
     for (int k = 0; k < 6; ++k) w[k] = t[k];
     return six_count_and_index(nb, w);
 }
+
+/* ------------------------------------------------------------------------ */
+/* weighted 2pCF and 3pCF (signed integer weights, exact)                    */
+/*
+ * GRAMSCI v2 §II.1 / §III.3: counts are accumulated with signed per-point
+ * weights (data positive, randoms negative), so that the pair sum is the
+ * Landy-Szalay numerator DD - 2DR + RR. Here the weights are integers (a
+ * caller scales real weights by 2^F); sums are exact, in 128 bits, written
+ * as two int64 words per bin (low word, then high word).
+ */
+
+static void put128(__int128 v, int64_t *out)
+{
+    out[0] = (int64_t)(uint64_t)v;               /* low 64 bits */
+    out[1] = (int64_t)(v >> 64);                  /* high 64 bits, signed */
+}
+
+/* sum over unordered pairs {i, j} in bin b of w_i w_j */
+void oracle_2pcf_weighted(const int32_t *xyz, int64_t n, int64_t box, int periodic, const int64_t *edges, int nb,
+                          const int16_t *w, int64_t *out)
+{
+    cat_t c = { xyz, n, box, periodic, edges, nb };
+    __int128 *acc = (__int128 *)calloc((size_t)nb, sizeof(__int128));
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = i + 1; j < n; ++j) {
+            int b = pair_bin(&c, i, j);
+            if (b >= 0) acc[b] += (__int128)w[i] * w[j];
+        }
+    for (int b = 0; b < nb; ++b) put128(acc[b], out + 2 * b);
+    free(acc);
+}
+
+typedef struct {
+    cat_t c;
+    const int64_t *row_ptr;
+    const int32_t *nbr;
+    const uint8_t *bin;
+    const int16_t *w;
+    const int32_t *t3;
+    int64_t ncfg;
+    __int128 *acc;          /* [threads][ncfg] */
+} wtri_ctx_t;
+
+static void wtri_hub(void *vctx, int tid, int64_t i)
+{
+    wtri_ctx_t *t = (wtri_ctx_t *)vctx;
+    __int128 *h = t->acc + (size_t)tid * (size_t)t->ncfg;
+    int nb = t->c.nb;
+    for (int64_t a = t->row_ptr[i]; a < t->row_ptr[i + 1]; ++a) {
+        int64_t j = t->nbr[a];
+        if (j <= i) continue;
+        for (int64_t b = a + 1; b < t->row_ptr[i + 1]; ++b) {
+            int64_t k = t->nbr[b];
+            int bjk = pair_bin(&t->c, j, k);
+            if (bjk < 0) continue;
+            int v[3] = { t->bin[a], t->bin[b], bjk };
+            sort3(v);
+            h[t->t3[((size_t)v[0] * nb + v[1]) * nb + v[2]]] += (__int128)t->w[i] * t->w[j] * t->w[k];
+        }
+    }
+}
+
+/* sum over triangles {i, j, k} in each sorted-bin configuration of w_i w_j w_k */
+void oracle_3pcf_weighted(const int32_t *xyz, int64_t n, int64_t box, int periodic, const int64_t *edges, int nb,
+                          const int64_t *row_ptr, const int32_t *nbr, const uint8_t *bin, const int16_t *w,
+                          int64_t *out)
+{
+    int nt = oracle_threads();
+    wtri_ctx_t t;
+    t.c = (cat_t){ xyz, n, box, periodic, edges, nb };
+    t.row_ptr = row_ptr; t.nbr = nbr; t.bin = bin; t.w = w;
+    t.t3 = table3(nb);
+    t.ncfg = oracle_nconfig3(nb);
+    t.acc = (__int128 *)calloc((size_t)nt * (size_t)t.ncfg, sizeof(__int128));
+    parallel_for(0, n, nt, wtri_hub, &t);
+    for (int64_t x = 0; x < t.ncfg; ++x) {
+        __int128 s = 0;
+        for (int q = 0; q < nt; ++q) s += t.acc[(size_t)q * t.ncfg + x];
+        put128(s, out + 2 * x);
+    }
+    free(t.acc);
+    free((void *)t.t3);
+}

@@ -367,3 +367,55 @@ def test_2pcf_matches_numpy_pairs(periodic):
     ref = np.bincount(b[b >= 0], minlength=len(edges) - 1).astype(np.uint64)
     assert np.array_equal(oracle.count_2pcf(xyz, box, periodic, edges), ref)
     assert ref.sum() > 100
+
+
+# ---------------------------------------------------------------- weighted counts (exact)
+
+def test_weighted_counts_reduce_to_unweighted_and_scale():
+    box = 20000
+    xyz = catalogues.neyman_scott(200, box / 1024, 6, 30.0, 1.5, 8)
+    edges = [0, 900, 1800, 3000]
+    ones = np.ones(len(xyz), dtype=np.int16)
+    assert oracle.count_2pcf_weighted(xyz, box, 1, edges, ones) == [int(v) for v in oracle.count_2pcf(xyz, box, 1, edges)]
+    assert oracle.count_3pcf_weighted(xyz, box, 1, edges, ones) == [int(v) for v in oracle.count_3pcf(xyz, box, 1, edges)]
+    big = np.full(len(xyz), 30000, dtype=np.int16)
+    h = oracle.count_3pcf(xyz, box, 1, edges)
+    assert oracle.count_3pcf_weighted(xyz, box, 1, edges, big) == [int(v) * 30000 ** 3 for v in h]
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+def test_weighted_counts_against_python_big_ints(periodic):
+    box = 16000
+    xyz = catalogues.neyman_scott(90, box / 1024, 5, 15.0, 1.5, 31 + periodic)
+    edges = [0, 700, 1500, 2600, 4000]
+    w = np.random.default_rng(4).integers(-32768, 32768, size=len(xyz)).astype(np.int16)
+    B, _ = fx.np_bins(xyz, box, periodic, edges)
+    nb = len(edges) - 1
+    ref2 = [0] * nb
+    for i, j in itertools.combinations(range(len(xyz)), 2):
+        if B[i, j] >= 0:
+            ref2[B[i, j]] += int(w[i]) * int(w[j])
+    assert oracle.count_2pcf_weighted(xyz, box, periodic, edges, w) == ref2
+    index = {c: n for n, c in enumerate(fx.configs3(nb))}
+    ref3 = [0] * len(index)
+    for i, j, k in itertools.combinations(range(len(xyz)), 3):
+        b = (B[i, j], B[i, k], B[j, k])
+        if min(b) >= 0:
+            ref3[index[tuple(sorted(int(x) for x in b))]] += int(w[i]) * int(w[j]) * int(w[k])
+    assert oracle.count_3pcf_weighted(xyz, box, periodic, edges, w) == ref3
+
+
+def test_weighted_pair_sum_is_the_landy_szalay_numerator():
+    # data weight +1, random weight -1 on the union: sum w_i w_j = DD - DR + RR,
+    # with DR = (pairs of the union) - DD - RR from unweighted counts
+    box = 30000
+    d = catalogues.neyman_scott(300, box / 1024, 6, 50.0, 1.5, 2)
+    r = catalogues.uniform(300, box / 1024, 3)
+    edges = catalogues.linear_edges_lu(6.0, 5)
+    u = np.vstack([d, r])
+    w = np.concatenate([np.ones(300), -np.ones(300)]).astype(np.int16)
+    dd = oracle.count_2pcf(d, box, 1, edges).astype(np.int64)
+    rr = oracle.count_2pcf(r, box, 1, edges).astype(np.int64)
+    tot = oracle.count_2pcf(u, box, 1, edges).astype(np.int64)
+    dr = tot - dd - rr
+    assert oracle.count_2pcf_weighted(u, box, 1, edges, w) == [int(v) for v in dd - dr + rr]
