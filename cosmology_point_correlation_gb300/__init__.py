@@ -61,6 +61,13 @@ def as_uint64(t) -> np.ndarray:
     return t.detach().cpu().numpy().view(np.uint64)
 
 
+def as_int128(t) -> list:
+    """Python ints from 128-bit two's-complement (low, high) int64 word pairs
+    (the weighted counts' output, shape [m, 2])."""
+    w = np.asarray(t.cpu().numpy() if hasattr(t, "cpu") else t, dtype=np.int64).reshape(-1, 2)
+    return [(int(hi) << 64) + (int(lo) & 0xFFFFFFFFFFFFFFFF) for lo, hi in w]
+
+
 def config_count_3pcf(nbins: int) -> int:
     return _lib.load().gs_config_count_3pcf(nbins)
 
@@ -116,6 +123,37 @@ class Graph:
         if out is None:
             out = torch.empty(self.nbins, dtype=torch.int64, device=self.device)
         _lib.check(_lib.load().gs_count_2pcf(self._h, ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+        return out
+
+    def set_weights(self, weights, stream=None):
+        """Attach int16 fixed-point point weights (input order, a CUDA tensor [n])
+        for the weighted counts; the library keeps its own copy."""
+        torch = _torch()
+        if not (isinstance(weights, torch.Tensor) and weights.is_cuda and weights.dtype == torch.int16):
+            raise TypeError("weights must be an int16 CUDA tensor of shape [n]")
+        weights = weights.contiguous().reshape(-1)
+        if weights.numel() != self.n:
+            raise ValueError(f"weights has {weights.numel()} entries, the graph {self.n} points")
+        _lib.check(_lib.load().gs_graph_set_weights(self._h, ctypes.c_void_p(weights.data_ptr()), _stream(stream)))
+
+    def count_2pcf_weighted(self, out=None, stream=None):
+        """Per bin, the exact sum of w_i w_j over pairs: int64 tensor [nbins, 2] of
+        (low, high) words of a 128-bit integer (see as_int128)."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty((self.nbins, 2), dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_count_2pcf_weighted(self._h, ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+        return out
+
+    def count_3pcf_weighted(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
+        """Per sorted-bin configuration, the exact sum of w_i w_j w_k over triangles:
+        int64 tensor [n_configs, 2] of 128-bit (low, high) words (see as_int128)."""
+        torch = _torch()
+        hub_end = self.n if hub_end is None else hub_end
+        if out is None:
+            out = torch.empty((config_count_3pcf(self.nbins), 2), dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_count_3pcf_weighted(self._h, ctypes.c_void_p(out.data_ptr()),
+                                                      int(hub_begin), int(hub_end), _stream(stream)))
         return out
 
     def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):

@@ -26,6 +26,9 @@ SIGNATURES = {
     "gs_count_4pcf_parity_static": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_count_3pcf_hubs": (_int, [_p, _p, _i64, _p, _p]),
     "gs_count_2pcf": (_int, [_p, _p, _p]),
+    "gs_graph_set_weights": (_int, [_p, _p, _p]),
+    "gs_count_2pcf_weighted": (_int, [_p, _p, _p]),
+    "gs_count_3pcf_weighted": (_int, [_p, _p, _i64, _i64, _p]),
     "gs_count_4pcf6": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_config_count_4pcf6": (_i64, [_int]),
     "gs_config_tuple_4pcf6": (_int, [_int, _i64, _p]),

@@ -416,6 +416,7 @@ static void free_graph_arrays(gs_graph *g)
     cudaFree(g->err);
     cudaFree(g->cfg3);
     cudaFree(g->cfg6);
+    cudaFree(g->w);
 }
 
 extern "C" void gs_graph_free(gs_graph_t g)

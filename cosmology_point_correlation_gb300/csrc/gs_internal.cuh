@@ -41,6 +41,7 @@ struct gs_graph {
     uint16_t *cfg3;            // [nb][nb][nb] idx3(sort(x, y, z)) at (z, x, y), nb <= 40; or NULL
     int32_t *cfg6;             // [nb^6] six-bin 4pCF configuration and orientation (built on first use)
     int ncfg6;
+    int16_t *w;                // [N] point weights in internal order (set by gs_graph_set_weights), or NULL
 };
 
 // ---------------------------------------------------------------- errors

@@ -192,6 +192,37 @@ gs_status gs_config_tuple_4pcf6(int nbins, int64_t config, int32_t *tuple_host);
  * Asynchronous. Errors: GS_ERR_ARG (NULL), GS_ERR_CUDA. */
 gs_status gs_count_2pcf(gs_graph_t g, uint64_t *hist_dev, void *cuda_stream);
 
+/* Point weights for the weighted counts (§II.1: counts accumulated with
+ * signed, normalised data-minus-random weights, the Landy-Szalay and
+ * Szapudi-Szalay estimators). The weights are int16 fixed-point values: a
+ * caller scales real weights by 2^F (|w| <= 32767), and the sums below are
+ * then exact integers in units of 2^(2F) (pairs) and 2^(3F) (triangles).
+ *   w_dev  int16 [n], device, in INPUT order; copied (gathered into the
+ *          graph's internal order), so the caller may free it afterwards.
+ * Asynchronous on cuda_stream; the first call allocates 2n bytes on the
+ * graph. Errors: GS_ERR_ARG (NULL), GS_ERR_NOMEM, GS_ERR_CUDA. */
+gs_status gs_graph_set_weights(gs_graph_t g, const int16_t *w_dev, void *cuda_stream);
+
+/* Weighted 2pCF: per radial bin, the sum over unordered pairs {i, j} of
+ * w_i w_j, exact (§III.3: with data weights summing to +1 and random
+ * weights to -1 this is the Landy-Szalay numerator DD - 2DR + RR).
+ *   sums_dev  int64 [2 * nbins], device, overwritten: bin b holds a 128-bit
+ *             two's-complement integer as (low word at 2b, high word at 2b+1)
+ * Asynchronous. Errors: GS_ERR_ARG (NULL, no weights set), GS_ERR_CUDA. */
+gs_status gs_count_2pcf_weighted(gs_graph_t g, int64_t *sums_dev, void *cuda_stream);
+
+/* Weighted 3pCF: per sorted-bin configuration (packed index of
+ * gs_config_index_3pcf), the sum over triangles {i, j, k} of w_i w_j w_k,
+ * exact (§II.1, §II.2: the hub-and-spoke triangle count with each triangle
+ * weighted by its three vertex weights).
+ *   sums_dev  int64 [2 * gs_config_count_3pcf(nbins)], device, overwritten,
+ *             128-bit sums as (low, high) word pairs
+ *   hub_begin, hub_end  internal-order hub range, as for gs_count_3pcf
+ * Limits: nbins <= 40. Errors: GS_ERR_ARG (NULL, no weights set, nbins,
+ * range), GS_ERR_CAPACITY, GS_ERR_CUDA. */
+gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int64_t hub_begin, int64_t hub_end,
+                                 void *cuda_stream);
+
 /* Sizes of a built graph (host outputs; any pointer may be NULL).
  *   n           number of points
  *   n_edges     directed edges, sum of degrees (= 2 x pairs)
