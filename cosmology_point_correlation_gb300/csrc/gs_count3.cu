@@ -18,6 +18,15 @@
 //     caller's uint64 histogram with one global atomic per non-zero bin
 //     before any counter could overflow and when the block exits.
 //
+// Weighted counts (§II.1: signed per-point weights) use the same walk: the
+// chunk also holds each key's weight and a hit adds w_j w_k (|.| <= 2^30) to
+// the block's int64 sum T[config] of the current hub (two 32-bit words with
+// a carry, so that a hit costs one 32-bit shared atomic). A pass over at most
+// C3_SPOKES spokes of one chunk closes at most 2^23 triangles, so |T| stays
+// below 2^53; after each pass the block adds w_i T, an exact 128-bit product,
+// into its own 128-bit slice of a global scratch array (no atomics: each
+// configuration has one owner thread), and a second kernel sums the slices.
+//
 // Rows longer than the table are processed in chunks of the hub row: chunk
 // [c0, c1) holds the k candidates, every spoke at position s < c1 - 1 is
 // walked over keys in (max(j, F[c0] - 1), F[c1 - 1]].
@@ -42,7 +51,12 @@ constexpr int C3_SPAN_PAIRS = C3_SPAN_BITS / 64;
 constexpr int C3_REGION_BITMAP = C3_SPAN_PAIRS * (8 + 2) + C3_TABLE / 4;
 constexpr int C3_REGION_HASH = C3_TABLE * 5;
 constexpr int C3_REGION = ((C3_REGION_BITMAP > C3_REGION_HASH ? C3_REGION_BITMAP : C3_REGION_HASH) + 15) & ~15;
+// weighted: the chunk's weights follow the bins (int16 per key / per slot)
+constexpr int C3_REGION_BITMAP_W = C3_REGION_BITMAP + C3_CHUNK * 2;
+constexpr int C3_REGION_HASH_W = C3_TABLE * 7;
+constexpr int C3_REGION_W = ((C3_REGION_BITMAP_W > C3_REGION_HASH_W ? C3_REGION_BITMAP_W : C3_REGION_HASH_W) + 15) & ~15;
 constexpr int C3_SMEM_HIST_MAX = 12288;          // configurations kept in shared memory (nbins <= 40)
+constexpr int C3_WEIGHTED_MAX_BINS = 40;
 constexpr int C3_EMPTY = -1;
 
 struct C3Args {
@@ -60,6 +74,10 @@ struct C3Args {
     // listed hub is counted for it (the whole row is staged, not its forward part)
     const int32_t *hubs;          // [nhubs] input indices, or NULL
     const int32_t *inv;           // input -> internal index
+    // weighted counts: weights in internal order; per-block 128-bit sums
+    // [gridDim.x][ncfg][2] (low, high)
+    const int16_t *w;
+    unsigned long long *gsum;
 };
 
 // Flush the shared histogram into the global one and clear it.
@@ -122,13 +140,16 @@ __device__ __forceinline__ int c3_block_scan(int v, int *s_warp)
     return r;
 }
 
-template <bool SMEM_HIST, bool HUB_LIST>
+template <bool SMEM_HIST, bool HUB_LIST, bool WEIGHTED>
 __global__ void __launch_bounds__(C3_THREADS, 2)
 k_count3(C3Args a)
 {
     // dynamic: the candidate-key region [C3_REGION bytes] (bitmap mode: bitmap,
     // per-pair ranks, chunk bins; hash mode: keys, bins), then (SMEM_HIST only)
-    // the histogram [ncfg] u32 and one nb x nb u16 table per warp
+    // the histogram [ncfg] u32 and one nb x nb u16 table per warp.
+    // WEIGHTED: the region [C3_REGION_W bytes] also holds the weights (bitmap
+    // mode: [C3_CHUNK] after the bins; hash mode: [C3_TABLE] after the bins),
+    // then the pass sums T [ncfg] int64
     extern __shared__ unsigned s_dyn[];
     __shared__ uint16_t s_order[C3_SPOKES];         // spoke positions grouped by b_ij
     __shared__ int s_next;                          // next entry of s_order to hand out
@@ -151,6 +172,10 @@ k_count3(C3Args a)
     unsigned *s_hist = (unsigned *)((char *)s_dyn + C3_REGION);
     uint16_t *tab = (uint16_t *)(s_hist + ((a.ncfg + 3) & ~3)) + warp * nb * nb;
     int tab_z = -1;
+    // weighted
+    int16_t *s_cw = (int16_t *)(s_cbin + C3_CHUNK);                   // [C3_CHUNK] weights in key order
+    int16_t *s_hw = (int16_t *)(s_bin + C3_TABLE);                    // [C3_TABLE] weights per slot
+    unsigned long long *s_T = (unsigned long long *)((char *)s_dyn + C3_REGION_W);
 
     // idx3(a, b, c) = F(a) - G(a) + G(b) - b + c with F(a) = idx3(a, a, a) and
     // G(t) = t nb - t (t - 1) / 2, split into two per-bin tables.
@@ -159,8 +184,11 @@ k_count3(C3Args a)
         s_lex_a[t] = (int)(gs_idx3(nb, t, t, t) - Gt);
         s_lex_b[t] = (int)(Gt - t);
     }
-    if (SMEM_HIST)
+    if (WEIGHTED) {
+        for (int t = threadIdx.x; t < a.ncfg; t += C3_THREADS) s_T[t] = 0ull;
+    } else if (SMEM_HIST) {
         for (int t = threadIdx.x; t < a.ncfg; t += C3_THREADS) s_hist[t] = 0;
+    }
     if (threadIdx.x == 0) s_pending = 0;
     __syncthreads();
 
@@ -173,6 +201,7 @@ k_count3(C3Args a)
         const long long i = HUB_LIST ? (long long)a.inv[a.hubs[s_hub]] : s_hub;
         const int64_t f0 = HUB_LIST ? a.row_ptr[i] : a.row_ptr[i] + a.fwd[i];
         const int f = (int)(a.row_ptr[i + 1] - f0);
+        const long long wi = WEIGHTED ? (long long)a.w[i] : 0;
         for (int c0 = 0; c0 < f; c0 += C3_CHUNK) {           // chunks of candidate keys
             const int c1 = min(f, c0 + C3_CHUNK);
             const int cn = c1 - c0;
@@ -186,7 +215,7 @@ k_count3(C3Args a)
             while ((1 << lg) < 4 * cn) ++lg;
             const int tsize = 1 << lg, shift = 32 - lg, mask = tsize - 1;
 
-            if (SMEM_HIST) {
+            if (SMEM_HIST && !WEIGHTED) {
                 // bound on the hits of this chunk: every spoke before c1 closes at
                 // most cn triangles
                 const unsigned long long bound = (unsigned long long)c1 * cn;
@@ -209,6 +238,7 @@ k_count3(C3Args a)
                     const int off = a.nbr[f0 + c0 + t] - kfirst;
                     atomicOr(reinterpret_cast<unsigned *>(s_bm) + (off >> 5), 1u << (off & 31));
                     s_cbin[t] = a.bin[f0 + c0 + t];
+                    if (WEIGHTED) s_cw[t] = a.w[off + kfirst];
                 }
                 __syncthreads();
                 const int per = (npairs + C3_THREADS - 1) / C3_THREADS;
@@ -228,6 +258,7 @@ k_count3(C3Args a)
                     uint32_t h = gs_hash(k, shift);
                     while (atomicCAS(&s_key[h], C3_EMPTY, k) != C3_EMPTY) h = (h + 1) & mask;
                     s_bin[h] = a.bin[f0 + c0 + t];
+                    if (WEIGHTED) s_hw[h] = a.w[k];
                 }
             }
 
@@ -271,7 +302,7 @@ k_count3(C3Args a)
                     const int s = sb + s_order[li];
                     const int32_t j = a.nbr[f0 + s];
                     const int bij = a.bin[f0 + s];
-                    if (SMEM_HIST && bij != tab_z) {
+                    if (SMEM_HIST && !WEIGHTED && bij != tab_z) {
                         c3_fill_tab(tab, a.cfg3, nb, bij);
                         tab_z = bij;
                     }
@@ -289,9 +320,21 @@ k_count3(C3Args a)
                         p0 = lo;
                     }
                     if (p0 >= pe) continue;
-                    // one triangle with sides (b_ij, b_ik, b_jk)
-                    auto hit = [&](int bik, int bjk) {
-                        if (SMEM_HIST) atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
+                    const int wj = WEIGHTED ? (int)a.w[j] : 0;
+                    // one triangle with sides (b_ij, b_ik, b_jk) and third vertex weight wk
+                    auto hit = [&](int bik, int bjk, int wk) {
+                        if (WEIGHTED) {
+                            // T[c] += w_j w_k (|.| <= 2^30) as a 64-bit integer held in two
+                            // 32-bit words: add to the low word, then the carry out of it
+                            // plus the sign extension to the high word (zero, and skipped,
+                            // for most adds)
+                            unsigned *q = reinterpret_cast<unsigned *>(s_T + c3_index(bij, bik, bjk, s_lex_a, s_lex_b));
+                            const int p = wj * wk;
+                            const unsigned old = atomicAdd(q, (unsigned)p);
+                            const unsigned up = (old + (unsigned)p < old ? 1u : 0u) + (p < 0 ? ~0u : 0u);
+                            if (up) atomicAdd(q + 1, up);
+                        }
+                        else if (SMEM_HIST) atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
                         else atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
                     };
                     // Walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
@@ -330,7 +373,7 @@ k_count3(C3Args a)
                                 if (in && ((vmask >> e) & 1u) && ((w >> (o & 31u)) & 1u)) {
                                     const int rank = s_rank[o >> 6] + ((o & 32u) ? __popc(pr.x) : 0) +
                                                      __popc(w & ((1u << (o & 31u)) - 1u));
-                                    hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu);
+                                    hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
                                 }
                             }
                         } else {
@@ -355,7 +398,8 @@ k_count3(C3Args a)
                             }
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (((vmask >> e) & 1u) && key[e] == k[e]) hit(s_bin[h[e]], (bb >> (8 * e)) & 0xffu);
+                                if (((vmask >> e) & 1u) && key[e] == k[e])
+                                    hit(s_bin[h[e]], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_hw[h[e]] : 0);
                         }
                         // rows are sorted: stop once the step's last key passes kmax
                         if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
@@ -364,34 +408,97 @@ k_count3(C3Args a)
                     }
                 }
                 __syncthreads();
+                if (WEIGHTED) {
+                    // slice[t] += w_i T[t] (128-bit); thread t owns configuration t
+                    unsigned long long *slice = a.gsum + 2 * (size_t)a.ncfg * blockIdx.x;
+                    for (int t = threadIdx.x; t < a.ncfg; t += C3_THREADS) {
+                        const long long v = (long long)s_T[t];
+                        if (v) {
+                            s_T[t] = 0ull;
+                            const unsigned long long lo = (unsigned long long)(wi * v);
+                            const unsigned long long hi = (unsigned long long)__mul64hi(wi, v);
+                            const unsigned long long l0 = slice[2 * t];
+                            slice[2 * t] = l0 + lo;
+                            slice[2 * t + 1] += hi + (l0 + lo < l0 ? 1ull : 0ull);
+                        }
+                    }
+                }
             }
         }
     }
-    if (SMEM_HIST) {
+    if (SMEM_HIST && !WEIGHTED) {
         __syncthreads();
         c3_flush(s_hist, a.ncfg, a.ghist);
+    }
+}
+
+// out[c] = sum over the slices of slice[c], 128-bit (low, high) words.
+__global__ void k_sum128_slices(const unsigned long long *__restrict__ slices, int nslices, int ncfg,
+                                unsigned long long *__restrict__ out)
+{
+    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < ncfg; c += gridDim.x * blockDim.x) {
+        unsigned long long lo = 0, hi = 0;
+        for (int b = 0; b < nslices; ++b) {
+            const unsigned long long l = slices[2 * ((size_t)b * ncfg + c)];
+            const unsigned long long h = slices[2 * ((size_t)b * ncfg + c) + 1];
+            lo += l;
+            hi += h + (lo < l ? 1ull : 0ull);
+        }
+        out[2 * c] = lo;
+        out[2 * c + 1] = hi;
     }
 }
 
 static gs_status launch_count3(gs_graph_t g, C3Args &a, int64_t hubs, cudaStream_t st)
 {
     const int ncfg = a.ncfg;
-    // shared-memory histogram unless it is too large or a chunk's hit bound
-    // (spokes x chunk) could overflow a 32-bit counter
-    const bool smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
-    const size_t dyn = C3_REGION +
-                       (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * g->nb * g->nb : 0);
+    const int nb2 = g->nb * g->nb;
     const bool list = a.hubs != nullptr;
-    auto kern = smem ? (list ? k_count3<true, true> : k_count3<true, false>)
-                     : (list ? k_count3<false, true> : k_count3<false, false>);
+    const bool weighted = a.w != nullptr;
+    bool smem;
+    size_t dyn;
+    decltype(&k_count3<true, true, false>) kern;
+    if (weighted) {
+        smem = true;
+        dyn = C3_REGION_W + sizeof(unsigned long long) * (size_t)ncfg;
+        kern = k_count3<true, false, true>;
+    } else {
+        // shared-memory histogram unless it is too large or a chunk's hit bound
+        // (spokes x chunk) could overflow a 32-bit counter
+        smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
+        dyn = C3_REGION + (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * nb2 : 0);
+        kern = smem ? (list ? k_count3<true, true, false> : k_count3<true, false, false>)
+                    : (list ? k_count3<false, true, false> : k_count3<false, false, false>);
+    }
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C3_THREADS, dyn));
-    per_sm = std::max(per_sm, 1);
+    if (per_sm < 1) return gs_set_error(GS_ERR_CAPACITY, "3pCF workspace of %zu bytes does not fit in shared memory", dyn);
     const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * per_sm, hubs);
-    kern<<<grid, C3_THREADS, dyn, st>>>(a);
-    gs_note_launch();
-    GS_TRY_CUDA(cudaGetLastError());
+    if (!weighted) {
+        kern<<<grid, C3_THREADS, dyn, st>>>(a);
+        gs_note_launch();
+        GS_TRY_CUDA(cudaGetLastError());
+        return GS_OK;
+    }
+    // weighted: one 128-bit slice per block, then their sum into the output
+    unsigned long long *out = a.gsum, *slices = nullptr;
+    const size_t bytes = 16 * (size_t)ncfg * grid;
+    GS_TRY_CUDA(cudaMallocAsync(&slices, bytes, st));
+    cudaError_t e = cudaMemsetAsync(slices, 0, bytes, st);
+    if (e == cudaSuccess) {
+        a.gsum = slices;
+        kern<<<grid, C3_THREADS, dyn, st>>>(a);
+        gs_note_launch();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        k_sum128_slices<<<(ncfg + 255) / 256, 256, 0, st>>>(slices, grid, ncfg, out);
+        gs_note_launch();
+        e = cudaGetLastError();
+    }
+    cudaFreeAsync(slices, st);
+    GS_TRY_CUDA(e);
     return GS_OK;
 }
 
@@ -470,4 +577,30 @@ extern "C" gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, i
     a.hub_end = count;
     a.hubs = hubs_dev;
     return launch_count3(g, a, count, st);
+}
+
+extern "C" gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int64_t hub_begin, int64_t hub_end,
+                                            void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !sums_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (!g->w) return gs_set_error(GS_ERR_ARG, "no weights: call gs_graph_set_weights first");
+    if (g->nb > C3_WEIGHTED_MAX_BINS)
+        return gs_set_error(GS_ERR_ARG, "the weighted 3pCF supports at most %d bins", C3_WEIGHTED_MAX_BINS);
+    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
+        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
+                            (long long)hub_end, (long long)g->n);
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const int ncfg = (int)gs_ncfg3(g->nb);
+    if (hub_end == hub_begin || g->n_edges == 0) {
+        GS_TRY_CUDA(cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
+        return GS_OK;
+    }
+    GS_TRY_CUDA(cudaMemsetAsync(g->work, 0, sizeof(unsigned long long), st));
+    C3Args a = count3_args(g, nullptr);
+    a.hub_begin = hub_begin;
+    a.hub_end = hub_end;
+    a.w = g->w;
+    a.gsum = (unsigned long long *)sums_dev;
+    return launch_count3(g, a, hub_end - hub_begin, st);
 }

@@ -128,3 +128,22 @@ __device__ __forceinline__ unsigned gs_lanemask_lt()
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
 }
+
+// v added to the 128-bit two's-complement integer (low word p[0], high word
+// p[1]) in global or shared memory: the low word takes v with a 64-bit atomic,
+// the high word the carry out of it plus the sign extension of v.
+__device__ __forceinline__ void gs_add128(unsigned long long *p, long long v)
+{
+    const unsigned long long u = (unsigned long long)v;
+    const unsigned long long old = atomicAdd(p, u);
+    const unsigned long long hi = (old + u < old ? 1ull : 0ull) + (v < 0 ? ~0ull : 0ull);
+    if (hi) atomicAdd(p + 1, hi);
+}
+
+// The 128-bit value (lo, hi) added to the 128-bit integer at p.
+__device__ __forceinline__ void gs_add128w(unsigned long long *p, unsigned long long lo, unsigned long long hi)
+{
+    const unsigned long long old = atomicAdd(p, lo);
+    const unsigned long long h = hi + (old + lo < old ? 1ull : 0ull);
+    if (h) atomicAdd(p + 1, h);
+}

@@ -33,6 +33,7 @@ def test_unit_weights_equal_the_counts():
         _set(g, np.ones(len(xyz), np.int16))
         assert as_int128(g.count_2pcf_weighted()) == [int(v) for v in as_uint64(g.count_2pcf())]
         assert as_int128(g.count_3pcf_weighted()) == [int(v) for v in as_uint64(g.count_3pcf())]
+        assert as_int128(g.count_2pcf_weighted()) == [int(v) for v in as_uint64(g.count_2pcf())]
 
 
 @pytest.mark.parametrize("periodic", [0, 1])
@@ -94,14 +95,17 @@ def test_hub_rows_longer_than_the_table():
     assert h3 == ref
 
 
-def test_many_bins_global_accumulators():
-    # 36 bins: 8436 configurations, beyond the block-local accumulators
-    xyz, box, _ = _clustered(8_000, 21)
-    edges = catalogues.linear_edges_lu(10.0, 36)
-    wt = _weights(len(xyz), 22)
+@pytest.mark.parametrize("nb", [1, 32, 33, 40])
+def test_bin_counts(nb):
+    # 40 bins: 11480 configurations (one block per SM); above 32 bins the
+    # 2pCF takes its shared 128-bit path
+    xyz, box, _ = _clustered(8_000, 21 + nb)
+    edges = catalogues.linear_edges_lu(10.0, nb)
+    wt = _weights(len(xyz), 22 + nb)
     with gpu_graph(xyz, box, 1, edges) as g:
         _set(g, wt)
         assert as_int128(g.count_3pcf_weighted()) == oracle.count_3pcf_weighted(xyz, box, 1, edges, wt)
+        assert as_int128(g.count_2pcf_weighted()) == oracle.count_2pcf_weighted(xyz, box, 1, edges, wt)
 
 
 def test_data_minus_random_weights_and_mirror():
@@ -148,10 +152,11 @@ def test_errors():
 
 @pytest.mark.slow
 def test_bao_workload_unit_weights():
-    # the 2M-point, 30-bin open-box workload: unit weights reproduce the
-    # triangle counts (block-local accumulators, 4960 configurations)
+    # the 2M-point, 30-bin open-box workload (4960 configurations): unit
+    # weights reproduce the triangle and pair counts
     w = configs.BAO_3PCF
     xyz = w.points()
     with gpu_graph(xyz, w.box_lu, w.periodic, w.edges_lu) as g:
         _set(g, np.ones(len(xyz), np.int16))
         assert as_int128(g.count_3pcf_weighted()) == [int(v) for v in as_uint64(g.count_3pcf())]
+        assert as_int128(g.count_2pcf_weighted()) == [int(v) for v in as_uint64(g.count_2pcf())]
