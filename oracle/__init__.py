@@ -70,6 +70,7 @@ def _load():
         lib.oracle_4pcf6.argtypes = cat + [_p, _p, _i64, _i64, _p, _p]
         lib.oracle_2pcf_weighted.argtypes = cat + [_p, _p]
         lib.oracle_3pcf_weighted.argtypes = cat + [_p, _p, _p, _p, _p]
+        lib.oracle_4pcf6_weighted.argtypes = cat + [_p, _p, _p, _i64, _i64, _p, _p]
         lib.oracle_brute4six.argtypes = cat + [_p, _p]
         lib.oracle_nconfig6.argtypes = [_int]
         lib.oracle_nconfig6.restype = _i64
@@ -261,6 +262,25 @@ def count_3pcf_weighted(xyz, box_lu, periodic, edges_lu, w, g: Graph | None = No
     gargs, keep = _graph_args(g)
     lib.oracle_3pcf_weighted(*cat, *gargs, _ptr(w), _ptr(out))
     return from_words128(out)
+
+
+def count_4pcf6_weighted(xyz, box_lu, periodic, edges_lu, w, g: Graph | None = None,
+                         hub_begin: int = 0, hub_end: int | None = None):
+    """Weighted six-bin 4pCF: (even, odd) lists of Python ints per configuration,
+    the exact sums of w_i w_j w_k w_l and of sign x w_i w_j w_k w_l."""
+    lib = _load()
+    xyz, edges, nb, cat = _cat(xyz, box_lu, periodic, edges_lu)
+    if g is None:
+        g = graph(xyz, box_lu, periodic, edges)
+    hub_end = len(xyz) if hub_end is None else hub_end
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.int16))
+    m = nconfig6(nb)
+    even = np.zeros(2 * m, dtype=np.int64)
+    odd = np.zeros(2 * m, dtype=np.int64)
+    nbr = g.nbr if len(g.nbr) else np.zeros(1, dtype=np.int32)
+    lib.oracle_4pcf6_weighted(*cat, _ptr(g.row_ptr), _ptr(nbr), _ptr(w), int(hub_begin), int(hub_end),
+                              _ptr(even), _ptr(odd))
+    return from_words128(even), from_words128(odd)
 
 
 def count_3pcf_hubs(xyz, box_lu, periodic, edges_lu, hubs) -> np.ndarray:

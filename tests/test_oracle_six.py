@@ -129,3 +129,65 @@ def test_invariances_and_hub_ranges(periodic):
     assert np.array_equal(e3, e) and np.array_equal(o3, -o)
     parts = [oracle.count_4pcf6(xyz, box, periodic, edges, g, a, b) for a, b in [(0, 77), (77, 300)]]
     assert np.array_equal(parts[0][0] + parts[1][0], e) and np.array_equal(parts[0][1] + parts[1][1], o)
+
+
+# ---------------------------------------------------------------- weighted (§II.1 signed weights)
+
+def _np_brute_six_weighted(xyz, box, periodic, edges, w):
+    """Python big-int sums of w_a w_b w_c w_d (even) and sign x that (odd)."""
+    nb = len(edges) - 1
+    B, D = fx.np_bins(xyz, box, periodic, edges)
+    index = {t: k for k, t in enumerate(_canonical_list(nb))}
+    even = [0] * len(index)
+    odd = [0] * len(index)
+    for q in itertools.combinations(range(len(xyz)), 4):
+        bm = [[B[q[a], q[b]] if a != b else 0 for b in range(4)] for a in range(4)]
+        if min(bm[a][b] for a, b in PAIRS) < 0:
+            continue
+        t, chiral, o = _canon(bm)
+        W = int(w[q[0]]) * int(w[q[1]]) * int(w[q[2]]) * int(w[q[3]])
+        even[index[t]] += W
+        if chiral:
+            v = fx.det3(D[q[o[0]], q[o[1]]], D[q[o[0]], q[o[2]]], D[q[o[0]], q[o[3]]])
+            odd[index[t]] += ((v > 0) - (v < 0)) * W
+    return even, odd
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+def test_weighted_matches_big_int_brute_force(periodic):
+    box = 9000
+    xyz = catalogues.neyman_scott(34, box / 1024, 3, 12.0, 1.2, 5 + periodic)
+    edges = [0, 1300, 2600, 4400]
+    w = np.random.default_rng(9 + periodic).integers(-32767, 32768, size=len(xyz)).astype(np.int16)
+    ref_e, ref_o = _np_brute_six_weighted(xyz, box, periodic, edges, w)
+    assert sum(1 for v in ref_e if v) > 3 and any(ref_o)
+    assert oracle.count_4pcf6_weighted(xyz, box, periodic, edges, w) == (ref_e, ref_o)
+
+
+def test_weighted_reduces_to_counts_and_subcatalogues():
+    box = 20000
+    xyz = catalogues.neyman_scott(300, box / 1024, 6, 50.0, 1.5, 12)
+    edges = catalogues.linear_edges_lu(4.0, 4)
+    e, o = oracle.count_4pcf6(xyz, box, 1, edges)
+    assert e.sum() > 1000
+    one = np.ones(len(xyz), np.int16)
+    assert oracle.count_4pcf6_weighted(xyz, box, 1, edges, one) == ([int(v) for v in e], [int(v) for v in o])
+    # a constant weight c scales both channels by c^4 (here beyond 2^63)
+    c = -32767
+    we, wo = oracle.count_4pcf6_weighted(xyz, box, 1, edges, np.full(len(xyz), c, np.int16))
+    assert we == [int(v) * c ** 4 for v in e] and wo == [int(v) * c ** 4 for v in o]
+    assert max(we) > 1 << 63
+    # 0/1 weights: only tetrahedra with all four vertices in the subset count,
+    # which is the unweighted count of the subset alone
+    keep = np.random.default_rng(1).uniform(size=len(xyz)) < 0.7
+    se, so = oracle.count_4pcf6(xyz[keep], box, 1, edges)
+    assert oracle.count_4pcf6_weighted(xyz, box, 1, edges, keep.astype(np.int16)) == \
+        ([int(v) for v in se], [int(v) for v in so])
+    # hub ranges add up
+    w = np.random.default_rng(2).integers(-32767, 32768, size=len(xyz)).astype(np.int16)
+    g = oracle.graph(xyz, box, 1, edges)
+    full = oracle.count_4pcf6_weighted(xyz, box, 1, edges, w, g)
+    p1 = oracle.count_4pcf6_weighted(xyz, box, 1, edges, w, g, 0, 123)
+    p2 = oracle.count_4pcf6_weighted(xyz, box, 1, edges, w, g, 123, 300)
+    assert [x + y for x, y in zip(p1[0], p2[0])] == full[0]
+    assert [x + y for x, y in zip(p1[1], p2[1])] == full[1]
