@@ -156,6 +156,22 @@ class Graph:
                                                       int(hub_begin), int(hub_end), _stream(stream)))
         return out
 
+    def count_4pcf6_weighted(self, hub_begin: int = 0, hub_end: int | None = None, stream=None):
+        """Weighted six-bin 4pCF: (even, odd) int64 tensors [n_configs, 2] of
+        128-bit (low, high) words: sums of w_i w_j w_k w_l and of the odd sign
+        times that product (see as_int128)."""
+        torch = _torch()
+        if self.nbins > 10:
+            raise GramsciError(_lib.GS_ERR_ARG, "the six-bin 4pCF supports at most 10 bins")
+        hub_end = self.n if hub_end is None else hub_end
+        m = _lib.load().gs_config_count_4pcf6(self.nbins)
+        even = torch.empty((m, 2), dtype=torch.int64, device=self.device)
+        odd = torch.empty((m, 2), dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_count_4pcf6_weighted(self._h, ctypes.c_void_p(even.data_ptr()),
+                                                       ctypes.c_void_p(odd.data_ptr()), int(hub_begin),
+                                                       int(hub_end), _stream(stream)))
+        return even, odd
+
     def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
         """uint64 triangle histogram over sorted bin triples (int64 tensor on the device)."""
         torch = _torch()

@@ -29,6 +29,7 @@ SIGNATURES = {
     "gs_graph_set_weights": (_int, [_p, _p, _p]),
     "gs_count_2pcf_weighted": (_int, [_p, _p, _p]),
     "gs_count_3pcf_weighted": (_int, [_p, _p, _i64, _i64, _p]),
+    "gs_count_4pcf6_weighted": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_count_4pcf6": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_config_count_4pcf6": (_i64, [_int]),
     "gs_config_tuple_4pcf6": (_int, [_int, _i64, _p]),

@@ -17,6 +17,12 @@
 //      channel adds that parity times sign(det[r_j1; r_j2; r_j3]).
 // Hubs with more than C6_M forward neighbours use a global scratch slice per
 // block instead of shared memory.
+//
+// Weighted counts (§II.1 signed weights): each tetrahedron adds
+// W = w_i w_j1 w_j2 w_j3 (|W| <= 2^60) to the even channel and sign x W to
+// the odd one, into exact 128-bit sums: per block in shared memory as four
+// 32-bit words (gs_add128_u32) when the configurations fit, else straight
+// into the global (low, high) pairs.
 
 #include <algorithm>
 #include <array>
@@ -29,6 +35,7 @@ constexpr int C6_WARPS = C6_THREADS / 32;
 constexpr int C6_M = 256;                   // forward degree kept in shared memory
 constexpr int C6_WORDS = C6_M / 32;
 constexpr int C6_SMEM_HIST_MAX = 4096;
+constexpr int C6_SMEM_W_MAX = 2500;         // weighted: configurations with shared 128-bit sums (nb <= 6)
 constexpr int C6_EMPTY = -1;
 constexpr int C6_MAX_BINS = 10;             // the tuple table holds nb^6 entries
 
@@ -47,6 +54,9 @@ struct C6Args {
     int big_m;                    // large path: forward degree the slices hold
     char *scratch;
     size_t scratch_stride;
+    // weighted counts: weights in internal order; 128-bit sums [ncfg][2]
+    const int16_t *w;
+    unsigned long long *weven, *wodd;
 };
 
 struct C6Space {
@@ -57,11 +67,12 @@ struct C6Space {
     int *vx, *vy, *vz; // [f] spoke vectors
     unsigned *bits;    // [f][W]
     uint8_t *sbin;     // [f][f] spoke-spoke bins (valid where the bit is set)
+    int16_t *ww;       // [f] spoke weights (weighted counts)
 };
 
-template <bool SMEM_HIST>
+template <bool SMEM_HIST, bool WEIGHTED>
 __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long long i, int64_t f0, int f,
-                                       int tlog, unsigned *s_even, int *s_odd)
+                                       int tlog, unsigned *s_even, int *s_odd, unsigned *s_w128)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int W = (f + 31) >> 5;
@@ -77,6 +88,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
         w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
         w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
         w.vz[t] = gs_delta(P.z, Q.z, a.box, a.periodic);
+        if (WEIGHTED) w.ww[t] = a.w[k];
         uint32_t h = gs_hash(k, shift);
         while (atomicCAS(&w.key[h], C6_EMPTY, k) != C6_EMPTY) h = (h + 1) & mask;
         w.pos[h] = t;
@@ -106,6 +118,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     }
     __syncthreads();
 
+    const long long wi = WEIGHTED ? (long long)a.w[i] : 0;
     for (int s1 = warp; s1 < f - 2; s1 += C6_WARPS) {
         const unsigned *row1 = w.bits + (size_t)s1 * W;
         const int b01 = w.hb[s1];
@@ -116,6 +129,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
             const int b02 = w.hb[s2], b12 = w.sbin[(size_t)s1 * f + s2];
             const long long x2 = w.vx[s2], y2 = w.vy[s2], z2 = w.vz[s2];
             const long long cx = y1 * z2 - z1 * y2, cy = z1 * x2 - x1 * z2, cz = x1 * y2 - y1 * x2;
+            const long long w12 = WEIGHTED ? wi * w.ww[s1] * w.ww[s2] : 0;     // |.| <= 2^45
             const int base = ((b01 * nb + b02) * nb) * nb * nb * nb;          // b03, b12, b13, b23 follow
             for (int wd = s2 >> 5; wd < W; ++wd) {
                 unsigned common = row1[wd] & row2[wd];
@@ -130,7 +144,16 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                     const int ci = v >> 2, par = (v & 3) - 1;
                     const long long d = cx * w.vx[s3] + cy * w.vy[s3] + cz * w.vz[s3];
                     const int sg = par * ((d > 0) - (d < 0));
-                    if (SMEM_HIST) {
+                    if (WEIGHTED) {
+                        const long long W = w12 * w.ww[s3];
+                        if (SMEM_HIST) {
+                            gs_add128_u32(s_w128 + 8 * ci, W);
+                            if (sg) gs_add128_u32(s_w128 + 8 * ci + 4, sg * W);
+                        } else {
+                            gs_add128(a.weven + 2 * ci, W);
+                            if (sg) gs_add128(a.wodd + 2 * ci, sg * W);
+                        }
+                    } else if (SMEM_HIST) {
                         atomicAdd(&s_even[ci], 1u);
                         if (sg) atomicAdd(&s_odd[ci], sg);
                     } else {
@@ -156,16 +179,19 @@ __device__ __forceinline__ void c6_flush(unsigned *se, int *so, int ncfg, unsign
 }
 
 // Hubs with 3..C6_M forward neighbours, workspace in shared memory.
-template <bool SMEM_HIST>
-__global__ void __launch_bounds__(C6_THREADS)
+template <bool SMEM_HIST, bool WEIGHTED>
+__global__ void __launch_bounds__(C6_THREADS, 2)
 k_count6_small(C6Args a)
 {
-    extern __shared__ unsigned s_dyn[];         // bits [C6_M*C6_WORDS], sbin [C6_M*C6_M], even, odd
+    // dynamic: bits [C6_M*C6_WORDS], sbin [C6_M*C6_M], then (SMEM_HIST) even,
+    // odd [ncfg] each, or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
+    extern __shared__ unsigned s_dyn[];
     __shared__ int32_t s_key[2 * C6_M];
     __shared__ int32_t s_pos[2 * C6_M];
     __shared__ int32_t s_row[C6_M];
     __shared__ uint8_t s_hb[C6_M];
     __shared__ int s_vx[C6_M], s_vy[C6_M], s_vz[C6_M];
+    __shared__ int16_t s_ww[C6_M];
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;
 
@@ -173,14 +199,17 @@ k_count6_small(C6Args a)
     uint8_t *s_sbin = (uint8_t *)(s_bits + C6_M * C6_WORDS);
     unsigned *s_even = (unsigned *)(s_sbin + C6_M * C6_M);
     int *s_odd = (int *)(s_even + a.ncfg);
-    if (SMEM_HIST)
+    unsigned *s_w128 = s_even;
+    if (SMEM_HIST && WEIGHTED)
+        for (int t = threadIdx.x; t < 8 * a.ncfg; t += C6_THREADS) s_w128[t] = 0;
+    else if (SMEM_HIST)
         for (int t = threadIdx.x; t < a.ncfg; t += C6_THREADS) {
             s_even[t] = 0;
             s_odd[t] = 0;
         }
     for (int t = threadIdx.x; t < 2 * C6_M; t += C6_THREADS) s_key[t] = C6_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
-    C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin };
+    C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin, s_ww };
 
     for (;;) {
         __syncthreads();
@@ -191,7 +220,7 @@ k_count6_small(C6Args a)
         const int64_t f0 = a.row_ptr[i] + a.fwd[i];
         const int f = (int)(a.row_ptr[i + 1] - f0);
         if (f < 3 || f > C6_M) continue;
-        if (SMEM_HIST) {
+        if (SMEM_HIST && !WEIGHTED) {
             const unsigned long long bound = (unsigned long long)f * (f - 1) * (f - 2) / 6;
             if (s_pending + bound > 0x7fffffffull) {
                 c6_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
@@ -203,15 +232,25 @@ k_count6_small(C6Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * f) ++tlog;
-        c6_hub<SMEM_HIST>(a, w, i, f0, f, tlog, s_even, s_odd);
+        c6_hub<SMEM_HIST, WEIGHTED>(a, w, i, f0, f, tlog, s_even, s_odd, s_w128);
     }
-    if (SMEM_HIST) {
+    if (SMEM_HIST && WEIGHTED) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < 2 * a.ncfg; t += C6_THREADS) {
+            const unsigned *q = s_w128 + 4 * t;
+            const unsigned long long lo = q[0] | ((unsigned long long)q[1] << 32);
+            const unsigned long long hi = q[2] | ((unsigned long long)q[3] << 32);
+            unsigned long long *dst = (t & 1) ? a.wodd + 2 * (t >> 1) : a.weven + 2 * (t >> 1);
+            if (lo | hi) gs_add128w(dst, lo, hi);
+        }
+    } else if (SMEM_HIST) {
         __syncthreads();
         c6_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
     }
 }
 
 // Hubs with more than C6_M forward neighbours: workspace in a global slice.
+template <bool WEIGHTED>
 __global__ void __launch_bounds__(C6_THREADS)
 k_count6_large(C6Args a)
 {
@@ -231,6 +270,7 @@ k_count6_large(C6Args a)
     w.bits = (unsigned *)(w.vz + M);
     w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
     w.sbin = w.hb + M;
+    w.ww = (int16_t *)(w.sbin + (size_t)M * M);          // M + M*M is even: 2-byte aligned
     for (int t = threadIdx.x; t < (1 << tlog); t += C6_THREADS) w.key[t] = C6_EMPTY;
 
     for (;;) {
@@ -244,7 +284,7 @@ k_count6_large(C6Args a)
         if (f <= C6_M) continue;
         int tl = 4;
         while ((1 << tl) < 2 * f) ++tl;
-        c6_hub<false>(a, w, i, f0, f, tl, nullptr, nullptr);
+        c6_hub<false, WEIGHTED>(a, w, i, f0, f, tl, nullptr, nullptr, nullptr);
     }
 }
 
@@ -254,7 +294,7 @@ static size_t c6_large_stride(int M)
     while ((1 << tlog) < 2 * M) ++tlog;
     const size_t WM = (size_t)(M + 31) / 32;
     const size_t bytes = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM +
-                         M + (size_t)M * M;
+                         M + (size_t)M * M + sizeof(int16_t) * M;
     return (bytes + 255) & ~(size_t)255;
 }
 
@@ -381,53 +421,24 @@ extern "C" int64_t gs_config_count_4pcf6(int nbins)
     return (b * b * b * b * b * b + 9 * b * b * b * b + 14 * b * b) / 24;
 }
 
-extern "C" gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
-                                    int64_t hub_end, void *cuda_stream)
+// Launch the small-hub and large-hub kernels over [hub_begin, hub_end) of a
+// prepared argument block (outputs already cleared).
+static gs_status c6_launch(gs_graph_t g, C6Args &a, cudaStream_t st)
 {
-    gs_clear_error();
-    if (!g || !even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
-    if (g->nb > C6_MAX_BINS)
-        return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF supports at most %d bins", C6_MAX_BINS);
-    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
-        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
-                            (long long)hub_end, (long long)g->n);
-    if (g->edges[g->nb] >= (1ll << 20))
-        return gs_set_error(GS_ERR_ARG, "the 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
-    gs_status s = c6_prepare(g);
-    if (s != GS_OK) return s;
-    const int ncfg = g->ncfg6;
-    cudaStream_t st = (cudaStream_t)cuda_stream;
-    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
-    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
-    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
-    GS_TRY_CUDA(cudaMemsetAsync(g->work + 3, 0, sizeof(unsigned long long), st));
-
-    C6Args a{};
-    a.pts = g->pts;
-    a.row_ptr = g->row_ptr;
-    a.fwd = g->fwd;
-    a.nbr = g->nbr;
-    a.bin = g->bin;
-    a.cfg6 = g->cfg6;
-    a.hub_begin = hub_begin;
-    a.hub_end = hub_end;
-    a.box = (int)g->box_lu;
-    a.periodic = g->periodic;
-    a.nb = g->nb;
-    a.ncfg = ncfg;
-    a.even = (unsigned long long *)even_dev;
-    a.odd = (long long *)odd_dev;
-    a.cursor = g->work + 3;
-
-    const int64_t hubs = hub_end - hub_begin;
+    const int64_t hubs = a.hub_end - a.hub_begin;
     const int sms = gs_sm_count();
-    const bool smem = ncfg <= C6_SMEM_HIST_MAX;
-    const size_t dyn = sizeof(unsigned) * C6_M * C6_WORDS + (size_t)C6_M * C6_M + (smem ? 8 * (size_t)ncfg : 0);
-    auto kern = smem ? k_count6_small<true> : k_count6_small<false>;
+    const int ncfg = a.ncfg;
+    const bool weighted = a.w != nullptr;
+    const bool smem = weighted ? ncfg <= C6_SMEM_W_MAX : ncfg <= C6_SMEM_HIST_MAX;
+    const size_t acc = weighted ? 32 * (size_t)ncfg : 8 * (size_t)ncfg;
+    const size_t dyn = sizeof(unsigned) * C6_M * C6_WORDS + (size_t)C6_M * C6_M + (smem ? acc : 0);
+    auto kern = weighted ? (smem ? k_count6_small<true, true> : k_count6_small<false, true>)
+                         : (smem ? k_count6_small<true, false> : k_count6_small<false, false>);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C6_THREADS, dyn));
-    per_sm = std::max(per_sm, 1);
+    if (per_sm < 1) return gs_set_error(GS_ERR_CAPACITY, "4pCF workspace of %zu bytes does not fit in shared memory", dyn);
+    GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
     kern<<<(int)std::min<int64_t>((int64_t)sms * per_sm, hubs), C6_THREADS, dyn, st>>>(a);
     gs_note_launch();
     GS_TRY_CUDA(cudaGetLastError());
@@ -440,16 +451,85 @@ extern "C" gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *o
                                                                    (int64_t)(budget / stride)));
         char *scratch = nullptr;
         GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
-        GS_TRY_CUDA(cudaMemsetAsync(g->work + 3, 0, sizeof(unsigned long long), st));
-        a.cursor = g->work + 3;
+        GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        k_count6_large<<<gl, C6_THREADS, 0, st>>>(a);
+        if (weighted) k_count6_large<true><<<gl, C6_THREADS, 0, st>>>(a);
+        else k_count6_large<false><<<gl, C6_THREADS, 0, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
         if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
     return GS_OK;
+}
+
+static gs_status c6_check(gs_graph_t g, int64_t hub_begin, int64_t hub_end)
+{
+    if (g->nb > C6_MAX_BINS)
+        return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF supports at most %d bins", C6_MAX_BINS);
+    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
+        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
+                            (long long)hub_end, (long long)g->n);
+    if (g->edges[g->nb] >= (1ll << 20))
+        return gs_set_error(GS_ERR_ARG, "the 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
+    return c6_prepare(g);
+}
+
+static C6Args c6_args(gs_graph_t g, int64_t hub_begin, int64_t hub_end)
+{
+    C6Args a{};
+    a.pts = g->pts;
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.cfg6 = g->cfg6;
+    a.hub_begin = hub_begin;
+    a.hub_end = hub_end;
+    a.box = (int)g->box_lu;
+    a.periodic = g->periodic;
+    a.nb = g->nb;
+    a.ncfg = g->ncfg6;
+    a.cursor = g->work + 3;
+    return a;
+}
+
+extern "C" gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
+                                    int64_t hub_end, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    gs_status s = c6_check(g, hub_begin, hub_end);
+    if (s != GS_OK) return s;
+    const int ncfg = g->ncfg6;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
+    C6Args a = c6_args(g, hub_begin, hub_end);
+    a.even = (unsigned long long *)even_dev;
+    a.odd = (long long *)odd_dev;
+    return c6_launch(g, a, st);
+}
+
+extern "C" gs_status gs_count_4pcf6_weighted(gs_graph_t g, int64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
+                                             int64_t hub_end, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g || !even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    if (!g->w) return gs_set_error(GS_ERR_ARG, "no weights: call gs_graph_set_weights first");
+    gs_status s = c6_check(g, hub_begin, hub_end);
+    if (s != GS_OK) return s;
+    const int ncfg = g->ncfg6;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
+    C6Args a = c6_args(g, hub_begin, hub_end);
+    a.w = g->w;
+    a.weven = (unsigned long long *)even_dev;
+    a.wodd = (unsigned long long *)odd_dev;
+    return c6_launch(g, a, st);
 }

@@ -147,3 +147,26 @@ __device__ __forceinline__ void gs_add128w(unsigned long long *p, unsigned long 
     const unsigned long long h = hi + (old + lo < old ? 1ull : 0ull);
     if (h) atomicAdd(p + 1, h);
 }
+
+// v added to the 128-bit two's-complement integer held in four 32-bit words
+// q[0..3], least significant first, with 32-bit atomics: each word takes its
+// part of v plus the carry out of the word below (computed from the value the
+// atomic returned); words whose addend is zero are skipped. The carries of
+// concurrent adds each count once, so the sum of all adds is exact mod 2^128.
+__device__ __forceinline__ void gs_add128_u32(unsigned *q, long long v)
+{
+    const unsigned long long u = (unsigned long long)v;
+    const unsigned ext = v < 0 ? 0xffffffffu : 0u;
+    const unsigned part[4] = { (unsigned)u, (unsigned)(u >> 32), ext, ext };
+    unsigned carry = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const unsigned long long add = (unsigned long long)part[k] + carry;   // <= 2^32
+        const unsigned lo = (unsigned)add;
+        carry = (unsigned)(add >> 32);                                      // 1 only when lo == 0
+        if (lo) {
+            const unsigned old = atomicAdd(q + k, lo);
+            carry = (old + lo < old) ? 1u : 0u;
+        }
+    }
+}

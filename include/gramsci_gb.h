@@ -180,6 +180,18 @@ gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
                          int64_t hub_begin, int64_t hub_end, void *cuda_stream);
 int64_t gs_config_count_4pcf6(int nbins);
 
+/* Weighted six-bin 4pCF (§II.1 signed weights, §III.3: NNNN of the
+ * estimator NNNN / RRRR): per configuration, the exact sums over tetrahedra
+ * of W = w_i w_j w_k w_l (even) and of s W (odd), s the tetrahedron's odd
+ * sign of gs_count_4pcf6 (+1, -1 or 0). Weights from gs_graph_set_weights.
+ *   even_dev, odd_dev  int64 [2 * gs_config_count_4pcf6(nbins)], device,
+ *             overwritten: 128-bit sums as (low, high) word pairs
+ *   hub_begin, hub_end  as for gs_count_4pcf6
+ * Limits and errors as gs_count_4pcf6, plus GS_ERR_ARG when no weights are
+ * set. */
+gs_status gs_count_4pcf6_weighted(gs_graph_t g, int64_t *even_dev, int64_t *odd_dev,
+                                  int64_t hub_begin, int64_t hub_end, void *cuda_stream);
+
 /* The smallest bin tuple (b01, b02, b03, b12, b13, b23) of six-bin 4pCF
  * configuration `config` (host call, no device work): tuple_host int32 [6].
  * Errors: GS_ERR_ARG (nbins outside 1..10, config out of range). */

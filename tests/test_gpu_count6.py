@@ -73,3 +73,71 @@ def test_parity_catalogue_four_bins_full_size():
     assert np.array_equal(e2, e) and np.array_equal(o2, o)
     e3, o3 = _gpu6(mirror(xyz, w.box_lu, True), w.box_lu, True, edges)
     assert np.array_equal(e3, e) and np.array_equal(o3, -o)
+
+
+# ---------------------------------------------------------------- weighted (§II.1 signed weights)
+
+def _gpu6w(xyz, box, periodic, edges, w, ranges=None):
+    from cosmology_point_correlation_gb300 import as_int128
+    from tests.gpu_util import torch_dev
+    torch, dev = torch_dev()
+    with gpu_graph(xyz, box, periodic, edges) as g:
+        g.set_weights(torch.from_numpy(np.ascontiguousarray(w, dtype=np.int16)).to(dev))
+        if ranges is None:
+            e, o = g.count_4pcf6_weighted()
+            return as_int128(e), as_int128(o)
+        parts = [g.count_4pcf6_weighted(a, b) for a, b in ranges]
+        return ([sum(c) for c in zip(*[as_int128(e) for e, _ in parts])],
+                [sum(c) for c in zip(*[as_int128(o) for _, o in parts])])
+
+
+def _weights(n, seed):
+    return np.random.default_rng(seed).integers(-32767, 32768, size=n).astype(np.int16)
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+@pytest.mark.parametrize("n,nb", [(3000, 4), (8000, 5), (3000, 7)])
+def test_weighted_matches_oracle(periodic, n, nb):
+    # 4 and 5 bins: block sums in shared memory; 7 bins (5475 configurations):
+    # straight into the global sums
+    L = 500.0 * (n / 200_000) ** (1 / 3)
+    box = catalogues.box_lattice(L)
+    xyz = catalogues.neyman_scott(n, L, max(1, n // 50), 50.0, 3.0, 21 + n + periodic)
+    edges = catalogues.linear_edges_lu(20.0, nb)
+    w = _weights(n, n + nb)
+    ref = oracle.count_4pcf6_weighted(xyz, box, periodic, edges, w)
+    assert any(ref[1])
+    assert _gpu6w(xyz, box, periodic, edges, w) == ref
+
+
+def test_weighted_large_hub_and_extreme_weights():
+    rng = np.random.default_rng(8)
+    R = 20000
+    v = rng.normal(size=(300, 3))
+    v *= (0.9 * R * (0.5 + 0.5 * rng.uniform(size=(300, 1)))) / np.linalg.norm(v, axis=1, keepdims=True)
+    xyz = (np.vstack([[[0, 0, 0]], np.rint(v)]) + 25000).astype(np.int32)
+    edges = [0, 8000, 12000, 16000, R]
+    w = _weights(len(xyz), 3)
+    assert _gpu6w(xyz, 50000, 0, edges, w) == oracle.count_4pcf6_weighted(xyz, 50000, 0, edges, w)
+    # constant -32767: every term is (-32767)^4 ~ 2^60, sums leave int64
+    c = np.full(len(xyz), -32767, np.int16)
+    e, o = oracle.count_4pcf6(xyz, 50000, 0, edges)
+    ge, go = _gpu6w(xyz, 50000, 0, edges, c)
+    assert ge == [int(x) * 32767 ** 4 for x in e] and go == [int(x) * 32767 ** 4 for x in o]
+    assert max(ge) > 1 << 63
+
+
+def test_weighted_parity_catalogue_unit_weights_and_ranges():
+    w = configs.PARITY_4PCF
+    xyz = w.points()
+    edges = catalogues.linear_edges_lu(w.r_max_mpc, 4)
+    e, o = _gpu6(xyz, w.box_lu, True, edges)
+    one = np.ones(len(xyz), np.int16)
+    assert _gpu6w(xyz, w.box_lu, True, edges, one) == ([int(x) for x in e], [int(x) for x in o])
+    n = len(xyz)
+    wt = _weights(n, 77)
+    full = _gpu6w(xyz, w.box_lu, True, edges, wt)
+    assert _gpu6w(xyz, w.box_lu, True, edges, wt, ranges=[(0, n // 3), (n // 3, n)]) == full
+    # mirror image: even unchanged, odd negated (weights travel with the points)
+    me, mo = _gpu6w(mirror(xyz, w.box_lu, True), w.box_lu, True, edges, wt)
+    assert me == full[0] and mo == [-x for x in full[1]]
