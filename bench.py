@@ -6,7 +6,10 @@ device memory: cell sort, neighbour graph (count + fill), 3pCF merge-walk
 count with its histogram. The default workload is the BAO-scale 3pCF
 (2,000,000 Neyman-Scott points in an open 2000 h^-1 Mpc box, r_max 150,
 30 bins, ~6.7e9 directed edges). The parity-4pCF path is timed the same way
-on its own workload and reported in the "parity_4pcf" object.
+on its own workload and reported in the "parity_4pcf" object; the six-bin
+4pCF, the internal 2pCF and the weighted (signed int16 weights, exact)
+2pCF / 3pCF / six-bin 4pCF counts are timed beside it ("fourpcf6", "twopcf",
+"weighted"), outside the headline step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -60,6 +63,8 @@ def parse_args():
     p.add_argument("--only-parity", action="store_true",
                    help="time only the parity-4pCF path and print its own line")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-weighted", action="store_true",
+                   help="skip the weighted 2pCF / 3pCF / six-bin 4pCF timings")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sample-points", type=int, default=10_000,
                    help="points in the sub-cube the CPU oracle counts")
@@ -330,6 +335,27 @@ def run_ours(args, w):
             torch.cuda.synchronize()
             t2.append(e0.elapsed_time(e1))
         pairs = int(as_uint64(dd).sum())
+        # weighted counts on the same graph: signed int16 weights, exact 128-bit sums
+        weighted = None
+        if not args.no_weighted:
+            wts = torch.from_numpy(np.random.default_rng(w.seed + 17).integers(
+                -32767, 32768, size=len(xyz)).astype(np.int16)).to(dev)
+            g.set_weights(wts)
+
+            def _timed(fn):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1)
+
+            g.count_3pcf_weighted(0, max(1, len(xyz) // 64))          # warm-up on a hub slice
+            g.count_2pcf_weighted()
+            t3w = _timed(lambda: g.count_3pcf_weighted())
+            t2w = statistics.mean(_timed(lambda: g.count_2pcf_weighted()) for _ in range(3))
+            weighted = {"weights": "uniform random int16 in [-32767, 32767]",
+                        "threepcf_count_ms": t3w, "twopcf_ms": t2w}
     alg_bytes = BYTES_PER_EDGE * (st["n_edges"] // 2 + st["spoke_walk"])
     peak, peak_kind = hbm_peak()
     t2_ms = statistics.mean(t2)
@@ -436,6 +462,22 @@ def run_ours(args, w):
                     "tetrahedra": res6[-1][2], "odd_sum": res6[-1][3],
                     "tetrahedra_per_s": res6[-1][2] / (s6 / 1e3)}
 
+    # weighted six-bin 4pCF on the same 4-bin parity catalogue
+    if fourpcf6 is not None and weighted is not None:
+        with build_graph(c6, box6, w6.periodic, w6.edges_lu) as g6:
+            g6.set_weights(torch.from_numpy(np.random.default_rng(w6.seed + 17).integers(
+                -32767, 32768, size=len(xyz6)).astype(np.int16)).to(dev))
+            g6.count_4pcf6_weighted()
+            t6 = []
+            for _ in range(max(1, args.steps)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g6.count_4pcf6_weighted()
+                e1.record()
+                torch.cuda.synchronize()
+                t6.append(e0.elapsed_time(e1))
+        weighted["fourpcf6_count_ms"] = statistics.mean(t6)
+
     # CPU oracle on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -467,7 +509,7 @@ def run_ours(args, w):
                 "count_ms": count_ms_max, "wall_s_timed": t_wall,
                 "graph_stats": st, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clocks, "parity_4pcf": parity,
-                "fourpcf6": fourpcf6, "twopcf": twopcf}
+                "fourpcf6": fourpcf6, "twopcf": twopcf, "weighted": weighted}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -26,7 +26,8 @@ from ._lib import GramsciError
 __all__ = ["Graph", "GramsciError", "build_graph", "count_3pcf_from_host",
            "count_4pcf_parity_from_host", "config_count_3pcf", "config_count_4pcf",
            "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path", "kernel_launches",
-           "equilateral", "isosceles", "xi_natural", "config_tuples_4pcf6", "zeta4_disconnected"]
+           "equilateral", "isosceles", "xi_natural", "config_tuples_4pcf6", "zeta4_disconnected",
+           "as_int128", "xi_signed", "zeta4_connected"]
 
 
 def library_path() -> str:
@@ -337,6 +338,31 @@ def zeta4_disconnected(xi, nbins: int) -> np.ndarray:
     x = np.asarray(xi, dtype=np.float64)
     t = config_tuples_4pcf6(nbins)
     return x[t[:, 0]] * x[t[:, 5]] + x[t[:, 1]] * x[t[:, 4]] + x[t[:, 2]] * x[t[:, 3]]
+
+
+def xi_signed(pair_sums, rr):
+    """2pCF per bin from the signed-weight pair sums (GRAMSCI v2 §III.3): with
+    data weights summing to +1 and random weights to -1 the pair sum is the
+    Landy-Szalay numerator DD - 2DR + RR, so xi = (signed pair sum) / RR. Both
+    arguments are per-bin sums in the same weight units (e.g. as_int128 of
+    count_2pcf_weighted on the joint catalogue, and on the randoms alone)."""
+    s = np.array([float(v) for v in pair_sums], dtype=np.float64)
+    r = np.array([float(v) for v in rr], dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return s / r
+
+
+def zeta4_connected(nnnn, rrrr, xi, nbins: int) -> np.ndarray:
+    """Connected six-bin 4pCF, Eq.(5): zeta = NNNN / RRRR per configuration
+    minus the disconnected part of Eq.(4) built from the binned xi. NNNN is the
+    even channel of count_4pcf6_weighted on the joint catalogue, RRRR the same
+    count on the randoms alone (same weight units). The odd channel needs no
+    subtraction: NNNN_odd / RRRR is already connected."""
+    n = np.array([float(v) for v in nnnn], dtype=np.float64)
+    r = np.array([float(v) for v in rrrr], dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        zeta = n / r
+    return zeta - zeta4_disconnected(xi, nbins)
 
 
 def _ids(ids, device):

@@ -93,3 +93,21 @@ def test_six_bin_configuration_tuples_and_disconnected_term(lib):
     # Eq.(4) is the same for every labelling of a tetrahedron
     k0 = oracle.config_index6(4, (0, 0, 0, 0, 0, 0))
     assert z[k0] == 3 * xi[0] ** 2
+
+
+def test_signed_xi_and_connected_four_point(lib):
+    import oracle
+    from cosmology_point_correlation_gb300 import as_int128, xi_signed, zeta4_connected, zeta4_disconnected
+    # 128-bit (low, high) words back to integers, signs included
+    words = np.array([[5, 0], [-1, -1], [0, 1], [-(1 << 63), 7]], dtype=np.int64)
+    assert as_int128(words) == [5, -1, 1 << 64, (7 << 64) + (1 << 63)]
+    # xi = signed pair sum / RR (Eq.(5)'s xi, §III.3)
+    assert xi_signed([3, -2, 0], [6, 8, 5]).tolist() == [0.5, -0.25, 0.0]
+    # zeta_conn = NNNN / RRRR - zeta_disc(xi), per configuration
+    xi = np.array([0.5, 0.25, 0.125, 0.0625])
+    rrrr = [1 << 70] * 276
+    nnnn = [(k + 1) << 66 for k in range(276)]
+    zc = zeta4_connected(nnnn, rrrr, xi, 4)
+    k = oracle.config_index6(4, (0, 1, 2, 2, 2, 3))
+    assert zc[k] == (k + 1) / 16 - (xi[0] * xi[3] + xi[1] * xi[2] + xi[2] * xi[2])
+    assert np.allclose(zc + zeta4_disconnected(xi, 4), [(k + 1) / 16 for k in range(276)], rtol=0, atol=0)
