@@ -111,6 +111,12 @@ class Graph:
     def max_degree(self) -> int:
         return self.info()[2]
 
+    def windows(self):
+        """(number of row windows, largest window's edges); 0 windows = device-resident."""
+        nw, m = ctypes.c_int32(), ctypes.c_int64()
+        _lib.check(_lib.load().gs_graph_windows(self._h, ctypes.byref(nw), ctypes.byref(m)))
+        return nw.value, m.value
+
     def stats(self, stream=None) -> dict:
         """Work statistics (sum C(f,2), sum b*f, max forward degree, ...); synchronises."""
         st = _lib.GraphStats()
@@ -371,18 +377,24 @@ def _ids(ids, device):
     return t.to(device=device, dtype=torch.int32).contiguous().reshape(-1)
 
 
-def build_graph(coords, box_lu: int, periodic: bool, edges_lu, stream=None) -> Graph:
-    """Neighbour graph of int32 lattice coordinates (a CUDA tensor [n, 3])."""
+def build_graph(coords, box_lu: int, periodic: bool, edges_lu, stream=None,
+                window_edges: int | None = None) -> Graph:
+    """Neighbour graph of int32 lattice coordinates (a CUDA tensor [n, 3]).
+    window_edges: keep the edge arrays in pinned host memory, in row windows of
+    at most this many directed edges (out-of-core mode)."""
     torch = _torch()
     if not (isinstance(coords, torch.Tensor) and coords.is_cuda and coords.dtype == torch.int32):
         raise TypeError("coords must be an int32 CUDA tensor of shape [n, 3]")
     coords = coords.contiguous().reshape(-1, 3)
     e = _edges(edges_lu)
     h = ctypes.c_void_p()
-    _lib.check(_lib.load().gs_build_graph(ctypes.c_void_p(coords.data_ptr()), coords.shape[0], int(box_lu),
-                                          int(bool(periodic)), int(e[-1]),
-                                          e.ctypes.data_as(ctypes.c_void_p), len(e) - 1,
-                                          _stream(stream), ctypes.byref(h)))
+    lib = _lib.load()
+    args = (ctypes.c_void_p(coords.data_ptr()), coords.shape[0], int(box_lu), int(bool(periodic)), int(e[-1]),
+            e.ctypes.data_as(ctypes.c_void_p), len(e) - 1)
+    if window_edges is None:
+        _lib.check(lib.gs_build_graph(*args, _stream(stream), ctypes.byref(h)))
+    else:
+        _lib.check(lib.gs_build_graph_windowed(*args, int(window_edges), _stream(stream), ctypes.byref(h)))
     return Graph(h, len(e) - 1, coords.device)
 
 

@@ -21,6 +21,8 @@ STATUS_NAMES = {0: "GS_OK", 1: "GS_ERR_ARG", 2: "GS_ERR_NOMEM", 3: "GS_ERR_CUDA"
 # name -> (restype, argtypes); every function the header declares
 SIGNATURES = {
     "gs_build_graph": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _p, ctypes.POINTER(_p)]),
+    "gs_build_graph_windowed": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _i64, _p, ctypes.POINTER(_p)]),
+    "gs_graph_windows": (_int, [_p, ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "gs_count_3pcf": (_int, [_p, _p, _i64, _i64, _p]),
     "gs_count_4pcf_parity": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_count_4pcf_parity_static": (_int, [_p, _p, _p, _i64, _i64, _p]),

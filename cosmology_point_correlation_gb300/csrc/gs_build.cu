@@ -13,6 +13,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -270,7 +271,7 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
             const long long *__restrict__ esq, int nb,
             int32_t *__restrict__ deg, int32_t *__restrict__ fwd,
             const int64_t *__restrict__ row_ptr, int32_t *__restrict__ nbr,
-            uint8_t *__restrict__ bin, unsigned *__restrict__ max_deg)
+            uint8_t *__restrict__ bin, unsigned *__restrict__ max_deg, int cell0, int64_t woff)
 {
     __shared__ int4 s_home[NB_HOME];
     __shared__ int s_cnt[NB_HOME];
@@ -280,7 +281,8 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
     __shared__ int s_r0[27], s_r1[27];
     __shared__ int s_nr;
 
-    const int c = blockIdx.x;
+    // cells [cell0, cell0 + gridDim.x); FILL writes edge e at nbr[e - woff]
+    const int c = cell0 + blockIdx.x;
     const int h0 = cell_start[c], h1 = cell_start[c + 1];
     if (h0 >= h1) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = NB_THREADS / 32;
@@ -360,7 +362,7 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
                         }
                         const unsigned m = __ballot_sync(0xffffffffu, hit);
                         if (FILL && hit) {
-                            const int64_t pos = rowp + cnt + __popc(m & gs_lanemask_lt());
+                            const int64_t pos = rowp + cnt + __popc(m & gs_lanemask_lt()) - woff;
                             int lo_b = 0, hi_b = nb;       // e_lo^2 <= d2 < e_hi^2
                             while (hi_b - lo_b > 1) {
                                 const int mid = (lo_b + hi_b) >> 1;
@@ -417,6 +419,16 @@ static void free_graph_arrays(gs_graph *g)
     cudaFree(g->cfg3);
     cudaFree(g->cfg6);
     cudaFree(g->w);
+    cudaFreeHost(g->h_nbr);
+    cudaFreeHost(g->h_bin);
+    for (int k = 0; k < GS_SLOTS; ++k) {
+        cudaFree(g->s_nbr[k]);
+        cudaFree(g->s_bin[k]);
+    }
+    delete[] g->win_row;
+    delete[] g->win_e0;
+    delete[] g->win_maxnbr;
+    delete[] g->win_pair;
 }
 
 extern "C" void gs_graph_free(gs_graph_t g)
@@ -446,13 +458,95 @@ static gs_status validate_build(const int32_t *coords, int64_t n, int64_t box, i
     return GS_OK;
 }
 
-extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
-                                    int64_t r_max_lu, const int64_t *edges_lu, int nbins,
-                                    void *cuda_stream, gs_graph_t *out)
+// Row windows over whole cells, each holding at most window_edges edges (a
+// single larger cell gets a window of its own). Fills the graph's window
+// tables; returns the first cell of every window and, last, the cell count.
+static std::vector<int> plan_windows(gs_graph *g, const std::vector<int32_t> &cs, const std::vector<int64_t> &rp,
+                                     int64_t window_edges)
+{
+    const int ncells = (int)cs.size() - 1;
+    std::vector<int> wc(1, 0);
+    for (int c = 0; c < ncells;) {
+        int c1 = c + 1;
+        while (c1 < ncells && rp[cs[c1 + 1]] - rp[cs[c]] <= window_edges) ++c1;
+        wc.push_back(c1);
+        c = c1;
+    }
+    const int nw = (int)wc.size() - 1;
+    g->n_win = nw;
+    g->win_row = new int64_t[nw + 1];
+    g->win_e0 = new int64_t[nw + 1];
+    g->win_maxnbr = new int32_t[nw];
+    g->win_cap = GS_EDGE_PAD;
+    for (int w = 0; w <= nw; ++w) {
+        g->win_row[w] = cs[wc[w]];
+        g->win_e0[w] = rp[g->win_row[w]];
+    }
+    for (int w = 0; w < nw; ++w) {
+        g->win_maxnbr[w] = -1;
+        g->win_cap = std::max(g->win_cap, g->win_e0[w + 1] + GS_EDGE_PAD - (g->win_e0[w] & ~(int64_t)3));
+    }
+    return wc;
+}
+
+// pair[w] = 1 for every window w that holds a forward neighbour of a row in
+// [r0, r1) (edges staged at nbr - off; win_row on the device, nw + 1 entries).
+__global__ void k_window_pairs(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd,
+                               const int32_t *__restrict__ nbr, int64_t off, int64_t r0, int64_t r1,
+                               const int64_t *__restrict__ win_row, int nw, unsigned *__restrict__ pair)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = r0 + w0; i < r1; i += nwarp)
+        for (int64_t p = row_ptr[i] + fwd[i] + lane; p < row_ptr[i + 1]; p += 32) {
+            const int64_t k = nbr[p - off];
+            int lo = 0, hi = nw;                         // window of k: win_row[lo] <= k < win_row[lo + 1]
+            while (hi - lo > 1) {
+                const int m = (lo + hi) >> 1;
+                if (win_row[m] <= k) lo = m; else hi = m;
+            }
+            if (!pair[lo]) atomicOr(pair + lo, 1u);
+        }
+}
+
+gs_status gs_stage_window(gs_graph_t g, int w, int slot, cudaStream_t st, int64_t *off)
+{
+    const int64_t a = g->win_e0[w] & ~(int64_t)3;
+    const int64_t b = g->win_e0[w + 1] + GS_EDGE_PAD;       // the host arrays hold E + GS_EDGE_PAD entries
+    GS_TRY_CUDA(cudaMemcpyAsync(g->s_nbr[slot], g->h_nbr + a, sizeof(int32_t) * (size_t)(b - a),
+                                cudaMemcpyHostToDevice, st));
+    GS_TRY_CUDA(cudaMemcpyAsync(g->s_bin[slot], g->h_bin + a, (size_t)(b - a), cudaMemcpyHostToDevice, st));
+    *off = a;
+    return GS_OK;
+}
+
+// Edge budget of a graph: window_edges > 0 forces row windows of that size;
+// 0 keeps the CSR on the device unless it would not fit (then windows of a
+// quarter of the free memory); the environment variable GS_WINDOW_EDGES, when
+// set to a positive count, overrides 0.
+static int64_t choose_window_edges(int64_t window_edges, int64_t n_edges)
+{
+    if (window_edges > 0) return window_edges;
+    if (const char *env = getenv("GS_WINDOW_EDGES")) {
+        const long long v = atoll(env);
+        if (v > 0) return v;
+    }
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return 0;
+    const size_t need = 5 * (size_t)(n_edges + GS_EDGE_PAD) + ((size_t)256 << 20);
+    if (need <= fr) return 0;
+    return std::max<int64_t>((int64_t)(fr / 4 / 5 / 2), (int64_t)1 << 20);
+}
+
+static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
+                            int64_t r_max_lu, const int64_t *edges_lu, int nbins, int64_t window_edges,
+                            void *cuda_stream, gs_graph_t *out)
 {
     gs_clear_error();
     gs_status s = validate_build(coords_dev, n, box_lu, periodic, r_max_lu, edges_lu, nbins, out);
     if (s != GS_OK) return s;
+    if (window_edges < 0) return gs_set_error(GS_ERR_ARG, "window_edges < 0");
     cudaStream_t st = (cudaStream_t)cuda_stream;
 
     gs_graph *g = new gs_graph();
@@ -470,6 +564,8 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
     int32_t *tmp = nullptr, *perm = nullptr, *deg = nullptr;
     long long *esq = nullptr;
     unsigned *maxd = nullptr;
+    int64_t *wrow_dev = nullptr;
+    unsigned *pair_dev = nullptr;
     const int sms = gs_sm_count();
     const int grid1 = (int)std::min<int64_t>(std::max<int64_t>((n + 255) / 256, 1), (int64_t)sms * 16);
 
@@ -540,7 +636,7 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
             k_neighbors<false><<<ncells, NB_THREADS, 0, st>>>(
                 g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                 (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
-                deg, g->fwd, nullptr, nullptr, nullptr, maxd);
+                deg, g->fwd, nullptr, nullptr, nullptr, maxd, 0, 0);
             gs_note_launch();
             GS_BUILD_CUDA(cudaGetLastError());
         }
@@ -561,17 +657,76 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
         g->max_forward = (int32_t)hmax[1];
 
         const size_t ne = (size_t)(g->n_edges + GS_EDGE_PAD);
-        GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));
-        GS_BUILD_CUDA(cudaMalloc(&g->bin, ne));
-        GS_BUILD_CUDA(cudaMemsetAsync(g->nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD, st));
-        GS_BUILD_CUDA(cudaMemsetAsync(g->bin + g->n_edges, 0, GS_EDGE_PAD, st));
-        if (n > 0 && g->n_edges > 0) {
-            k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
-                g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
-                (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
-                nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr);
-            gs_note_launch();
-            GS_BUILD_CUDA(cudaGetLastError());
+        const int64_t wedges = choose_window_edges(window_edges, g->n_edges);
+        if (wedges == 0) {
+            GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));
+            GS_BUILD_CUDA(cudaMalloc(&g->bin, ne));
+            GS_BUILD_CUDA(cudaMemsetAsync(g->nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD, st));
+            GS_BUILD_CUDA(cudaMemsetAsync(g->bin + g->n_edges, 0, GS_EDGE_PAD, st));
+            if (n > 0 && g->n_edges > 0) {
+                k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
+                    g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
+                    (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
+                    nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr, 0, 0);
+                gs_note_launch();
+                GS_BUILD_CUDA(cudaGetLastError());
+            }
+        } else {
+            // row windows: rows filled one window at a time into a device slot,
+            // then copied to pinned host memory
+            std::vector<int32_t> hcs((size_t)ncells + 1);
+            std::vector<int64_t> hrp((size_t)n + 1);
+            GS_BUILD_CUDA(cudaMemcpyAsync(hcs.data(), cell_start, sizeof(int32_t) * hcs.size(),
+                                          cudaMemcpyDeviceToHost, st));
+            GS_BUILD_CUDA(cudaMemcpyAsync(hrp.data(), g->row_ptr, sizeof(int64_t) * hrp.size(),
+                                          cudaMemcpyDeviceToHost, st));
+            GS_BUILD_CUDA(cudaStreamSynchronize(st));
+            const std::vector<int> wc = plan_windows(g, hcs, hrp, wedges);
+            GS_BUILD_CUDA(cudaMallocHost(&g->h_nbr, sizeof(int32_t) * ne));
+            GS_BUILD_CUDA(cudaMallocHost(&g->h_bin, ne));
+            memset(g->h_nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD);
+            memset(g->h_bin + g->n_edges, 0, GS_EDGE_PAD);
+            for (int k = 0; k < GS_SLOTS; ++k) {
+                GS_BUILD_CUDA(cudaMalloc(&g->s_nbr[k], sizeof(int32_t) * (size_t)g->win_cap));
+                GS_BUILD_CUDA(cudaMalloc(&g->s_bin[k], (size_t)g->win_cap));
+            }
+            const int nw = g->n_win;
+            g->win_pair = new uint8_t[(size_t)nw * nw]();
+            std::vector<unsigned> hpair((size_t)nw * nw, 0u);
+            GS_BUILD_CUDA(cudaMallocAsync(&wrow_dev, sizeof(int64_t) * (nw + 1), st));
+            GS_BUILD_CUDA(cudaMallocAsync(&pair_dev, sizeof(unsigned) * (size_t)nw * nw, st));
+            GS_BUILD_CUDA(cudaMemcpyAsync(wrow_dev, g->win_row, sizeof(int64_t) * (nw + 1), cudaMemcpyHostToDevice, st));
+            GS_BUILD_CUDA(cudaMemsetAsync(pair_dev, 0, sizeof(unsigned) * (size_t)nw * nw, st));
+            for (int w = 0; w < g->n_win; ++w) {
+                const int cell0 = wc[w], cell1 = wc[w + 1];
+                const int64_t e0 = g->win_e0[w], e1 = g->win_e0[w + 1];
+                if (e1 > e0) {
+                    const int64_t a = e0 & ~(int64_t)3;
+                    k_neighbors<true><<<cell1 - cell0, NB_THREADS, 0, st>>>(
+                        g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
+                        (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
+                        nullptr, nullptr, g->row_ptr, g->s_nbr[0], g->s_bin[0], nullptr, cell0, a);
+                    gs_note_launch();
+                    GS_BUILD_CUDA(cudaGetLastError());
+                    GS_BUILD_CUDA(cudaMemcpyAsync(g->h_nbr + e0, g->s_nbr[0] + (e0 - a), sizeof(int32_t) * (e1 - e0),
+                                                  cudaMemcpyDeviceToHost, st));
+                    GS_BUILD_CUDA(cudaMemcpyAsync(g->h_bin + e0, g->s_bin[0] + (e0 - a), (size_t)(e1 - e0),
+                                                  cudaMemcpyDeviceToHost, st));
+                    const int64_t rows = g->win_row[w + 1] - g->win_row[w];
+                    const int gp = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)sms * 8);
+                    k_window_pairs<<<gp, 256, 0, st>>>(g->row_ptr, g->fwd, g->s_nbr[0], a, g->win_row[w],
+                                                       g->win_row[w + 1], wrow_dev, nw, pair_dev + (size_t)w * nw);
+                    gs_note_launch();
+                    GS_BUILD_CUDA(cudaGetLastError());
+                }
+            }
+            GS_BUILD_CUDA(cudaMemcpyAsync(hpair.data(), pair_dev, sizeof(unsigned) * hpair.size(),
+                                          cudaMemcpyDeviceToHost, st));
+            GS_BUILD_CUDA(cudaStreamSynchronize(st));
+            for (size_t q = 0; q < hpair.size(); ++q) g->win_pair[q] = hpair[q] ? 1 : 0;
+            for (int w = 0; w < g->n_win; ++w)        // rows are sorted: the last entry is the row's largest
+                for (int64_t i = g->win_row[w]; i < g->win_row[w + 1]; ++i)
+                    if (hrp[i + 1] > hrp[i]) g->win_maxnbr[w] = std::max(g->win_maxnbr[w], g->h_nbr[hrp[i + 1] - 1]);
         }
     }
     cudaFreeAsync(cell, st);
@@ -583,6 +738,8 @@ extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_
     cudaFreeAsync(cell_start, st);
     cudaFreeAsync(esq, st);
     cudaFreeAsync(maxd, st);
+    cudaFreeAsync(wrow_dev, st);
+    cudaFreeAsync(pair_dev, st);
     *out = g;
     return GS_OK;
 
@@ -597,6 +754,8 @@ fail:
     cudaFree(cell_start);
     cudaFree(esq);
     cudaFree(maxd);
+    cudaFree(wrow_dev);
+    cudaFree(pair_dev);
     free_graph_arrays(g);
     delete g;
     return s;
@@ -624,14 +783,16 @@ constexpr int EX_SMEM = 4096;   // rows up to this length are sorted in shared m
 __global__ void __launch_bounds__(EX_THREADS)
 k_export_rows(const int4 *__restrict__ pts, const int32_t *__restrict__ inv, const int32_t *__restrict__ ids,
               const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ nbr,
-              const uint8_t *__restrict__ bin, int64_t n, const int64_t *__restrict__ out_ptr,
-              int32_t *__restrict__ out_nbr, uint8_t *__restrict__ out_bin)
+              const uint8_t *__restrict__ bin, int64_t off, int64_t p_lo, int64_t p_hi, int64_t n,
+              const int64_t *__restrict__ out_ptr, int32_t *__restrict__ out_nbr, uint8_t *__restrict__ out_bin)
 {
+    // rows of internal index p in [p_lo, p_hi) only; their edges at (nbr, bin) - off
     __shared__ unsigned long long s_kv[EX_SMEM];
     for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
         const int p = inv[ids ? ids[i] : i];
-        const int64_t r0 = row_ptr[p];
-        const int len = (int)(row_ptr[p + 1] - r0);
+        if (p < p_lo || p >= p_hi) continue;             // block-uniform
+        const int64_t r0 = row_ptr[p] - off;
+        const int len = (int)(row_ptr[p + 1] - row_ptr[p]);
         const int64_t o0 = out_ptr[i];
         if (len <= EX_SMEM) {
             int pw = 1;
@@ -692,9 +853,21 @@ static gs_status export_rows(gs_graph_t g, const int32_t *ids, int64_t count, in
     if (s != GS_OK) return s;
     if (nbr_dev && g->n_edges > 0) {
         const int gridr = (int)std::min<int64_t>(count, (int64_t)sms * 8);
-        k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, ids, g->row_ptr, g->nbr, g->bin, count,
-                                                    row_ptr_dev, nbr_dev, bin_dev);
-        gs_note_launch();
+        if (g->n_win == 0) {
+            k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, ids, g->row_ptr, g->nbr, g->bin, 0, 0, g->n,
+                                                        count, row_ptr_dev, nbr_dev, bin_dev);
+            gs_note_launch();
+        }
+        for (int w = 0; w < g->n_win; ++w) {            // windowed: the rows of one staged window at a time
+            if (g->win_e0[w + 1] == g->win_e0[w]) continue;
+            int64_t off = 0;
+            s = gs_stage_window(g, w, 0, st, &off);
+            if (s != GS_OK) return s;
+            k_export_rows<<<gridr, EX_THREADS, 0, st>>>(g->pts, g->inv, ids, g->row_ptr, g->s_nbr[0], g->s_bin[0],
+                                                        off, g->win_row[w], g->win_row[w + 1], count, row_ptr_dev,
+                                                        nbr_dev, bin_dev);
+            gs_note_launch();
+        }
     }
     GS_TRY_CUDA(cudaGetLastError());
     return GS_OK;
@@ -805,5 +978,32 @@ extern "C" gs_status gs_graph_info(gs_graph_t g, int64_t *n, int64_t *n_edges, i
     if (n) *n = g->n;
     if (n_edges) *n_edges = g->n_edges;
     if (max_degree) *max_degree = g->max_degree;
+    return GS_OK;
+}
+
+extern "C" gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
+                                    int64_t r_max_lu, const int64_t *edges_lu, int nbins,
+                                    void *cuda_stream, gs_graph_t *out)
+{
+    return build_impl(coords_dev, n, box_lu, periodic, r_max_lu, edges_lu, nbins, 0, cuda_stream, out);
+}
+
+extern "C" gs_status gs_build_graph_windowed(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
+                                             int64_t r_max_lu, const int64_t *edges_lu, int nbins,
+                                             int64_t window_edges, void *cuda_stream, gs_graph_t *out)
+{
+    gs_clear_error();
+    if (window_edges < 1) return gs_set_error(GS_ERR_ARG, "window_edges must be >= 1");
+    return build_impl(coords_dev, n, box_lu, periodic, r_max_lu, edges_lu, nbins, window_edges, cuda_stream, out);
+}
+
+extern "C" gs_status gs_graph_windows(gs_graph_t g, int32_t *n_windows, int64_t *window_edges_max)
+{
+    gs_clear_error();
+    if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    int64_t m = 0;
+    for (int w = 0; w < g->n_win; ++w) m = std::max(m, g->win_e0[w + 1] - g->win_e0[w]);
+    if (n_windows) *n_windows = g->n_win;
+    if (window_edges_max) *window_edges_max = g->n_win ? m : g->n_edges;
     return GS_OK;
 }

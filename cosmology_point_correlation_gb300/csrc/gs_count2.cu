@@ -23,7 +23,13 @@ k_count2(const uint8_t *__restrict__ bin, int64_t n_edges, int nb, unsigned long
     for (int t = threadIdx.x; t < C2_WARPS * 256; t += C2_THREADS) (&s_h[0][0])[t] = 0u;
     __syncthreads();
     unsigned *h = s_h[warp];
-    // whole 16-byte vectors first (the bin array starts 256-byte aligned)
+    // bytes up to the first 16-byte boundary, then whole 16-byte vectors, then the tail
+    const int64_t mis = (int64_t)((16 - ((uintptr_t)bin & 15)) & 15);
+    const int64_t head = mis < n_edges ? mis : n_edges;
+    for (int64_t e = (int64_t)blockIdx.x * C2_THREADS + threadIdx.x; e < head; e += (int64_t)gridDim.x * C2_THREADS)
+        atomicAdd(&h[bin[e]], 1u);
+    bin += head;
+    n_edges -= head;
     const int64_t nvec = n_edges >> 4;
     const uint4 *v = reinterpret_cast<const uint4 *>(bin);
     for (int64_t q = (int64_t)blockIdx.x * C2_THREADS + threadIdx.x; q < nvec;
@@ -52,6 +58,21 @@ __global__ void k_halve(unsigned long long *__restrict__ hist, int nb)
     if (b < nb) hist[b] >>= 1;
 }
 
+// Add the bin bytes [bin, bin + n) into hist.
+static gs_status count2_bytes(const uint8_t *bin, int64_t n, int nb, unsigned long long *hist, cudaStream_t st)
+{
+    if (n == 0) return GS_OK;
+    // a per-warp u32 counter receives at most (edges per warp) adds: bound the
+    // grid so that no warp sees 2^32 edges
+    const int64_t min_blocks = n / ((int64_t)C2_WARPS << 31) + 1;
+    const int grid = (int)std::max<int64_t>(std::min<int64_t>((n + 4095) / 4096, (int64_t)gs_sm_count() * 8),
+                                            min_blocks);
+    k_count2<<<grid, C2_THREADS, 0, st>>>(bin, n, nb, hist);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
+    return GS_OK;
+}
+
 extern "C" gs_status gs_count_2pcf(gs_graph_t g, uint64_t *hist_dev, void *cuda_stream)
 {
     gs_clear_error();
@@ -59,14 +80,21 @@ extern "C" gs_status gs_count_2pcf(gs_graph_t g, uint64_t *hist_dev, void *cuda_
     cudaStream_t st = (cudaStream_t)cuda_stream;
     GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * g->nb, st));
     if (g->n_edges == 0) return GS_OK;
-    // a per-warp u32 counter receives at most (edges per warp) adds: bound the
-    // grid so that no warp sees 2^32 edges
-    const int64_t min_blocks = g->n_edges / ((int64_t)C2_WARPS << 31) + 1;
-    const int grid = (int)std::max<int64_t>(std::min<int64_t>((g->n_edges + 4095) / 4096,
-                                                              (int64_t)gs_sm_count() * 8), min_blocks);
-    k_count2<<<grid, C2_THREADS, 0, st>>>(g->bin, g->n_edges, g->nb, (unsigned long long *)hist_dev);
-    gs_note_launch();
-    k_halve<<<(g->nb + 255) / 256, 256, 0, st>>>((unsigned long long *)hist_dev, g->nb);
+    unsigned long long *hist = (unsigned long long *)hist_dev;
+    if (g->n_win == 0) {
+        gs_status s = count2_bytes(g->bin, g->n_edges, g->nb, hist, st);
+        if (s != GS_OK) return s;
+    } else {
+        for (int w = 0; w < g->n_win; ++w) {             // one staged window at a time
+            const int64_t e0 = g->win_e0[w], e1 = g->win_e0[w + 1];
+            if (e1 == e0) continue;
+            int64_t off = 0;
+            gs_status s = gs_stage_window(g, w, 0, st, &off);
+            if (s == GS_OK) s = count2_bytes(g->s_bin[0] + (e0 - off), e1 - e0, g->nb, hist, st);
+            if (s != GS_OK) return s;
+        }
+    }
+    k_halve<<<(g->nb + 255) / 256, 256, 0, st>>>(hist, g->nb);
     gs_note_launch();
     GS_TRY_CUDA(cudaGetLastError());
     return GS_OK;

@@ -36,6 +36,8 @@
 // rows overlap and stay in L2.
 
 #include <algorithm>
+#include <utility>
+#include <vector>
 
 #include "gs_internal.cuh"
 
@@ -62,8 +64,15 @@ constexpr int C3_EMPTY = -1;
 struct C3Args {
     const int64_t *row_ptr;
     const int32_t *fwd;
-    const int32_t *nbr;
-    const uint8_t *bin;
+    // edge arrays: hub rows from (hnbr, hbin), spoke rows from (snbr, sbin);
+    // global edge e sits at index e - hoff (e - soff). A device-resident graph
+    // passes its own arrays with offset 0; a windowed graph (§III.5.3) the
+    // staged hub and spoke windows, and only spokes j in [s_lo, s_hi) are walked
+    const int32_t *hnbr, *snbr;
+    const uint8_t *hbin, *sbin;
+    int64_t hoff, soff;
+    int windowed;
+    int32_t s_lo, s_hi;
     int64_t hub_begin, hub_end;
     int nb;
     int ncfg;
@@ -140,7 +149,7 @@ __device__ __forceinline__ int c3_block_scan(int v, int *s_warp)
     return r;
 }
 
-template <bool SMEM_HIST, bool HUB_LIST, bool WEIGHTED>
+template <bool SMEM_HIST, bool HUB_LIST, bool WEIGHTED, bool WINDOWED>
 __global__ void __launch_bounds__(C3_THREADS, 2)
 k_count3(C3Args a)
 {
@@ -159,6 +168,7 @@ k_count3(C3Args a)
     __shared__ int s_warp[C3_WARPS];
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;        // bound on hits since the last flush
+    __shared__ int s_q[2];                          // windowed: spoke positions [q_lo, q_hi) of F
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nb = a.nb;
@@ -201,13 +211,34 @@ k_count3(C3Args a)
         const long long i = HUB_LIST ? (long long)a.inv[a.hubs[s_hub]] : s_hub;
         const int64_t f0 = HUB_LIST ? a.row_ptr[i] : a.row_ptr[i] + a.fwd[i];
         const int f = (int)(a.row_ptr[i + 1] - f0);
+        const int64_t hoff = WINDOWED ? a.hoff : 0;
+        const int32_t *F = a.hnbr + (f0 - hoff);            // the hub's row and its bins
+        const uint8_t *FB = a.hbin + (f0 - hoff);
         const long long wi = WEIGHTED ? (long long)a.w[i] : 0;
+        // spokes whose rows are walked: positions [q_lo, q_hi) of F (all of F
+        // unless the graph is windowed; rows are sorted, so a window is a range)
+        int q_lo = 0, q_hi = f;
+        if (WINDOWED) {
+            if (threadIdx.x == 0) {
+                int lo = 0, hi = f;
+                while (lo < hi) { const int m = (lo + hi) >> 1; if (F[m] < a.s_lo) lo = m + 1; else hi = m; }
+                s_q[0] = lo;
+                hi = f;
+                while (lo < hi) { const int m = (lo + hi) >> 1; if (F[m] < a.s_hi) lo = m + 1; else hi = m; }
+                s_q[1] = lo;
+            }
+            __syncthreads();
+            q_lo = s_q[0];
+            q_hi = s_q[1];
+        }
         for (int c0 = 0; c0 < f; c0 += C3_CHUNK) {           // chunks of candidate keys
             const int c1 = min(f, c0 + C3_CHUNK);
             const int cn = c1 - c0;
             if (c1 < 2) break;                               // a lone key closes nothing
-            const int32_t kmax = a.nbr[f0 + c1 - 1];
-            const int32_t kfirst = a.nbr[f0 + c0];
+            const int s_end = min(c1 - 1, q_hi);             // spokes [q_lo, s_end) meet this chunk
+            if (s_end <= q_lo) continue;                     // block-uniform
+            const int32_t kmax = F[c1 - 1];
+            const int32_t kfirst = F[c0];
             const int64_t span64 = (int64_t)kmax - kfirst + 1;
             const bool bmode = span64 <= C3_SPAN_BITS;       // block-uniform
             const int span = (int)(span64 < C3_SPAN_BITS ? span64 : C3_SPAN_BITS);
@@ -235,9 +266,9 @@ k_count3(C3Args a)
                 for (int t = threadIdx.x; t < npairs; t += C3_THREADS) s_bm[t] = make_uint2(0u, 0u);
                 __syncthreads();
                 for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
-                    const int off = a.nbr[f0 + c0 + t] - kfirst;
+                    const int off = F[c0 + t] - kfirst;
                     atomicOr(reinterpret_cast<unsigned *>(s_bm) + (off >> 5), 1u << (off & 31));
-                    s_cbin[t] = a.bin[f0 + c0 + t];
+                    s_cbin[t] = FB[c0 + t];
                     if (WEIGHTED) s_cw[t] = a.w[off + kfirst];
                 }
                 __syncthreads();
@@ -254,23 +285,23 @@ k_count3(C3Args a)
                 for (int t = threadIdx.x; t < tsize; t += C3_THREADS) s_key[t] = C3_EMPTY;
                 __syncthreads();
                 for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
-                    const int32_t k = a.nbr[f0 + c0 + t];
+                    const int32_t k = F[c0 + t];
                     uint32_t h = gs_hash(k, shift);
                     while (atomicCAS(&s_key[h], C3_EMPTY, k) != C3_EMPTY) h = (h + 1) & mask;
-                    s_bin[h] = a.bin[f0 + c0 + t];
+                    s_bin[h] = FB[c0 + t];
                     if (WEIGHTED) s_hw[h] = a.w[k];
                 }
             }
 
-            // spokes s in [sb, se) of [0, c1 - 1), at most C3_SPOKES at a time
-            for (int sb = 0; sb < c1 - 1; sb += C3_SPOKES) {
-                const int se = min(c1 - 1, sb + C3_SPOKES);
+            // spokes s in [sb, se) of [q_lo, s_end), at most C3_SPOKES at a time
+            for (int sb = q_lo; sb < s_end; sb += C3_SPOKES) {
+                const int se = min(s_end, sb + C3_SPOKES);
                 const int ns = se - sb;
                 // counting sort of the spokes by b_ij, so that a warp's spokes
                 // share their bin and its configuration table changes rarely
                 for (int t = threadIdx.x; t <= nb; t += C3_THREADS) s_bucket[t] = 0;
                 __syncthreads();
-                for (int t = threadIdx.x; t < ns; t += C3_THREADS) atomicAdd(&s_bucket[a.bin[f0 + sb + t] + 1], 1);
+                for (int t = threadIdx.x; t < ns; t += C3_THREADS) atomicAdd(&s_bucket[FB[sb + t] + 1], 1);
                 __syncthreads();
                 if (warp == 0) {
                     int carry = 0;
@@ -288,7 +319,7 @@ k_count3(C3Args a)
                 }
                 __syncthreads();
                 for (int t = threadIdx.x; t < ns; t += C3_THREADS) {
-                    const int b = a.bin[f0 + sb + t];
+                    const int b = FB[sb + t];
                     s_order[atomicAdd(&s_bucket[b], 1)] = (uint16_t)t;
                 }
                 if (threadIdx.x == 0) s_next = 0;
@@ -300,8 +331,8 @@ k_count3(C3Args a)
                     li = __shfl_sync(0xffffffffu, li, 0);
                     if (li >= ns) break;
                     const int s = sb + s_order[li];
-                    const int32_t j = a.nbr[f0 + s];
-                    const int bij = a.bin[f0 + s];
+                    const int32_t j = F[s];
+                    const int bij = FB[s];
                     if (SMEM_HIST && !WEIGHTED && bij != tab_z) {
                         c3_fill_tab(tab, a.cfg3, nb, bij);
                         tab_z = bij;
@@ -315,7 +346,7 @@ k_count3(C3Args a)
                         int64_t lo = a.row_ptr[j] + a.fwd[j], hi = pe;
                         while (lo < hi) {
                             const int64_t mid = (lo + hi) >> 1;
-                            if (a.nbr[mid] < kfirst) lo = mid + 1; else hi = mid;
+                            if (a.snbr[mid - (WINDOWED ? a.soff : 0)] < kfirst) lo = mid + 1; else hi = mid;
                         }
                         p0 = lo;
                     }
@@ -342,8 +373,9 @@ k_count3(C3Args a)
                     const int64_t pa = p0 & ~(int64_t)3;
                     const int head = (int)(p0 - pa);
                     const int total = head + (int)(pe - p0);
-                    const int4 *vk = reinterpret_cast<const int4 *>(a.nbr + pa) + lane;
-                    const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.bin + pa) + lane;
+                    const int64_t soff = WINDOWED ? a.soff : 0;
+                    const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + lane;
+                    const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + lane;
                     int4 kk = __ldg(vk);                            // step 0, then prefetch
                     uint32_t bb = __ldg(vb);
                     for (int base = 0; base < total; base += 128) {
@@ -432,12 +464,12 @@ k_count3(C3Args a)
     }
 }
 
-// out[c] = sum over the slices of slice[c], 128-bit (low, high) words.
+// out[c] += sum over the slices of slice[c], 128-bit (low, high) words.
 __global__ void k_sum128_slices(const unsigned long long *__restrict__ slices, int nslices, int ncfg,
                                 unsigned long long *__restrict__ out)
 {
     for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < ncfg; c += gridDim.x * blockDim.x) {
-        unsigned long long lo = 0, hi = 0;
+        unsigned long long lo = out[2 * c], hi = out[2 * c + 1];
         for (int b = 0; b < nslices; ++b) {
             const unsigned long long l = slices[2 * ((size_t)b * ncfg + c)];
             const unsigned long long h = slices[2 * ((size_t)b * ncfg + c) + 1];
@@ -449,7 +481,7 @@ __global__ void k_sum128_slices(const unsigned long long *__restrict__ slices, i
     }
 }
 
-static gs_status launch_count3(gs_graph_t g, C3Args &a, int64_t hubs, cudaStream_t st)
+static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_t st)
 {
     const int ncfg = a.ncfg;
     const int nb2 = g->nb * g->nb;
@@ -457,31 +489,36 @@ static gs_status launch_count3(gs_graph_t g, C3Args &a, int64_t hubs, cudaStream
     const bool weighted = a.w != nullptr;
     bool smem;
     size_t dyn;
-    decltype(&k_count3<true, true, false>) kern;
+    const bool win = a.windowed != 0;
+    decltype(&k_count3<true, true, false, false>) kern;
     if (weighted) {
         smem = true;
         dyn = C3_REGION_W + sizeof(unsigned long long) * (size_t)ncfg;
-        kern = k_count3<true, false, true>;
+        kern = win ? k_count3<true, false, true, true> : k_count3<true, false, true, false>;
     } else {
         // shared-memory histogram unless it is too large or a chunk's hit bound
         // (spokes x chunk) could overflow a 32-bit counter
         smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
         dyn = C3_REGION + (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * nb2 : 0);
-        kern = smem ? (list ? k_count3<true, true, false> : k_count3<true, false, false>)
-                    : (list ? k_count3<false, true, false> : k_count3<false, false, false>);
+        if (win)
+            kern = smem ? k_count3<true, false, false, true> : k_count3<false, false, false, true>;
+        else
+            kern = smem ? (list ? k_count3<true, true, false, false> : k_count3<true, false, false, false>)
+                        : (list ? k_count3<false, true, false, false> : k_count3<false, false, false, false>);
     }
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C3_THREADS, dyn));
     if (per_sm < 1) return gs_set_error(GS_ERR_CAPACITY, "3pCF workspace of %zu bytes does not fit in shared memory", dyn);
     const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * per_sm, hubs);
+    GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
     if (!weighted) {
         kern<<<grid, C3_THREADS, dyn, st>>>(a);
         gs_note_launch();
         GS_TRY_CUDA(cudaGetLastError());
         return GS_OK;
     }
-    // weighted: one 128-bit slice per block, then their sum into the output
+    // weighted: one 128-bit slice per block, then their sum added to the output
     unsigned long long *out = a.gsum, *slices = nullptr;
     const size_t bytes = 16 * (size_t)ncfg * grid;
     GS_TRY_CUDA(cudaMallocAsync(&slices, bytes, st));
@@ -502,13 +539,136 @@ static gs_status launch_count3(gs_graph_t g, C3Args &a, int64_t hubs, cudaStream
     return GS_OK;
 }
 
+// The hubs [hub_begin, hub_end): one launch on a device-resident graph; on a
+// windowed graph one launch per (hub window h, spoke window w >= h) tile that
+// holds work. A triangle (i < j < k) is closed in the tile of i's and j's
+// windows only, so the tiles add up to the full histogram (§III.5.3).
+// Windows are staged into three device slots on a copy stream: a window
+// already in a slot is not copied again (the spoke window of tile (h, h+1) is
+// the hub window of (h+1, h+1)), and the next tile's missing window is copied
+// into the free slot while the current tile runs. Outputs accumulate; the
+// caller clears them first.
+static gs_status run_count3(gs_graph_t g, C3Args a, int64_t hub_begin, int64_t hub_end, cudaStream_t st)
+{
+    if (g->n_win == 0) {
+        a.hub_begin = hub_begin;
+        a.hub_end = hub_end;
+        return launch_count3(g, a, hub_end - hub_begin, st);
+    }
+    std::vector<std::pair<int, int>> tiles;
+    for (int h = 0; h < g->n_win; ++h) {
+        if (std::max(hub_begin, g->win_row[h]) >= std::min(hub_end, g->win_row[h + 1])) continue;
+        if (g->win_e0[h + 1] == g->win_e0[h]) continue;
+        for (int w = h; w < g->n_win; ++w)
+            if (g->win_pair[(size_t)h * g->n_win + w] && g->win_e0[w + 1] > g->win_e0[w]) tiles.push_back({ h, w });
+    }
+    if (tiles.empty()) return GS_OK;
+
+    cudaStream_t cs = nullptr;
+    cudaEvent_t start = nullptr, fin = nullptr, ready[GS_SLOTS] = {}, done[GS_SLOTS] = {};
+    int held[GS_SLOTS];
+    int64_t off[GS_SLOTS] = {};
+    for (int k = 0; k < GS_SLOTS; ++k) held[k] = -1;
+    gs_status s = GS_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fin, cudaEventDisableTiming);
+    for (int k = 0; k < GS_SLOTS && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&ready[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done[k], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(start, st);     // slots are free once earlier work on st is done
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
+
+    auto slot_of = [&](int w) {
+        for (int k = 0; k < GS_SLOTS; ++k)
+            if (held[k] == w) return k;
+        return -1;
+    };
+    // copy window w into slot k once the last tile that read slot k is done
+    auto stage_into = [&](int k, int w) {
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, done[k], 0);
+        if (e == cudaSuccess && s == GS_OK) s = gs_stage_window(g, w, k, cs, &off[k]);
+        if (e == cudaSuccess && s == GS_OK) e = cudaEventRecord(ready[k], cs);
+        held[k] = w;
+    };
+    // a slot other than keep0 / keep1, preferring one whose window the tile
+    // after t does not need
+    auto victim = [&](int keep0, int keep1, size_t t) {
+        for (int pass = 0; pass < 2; ++pass)
+            for (int k = 0; k < GS_SLOTS; ++k) {
+                if (k == keep0 || k == keep1) continue;
+                const bool wanted = t + 1 < tiles.size() &&
+                                    (held[k] == tiles[t + 1].first || held[k] == tiles[t + 1].second);
+                if (pass == 1 || !wanted) return k;
+            }
+        return -1;
+    };
+
+    a.windowed = 1;
+    for (size_t t = 0; t < tiles.size() && e == cudaSuccess && s == GS_OK; ++t) {
+        const int h = tiles[t].first, w = tiles[t].second;
+        int sh = slot_of(h);
+        if (sh < 0) stage_into(sh = victim(slot_of(w), -1, t), h);
+        int sw = slot_of(w);
+        if (sw < 0) stage_into(sw = victim(sh, -1, t), w);
+        if (e != cudaSuccess || s != GS_OK) break;
+        e = cudaStreamWaitEvent(st, ready[sh], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ready[sw], 0);
+        if (e != cudaSuccess) break;
+        a.hnbr = g->s_nbr[sh];
+        a.hbin = g->s_bin[sh];
+        a.hoff = off[sh];
+        a.snbr = g->s_nbr[sw];
+        a.sbin = g->s_bin[sw];
+        a.soff = off[sw];
+        a.s_lo = (int32_t)g->win_row[w];
+        a.s_hi = (int32_t)g->win_row[w + 1];
+        a.hub_begin = std::max(hub_begin, g->win_row[h]);
+        a.hub_end = std::min(hub_end, g->win_row[h + 1]);
+        s = launch_count3(g, a, a.hub_end - a.hub_begin, st);
+        if (s != GS_OK) break;
+        e = cudaEventRecord(done[sh], st);
+        if (e == cudaSuccess) e = cudaEventRecord(done[sw], st);
+        // prefetch the next tile's missing windows into slots this tile does not read
+        if (t + 1 < tiles.size())
+            for (int q = 0; q < 2; ++q) {
+                const int x = q ? tiles[t + 1].second : tiles[t + 1].first;
+                const int y = q ? tiles[t + 1].first : tiles[t + 1].second;
+                if (slot_of(x) >= 0) continue;
+                for (int k = 0; k < GS_SLOTS; ++k)
+                    if (k != sh && k != sw && k != slot_of(y)) {
+                        stage_into(k, x);
+                        break;
+                    }
+            }
+    }
+    // the caller's stream waits for the last copies; then release the helpers
+    if (e == cudaSuccess) e = cudaEventRecord(fin, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, fin, 0);
+    for (int k = 0; k < GS_SLOTS; ++k) {
+        if (ready[k]) cudaEventDestroy(ready[k]);
+        if (done[k]) cudaEventDestroy(done[k]);
+    }
+    if (start) cudaEventDestroy(start);
+    if (fin) cudaEventDestroy(fin);
+    if (cs) cudaStreamDestroy(cs);
+    if (s != GS_OK) return s;
+    if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "windowed 3pCF: %s", cudaGetErrorString(e));
+    return GS_OK;
+}
+
 static C3Args count3_args(gs_graph_t g, uint64_t *hist_dev)
 {
     C3Args a{};
     a.row_ptr = g->row_ptr;
     a.fwd = g->fwd;
-    a.nbr = g->nbr;
-    a.bin = g->bin;
+    a.hnbr = a.snbr = g->nbr;
+    a.hbin = a.sbin = g->bin;
+    a.hoff = a.soff = 0;
+    a.windowed = 0;
+    a.s_lo = 0;
+    a.s_hi = 0x7fffffff;
     a.nb = g->nb;
     a.ncfg = (int)gs_ncfg3(g->nb);
     a.ghist = (unsigned long long *)hist_dev;
@@ -530,11 +690,7 @@ extern "C" gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub
     const int ncfg = (int)gs_ncfg3(g->nb);
     GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * ncfg, st));
     if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
-    GS_TRY_CUDA(cudaMemsetAsync(g->work, 0, sizeof(unsigned long long), st));
-    C3Args a = count3_args(g, hist_dev);
-    a.hub_begin = hub_begin;
-    a.hub_end = hub_end;
-    return launch_count3(g, a, hub_end - hub_begin, st);
+    return run_count3(g, count3_args(g, hist_dev), hub_begin, hub_end, st);
 }
 
 // Range check of a device list of input indices, one flag word for the host.
@@ -565,13 +721,13 @@ extern "C" gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, i
     gs_clear_error();
     if (!g || !hist_dev || (count > 0 && !hubs_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
     if (count < 0) return gs_set_error(GS_ERR_ARG, "negative hub count");
+    if (g->n_win) return gs_set_error(GS_ERR_ARG, "hub lists need a device-resident graph (this one is windowed)");
     cudaStream_t st = (cudaStream_t)cuda_stream;
     gs_status s = gs_check_ids(g, hubs_dev, count, st);
     if (s != GS_OK) return s;
     const int ncfg = (int)gs_ncfg3(g->nb);
     GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * ncfg, st));
     if (count == 0 || g->n_edges == 0) return GS_OK;
-    GS_TRY_CUDA(cudaMemsetAsync(g->work, 0, sizeof(unsigned long long), st));
     C3Args a = count3_args(g, hist_dev);
     a.hub_begin = 0;
     a.hub_end = count;
@@ -592,15 +748,10 @@ extern "C" gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int
                             (long long)hub_end, (long long)g->n);
     cudaStream_t st = (cudaStream_t)cuda_stream;
     const int ncfg = (int)gs_ncfg3(g->nb);
-    if (hub_end == hub_begin || g->n_edges == 0) {
-        GS_TRY_CUDA(cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
-        return GS_OK;
-    }
-    GS_TRY_CUDA(cudaMemsetAsync(g->work, 0, sizeof(unsigned long long), st));
+    GS_TRY_CUDA(cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
     C3Args a = count3_args(g, nullptr);
-    a.hub_begin = hub_begin;
-    a.hub_end = hub_end;
     a.w = g->w;
     a.gsum = (unsigned long long *)sums_dev;
-    return launch_count3(g, a, hub_end - hub_begin, st);
+    return run_count3(g, a, hub_begin, hub_end, st);
 }

@@ -288,6 +288,7 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
 {
     gs_clear_error();
     if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    if (g->n_win) return gs_set_error(GS_ERR_ARG, "the parity 4pCF needs a device-resident graph (this one is windowed)");
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
         return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
                             (long long)hub_end, (long long)g->n);
@@ -361,6 +362,7 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
     gs_clear_error();
     if (!g || (count > 0 && !hubs_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
     if (count < 0) return gs_set_error(GS_ERR_ARG, "negative hub count");
+    if (g->n_win) return gs_set_error(GS_ERR_ARG, "the parity 4pCF needs a device-resident graph (this one is windowed)");
     if (g->edges[g->nb] >= (1ll << 20))
         return gs_set_error(GS_ERR_ARG, "parity 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
     const int64_t ncfg = gs_ncfg4(g->nb);
@@ -469,6 +471,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
 {
     gs_clear_error();
     if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    if (g->n_win) return gs_set_error(GS_ERR_ARG, "the parity 4pCF needs a device-resident graph (this one is windowed)");
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
         return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
                             (long long)hub_end, (long long)g->n);

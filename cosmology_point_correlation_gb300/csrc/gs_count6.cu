@@ -467,6 +467,7 @@ static gs_status c6_launch(gs_graph_t g, C6Args &a, cudaStream_t st)
 
 static gs_status c6_check(gs_graph_t g, int64_t hub_begin, int64_t hub_end)
 {
+    if (g->n_win) return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF needs a device-resident graph (this one is windowed)");
     if (g->nb > C6_MAX_BINS)
         return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF supports at most %d bins", C6_MAX_BINS);
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)

@@ -7,7 +7,10 @@
 #include "gramsci_gb.h"
 
 // ---------------------------------------------------------------- the graph
-//
+
+// Device staging slots of a windowed graph.
+constexpr int GS_SLOTS = 3;
+
 // HBM layout of one graph (N points, E directed edges):
 //   pts      int4   [N]    x, y, z and the input index, points sorted by cell
 //                          (16-byte rows: one aligned vector load per point)
@@ -42,7 +45,31 @@ struct gs_graph {
     int32_t *cfg6;             // [nb^6] six-bin 4pCF configuration and orientation (built on first use)
     int ncfg6;
     int16_t *w;                // [N] point weights in internal order (set by gs_graph_set_weights), or NULL
+
+    // Row windows (§III.5.3 out-of-core operation). With n_win > 0 the edge
+    // arrays live in pinned host memory (h_nbr, h_bin, padded like nbr / bin)
+    // and nbr / bin are NULL. Window w holds the rows [win_row[w], win_row[w+1])
+    // (whole cells), i.e. the edges [win_e0[w], win_e0[w+1]); win_maxnbr[w] is
+    // the largest neighbour id in those rows (-1 if none). A window is staged
+    // into one of two device slots from edge (win_e0[w] & ~3) on, through
+    // win_e0[w+1] + GS_EDGE_PAD, so 16-byte vector reads stay aligned and in
+    // bounds.
+    int n_win;
+    int64_t *win_row;          // host [n_win + 1]
+    int64_t *win_e0;           // host [n_win + 1]
+    int32_t *win_maxnbr;       // host [n_win]
+    uint8_t *win_pair;         // host [n_win][n_win]: 1 if a row of window h has a forward neighbour in window w
+    int32_t *h_nbr;
+    uint8_t *h_bin;
+    int64_t win_cap;           // edges a staging slot holds
+    int32_t *s_nbr[GS_SLOTS];  // device staging slots (three: a hub window, a spoke window and
+    uint8_t *s_bin[GS_SLOTS];  // the next tile's window, copied while the current tile runs)
 };
+
+// Copy window w of a windowed graph into staging slot `slot` (asynchronously
+// on st); *off is the global edge index of the slot's first entry (a multiple
+// of 4).
+gs_status gs_stage_window(gs_graph_t g, int w, int slot, cudaStream_t st, int64_t *off);
 
 // ---------------------------------------------------------------- errors
 

@@ -48,8 +48,8 @@ constexpr int W2_LANE_BINS = 32;     // lane-private sums up to this many bins
 // 32 x warps values per bin into 128 bits, then into the global sums.
 __global__ void __launch_bounds__(W2_THREADS)
 k_count2w_lanes(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd, const int32_t *__restrict__ nbr,
-                const uint8_t *__restrict__ bin, const int16_t *__restrict__ w, int64_t n, int nb,
-                unsigned long long *__restrict__ out)
+                const uint8_t *__restrict__ bin, int64_t off, const int16_t *__restrict__ w, int64_t i0, int64_t i1,
+                int nb, unsigned long long *__restrict__ out)
 {
     extern __shared__ long long s_lane[];             // [W2_WARPS][nb][32]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -58,10 +58,10 @@ k_count2w_lanes(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__
     long long *mine = s_lane + (size_t)warp * nb * 32 + lane;
     const int64_t w0 = ((int64_t)blockIdx.x * W2_THREADS + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * W2_THREADS) >> 5;
-    for (int64_t i = w0; i < n; i += nw) {
+    for (int64_t i = i0 + w0; i < i1; i += nw) {
         const long long wi = w[i];
         const int64_t p1 = row_ptr[i + 1];
-        for (int64_t p = row_ptr[i] + fwd[i] + lane; p < p1; p += 32) mine[32 * bin[p]] += wi * w[nbr[p]];
+        for (int64_t p = row_ptr[i] + fwd[i] + lane; p < p1; p += 32) mine[32 * bin[p - off]] += wi * w[nbr[p - off]];
     }
     __syncthreads();
     for (int b = threadIdx.x; b < nb; b += W2_THREADS) {
@@ -80,7 +80,7 @@ k_count2w_lanes(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__
 // Any number of bins: 128-bit sums per block in shared memory (gs_add128).
 __global__ void __launch_bounds__(W2_THREADS)
 k_count2w(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd, const int32_t *__restrict__ nbr,
-          const uint8_t *__restrict__ bin, const int16_t *__restrict__ w, int64_t n, int nb,
+          const uint8_t *__restrict__ bin, int64_t off, const int16_t *__restrict__ w, int64_t i0, int64_t i1, int nb,
           unsigned long long *__restrict__ out)
 {
     __shared__ unsigned long long s_acc[2 * 256];
@@ -89,11 +89,11 @@ k_count2w(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd, 
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * W2_THREADS + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * W2_THREADS) >> 5;
-    for (int64_t i = w0; i < n; i += nw) {
+    for (int64_t i = i0 + w0; i < i1; i += nw) {
         const long long wi = w[i];
         const int64_t p1 = row_ptr[i + 1];
         for (int64_t p = row_ptr[i] + fwd[i] + lane; p < p1; p += 32)
-            gs_add128(s_acc + 2 * bin[p], wi * w[nbr[p]]);
+            gs_add128(s_acc + 2 * bin[p - off], wi * w[nbr[p - off]]);
     }
     __syncthreads();
     for (int b = threadIdx.x; b < nb; b += W2_THREADS)
@@ -108,17 +108,30 @@ extern "C" gs_status gs_count_2pcf_weighted(gs_graph_t g, int64_t *sums_dev, voi
     cudaStream_t st = (cudaStream_t)cuda_stream;
     GS_TRY_CUDA(cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * g->nb, st));
     if (g->n_edges == 0) return GS_OK;
-    const int grid = (int)std::min<int64_t>((g->n + W2_WARPS - 1) / W2_WARPS, (int64_t)gs_sm_count() * 8);
-    if (g->nb <= W2_LANE_BINS && g->n_edges < (1ll << 36)) {
-        const size_t dyn = sizeof(long long) * W2_WARPS * 32 * (size_t)g->nb;
-        GS_TRY_CUDA(cudaFuncSetAttribute(k_count2w_lanes, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
-        k_count2w_lanes<<<grid, W2_THREADS, dyn, st>>>(g->row_ptr, g->fwd, g->nbr, g->bin, g->w, g->n, g->nb,
-                                                        (unsigned long long *)sums_dev);
-    } else {
-        k_count2w<<<grid, W2_THREADS, 0, st>>>(g->row_ptr, g->fwd, g->nbr, g->bin, g->w, g->n, g->nb,
-                                               (unsigned long long *)sums_dev);
+    const bool lanes = g->nb <= W2_LANE_BINS && g->n_edges < (1ll << 36);
+    const size_t dyn = lanes ? sizeof(long long) * W2_WARPS * 32 * (size_t)g->nb : 0;
+    if (lanes) GS_TRY_CUDA(cudaFuncSetAttribute(k_count2w_lanes, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+    // hubs [i0, i1) with their rows at (nbr, bin) - off
+    auto launch = [&](int64_t i0, int64_t i1, const int32_t *nbr, const uint8_t *bin, int64_t off) -> gs_status {
+        const int grid = (int)std::min<int64_t>((i1 - i0 + W2_WARPS - 1) / W2_WARPS, (int64_t)gs_sm_count() * 8);
+        if (grid < 1) return GS_OK;
+        if (lanes)
+            k_count2w_lanes<<<grid, W2_THREADS, dyn, st>>>(g->row_ptr, g->fwd, nbr, bin, off, g->w, i0, i1, g->nb,
+                                                            (unsigned long long *)sums_dev);
+        else
+            k_count2w<<<grid, W2_THREADS, 0, st>>>(g->row_ptr, g->fwd, nbr, bin, off, g->w, i0, i1, g->nb,
+                                                   (unsigned long long *)sums_dev);
+        gs_note_launch();
+        GS_TRY_CUDA(cudaGetLastError());
+        return GS_OK;
+    };
+    if (g->n_win == 0) return launch(0, g->n, g->nbr, g->bin, 0);
+    for (int w = 0; w < g->n_win; ++w) {              // one staged window of hub rows at a time
+        if (g->win_e0[w + 1] == g->win_e0[w]) continue;
+        int64_t off = 0;
+        gs_status s = gs_stage_window(g, w, 0, st, &off);
+        if (s == GS_OK) s = launch(g->win_row[w], g->win_row[w + 1], g->s_nbr[0], g->s_bin[0], off);
+        if (s != GS_OK) return s;
     }
-    gs_note_launch();
-    GS_TRY_CUDA(cudaGetLastError());
     return GS_OK;
 }
