@@ -9,7 +9,8 @@ count with its histogram. The default workload is the BAO-scale 3pCF
 on its own workload and reported in the "parity_4pcf" object; the six-bin
 4pCF, the internal 2pCF and the weighted (signed int16 weights, exact)
 2pCF / 3pCF / six-bin 4pCF counts are timed beside it ("fourpcf6", "twopcf",
-"weighted"), outside the headline step.
+"weighted"), and so is the 3pCF count on a graph kept in pinned host
+memory in row windows ("windowed"), all outside the headline step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -63,6 +64,9 @@ def parse_args():
     p.add_argument("--only-parity", action="store_true",
                    help="time only the parity-4pCF path and print its own line")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-windowed", action="store_true",
+                   help="skip the out-of-core (row window) 3pCF timings")
+    p.add_argument("--windowed-workload", default="large_3pcf")
     p.add_argument("--no-weighted", action="store_true",
                    help="skip the weighted 2pCF / 3pCF / six-bin 4pCF timings")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -478,6 +482,36 @@ def run_ours(args, w):
                 t6.append(e0.elapsed_time(e1))
         weighted["fourpcf6_count_ms"] = statistics.mean(t6)
 
+    # out-of-core row windows: the 3pCF count with the edge arrays in pinned
+    # host memory, against the device-resident count, on the 2M-point uniform
+    # workload (inputs staged per tile inside the timed call)
+    windowed = None
+    if not args.no_windowed:
+        ww = configs.ALL[args.windowed_workload]
+        wxyz, wbox, wdesc = catalogue(ww, args.scale, rank)
+        wc = torch.from_numpy(wxyz).to(dev)
+
+        def _count_ms(g):
+            g.count_3pcf()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            h = g.count_3pcf()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1), as_uint64(h)
+
+        with build_graph(wc, wbox, ww.periodic, ww.edges_lu) as g:
+            t_res, h_res = _count_ms(g)
+            e_all = g.n_edges
+        rows = []
+        for nwin in (2, 4, 8):
+            with build_graph(wc, wbox, ww.periodic, ww.edges_lu, window_edges=e_all // nwin + 1) as g:
+                t_w, h_w = _count_ms(g)
+                rows.append({"window_edges": e_all // nwin + 1, "windows": g.windows()[0], "count_ms": t_w,
+                             "overhead": t_w / t_res - 1.0, "exact": bool(np.array_equal(h_w, h_res))})
+        windowed = {"config": wdesc, "resident_count_ms": t_res, "n_edges": e_all, "tiles": rows}
+
     # CPU oracle on a bounded sample (rank 0 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -509,7 +543,7 @@ def run_ours(args, w):
                 "count_ms": count_ms_max, "wall_s_timed": t_wall,
                 "graph_stats": st, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clocks, "parity_4pcf": parity,
-                "fourpcf6": fourpcf6, "twopcf": twopcf, "weighted": weighted}
+                "fourpcf6": fourpcf6, "twopcf": twopcf, "weighted": weighted, "windowed": windowed}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -521,6 +521,29 @@ gs_status gs_stage_window(gs_graph_t g, int w, int slot, cudaStream_t st, int64_
     return GS_OK;
 }
 
+gs_status gs_stage_set(gs_graph_t g, int *held, int64_t *off, const int *need, int n, int *slot, cudaStream_t st)
+{
+    bool used[GS_SLOTS] = {};
+    for (int q = 0; q < n; ++q) {
+        slot[q] = -1;
+        for (int k = 0; k < GS_SLOTS; ++k)
+            if (held[k] == need[q]) slot[q] = k;
+        if (slot[q] >= 0) used[slot[q]] = true;
+    }
+    for (int q = 0; q < n; ++q) {
+        if (slot[q] >= 0) continue;
+        int k = 0;
+        while (used[k]) ++k;                 // n <= GS_SLOTS distinct windows: a free slot exists
+        gs_status s = gs_stage_window(g, need[q], k, st, &off[k]);
+        if (s != GS_OK) return s;
+        held[k] = need[q];
+        used[k] = true;
+        for (int r = q; r < n; ++r)          // the same window asked for twice
+            if (need[r] == need[q]) slot[r] = k;
+    }
+    return GS_OK;
+}
+
 // Edge budget of a graph: window_edges > 0 forces row windows of that size;
 // 0 keeps the CSR on the device unless it would not fit (then windows of a
 // quarter of the free memory); the environment variable GS_WINDOW_EDGES, when

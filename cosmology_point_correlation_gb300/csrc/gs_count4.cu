@@ -22,9 +22,16 @@
 // shared histograms; rarer hubs of higher degree run in a second kernel whose
 // per-block matrix lives in a global scratch slice and which adds straight
 // into the global histograms.
+//
+// Windowed graphs (§III.5.3: tiles over pairs of search windows c1 <= c2):
+// a tile stages the hub window and windows c1, c2; the bit rows of spokes in
+// c1 and c2 are built, and only cliques s1 < s2 < s3 with s1 in c1 and s2 in
+// c2 are counted. The rows of s1 and s2 give all three bits, and the windows
+// of s1 <= s2 fix one tile, so every clique is counted once.
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "gs_internal.cuh"
 
@@ -55,7 +62,25 @@ struct C4Args {
     int big_m;                    // largest degree the scratch slices hold
     char *scratch;                // gridDim.x slices of scratch_stride bytes
     size_t scratch_stride;
+    // windowed graphs: hub rows at hnbr / hbin (edge e at e - hoff); spoke rows
+    // of ids in [a_lo, a_hi) at anbr - aoff, of ids in [b_lo, b_hi) at
+    // bnbr - boff (the same window when a_lo == b_lo)
+    const int32_t *hnbr, *anbr, *bnbr;
+    const uint8_t *hbin;
+    int64_t hoff, aoff, boff;
+    int32_t a_lo, a_hi, b_lo, b_hi;
 };
+
+// First position of a sorted row whose id is >= key.
+__device__ __forceinline__ int c4_lower(const int32_t *row, int m, int32_t key)
+{
+    int lo = 0, hi = m;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (row[mid] < key) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
 
 // Workspace of one hub: either shared memory or a global scratch slice.
 struct HubSpace {
@@ -67,22 +92,39 @@ struct HubSpace {
     unsigned *bits;    // [m][W] adjacency bits
 };
 
-template <bool SMEM_HIST>
+template <bool SMEM_HIST, bool WINDOWED>
 __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long long i, int m,
                                        int tlog, unsigned *s_even, int *s_odd,
                                        const int *lex_a, const int *lex_b)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t r0 = a.row_ptr[i];
+    const int32_t *R = WINDOWED ? a.hnbr + (r0 - a.hoff) : a.nbr + r0;     // the hub row and its bins
+    const uint8_t *RB = WINDOWED ? a.hbin + (r0 - a.hoff) : a.bin + r0;
+    // spokes whose rows are walked: positions [pa0, pa1) (window c1) and
+    // [pb0, pb1) (window c2 when it differs); cliques take s1 in [pa0, pa1) and
+    // s2 in [q2_lo, q2_hi)
+    int pa0 = 0, pa1 = m, pb0 = 0, pb1 = 0, q2_lo = 0, q2_hi = m;
+    if (WINDOWED) {                                            // the same values in every thread
+        pa0 = c4_lower(R, m, a.a_lo);
+        pa1 = c4_lower(R, m, a.a_hi);
+        q2_lo = pa0;
+        q2_hi = pa1;
+        if (a.b_lo != a.a_lo) {
+            pb0 = q2_lo = c4_lower(R, m, a.b_lo);
+            pb1 = q2_hi = c4_lower(R, m, a.b_hi);
+        }
+        if (pa0 >= pa1 || q2_lo >= q2_hi || pa0 >= q2_hi - 1) return;   // no clique in this tile
+    }
     const int W = (m + 31) >> 5;
     const int tsize = 1 << tlog, shift = 32 - tlog, mask = tsize - 1;
     const int4 P = a.pts[i];
 
     // 1. stage the row and the table
     for (int t = threadIdx.x; t < m; t += C4_THREADS) {
-        const int32_t k = a.nbr[r0 + t];
+        const int32_t k = R[t];
         w.row[t] = k;
-        w.hb[t] = a.bin[r0 + t];
+        w.hb[t] = RB[t];
         const int4 Q = a.pts[k];
         w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
         w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
@@ -96,12 +138,18 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
 
     // 2. adjacency among the spokes: bit (s, t) for t > s
     const int32_t kmax = w.row[m - 1];
-    for (int s = warp; s < m - 1; s += C4_WARPS) {
+    const int na = pa1 - pa0, nab = na + (pb1 - pb0);
+    for (int u = warp; u < nab; u += C4_WARPS) {
+        const bool in_a = u < na;
+        const int s = in_a ? pa0 + u : pb0 + (u - na);
+        if (s >= m - 1) continue;                              // no position above the last
+        const int32_t *SN = WINDOWED ? (in_a ? a.anbr : a.bnbr) : a.nbr;
+        const int64_t soff = WINDOWED ? (in_a ? a.aoff : a.boff) : 0;
         const int32_t j = w.row[s];
         const int64_t pe = a.row_ptr[j + 1];
         for (int64_t p = a.row_ptr[j] + a.fwd[j]; p < pe; p += 32) {
             const int64_t q = p + lane;
-            const int32_t k = q < pe ? a.nbr[q] : 0x7fffffff;
+            const int32_t k = q < pe ? SN[q - soff] : 0x7fffffff;
             if (k <= kmax) {
                 uint32_t h = gs_hash(k, shift);
                 int32_t key;
@@ -117,10 +165,11 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
     __syncthreads();
 
     // 3. cliques (s1 < s2 < s3), distinct hub bins: a warp per s1, lanes over s2
-    for (int s1 = warp; s1 < m - 2; s1 += C4_WARPS) {
+    const int s1_end = min(pa1, m - 2), s2_end = min(q2_hi, m - 1);
+    for (int s1 = pa0 + warp; s1 < s1_end; s1 += C4_WARPS) {
         const int b1 = w.hb[s1];
         const unsigned *row1 = w.bits + (size_t)s1 * W;
-        for (int s2 = s1 + 1 + lane; s2 < m - 1; s2 += 32) {
+        for (int s2 = max(s1 + 1, q2_lo) + lane; s2 < s2_end; s2 += 32) {
             if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
             const int b2 = w.hb[s2];
             if (b1 == b2) continue;
@@ -187,7 +236,7 @@ __device__ __forceinline__ void c4_flush(unsigned *se, int *so, int ncfg, unsign
 
 // Hubs of degree 3..C4_M, workspace in shared memory; histograms in shared
 // memory too unless there are too many configurations.
-template <bool SMEM_HIST, bool HUB_LIST>
+template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
 __global__ void __launch_bounds__(C4_THREADS)
 k_count4_small(C4Args a)
 {
@@ -235,7 +284,7 @@ k_count4_small(C4Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * m) ++tlog;
-        c4_hub<SMEM_HIST>(a, w, i, m, tlog, s_even, s_odd, s_lex_a, s_lex_b);
+        c4_hub<SMEM_HIST, WINDOWED>(a, w, i, m, tlog, s_even, s_odd, s_lex_a, s_lex_b);
     }
     if (SMEM_HIST) {
         __syncthreads();
@@ -245,7 +294,7 @@ k_count4_small(C4Args a)
 
 // Hubs of degree > C4_M: workspace in a global scratch slice per block,
 // histograms added straight to global memory.
-template <bool HUB_LIST>
+template <bool HUB_LIST, bool WINDOWED>
 __global__ void __launch_bounds__(C4_THREADS)
 k_count4_large(C4Args a)
 {
@@ -279,54 +328,24 @@ k_count4_large(C4Args a)
         if (m <= C4_M) continue;
         int tl = 4;
         while ((1 << tl) < 2 * m) ++tl;
-        c4_hub<false>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
+        c4_hub<false, WINDOWED>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
     }
 }
 
-extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
-                                          int64_t hub_begin, int64_t hub_end, void *cuda_stream)
+// Both kernels over the hubs [a.hub_begin, a.hub_end) (outputs accumulate).
+static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t st)
 {
-    gs_clear_error();
-    if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
-    if (g->n_win) return gs_set_error(GS_ERR_ARG, "the parity 4pCF needs a device-resident graph (this one is windowed)");
-    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
-        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
-                            (long long)hub_end, (long long)g->n);
-    if (g->edges[g->nb] >= (1ll << 20))
-        return gs_set_error(GS_ERR_ARG, "parity 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
-    const int64_t ncfg = gs_ncfg4(g->nb);
-    if (ncfg <= 0) return GS_OK;
-    if (!even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL histogram");
-    cudaStream_t st = (cudaStream_t)cuda_stream;
-    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
-    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
-    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
-    GS_TRY_CUDA(cudaMemsetAsync(g->work + 1, 0, 2 * sizeof(unsigned long long), st));
-
-    C4Args a{};
-    a.pts = g->pts;
-    a.row_ptr = g->row_ptr;
-    a.fwd = g->fwd;
-    a.nbr = g->nbr;
-    a.bin = g->bin;
-    a.hub_begin = hub_begin;
-    a.hub_end = hub_end;
-    a.box = (int)g->box_lu;
-    a.periodic = g->periodic;
-    a.nb = g->nb;
-    a.ncfg = (int)ncfg;
-    a.even = (unsigned long long *)even_dev;
-    a.odd = (long long *)odd_dev;
-
-    const int64_t hubs = hub_end - hub_begin;
+    const int64_t hubs = a.hub_end - a.hub_begin;
     const int sms = gs_sm_count();
-    const bool smem = ncfg <= C4_SMEM_HIST_MAX;
-    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true, false> : k_count4_small<false, false>;
+    const bool smem = a.ncfg <= C4_SMEM_HIST_MAX;
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * (size_t)a.ncfg : 0));
+    auto kern = windowed ? (smem ? k_count4_small<true, false, true> : k_count4_small<false, false, true>)
+                         : (smem ? k_count4_small<true, false, false> : k_count4_small<false, false, false>);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
     per_sm = std::max(per_sm, 1);
+    GS_TRY_CUDA(cudaMemsetAsync(g->work + 1, 0, 2 * sizeof(unsigned long long), st));
     a.cursor = g->work + 1;
     const int grid = (int)std::min<int64_t>((int64_t)sms * per_sm, hubs);
     kern<<<grid, C4_THREADS, dyn, st>>>(a);
@@ -347,11 +366,82 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        k_count4_large<false><<<gl, C4_THREADS, 0, st>>>(a);
+        if (windowed) k_count4_large<false, true><<<gl, C4_THREADS, 0, st>>>(a);
+        else k_count4_large<false, false><<<gl, C4_THREADS, 0, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
         if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    return GS_OK;
+}
+
+extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
+                                          int64_t hub_begin, int64_t hub_end, void *cuda_stream)
+{
+    gs_clear_error();
+    if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
+        return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
+                            (long long)hub_end, (long long)g->n);
+    if (g->edges[g->nb] >= (1ll << 20))
+        return gs_set_error(GS_ERR_ARG, "parity 4pCF needs r_max_lu < 2^20 for an exact int64 volume");
+    const int64_t ncfg = gs_ncfg4(g->nb);
+    if (ncfg <= 0) return GS_OK;
+    if (!even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL histogram");
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
+    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
+    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
+
+    C4Args a{};
+    a.pts = g->pts;
+    a.row_ptr = g->row_ptr;
+    a.fwd = g->fwd;
+    a.nbr = g->nbr;
+    a.bin = g->bin;
+    a.hub_begin = hub_begin;
+    a.hub_end = hub_end;
+    a.box = (int)g->box_lu;
+    a.periodic = g->periodic;
+    a.nb = g->nb;
+    a.ncfg = (int)ncfg;
+    a.even = (unsigned long long *)even_dev;
+    a.odd = (long long *)odd_dev;
+    if (!g->n_win) return c4_launch(g, a, false, st);
+
+    // windowed: tiles (hub window h, spoke windows c1 <= c2), both adjacent to h
+    int held[GS_SLOTS];
+    int64_t off[GS_SLOTS] = {};
+    for (int k = 0; k < GS_SLOTS; ++k) held[k] = -1;
+    for (int h = 0; h < g->n_win; ++h) {
+        const int64_t b0 = std::max(hub_begin, g->win_row[h]), b1 = std::min(hub_end, g->win_row[h + 1]);
+        if (b0 >= b1 || g->win_e0[h + 1] == g->win_e0[h]) continue;
+        std::vector<int> adj;
+        for (int c = 0; c < g->n_win; ++c)
+            if (g->win_e0[c + 1] > g->win_e0[c] && gs_windows_adjacent(g, h, c)) adj.push_back(c);
+        for (size_t x = 0; x < adj.size(); ++x)
+            for (size_t y = x; y < adj.size(); ++y) {
+                const int need[3] = { h, adj[x], adj[y] };
+                int slot[3];
+                gs_status s = gs_stage_set(g, held, off, need, 3, slot, st);
+                if (s != GS_OK) return s;
+                a.hnbr = g->s_nbr[slot[0]];
+                a.hbin = g->s_bin[slot[0]];
+                a.hoff = off[slot[0]];
+                a.anbr = g->s_nbr[slot[1]];
+                a.aoff = off[slot[1]];
+                a.bnbr = g->s_nbr[slot[2]];
+                a.boff = off[slot[2]];
+                a.a_lo = (int32_t)g->win_row[adj[x]];
+                a.a_hi = (int32_t)g->win_row[adj[x] + 1];
+                a.b_lo = (int32_t)g->win_row[adj[y]];
+                a.b_hi = (int32_t)g->win_row[adj[y] + 1];
+                a.hub_begin = b0;
+                a.hub_end = b1;
+                s = c4_launch(g, a, true, st);
+                if (s != GS_OK) return s;
+            }
     }
     return GS_OK;
 }
@@ -396,7 +486,7 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true, true> : k_count4_small<false, true>;
+    auto kern = smem ? k_count4_small<true, true, false> : k_count4_small<false, true, false>;
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -419,7 +509,7 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        k_count4_large<true><<<gl, C4_THREADS, 0, st>>>(a);
+        k_count4_large<true, false><<<gl, C4_THREADS, 0, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
@@ -525,7 +615,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true, false> : k_count4_small<false, false>;
+    auto kern = smem ? k_count4_small<true, false, false> : k_count4_small<false, false, false>;
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -543,7 +633,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
         a.big_m = M;
         a.scratch = base + GS_C4_STATIC_HEAD;
         a.scratch_stride = stride;
-        k_count4_large<false><<<gl, C4_THREADS, 0, st>>>(a);
+        k_count4_large<false, false><<<gl, C4_THREADS, 0, st>>>(a);
         gs_note_launch();
         GS_TRY_CUDA(cudaGetLastError());
     }

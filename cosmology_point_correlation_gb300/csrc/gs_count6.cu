@@ -18,6 +18,10 @@
 // Hubs with more than C6_M forward neighbours use a global scratch slice per
 // block instead of shared memory.
 //
+// Windowed graphs (§III.5.3): tiles (hub window, spoke windows c1 <= c2) as
+// for the parity count; only tetrahedra whose two lowest spokes lie in c1 and
+// c2 are counted in a tile, so each is counted once.
+//
 // Weighted counts (§II.1 signed weights): each tetrahedron adds
 // W = w_i w_j1 w_j2 w_j3 (|W| <= 2^60) to the even channel and sign x W to
 // the odd one, into exact 128-bit sums: per block in shared memory as four
@@ -57,7 +61,25 @@ struct C6Args {
     // weighted counts: weights in internal order; 128-bit sums [ncfg][2]
     const int16_t *w;
     unsigned long long *weven, *wodd;
+    // windowed graphs: hub rows at hnbr / hbin (edge e at e - hoff); spoke rows
+    // of ids in [a_lo, a_hi) at anbr / abin - aoff, of ids in [b_lo, b_hi) at
+    // bnbr / bbin - boff (the same window when a_lo == b_lo)
+    const int32_t *hnbr, *anbr, *bnbr;
+    const uint8_t *hbin, *abin, *bbin;
+    int64_t hoff, aoff, boff;
+    int32_t a_lo, a_hi, b_lo, b_hi;
 };
+
+// First position of a sorted row whose id is >= key.
+__device__ __forceinline__ int c6_lower(const int32_t *row, int m, int32_t key)
+{
+    int lo = 0, hi = m;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (row[mid] < key) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
 
 struct C6Space {
     int32_t *key;      // hash table
@@ -70,20 +92,36 @@ struct C6Space {
     int16_t *ww;       // [f] spoke weights (weighted counts)
 };
 
-template <bool SMEM_HIST, bool WEIGHTED>
+template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
 __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long long i, int64_t f0, int f,
                                        int tlog, unsigned *s_even, int *s_odd, unsigned *s_w128)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t *F = WINDOWED ? a.hnbr + (f0 - a.hoff) : a.nbr + f0;       // forward row and its bins
+    const uint8_t *FB = WINDOWED ? a.hbin + (f0 - a.hoff) : a.bin + f0;
+    // spokes walked: positions [pa0, pa1) (window c1) and [pb0, pb1) (c2 when
+    // it differs); tetrahedra take s1 in [pa0, pa1), s2 in [q2_lo, q2_hi)
+    int pa0 = 0, pa1 = f, pb0 = 0, pb1 = 0, q2_lo = 0, q2_hi = f;
+    if (WINDOWED) {                                            // the same values in every thread
+        pa0 = c6_lower(F, f, a.a_lo);
+        pa1 = c6_lower(F, f, a.a_hi);
+        q2_lo = pa0;
+        q2_hi = pa1;
+        if (a.b_lo != a.a_lo) {
+            pb0 = q2_lo = c6_lower(F, f, a.b_lo);
+            pb1 = q2_hi = c6_lower(F, f, a.b_hi);
+        }
+        if (pa0 >= pa1 || q2_lo >= q2_hi || pa0 >= q2_hi - 1) return;   // nothing in this tile
+    }
     const int W = (f + 31) >> 5;
     const int tsize = 1 << tlog, shift = 32 - tlog, mask = tsize - 1;
     const int4 P = a.pts[i];
     const int nb = a.nb;
 
     for (int t = threadIdx.x; t < f; t += C6_THREADS) {
-        const int32_t k = a.nbr[f0 + t];
+        const int32_t k = F[t];
         w.row[t] = k;
-        w.hb[t] = a.bin[f0 + t];
+        w.hb[t] = FB[t];
         const int4 Q = a.pts[k];
         w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
         w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
@@ -97,12 +135,19 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     __syncthreads();
 
     const int32_t kmax = w.row[f - 1];
-    for (int s = warp; s < f - 1; s += C6_WARPS) {
+    const int na = pa1 - pa0, nab = na + (pb1 - pb0);
+    for (int u = warp; u < nab; u += C6_WARPS) {
+        const bool in_a = u < na;
+        const int s = in_a ? pa0 + u : pb0 + (u - na);
+        if (s >= f - 1) continue;                              // no position above the last
+        const int32_t *SN = WINDOWED ? (in_a ? a.anbr : a.bnbr) : a.nbr;
+        const uint8_t *SB = WINDOWED ? (in_a ? a.abin : a.bbin) : a.bin;
+        const int64_t soff = WINDOWED ? (in_a ? a.aoff : a.boff) : 0;
         const int32_t j = w.row[s];
         const int64_t pe = a.row_ptr[j + 1];
         for (int64_t p = a.row_ptr[j] + a.fwd[j]; p < pe; p += 32) {
             const int64_t q = p + lane;
-            const int32_t k = q < pe ? a.nbr[q] : 0x7fffffff;
+            const int32_t k = q < pe ? SN[q - soff] : 0x7fffffff;
             if (k <= kmax) {
                 uint32_t h = gs_hash(k, shift);
                 int32_t key;
@@ -110,7 +155,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                 if (key == k) {
                     const int t = w.pos[h];
                     atomicOr(&w.bits[(size_t)s * W + (t >> 5)], 1u << (t & 31));
-                    w.sbin[(size_t)s * f + t] = a.bin[q];
+                    w.sbin[(size_t)s * f + t] = SB[q - soff];
                 }
             }
             if (__shfl_sync(0xffffffffu, k, 31) > kmax) break;
@@ -119,11 +164,12 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     __syncthreads();
 
     const long long wi = WEIGHTED ? (long long)a.w[i] : 0;
-    for (int s1 = warp; s1 < f - 2; s1 += C6_WARPS) {
+    const int s1_end = min(pa1, f - 2), s2_end = min(q2_hi, f - 1);
+    for (int s1 = pa0 + warp; s1 < s1_end; s1 += C6_WARPS) {
         const unsigned *row1 = w.bits + (size_t)s1 * W;
         const int b01 = w.hb[s1];
         const long long x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
-        for (int s2 = s1 + 1 + lane; s2 < f - 1; s2 += 32) {
+        for (int s2 = max(s1 + 1, q2_lo) + lane; s2 < s2_end; s2 += 32) {
             if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
             const unsigned *row2 = w.bits + (size_t)s2 * W;
             const int b02 = w.hb[s2], b12 = w.sbin[(size_t)s1 * f + s2];
@@ -179,7 +225,7 @@ __device__ __forceinline__ void c6_flush(unsigned *se, int *so, int ncfg, unsign
 }
 
 // Hubs with 3..C6_M forward neighbours, workspace in shared memory.
-template <bool SMEM_HIST, bool WEIGHTED>
+template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
 __global__ void __launch_bounds__(C6_THREADS, 2)
 k_count6_small(C6Args a)
 {
@@ -232,7 +278,7 @@ k_count6_small(C6Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * f) ++tlog;
-        c6_hub<SMEM_HIST, WEIGHTED>(a, w, i, f0, f, tlog, s_even, s_odd, s_w128);
+        c6_hub<SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tlog, s_even, s_odd, s_w128);
     }
     if (SMEM_HIST && WEIGHTED) {
         __syncthreads();
@@ -250,7 +296,7 @@ k_count6_small(C6Args a)
 }
 
 // Hubs with more than C6_M forward neighbours: workspace in a global slice.
-template <bool WEIGHTED>
+template <bool WEIGHTED, bool WINDOWED>
 __global__ void __launch_bounds__(C6_THREADS)
 k_count6_large(C6Args a)
 {
@@ -284,7 +330,7 @@ k_count6_large(C6Args a)
         if (f <= C6_M) continue;
         int tl = 4;
         while ((1 << tl) < 2 * f) ++tl;
-        c6_hub<false, WEIGHTED>(a, w, i, f0, f, tl, nullptr, nullptr, nullptr);
+        c6_hub<false, WEIGHTED, WINDOWED>(a, w, i, f0, f, tl, nullptr, nullptr, nullptr);
     }
 }
 
@@ -423,7 +469,7 @@ extern "C" int64_t gs_config_count_4pcf6(int nbins)
 
 // Launch the small-hub and large-hub kernels over [hub_begin, hub_end) of a
 // prepared argument block (outputs already cleared).
-static gs_status c6_launch(gs_graph_t g, C6Args &a, cudaStream_t st)
+static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t st)
 {
     const int64_t hubs = a.hub_end - a.hub_begin;
     const int sms = gs_sm_count();
@@ -432,8 +478,13 @@ static gs_status c6_launch(gs_graph_t g, C6Args &a, cudaStream_t st)
     const bool smem = weighted ? ncfg <= C6_SMEM_W_MAX : ncfg <= C6_SMEM_HIST_MAX;
     const size_t acc = weighted ? 32 * (size_t)ncfg : 8 * (size_t)ncfg;
     const size_t dyn = sizeof(unsigned) * C6_M * C6_WORDS + (size_t)C6_M * C6_M + (smem ? acc : 0);
-    auto kern = weighted ? (smem ? k_count6_small<true, true> : k_count6_small<false, true>)
-                         : (smem ? k_count6_small<true, false> : k_count6_small<false, false>);
+    decltype(&k_count6_small<true, true, true>) kern;
+    if (windowed)
+        kern = weighted ? (smem ? k_count6_small<true, true, true> : k_count6_small<false, true, true>)
+                        : (smem ? k_count6_small<true, false, true> : k_count6_small<false, false, true>);
+    else
+        kern = weighted ? (smem ? k_count6_small<true, true, false> : k_count6_small<false, true, false>)
+                        : (smem ? k_count6_small<true, false, false> : k_count6_small<false, false, false>);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C6_THREADS, dyn));
@@ -455,8 +506,9 @@ static gs_status c6_launch(gs_graph_t g, C6Args &a, cudaStream_t st)
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        if (weighted) k_count6_large<true><<<gl, C6_THREADS, 0, st>>>(a);
-        else k_count6_large<false><<<gl, C6_THREADS, 0, st>>>(a);
+        auto big = windowed ? (weighted ? k_count6_large<true, true> : k_count6_large<false, true>)
+                            : (weighted ? k_count6_large<true, false> : k_count6_large<false, false>);
+        big<<<gl, C6_THREADS, 0, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
@@ -465,9 +517,55 @@ static gs_status c6_launch(gs_graph_t g, C6Args &a, cudaStream_t st)
     return GS_OK;
 }
 
+// The hubs [hub_begin, hub_end): one pass on a device-resident graph; on a
+// windowed graph one pass per tile (hub window h, spoke windows c1 <= c2 that
+// hold forward neighbours of window h), the three windows staged.
+static gs_status c6_run(gs_graph_t g, C6Args a, int64_t hub_begin, int64_t hub_end, cudaStream_t st)
+{
+    if (!g->n_win) {
+        a.hub_begin = hub_begin;
+        a.hub_end = hub_end;
+        return c6_launch(g, a, false, st);
+    }
+    int held[GS_SLOTS];
+    int64_t off[GS_SLOTS] = {};
+    for (int k = 0; k < GS_SLOTS; ++k) held[k] = -1;
+    for (int h = 0; h < g->n_win; ++h) {
+        const int64_t b0 = std::max(hub_begin, g->win_row[h]), b1 = std::min(hub_end, g->win_row[h + 1]);
+        if (b0 >= b1 || g->win_e0[h + 1] == g->win_e0[h]) continue;
+        std::vector<int> fw;
+        for (int c = h; c < g->n_win; ++c)
+            if (g->win_e0[c + 1] > g->win_e0[c] && g->win_pair[(size_t)h * g->n_win + c]) fw.push_back(c);
+        for (size_t x = 0; x < fw.size(); ++x)
+            for (size_t y = x; y < fw.size(); ++y) {
+                const int need[3] = { h, fw[x], fw[y] };
+                int slot[3];
+                gs_status s = gs_stage_set(g, held, off, need, 3, slot, st);
+                if (s != GS_OK) return s;
+                a.hnbr = g->s_nbr[slot[0]];
+                a.hbin = g->s_bin[slot[0]];
+                a.hoff = off[slot[0]];
+                a.anbr = g->s_nbr[slot[1]];
+                a.abin = g->s_bin[slot[1]];
+                a.aoff = off[slot[1]];
+                a.bnbr = g->s_nbr[slot[2]];
+                a.bbin = g->s_bin[slot[2]];
+                a.boff = off[slot[2]];
+                a.a_lo = (int32_t)g->win_row[fw[x]];
+                a.a_hi = (int32_t)g->win_row[fw[x] + 1];
+                a.b_lo = (int32_t)g->win_row[fw[y]];
+                a.b_hi = (int32_t)g->win_row[fw[y] + 1];
+                a.hub_begin = b0;
+                a.hub_end = b1;
+                s = c6_launch(g, a, true, st);
+                if (s != GS_OK) return s;
+            }
+    }
+    return GS_OK;
+}
+
 static gs_status c6_check(gs_graph_t g, int64_t hub_begin, int64_t hub_end)
 {
-    if (g->n_win) return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF needs a device-resident graph (this one is windowed)");
     if (g->nb > C6_MAX_BINS)
         return gs_set_error(GS_ERR_ARG, "the six-bin 4pCF supports at most %d bins", C6_MAX_BINS);
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
@@ -512,7 +610,7 @@ extern "C" gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *o
     C6Args a = c6_args(g, hub_begin, hub_end);
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
-    return c6_launch(g, a, st);
+    return c6_run(g, a, hub_begin, hub_end, st);
 }
 
 extern "C" gs_status gs_count_4pcf6_weighted(gs_graph_t g, int64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
@@ -532,5 +630,5 @@ extern "C" gs_status gs_count_4pcf6_weighted(gs_graph_t g, int64_t *even_dev, in
     a.w = g->w;
     a.weven = (unsigned long long *)even_dev;
     a.wodd = (unsigned long long *)odd_dev;
-    return c6_launch(g, a, st);
+    return c6_run(g, a, hub_begin, hub_end, st);
 }

@@ -71,6 +71,20 @@ struct gs_graph {
 // of 4).
 gs_status gs_stage_window(gs_graph_t g, int w, int slot, cudaStream_t st, int64_t *off);
 
+// Make the windows need[0..n) (n <= GS_SLOTS) resident in the staging slots,
+// stream-ordered on st: a window already held (held[k] == window) is reused,
+// others are copied into slots this call does not need. On return slot[q] is
+// the slot of need[q] and off[slot[q]] its first edge. held / off persist
+// across calls of one query (initialise held to -1).
+gs_status gs_stage_set(gs_graph_t g, int *held, int64_t *off, const int *need, int n, int *slot, cudaStream_t st);
+
+// Is there an edge between a row of window h and a row of window c (either
+// direction)?
+inline bool gs_windows_adjacent(gs_graph_t g, int h, int c)
+{
+    return g->win_pair[(size_t)h * g->n_win + c] || g->win_pair[(size_t)c * g->n_win + h];
+}
+
 // ---------------------------------------------------------------- errors
 
 gs_status gs_set_error(gs_status s, const char *fmt, ...);

@@ -268,16 +268,16 @@ gs_status gs_graph_stats(gs_graph_t g, gs_graph_stats_t *out, void *cuda_stream)
  * a larger cell gets a window of its own). This is the out-of-core mode of
  * §III.5.3 for graphs larger than device memory: a query stages one hub
  * window and one spoke window at a time (two device slots of the largest
- * window) and runs one tile per (hub window, spoke window >= it) pair; every
- * triangle lands in exactly one tile, so results equal those of the resident
- * graph bit for bit. gs_build_graph itself switches to this mode when the CSR
+ * window) and runs one tile per (hub window, spoke window >= it) pair; the
+ * 4pCF counts run one tile per (hub window, spoke windows c1 <= c2) triple
+ * (three slots). Every triangle and clique lands in exactly one tile, so
+ * results equal those of the resident graph bit for bit. gs_build_graph itself switches to this mode when the CSR
  * does not fit in free device memory, or when the environment variable
  * GS_WINDOW_EDGES holds a positive edge count.
  *   window_edges  >= 1
- * Windowed graphs support gs_count_3pcf, gs_count_3pcf_weighted,
- * gs_count_2pcf, gs_count_2pcf_weighted, the exports, stats and info; the
- * 4pCF counts and hub lists return GS_ERR_ARG. Needs 5 B per edge of host
- * memory. Errors: as gs_build_graph. */
+ * Windowed graphs support every count (plain and weighted), the exports,
+ * stats and info; the hub-list counts and gs_count_4pcf_parity_static return
+ * GS_ERR_ARG. Needs 5 B per edge of host memory. Errors: as gs_build_graph. */
 gs_status gs_build_graph_windowed(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
                                   int64_t r_max_lu, const int64_t *edges_lu, int nbins,
                                   int64_t window_edges, void *cuda_stream, gs_graph_t *out);
