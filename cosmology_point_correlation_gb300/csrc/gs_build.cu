@@ -545,9 +545,9 @@ gs_status gs_stage_set(gs_graph_t g, int *held, int64_t *off, const int *need, i
 }
 
 // Edge budget of a graph: window_edges > 0 forces row windows of that size;
-// 0 keeps the CSR on the device unless it would not fit (then windows of a
-// quarter of the free memory); the environment variable GS_WINDOW_EDGES, when
-// set to a positive count, overrides 0.
+// 0 keeps the CSR on the device unless it would not fit, and then uses windows
+// of an eighth of the free memory each (three staging slots); the environment
+// variable GS_WINDOW_EDGES, when set to a positive count, overrides 0.
 static int64_t choose_window_edges(int64_t window_edges, int64_t n_edges)
 {
     if (window_edges > 0) return window_edges;
@@ -559,7 +559,7 @@ static int64_t choose_window_edges(int64_t window_edges, int64_t n_edges)
     if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return 0;
     const size_t need = 5 * (size_t)(n_edges + GS_EDGE_PAD) + ((size_t)256 << 20);
     if (need <= fr) return 0;
-    return std::max<int64_t>((int64_t)(fr / 4 / 5 / 2), (int64_t)1 << 20);
+    return std::max<int64_t>((int64_t)(fr / 8 / 5), (int64_t)1 << 20);     // 5 B per edge
 }
 
 static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu, int periodic,
