@@ -30,6 +30,7 @@
 
 #include <algorithm>
 #include <array>
+#include <type_traits>
 #include <vector>
 
 #include "gs_internal.cuh"
@@ -37,7 +38,7 @@
 constexpr int C6_THREADS = 256;
 constexpr int C6_WARPS = C6_THREADS / 32;
 constexpr int C6_M = 256;                   // forward degree kept in shared memory
-constexpr int C6_WORDS = C6_M / 32;
+constexpr int C6_M_SMALL = 128;             // hubs up to this degree run in a lighter kernel (more blocks per SM)
 constexpr int C6_SMEM_HIST_MAX = 4096;
 constexpr int C6_SMEM_W_MAX = 2500;         // weighted: configurations with shared 128-bit sums (nb <= 6)
 constexpr int C6_EMPTY = -1;
@@ -55,6 +56,7 @@ struct C6Args {
     unsigned long long *even;
     long long *odd;
     unsigned long long *cursor;
+    int f_lo;                     // small paths: hubs with f_lo < f <= M
     int big_m;                    // large path: forward degree the slices hold
     char *scratch;
     size_t scratch_stride;
@@ -224,26 +226,28 @@ __device__ __forceinline__ void c6_flush(unsigned *se, int *so, int ncfg, unsign
     }
 }
 
-// Hubs with 3..C6_M forward neighbours, workspace in shared memory.
-template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
-__global__ void __launch_bounds__(C6_THREADS, 2)
+// Hubs with max(3, a.f_lo + 1) .. M forward neighbours, workspace in shared
+// memory. M = 128 keeps the per-block footprint near 25 KB (about four
+// resident blocks per SM); M = 256 takes the rarer hubs up to C6_M.
+template <int M, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
+__global__ void __launch_bounds__(C6_THREADS, M <= C6_M_SMALL ? 4 : 2)
 k_count6_small(C6Args a)
 {
-    // dynamic: bits [C6_M*C6_WORDS], sbin [C6_M*C6_M], then (SMEM_HIST) even,
-    // odd [ncfg] each, or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
+    // dynamic: bits [M*M/32], sbin [M*M], then (SMEM_HIST) even, odd [ncfg]
+    // each, or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
     extern __shared__ unsigned s_dyn[];
-    __shared__ int32_t s_key[2 * C6_M];
-    __shared__ int32_t s_pos[2 * C6_M];
-    __shared__ int32_t s_row[C6_M];
-    __shared__ uint8_t s_hb[C6_M];
-    __shared__ int s_vx[C6_M], s_vy[C6_M], s_vz[C6_M];
-    __shared__ int16_t s_ww[C6_M];
+    __shared__ int32_t s_key[2 * M];
+    __shared__ int32_t s_pos[2 * M];
+    __shared__ int32_t s_row[M];
+    __shared__ uint8_t s_hb[M];
+    __shared__ int s_vx[M], s_vy[M], s_vz[M];
+    __shared__ int16_t s_ww[M];
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;
 
     unsigned *s_bits = s_dyn;
-    uint8_t *s_sbin = (uint8_t *)(s_bits + C6_M * C6_WORDS);
-    unsigned *s_even = (unsigned *)(s_sbin + C6_M * C6_M);
+    uint8_t *s_sbin = (uint8_t *)(s_bits + M * (M / 32));
+    unsigned *s_even = (unsigned *)(s_sbin + M * M);
     int *s_odd = (int *)(s_even + a.ncfg);
     unsigned *s_w128 = s_even;
     if (SMEM_HIST && WEIGHTED)
@@ -253,7 +257,7 @@ k_count6_small(C6Args a)
             s_even[t] = 0;
             s_odd[t] = 0;
         }
-    for (int t = threadIdx.x; t < 2 * C6_M; t += C6_THREADS) s_key[t] = C6_EMPTY;
+    for (int t = threadIdx.x; t < 2 * M; t += C6_THREADS) s_key[t] = C6_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
     C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin, s_ww };
 
@@ -265,7 +269,7 @@ k_count6_small(C6Args a)
         if (i >= a.hub_end) break;
         const int64_t f0 = a.row_ptr[i] + a.fwd[i];
         const int f = (int)(a.row_ptr[i + 1] - f0);
-        if (f < 3 || f > C6_M) continue;
+        if (f < 3 || f <= a.f_lo || f > M) continue;
         if (SMEM_HIST && !WEIGHTED) {
             const unsigned long long bound = (unsigned long long)f * (f - 1) * (f - 2) / 6;
             if (s_pending + bound > 0x7fffffffull) {
@@ -477,22 +481,31 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
     const bool weighted = a.w != nullptr;
     const bool smem = weighted ? ncfg <= C6_SMEM_W_MAX : ncfg <= C6_SMEM_HIST_MAX;
     const size_t acc = weighted ? 32 * (size_t)ncfg : 8 * (size_t)ncfg;
-    const size_t dyn = sizeof(unsigned) * C6_M * C6_WORDS + (size_t)C6_M * C6_M + (smem ? acc : 0);
-    decltype(&k_count6_small<true, true, true>) kern;
-    if (windowed)
-        kern = weighted ? (smem ? k_count6_small<true, true, true> : k_count6_small<false, true, true>)
-                        : (smem ? k_count6_small<true, false, true> : k_count6_small<false, false, true>);
-    else
-        kern = weighted ? (smem ? k_count6_small<true, true, false> : k_count6_small<false, true, false>)
-                        : (smem ? k_count6_small<true, false, false> : k_count6_small<false, false, false>);
-    int per_sm = 0;
-    GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
-    GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C6_THREADS, dyn));
-    if (per_sm < 1) return gs_set_error(GS_ERR_CAPACITY, "4pCF workspace of %zu bytes does not fit in shared memory", dyn);
-    GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
-    kern<<<(int)std::min<int64_t>((int64_t)sms * per_sm, hubs), C6_THREADS, dyn, st>>>(a);
-    gs_note_launch();
-    GS_TRY_CUDA(cudaGetLastError());
+    // the two shared-memory kernels: hubs of forward degree 3..128, then 129..256
+    for (int pass = 0; pass < 2; ++pass) {
+        const int m = pass ? C6_M : C6_M_SMALL;
+        if (pass && g->max_forward <= C6_M_SMALL) break;
+        const size_t dyn = sizeof(unsigned) * m * (m / 32) + (size_t)m * m + (smem ? acc : 0);
+        using K = decltype(&k_count6_small<C6_M, true, true, true>);
+        auto pick = [&](auto mtag) -> K {
+            constexpr int MM = decltype(mtag)::value;
+            if (windowed)
+                return weighted ? (smem ? k_count6_small<MM, true, true, true> : k_count6_small<MM, false, true, true>)
+                                : (smem ? k_count6_small<MM, true, false, true> : k_count6_small<MM, false, false, true>);
+            return weighted ? (smem ? k_count6_small<MM, true, true, false> : k_count6_small<MM, false, true, false>)
+                            : (smem ? k_count6_small<MM, true, false, false> : k_count6_small<MM, false, false, false>);
+        };
+        const K kern = pass ? pick(std::integral_constant<int, C6_M>()) : pick(std::integral_constant<int, C6_M_SMALL>());
+        int per_sm = 0;
+        GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+        GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C6_THREADS, dyn));
+        if (per_sm < 1) return gs_set_error(GS_ERR_CAPACITY, "4pCF workspace of %zu bytes does not fit in shared memory", dyn);
+        GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
+        a.f_lo = pass ? C6_M_SMALL : 0;
+        kern<<<(int)std::min<int64_t>((int64_t)sms * per_sm, hubs), C6_THREADS, dyn, st>>>(a);
+        gs_note_launch();
+        GS_TRY_CUDA(cudaGetLastError());
+    }
 
     const int M = g->max_forward;              // bounds the large path's slices
     if (M > C6_M) {

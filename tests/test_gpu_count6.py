@@ -47,19 +47,24 @@ def test_fixture_shapes():
     assert e[k] == 1 and o[k] == 1
 
 
-def test_hub_with_more_forward_neighbours_than_shared_memory_holds():
-    # one hub (input index 0, all points in one cell) with 300 forward
-    # neighbours on a shell of radius 0.9 r_max: the global-scratch path
+@pytest.mark.parametrize("m", [100, 200, 300])
+def test_hubs_of_each_shared_memory_size(m):
+    # a hub (input index 0) at the corner of cell 0 with m neighbours on an
+    # octant shell of radius 0.45..0.9 r_max, all in cell 0, so all m are
+    # forward neighbours: the 128-slot kernel, the 256-slot kernel and the
+    # global-scratch path
     rng = np.random.default_rng(8)
     R = 20000
-    v = rng.normal(size=(300, 3))
-    v *= (0.9 * R * (0.5 + 0.5 * rng.uniform(size=(300, 1)))) / np.linalg.norm(v, axis=1, keepdims=True)
-    xyz = (np.vstack([[[0, 0, 0]], np.rint(v)]) + 25000).astype(np.int32)
+    v = np.abs(rng.normal(size=(m, 3)))
+    v *= (0.9 * R * (0.5 + 0.5 * rng.uniform(size=(m, 1)))) / np.linalg.norm(v, axis=1, keepdims=True)
+    xyz = (np.vstack([[[0, 0, 0]], np.rint(v)]) + 100).astype(np.int32)
     edges = [0, 8000, 12000, 16000, R]
-    ref_e, ref_o = oracle.count_4pcf6(xyz, 50000, 0, edges)
+    ref_e, ref_o = oracle.count_4pcf6(xyz, 80000, 0, edges)
     assert ref_e.sum() > 1000
-    e, o = _gpu6(xyz, 50000, 0, edges)
-    assert np.array_equal(e, ref_e) and np.array_equal(o, ref_o)
+    with gpu_graph(xyz, 80000, 0, edges) as g:
+        assert g.stats()["max_forward"] == m
+        e, o = g.count_4pcf6()
+        assert np.array_equal(as_uint64(e), ref_e) and np.array_equal(o.cpu().numpy(), ref_o)
 
 
 def test_parity_catalogue_four_bins_full_size():
