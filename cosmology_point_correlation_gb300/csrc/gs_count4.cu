@@ -164,43 +164,72 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
     }
     __syncthreads();
 
-    // 3. cliques (s1 < s2 < s3), distinct hub bins: a warp per s1, lanes over s2
+    // 3. cliques (s1 < s2 < s3), distinct hub bins. A warp takes s1 and 32
+    // candidates s2 at a time (one per lane); for each word of the bit rows
+    // the lanes' common bits (s3 > s2) are counted, prefix-summed across the
+    // warp, and handed out 32 at a time, so that all lanes work on cliques
+    // however unevenly they are spread over the pairs (s1, s2).
+    auto clique = [&](int s1, int b1, int s2, int b2, int s3) {
+        const int b3 = w.hb[s3];
+        if (b3 == b1 || b3 == b2) return;
+        // order the three spokes by hub bin
+        int sa = s1, sb = s2, sc = s3, ba = b1, bb = b2, bc = b3, tt;
+        if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
+        if (bb > bc) { tt = bb; bb = bc; bc = tt; tt = sb; sb = sc; sc = tt; }
+        if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
+        const long long ax = w.vx[sa], ay = w.vy[sa], az = w.vz[sa];
+        const long long bx = w.vx[sb], by = w.vy[sb], bz = w.vz[sb];
+        const long long cx = w.vx[sc], cy = w.vy[sc], cz = w.vz[sc];
+        const long long v = (ay * bz - az * by) * cx + (az * bx - ax * bz) * cy + (ax * by - ay * bx) * cz;
+        const int sg = (v > 0) - (v < 0);
+        const int idx = lex_a[ba] + lex_b[bb] + bc;
+        if (SMEM_HIST) {
+            atomicAdd(&s_even[idx], 1u);
+            if (sg) atomicAdd(&s_odd[idx], sg);
+        } else {
+            atomicAdd(a.even + idx, 1ull);
+            if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
+        }
+    };
     const int s1_end = min(pa1, m - 2), s2_end = min(q2_hi, m - 1);
     for (int s1 = pa0 + warp; s1 < s1_end; s1 += C4_WARPS) {
         const int b1 = w.hb[s1];
         const unsigned *row1 = w.bits + (size_t)s1 * W;
-        for (int s2 = max(s1 + 1, q2_lo) + lane; s2 < s2_end; s2 += 32) {
-            if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
-            const int b2 = w.hb[s2];
-            if (b1 == b2) continue;
-            const unsigned *row2 = w.bits + (size_t)s2 * W;
-            for (int wd = s2 >> 5; wd < W; ++wd) {
-                unsigned common = row1[wd] & row2[wd];
-                if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);     // keep s3 > s2
-                while (common) {
-                    const int s3 = (wd << 5) + __ffs(common) - 1;
-                    common &= common - 1;
-                    const int b3 = w.hb[s3];
-                    if (b3 == b1 || b3 == b2) continue;
-                    // order the three spokes by hub bin
-                    int sa = s1, sb = s2, sc = s3, ba = b1, bb = b2, bc = b3, tt;
-                    if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
-                    if (bb > bc) { tt = bb; bb = bc; bc = tt; tt = sb; sb = sc; sc = tt; }
-                    if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
-                    const long long ax = w.vx[sa], ay = w.vy[sa], az = w.vz[sa];
-                    const long long bx = w.vx[sb], by = w.vy[sb], bz = w.vz[sb];
-                    const long long cx = w.vx[sc], cy = w.vy[sc], cz = w.vz[sc];
-                    const long long v = (ay * bz - az * by) * cx + (az * bx - ax * bz) * cy +
-                                        (ax * by - ay * bx) * cz;
-                    const int sg = (v > 0) - (v < 0);
-                    const int idx = lex_a[ba] + lex_b[bb] + bc;
-                    if (SMEM_HIST) {
-                        atomicAdd(&s_even[idx], 1u);
-                        if (sg) atomicAdd(&s_odd[idx], sg);
-                    } else {
-                        atomicAdd(a.even + idx, 1ull);
-                        if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
-                    }
+        for (int c2 = max(s1 + 1, q2_lo); c2 < s2_end; c2 += 32) {        // warp-uniform
+            const int s2 = c2 + lane;
+            bool valid = s2 < s2_end && ((row1[s2 >> 5] >> (s2 & 31)) & 1u);
+            int b2 = 0;
+            if (valid) {
+                b2 = w.hb[s2];
+                valid = b2 != b1;
+            }
+            if (!__any_sync(0xffffffffu, valid)) continue;
+            const unsigned *row2 = w.bits + (size_t)(valid ? s2 : s1) * W;
+            for (int wd = c2 >> 5; wd < W; ++wd) {
+                unsigned common = 0u;
+                if (valid && wd >= (s2 >> 5)) {
+                    common = row1[wd] & row2[wd];
+                    if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // keep s3 > s2
+                }
+                const int cnt = __popc(common);
+                int inc = cnt;                                     // inclusive prefix over lanes
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const int total = __shfl_sync(0xffffffffu, inc, 31);
+                for (int k = 0; k < total; k += 32) {
+                    const int q = k + lane;
+                    int owner = 0;                                 // first lane whose prefix exceeds q
+#pragma unroll
+                    for (int step = 16; step > 0; step >>= 1)
+                        if (__shfl_sync(0xffffffffu, inc, owner + step - 1) <= q) owner += step;
+                    const unsigned cm = __shfl_sync(0xffffffffu, common, owner);
+                    const int first = __shfl_sync(0xffffffffu, inc - cnt, owner);
+                    const int o_s2 = __shfl_sync(0xffffffffu, s2, owner);
+                    const int o_b2 = __shfl_sync(0xffffffffu, b2, owner);
+                    if (q < total) clique(s1, b1, o_s2, o_b2, (wd << 5) + (int)__fns(cm, 0, q - first + 1));
                 }
             }
         }
@@ -237,7 +266,7 @@ __device__ __forceinline__ void c4_flush(unsigned *se, int *so, int ncfg, unsign
 // Hubs of degree 3..C4_M, workspace in shared memory; histograms in shared
 // memory too unless there are too many configurations.
 template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
-__global__ void __launch_bounds__(C4_THREADS)
+__global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_small(C4Args a)
 {
     extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], even [ncfg], odd [ncfg]
