@@ -167,47 +167,105 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
 
     const long long wi = WEIGHTED ? (long long)a.w[i] : 0;
     const int s1_end = min(pa1, f - 2), s2_end = min(q2_hi, f - 1);
+    // A warp per s1, its lanes over the spokes s2. Unweighted, each lane walks
+    // the common bits of its own pairs (s1, s2). Weighted, where a tetrahedron
+    // costs several atomics, the warp takes 32 candidates s2 at a time and, for
+    // each word of the bit rows, prefix-sums the lanes' common-bit counts and
+    // hands the tetrahedra out 32 at a time, so that all lanes stay busy however
+    // unevenly the tetrahedra are spread over the pairs.
+    struct Pair {
+        int s2, b02, b12;
+        long long cx, cy, cz, w12;
+    };
     for (int s1 = pa0 + warp; s1 < s1_end; s1 += C6_WARPS) {
         const unsigned *row1 = w.bits + (size_t)s1 * W;
         const int b01 = w.hb[s1];
         const long long x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
-        for (int s2 = max(s1 + 1, q2_lo) + lane; s2 < s2_end; s2 += 32) {
-            if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
-            const unsigned *row2 = w.bits + (size_t)s2 * W;
-            const int b02 = w.hb[s2], b12 = w.sbin[(size_t)s1 * f + s2];
+        const long long w1 = WEIGHTED ? wi * w.ww[s1] : 0;
+        auto make_pair = [&](int s2) {
+            Pair p;
+            p.s2 = s2;
+            p.b02 = w.hb[s2];
+            p.b12 = w.sbin[(size_t)s1 * f + s2];
             const long long x2 = w.vx[s2], y2 = w.vy[s2], z2 = w.vz[s2];
-            const long long cx = y1 * z2 - z1 * y2, cy = z1 * x2 - x1 * z2, cz = x1 * y2 - y1 * x2;
-            const long long w12 = WEIGHTED ? wi * w.ww[s1] * w.ww[s2] : 0;     // |.| <= 2^45
-            const int base = ((b01 * nb + b02) * nb) * nb * nb * nb;          // b03, b12, b13, b23 follow
-            for (int wd = s2 >> 5; wd < W; ++wd) {
-                unsigned common = row1[wd] & row2[wd];
-                if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
-                while (common) {
-                    const int s3 = (wd << 5) + __ffs(common) - 1;
-                    common &= common - 1;
-                    const int b03 = w.hb[s3];
-                    const int b13 = w.sbin[(size_t)s1 * f + s3], b23 = w.sbin[(size_t)s2 * f + s3];
-                    const int pk = base + ((b03 * nb + b12) * nb + b13) * nb + b23;
-                    const int v = __ldg(a.cfg6 + pk);
-                    const int ci = v >> 2, par = (v & 3) - 1;
-                    const long long d = cx * w.vx[s3] + cy * w.vy[s3] + cz * w.vz[s3];
-                    const int sg = par * ((d > 0) - (d < 0));
-                    if (WEIGHTED) {
-                        const long long W = w12 * w.ww[s3];
-                        if (SMEM_HIST) {
-                            gs_add128_u32(s_w128 + 8 * ci, W);
-                            if (sg) gs_add128_u32(s_w128 + 8 * ci + 4, sg * W);
-                        } else {
-                            gs_add128(a.weven + 2 * ci, W);
-                            if (sg) gs_add128(a.wodd + 2 * ci, sg * W);
-                        }
-                    } else if (SMEM_HIST) {
-                        atomicAdd(&s_even[ci], 1u);
-                        if (sg) atomicAdd(&s_odd[ci], sg);
-                    } else {
-                        atomicAdd(a.even + ci, 1ull);
-                        if (sg) atomicAdd((unsigned long long *)(a.odd + ci), (unsigned long long)(long long)sg);
+            p.cx = y1 * z2 - z1 * y2;
+            p.cy = z1 * x2 - x1 * z2;
+            p.cz = x1 * y2 - y1 * x2;
+            p.w12 = WEIGHTED ? w1 * w.ww[s2] : 0;                          // |.| <= 2^45
+            return p;
+        };
+        // one tetrahedron (i, s1, s2, s3)
+        auto tetra = [&](const Pair &p, int s3) {
+            const int b03 = w.hb[s3];
+            const int b13 = w.sbin[(size_t)s1 * f + s3], b23 = w.sbin[(size_t)p.s2 * f + s3];
+            const int pk = ((((b01 * nb + p.b02) * nb + b03) * nb + p.b12) * nb + b13) * nb + b23;
+            const int v = __ldg(a.cfg6 + pk);
+            const int ci = v >> 2, par = (v & 3) - 1;
+            const long long d = p.cx * w.vx[s3] + p.cy * w.vy[s3] + p.cz * w.vz[s3];
+            const int sg = par * ((d > 0) - (d < 0));
+            if (WEIGHTED) {
+                const long long W4 = p.w12 * w.ww[s3];                    // |.| <= 2^60
+                if (SMEM_HIST) {
+                    gs_add128_u32(s_w128 + 8 * ci, W4);
+                    if (sg) gs_add128_u32(s_w128 + 8 * ci + 4, sg * W4);
+                } else {
+                    gs_add128(a.weven + 2 * ci, W4);
+                    if (sg) gs_add128(a.wodd + 2 * ci, sg * W4);
+                }
+            } else if (SMEM_HIST) {
+                atomicAdd(&s_even[ci], 1u);
+                if (sg) atomicAdd(&s_odd[ci], sg);
+            } else {
+                atomicAdd(a.even + ci, 1ull);
+                if (sg) atomicAdd((unsigned long long *)(a.odd + ci), (unsigned long long)(long long)sg);
+            }
+        };
+        if (!WEIGHTED) {
+            for (int s2 = max(s1 + 1, q2_lo) + lane; s2 < s2_end; s2 += 32) {
+                if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
+                const unsigned *row2 = w.bits + (size_t)s2 * W;
+                const Pair p = make_pair(s2);
+                for (int wd = s2 >> 5; wd < W; ++wd) {
+                    unsigned common = row1[wd] & row2[wd];
+                    if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
+                    while (common) {
+                        const int s3 = (wd << 5) + __ffs(common) - 1;
+                        common &= common - 1;
+                        tetra(p, s3);
                     }
+                }
+            }
+            continue;
+        }
+        for (int c2 = max(s1 + 1, q2_lo); c2 < s2_end; c2 += 32) {        // warp-uniform
+            const int s2 = c2 + lane;
+            const bool valid = s2 < s2_end && ((row1[s2 >> 5] >> (s2 & 31)) & 1u);
+            if (!__any_sync(0xffffffffu, valid)) continue;
+            const unsigned *row2 = w.bits + (size_t)(valid ? s2 : s1) * W;
+            for (int wd = c2 >> 5; wd < W; ++wd) {
+                unsigned common = 0u;
+                if (valid && wd >= (s2 >> 5)) {
+                    common = row1[wd] & row2[wd];
+                    if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
+                }
+                const int cnt = __popc(common);
+                int inc = cnt;                                     // inclusive prefix over lanes
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const int total = __shfl_sync(0xffffffffu, inc, 31);
+                for (int k = 0; k < total; k += 32) {
+                    const int q = k + lane;
+                    int owner = 0;                                 // first lane whose prefix exceeds q
+#pragma unroll
+                    for (int step = 16; step > 0; step >>= 1)
+                        if (__shfl_sync(0xffffffffu, inc, owner + step - 1) <= q) owner += step;
+                    const unsigned cm = __shfl_sync(0xffffffffu, common, owner);
+                    const int first = __shfl_sync(0xffffffffu, inc - cnt, owner);
+                    const int o_s2 = __shfl_sync(0xffffffffu, s2, owner);
+                    if (q < total) tetra(make_pair(o_s2), (wd << 5) + (int)__fns(cm, 0, q - first + 1));
                 }
             }
         }
