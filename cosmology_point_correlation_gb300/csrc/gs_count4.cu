@@ -90,6 +90,7 @@ struct HubSpace {
     uint8_t *hb;       // [m] hub bins
     int *vx, *vy, *vz; // [m] spoke vectors
     unsigned *bits;    // [m][W] adjacency bits
+    int *next;         // shared counter handing out the rows s1 of the clique search
 };
 
 template <bool SMEM_HIST, bool WINDOWED>
@@ -137,6 +138,7 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
     __syncthreads();
 
     // 2. adjacency among the spokes: bit (s, t) for t > s
+    if (threadIdx.x == 0) *w.next = pa0;                       // read after the barrier below
     const int32_t kmax = w.row[m - 1];
     const int na = pa1 - pa0, nab = na + (pb1 - pb0);
     for (int u = warp; u < nab; u += C4_WARPS) {
@@ -164,44 +166,52 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
     }
     __syncthreads();
 
-    // 3. cliques (s1 < s2 < s3), distinct hub bins. A warp takes s1 and 32
-    // candidates s2 at a time (one per lane); for each word of the bit rows
-    // the lanes' common bits (s3 > s2) are counted, prefix-summed across the
-    // warp, and handed out 32 at a time, so that all lanes work on cliques
-    // however unevenly they are spread over the pairs (s1, s2).
-    auto clique = [&](int s1, int b1, int s2, int b2, int s3) {
-        const int b3 = w.hb[s3];
-        if (b3 == b1 || b3 == b2) return;
-        // order the three spokes by hub bin
-        int sa = s1, sb = s2, sc = s3, ba = b1, bb = b2, bc = b3, tt;
-        if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
-        if (bb > bc) { tt = bb; bb = bc; bc = tt; tt = sb; sb = sc; sc = tt; }
-        if (ba > bb) { tt = ba; ba = bb; bb = tt; tt = sa; sa = sb; sb = tt; }
-        const long long ax = w.vx[sa], ay = w.vy[sa], az = w.vz[sa];
-        const long long bx = w.vx[sb], by = w.vy[sb], bz = w.vz[sb];
-        const long long cx = w.vx[sc], cy = w.vy[sc], cz = w.vz[sc];
-        const long long v = (ay * bz - az * by) * cx + (az * bx - ax * bz) * cy + (ax * by - ay * bx) * cz;
-        const int sg = (v > 0) - (v < 0);
-        const int idx = lex_a[ba] + lex_b[bb] + bc;
-        if (SMEM_HIST) {
-            atomicAdd(&s_even[idx], 1u);
-            if (sg) atomicAdd(&s_odd[idx], sg);
-        } else {
-            atomicAdd(a.even + idx, 1ull);
-            if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
-        }
-    };
+    // 3. cliques (s1 < s2 < s3), distinct hub bins. Warps take rows s1 from a
+    // shared counter (low rows, with the most candidates, first) and 32
+    // candidates s2 at a time (one per lane). For each word of the bit rows the
+    // lanes' common bits (s3 > s2) are counted, prefix-summed across the warp
+    // and handed out 32 at a time, so that all lanes work on cliques however
+    // unevenly they are spread over the pairs (s1, s2). The volume is taken in
+    // position order, D = (r_s1 x r_s2) . r_s3 with the cross product once per
+    // pair, and V of the bin-ordered spokes is D times the sign of the
+    // permutation that sorts (b1, b2, b3).
     const int s1_end = min(pa1, m - 2), s2_end = min(q2_hi, m - 1);
-    for (int s1 = pa0 + warp; s1 < s1_end; s1 += C4_WARPS) {
+    for (;;) {
+        int s1 = 0;
+        if (lane == 0) s1 = atomicAdd(w.next, 1);
+        s1 = __shfl_sync(0xffffffffu, s1, 0);
+        if (s1 >= s1_end) break;
         const int b1 = w.hb[s1];
+        const int x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
         const unsigned *row1 = w.bits + (size_t)s1 * W;
+        auto clique = [&](int b2, long long cx, long long cy, long long cz, int s3) {
+            const int b3 = w.hb[s3];
+            if (b3 == b1 || b3 == b2) return;
+            const long long d = cx * w.vx[s3] + cy * w.vy[s3] + cz * w.vz[s3];   // |d| < 3 * 2^60
+            int sg = (d > 0) - (d < 0);
+            if (((b1 > b2) + (b1 > b3) + (b2 > b3)) & 1) sg = -sg;
+            const int lo = min(b1, min(b2, b3)), hi = max(b1, max(b2, b3));
+            const int idx = lex_a[lo] + lex_b[b1 + b2 + b3 - lo - hi] + hi;
+            if (SMEM_HIST) {
+                atomicAdd(&s_even[idx], 1u);
+                if (sg) atomicAdd(&s_odd[idx], sg);
+            } else {
+                atomicAdd(a.even + idx, 1ull);
+                if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
+            }
+        };
         for (int c2 = max(s1 + 1, q2_lo); c2 < s2_end; c2 += 32) {        // warp-uniform
             const int s2 = c2 + lane;
             bool valid = s2 < s2_end && ((row1[s2 >> 5] >> (s2 & 31)) & 1u);
             int b2 = 0;
+            long long cx = 0, cy = 0, cz = 0;
             if (valid) {
                 b2 = w.hb[s2];
                 valid = b2 != b1;
+                const int x2 = w.vx[s2], y2 = w.vy[s2], z2 = w.vz[s2];      // r_s1 x r_s2, |.| < 2^41
+                cx = (long long)y1 * z2 - (long long)z1 * y2;
+                cy = (long long)z1 * x2 - (long long)x1 * z2;
+                cz = (long long)x1 * y2 - (long long)y1 * x2;
             }
             if (!__any_sync(0xffffffffu, valid)) continue;
             const unsigned *row2 = w.bits + (size_t)(valid ? s2 : s1) * W;
@@ -227,9 +237,11 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
                         if (__shfl_sync(0xffffffffu, inc, owner + step - 1) <= q) owner += step;
                     const unsigned cm = __shfl_sync(0xffffffffu, common, owner);
                     const int first = __shfl_sync(0xffffffffu, inc - cnt, owner);
-                    const int o_s2 = __shfl_sync(0xffffffffu, s2, owner);
                     const int o_b2 = __shfl_sync(0xffffffffu, b2, owner);
-                    if (q < total) clique(s1, b1, o_s2, o_b2, (wd << 5) + (int)__fns(cm, 0, q - first + 1));
+                    const long long ocx = __shfl_sync(0xffffffffu, cx, owner);
+                    const long long ocy = __shfl_sync(0xffffffffu, cy, owner);
+                    const long long ocz = __shfl_sync(0xffffffffu, cz, owner);
+                    if (q < total) clique(o_b2, ocx, ocy, ocz, (wd << 5) + (int)__fns(cm, 0, q - first + 1));
                 }
             }
         }
@@ -278,6 +290,7 @@ k_count4_small(C4Args a)
     __shared__ int s_lex_a[256], s_lex_b[256];
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;
+    __shared__ int s_next;
 
     unsigned *s_bits = s_dyn;
     unsigned *s_even = s_dyn + C4_M * C4_WORDS;
@@ -290,7 +303,7 @@ k_count4_small(C4Args a)
         }
     for (int t = threadIdx.x; t < C4_TABLE; t += C4_THREADS) s_key[t] = C4_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
-    HubSpace w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits };
+    HubSpace w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, &s_next };
 
     for (;;) {
         __syncthreads();
@@ -329,6 +342,7 @@ k_count4_large(C4Args a)
 {
     __shared__ int s_lex_a[256], s_lex_b[256];
     __shared__ long long s_hub;
+    __shared__ int s_next;
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
 
     const int M = a.big_m;
@@ -345,6 +359,7 @@ k_count4_large(C4Args a)
     w.vz = w.vy + M;
     w.bits = (unsigned *)(w.vz + M);
     w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
+    w.next = &s_next;
     for (int t = threadIdx.x; t < (1 << tlog); t += C4_THREADS) w.key[t] = C4_EMPTY;
 
     for (;;) {
