@@ -92,6 +92,7 @@ struct C6Space {
     unsigned *bits;    // [f][W]
     uint8_t *sbin;     // [f][f] spoke-spoke bins (valid where the bit is set)
     int16_t *ww;       // [f] spoke weights (weighted counts)
+    int *next;         // shared counter handing out the rows s1 of the tetrahedron search
 };
 
 template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
@@ -136,6 +137,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     for (int t = threadIdx.x; t < f * W; t += C6_THREADS) w.bits[t] = 0u;
     __syncthreads();
 
+    if (threadIdx.x == 0) *w.next = pa0;                       // read after the barrier below
     const int32_t kmax = w.row[f - 1];
     const int na = pa1 - pa0, nab = na + (pb1 - pb0);
     for (int u = warp; u < nab; u += C6_WARPS) {
@@ -177,7 +179,15 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
         int s2, b02, b12;
         long long cx, cy, cz, w12;
     };
-    for (int s1 = pa0 + warp; s1 < s1_end; s1 += C6_WARPS) {
+    // rows s1: weighted, from the shared counter (low rows, with the most
+    // candidates, first); unweighted, where rows are cheap, strided by warp
+    auto next_row = [&](int prev) {
+        if (!WEIGHTED) return prev < 0 ? pa0 + warp : prev + C6_WARPS;
+        int r = 0;
+        if (lane == 0) r = atomicAdd(w.next, 1);
+        return __shfl_sync(0xffffffffu, r, 0);
+    };
+    for (int s1 = next_row(-1); s1 < s1_end; s1 = next_row(s1)) {
         const unsigned *row1 = w.bits + (size_t)s1 * W;
         const int b01 = w.hb[s1];
         const long long x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
@@ -301,6 +311,7 @@ k_count6_small(C6Args a)
     __shared__ int s_vx[M], s_vy[M], s_vz[M];
     __shared__ int16_t s_ww[M];
     __shared__ long long s_hub;
+    __shared__ int s_next;
     __shared__ unsigned long long s_pending;
 
     unsigned *s_bits = s_dyn;
@@ -317,7 +328,7 @@ k_count6_small(C6Args a)
         }
     for (int t = threadIdx.x; t < 2 * M; t += C6_THREADS) s_key[t] = C6_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
-    C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin, s_ww };
+    C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin, s_ww, &s_next };
 
     for (;;) {
         __syncthreads();
@@ -359,10 +370,11 @@ k_count6_small(C6Args a)
 
 // Hubs with more than C6_M forward neighbours: workspace in a global slice.
 template <bool WEIGHTED, bool WINDOWED>
-__global__ void __launch_bounds__(C6_THREADS)
+__global__ void __launch_bounds__(C6_THREADS, 2)
 k_count6_large(C6Args a)
 {
     __shared__ long long s_hub;
+    __shared__ int s_next;
     const int M = a.big_m;
     int tlog = 4;
     while ((1 << tlog) < 2 * M) ++tlog;
@@ -379,6 +391,7 @@ k_count6_large(C6Args a)
     w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
     w.sbin = w.hb + M;
     w.ww = (int16_t *)(w.sbin + (size_t)M * M);          // M + M*M is even: 2-byte aligned
+    w.next = &s_next;
     for (int t = threadIdx.x; t < (1 << tlog); t += C6_THREADS) w.key[t] = C6_EMPTY;
 
     for (;;) {
