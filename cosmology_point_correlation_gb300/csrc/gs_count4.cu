@@ -334,16 +334,28 @@ k_count4_small(C4Args a)
     }
 }
 
-// Hubs of degree > C4_M: workspace in a global scratch slice per block,
-// histograms added straight to global memory.
-template <bool HUB_LIST, bool WINDOWED>
+// Hubs of degree > C4_M: workspace in a global scratch slice per block;
+// histograms in shared memory (SMEM_HIST) as in the small kernel, except for
+// a hub whose clique bound could overflow the 32-bit counters, which adds
+// straight to global memory.
+template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
 __global__ void __launch_bounds__(C4_THREADS)
 k_count4_large(C4Args a)
 {
+    extern __shared__ unsigned s_dyn[];             // (SMEM_HIST) even, odd [ncfg]
     __shared__ int s_lex_a[256], s_lex_b[256];
     __shared__ long long s_hub;
     __shared__ int s_next;
+    __shared__ unsigned long long s_pending;
+    unsigned *s_even = s_dyn;
+    int *s_odd = (int *)(s_even + a.ncfg);
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
+    if (SMEM_HIST)
+        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) {
+            s_even[t] = 0;
+            s_odd[t] = 0;
+        }
+    if (threadIdx.x == 0) s_pending = 0;
 
     const int M = a.big_m;
     int tlog = 4;
@@ -372,7 +384,23 @@ k_count4_large(C4Args a)
         if (m <= C4_M) continue;
         int tl = 4;
         while ((1 << tl) < 2 * m) ++tl;
-        c4_hub<false, WINDOWED>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
+        const unsigned long long bound = (unsigned long long)m * (m - 1) * (m - 2) / 6;
+        if (!SMEM_HIST || bound > 0x7fffffffull) {
+            c4_hub<false, WINDOWED>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
+            continue;
+        }
+        if (s_pending + bound > 0x7fffffffull) {
+            c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+            __syncthreads();
+            if (threadIdx.x == 0) s_pending = 0;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_pending += bound;
+        c4_hub<SMEM_HIST, WINDOWED>(a, w, i, m, tl, s_even, s_odd, s_lex_a, s_lex_b);
+    }
+    if (SMEM_HIST) {
+        __syncthreads();
+        c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -410,8 +438,11 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        if (windowed) k_count4_large<false, true><<<gl, C4_THREADS, 0, st>>>(a);
-        else k_count4_large<false, false><<<gl, C4_THREADS, 0, st>>>(a);
+        const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)a.ncfg : 0;
+        auto big = windowed ? (smem ? k_count4_large<true, false, true> : k_count4_large<false, false, true>)
+                            : (smem ? k_count4_large<true, false, false> : k_count4_large<false, false, false>);
+        GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
+        big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
@@ -553,7 +584,10 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        k_count4_large<true, false><<<gl, C4_THREADS, 0, st>>>(a);
+        const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
+        auto big = smem ? k_count4_large<true, true, false> : k_count4_large<false, true, false>;
+        GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
+        big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
@@ -677,7 +711,10 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
         a.big_m = M;
         a.scratch = base + GS_C4_STATIC_HEAD;
         a.scratch_stride = stride;
-        k_count4_large<false, false><<<gl, C4_THREADS, 0, st>>>(a);
+        const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
+        auto big = smem ? k_count4_large<true, false, false> : k_count4_large<false, false, false>;
+        GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
+        big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
         GS_TRY_CUDA(cudaGetLastError());
     }

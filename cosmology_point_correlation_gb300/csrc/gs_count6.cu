@@ -36,7 +36,7 @@
 #include "gs_internal.cuh"
 
 constexpr int C6_THREADS = 256;
-constexpr int C6_WARPS = C6_THREADS / 32;
+constexpr int C6_LARGE_THREADS = 1024;       // hubs above C6_M: few and large, a wide block each
 constexpr int C6_M = 256;                   // forward degree kept in shared memory
 constexpr int C6_M_SMALL = 128;             // hubs up to this degree run in a lighter kernel (more blocks per SM)
 constexpr int C6_SMEM_HIST_MAX = 4096;
@@ -95,7 +95,7 @@ struct C6Space {
     int *next;         // shared counter handing out the rows s1 of the tetrahedron search
 };
 
-template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
+template <int NT, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
 __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long long i, int64_t f0, int f,
                                        int tlog, unsigned *s_even, int *s_odd, unsigned *s_w128)
 {
@@ -121,7 +121,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     const int4 P = a.pts[i];
     const int nb = a.nb;
 
-    for (int t = threadIdx.x; t < f; t += C6_THREADS) {
+    for (int t = threadIdx.x; t < f; t += NT) {
         const int32_t k = F[t];
         w.row[t] = k;
         w.hb[t] = FB[t];
@@ -134,13 +134,13 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
         while (atomicCAS(&w.key[h], C6_EMPTY, k) != C6_EMPTY) h = (h + 1) & mask;
         w.pos[h] = t;
     }
-    for (int t = threadIdx.x; t < f * W; t += C6_THREADS) w.bits[t] = 0u;
+    for (int t = threadIdx.x; t < f * W; t += NT) w.bits[t] = 0u;
     __syncthreads();
 
     if (threadIdx.x == 0) *w.next = pa0;                       // read after the barrier below
     const int32_t kmax = w.row[f - 1];
     const int na = pa1 - pa0, nab = na + (pb1 - pb0);
-    for (int u = warp; u < nab; u += C6_WARPS) {
+    for (int u = warp; u < nab; u += (NT / 32)) {
         const bool in_a = u < na;
         const int s = in_a ? pa0 + u : pb0 + (u - na);
         if (s >= f - 1) continue;                              // no position above the last
@@ -182,7 +182,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     // rows s1: weighted, from the shared counter (low rows, with the most
     // candidates, first); unweighted, where rows are cheap, strided by warp
     auto next_row = [&](int prev) {
-        if (!WEIGHTED) return prev < 0 ? pa0 + warp : prev + C6_WARPS;
+        if (!WEIGHTED) return prev < 0 ? pa0 + warp : prev + (NT / 32);
         int r = 0;
         if (lane == 0) r = atomicAdd(w.next, 1);
         return __shfl_sync(0xffffffffu, r, 0);
@@ -281,7 +281,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
         }
     }
     __syncthreads();
-    for (int t = threadIdx.x; t < tsize; t += C6_THREADS) w.key[t] = C6_EMPTY;
+    for (int t = threadIdx.x; t < tsize; t += NT) w.key[t] = C6_EMPTY;
 }
 
 __device__ __forceinline__ void c6_flush(unsigned *se, int *so, int ncfg, unsigned long long *ge, long long *go)
@@ -351,7 +351,7 @@ k_count6_small(C6Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * f) ++tlog;
-        c6_hub<SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tlog, s_even, s_odd, s_w128);
+        c6_hub<C6_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tlog, s_even, s_odd, s_w128);
     }
     if (SMEM_HIST && WEIGHTED) {
         __syncthreads();
@@ -368,13 +368,30 @@ k_count6_small(C6Args a)
     }
 }
 
-// Hubs with more than C6_M forward neighbours: workspace in a global slice.
-template <bool WEIGHTED, bool WINDOWED>
-__global__ void __launch_bounds__(C6_THREADS, 2)
+// Hubs with more than C6_M forward neighbours: workspace in a global slice,
+// one wide block per hub; the histograms stay in shared memory as in the
+// small kernels (global atomics on a few hundred configurations would
+// serialise in L2).
+template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
+__global__ void __launch_bounds__(C6_LARGE_THREADS, 1)
 k_count6_large(C6Args a)
 {
+    // dynamic (SMEM_HIST): even, odd [ncfg] each, or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
+    extern __shared__ unsigned s_dyn[];
     __shared__ long long s_hub;
     __shared__ int s_next;
+    __shared__ unsigned long long s_pending;
+    unsigned *s_even = s_dyn;
+    int *s_odd = (int *)(s_even + a.ncfg);
+    unsigned *s_w128 = s_dyn;
+    if (SMEM_HIST && WEIGHTED)
+        for (int t = threadIdx.x; t < 8 * a.ncfg; t += C6_LARGE_THREADS) s_w128[t] = 0;
+    else if (SMEM_HIST)
+        for (int t = threadIdx.x; t < a.ncfg; t += C6_LARGE_THREADS) {
+            s_even[t] = 0;
+            s_odd[t] = 0;
+        }
+    if (threadIdx.x == 0) s_pending = 0;
     const int M = a.big_m;
     int tlog = 4;
     while ((1 << tlog) < 2 * M) ++tlog;
@@ -392,7 +409,7 @@ k_count6_large(C6Args a)
     w.sbin = w.hb + M;
     w.ww = (int16_t *)(w.sbin + (size_t)M * M);          // M + M*M is even: 2-byte aligned
     w.next = &s_next;
-    for (int t = threadIdx.x; t < (1 << tlog); t += C6_THREADS) w.key[t] = C6_EMPTY;
+    for (int t = threadIdx.x; t < (1 << tlog); t += C6_LARGE_THREADS) w.key[t] = C6_EMPTY;
 
     for (;;) {
         __syncthreads();
@@ -405,7 +422,43 @@ k_count6_large(C6Args a)
         if (f <= C6_M) continue;
         int tl = 4;
         while ((1 << tl) < 2 * f) ++tl;
-        c6_hub<false, WEIGHTED, WINDOWED>(a, w, i, f0, f, tl, nullptr, nullptr, nullptr);
+        const unsigned long long bound = (unsigned long long)f * (f - 1) * (f - 2) / 6;
+        if (SMEM_HIST && !WEIGHTED && bound > 0x7fffffffull) {
+            // one hub could overflow the 32-bit shared counters: global atomics
+            c6_hub<C6_LARGE_THREADS, false, false, WINDOWED>(a, w, i, f0, f, tl, nullptr, nullptr, nullptr);
+            continue;
+        }
+        if (SMEM_HIST && !WEIGHTED) {
+            if (s_pending + bound > 0x7fffffffull) {
+                for (int t = threadIdx.x; t < a.ncfg; t += C6_LARGE_THREADS) {
+                    if (s_even[t]) atomicAdd(a.even + t, (unsigned long long)s_even[t]);
+                    if (s_odd[t]) atomicAdd((unsigned long long *)(a.odd + t), (unsigned long long)(long long)s_odd[t]);
+                    s_even[t] = 0;
+                    s_odd[t] = 0;
+                }
+                __syncthreads();
+                if (threadIdx.x == 0) s_pending = 0;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) s_pending += bound;
+        }
+        c6_hub<C6_LARGE_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tl, s_even, s_odd, s_w128);
+    }
+    if (SMEM_HIST && WEIGHTED) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < 2 * a.ncfg; t += C6_LARGE_THREADS) {
+            const unsigned *q = s_w128 + 4 * t;
+            const unsigned long long lo = q[0] | ((unsigned long long)q[1] << 32);
+            const unsigned long long hi = q[2] | ((unsigned long long)q[3] << 32);
+            unsigned long long *dst = (t & 1) ? a.wodd + 2 * (t >> 1) : a.weven + 2 * (t >> 1);
+            if (lo | hi) gs_add128w(dst, lo, hi);
+        }
+    } else if (SMEM_HIST) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < a.ncfg; t += C6_LARGE_THREADS) {
+            if (s_even[t]) atomicAdd(a.even + t, (unsigned long long)s_even[t]);
+            if (s_odd[t]) atomicAdd((unsigned long long *)(a.odd + t), (unsigned long long)(long long)s_odd[t]);
+        }
     }
 }
 
@@ -590,9 +643,16 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
         a.big_m = M;
         a.scratch = scratch;
         a.scratch_stride = stride;
-        auto big = windowed ? (weighted ? k_count6_large<true, true> : k_count6_large<false, true>)
-                            : (weighted ? k_count6_large<true, false> : k_count6_large<false, false>);
-        big<<<gl, C6_THREADS, 0, st>>>(a);
+        const size_t bdyn = smem ? acc : 0;
+        decltype(&k_count6_large<true, true, true>) big;
+        if (windowed)
+            big = weighted ? (smem ? k_count6_large<true, true, true> : k_count6_large<false, true, true>)
+                           : (smem ? k_count6_large<true, false, true> : k_count6_large<false, false, true>);
+        else
+            big = weighted ? (smem ? k_count6_large<true, true, false> : k_count6_large<false, true, false>)
+                           : (smem ? k_count6_large<true, false, false> : k_count6_large<false, false, false>);
+        GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bdyn));
+        big<<<gl, C6_LARGE_THREADS, bdyn, st>>>(a);
         gs_note_launch();
         cudaError_t e = cudaGetLastError();
         cudaFreeAsync(scratch, st);
