@@ -88,8 +88,9 @@ struct HubSpace {
     int32_t *pos;      // row position of each table slot
     int32_t *row;      // [m] neighbour ids
     uint8_t *hb;       // [m] hub bins
-    int *vx, *vy, *vz; // [m] spoke vectors
+    int4 *v;           // [m] spoke vector x_s - x_i and hub bin (.w)
     unsigned *bits;    // [m][W] adjacency bits
+    unsigned *bm;      // [nb][W] positions of each hub bin, as bits (zero between hubs)
     int *next;         // shared counter handing out the rows s1 of the clique search
 };
 
@@ -125,11 +126,12 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
     for (int t = threadIdx.x; t < m; t += C4_THREADS) {
         const int32_t k = R[t];
         w.row[t] = k;
-        w.hb[t] = RB[t];
+        const int b = RB[t];
+        w.hb[t] = (uint8_t)b;
         const int4 Q = a.pts[k];
-        w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
-        w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
-        w.vz[t] = gs_delta(P.z, Q.z, a.box, a.periodic);
+        w.v[t] = make_int4(gs_delta(P.x, Q.x, a.box, a.periodic), gs_delta(P.y, Q.y, a.box, a.periodic),
+                           gs_delta(P.z, Q.z, a.box, a.periodic), b);
+        atomicOr(&w.bm[b * W + (t >> 5)], 1u << (t & 31));
         uint32_t h = gs_hash(k, shift);
         while (atomicCAS(&w.key[h], C4_EMPTY, k) != C4_EMPTY) h = (h + 1) & mask;
         w.pos[h] = t;
@@ -181,13 +183,15 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
         if (lane == 0) s1 = atomicAdd(w.next, 1);
         s1 = __shfl_sync(0xffffffffu, s1, 0);
         if (s1 >= s1_end) break;
-        const int b1 = w.hb[s1];
-        const int x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
+        const int4 r1 = w.v[s1];
+        const int b1 = r1.w, x1 = r1.x, y1 = r1.y, z1 = r1.z;
+        const unsigned *bm1 = w.bm + b1 * W;
         const unsigned *row1 = w.bits + (size_t)s1 * W;
+        // s3's hub bin differs from b1 and b2 (the common bits were masked)
         auto clique = [&](int b2, long long cx, long long cy, long long cz, int s3) {
-            const int b3 = w.hb[s3];
-            if (b3 == b1 || b3 == b2) return;
-            const long long d = cx * w.vx[s3] + cy * w.vy[s3] + cz * w.vz[s3];   // |d| < 3 * 2^60
+            const int4 r3 = w.v[s3];
+            const int b3 = r3.w;
+            const long long d = cx * r3.x + cy * r3.y + cz * r3.z;                // |d| < 3 * 2^60
             int sg = (d > 0) - (d < 0);
             if (((b1 > b2) + (b1 > b3) + (b2 > b3)) & 1) sg = -sg;
             const int lo = min(b1, min(b2, b3)), hi = max(b1, max(b2, b3));
@@ -206,19 +210,21 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
             int b2 = 0;
             long long cx = 0, cy = 0, cz = 0;
             if (valid) {
-                b2 = w.hb[s2];
+                const int4 r2 = w.v[s2];
+                b2 = r2.w;
                 valid = b2 != b1;
-                const int x2 = w.vx[s2], y2 = w.vy[s2], z2 = w.vz[s2];      // r_s1 x r_s2, |.| < 2^41
+                const int x2 = r2.x, y2 = r2.y, z2 = r2.z;                       // r_s1 x r_s2, |.| < 2^41
                 cx = (long long)y1 * z2 - (long long)z1 * y2;
                 cy = (long long)z1 * x2 - (long long)x1 * z2;
                 cz = (long long)x1 * y2 - (long long)y1 * x2;
             }
             if (!__any_sync(0xffffffffu, valid)) continue;
             const unsigned *row2 = w.bits + (size_t)(valid ? s2 : s1) * W;
+            const unsigned *bm2 = w.bm + b2 * W;
             for (int wd = c2 >> 5; wd < W; ++wd) {
                 unsigned common = 0u;
-                if (valid && wd >= (s2 >> 5)) {
-                    common = row1[wd] & row2[wd];
+                if (valid && wd >= (s2 >> 5)) {                // s3 adjacent to both, hub bin not b1 or b2
+                    common = row1[wd] & row2[wd] & ~(bm1[wd] | bm2[wd]);
                     if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // keep s3 > s2
                 }
                 const int cnt = __popc(common);
@@ -248,6 +254,7 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
     }
     __syncthreads();
     for (int t = threadIdx.x; t < tsize; t += C4_THREADS) w.key[t] = C4_EMPTY;
+    for (int t = threadIdx.x; t < a.nb * W; t += C4_THREADS) w.bm[t] = 0u;
 }
 
 // gs_idx4(a, b, c) = F4(a) - H(a + 1) + H(b) + c - b - 1 with
@@ -281,19 +288,20 @@ template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
 __global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_small(C4Args a)
 {
-    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], even [ncfg], odd [ncfg]
+    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], bin masks [nb * C4_WORDS], even, odd [ncfg]
     __shared__ int32_t s_key[C4_TABLE];
     __shared__ int32_t s_pos[C4_TABLE];
     __shared__ int32_t s_row[C4_M];
     __shared__ uint8_t s_hb[C4_M];
-    __shared__ int s_vx[C4_M], s_vy[C4_M], s_vz[C4_M];
+    __shared__ int4 s_v[C4_M];
     __shared__ int s_lex_a[256], s_lex_b[256];
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;
     __shared__ int s_next;
 
     unsigned *s_bits = s_dyn;
-    unsigned *s_even = s_dyn + C4_M * C4_WORDS;
+    unsigned *s_bm = s_dyn + C4_M * C4_WORDS;                 // [nb][C4_WORDS]
+    unsigned *s_even = s_bm + a.nb * C4_WORDS;
     int *s_odd = (int *)(s_even + a.ncfg);
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
     if (SMEM_HIST)
@@ -303,7 +311,8 @@ k_count4_small(C4Args a)
         }
     for (int t = threadIdx.x; t < C4_TABLE; t += C4_THREADS) s_key[t] = C4_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
-    HubSpace w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, &s_next };
+    HubSpace w{ s_key, s_pos, s_row, s_hb, s_v, s_bits, s_bm, &s_next };
+    for (int t = threadIdx.x; t < a.nb * C4_WORDS; t += C4_THREADS) s_bm[t] = 0u;
 
     for (;;) {
         __syncthreads();
@@ -339,7 +348,7 @@ k_count4_small(C4Args a)
 // a hub whose clique bound could overflow the 32-bit counters, which adds
 // straight to global memory.
 template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
-__global__ void __launch_bounds__(C4_THREADS)
+__global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_large(C4Args a)
 {
     extern __shared__ unsigned s_dyn[];             // (SMEM_HIST) even, odd [ncfg]
@@ -363,14 +372,14 @@ k_count4_large(C4Args a)
     const int WM = (M + 31) >> 5;
     char *base = a.scratch + (size_t)blockIdx.x * a.scratch_stride;
     HubSpace w;
-    w.key = (int32_t *)base;
+    w.v = (int4 *)base;                                   // slices start 256-byte aligned
+    w.key = (int32_t *)(w.v + M);
     w.pos = w.key + (1 << tlog);
     w.row = w.pos + (1 << tlog);
-    w.vx = w.row + M;
-    w.vy = w.vx + M;
-    w.vz = w.vy + M;
-    w.bits = (unsigned *)(w.vz + M);
-    w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
+    w.bits = (unsigned *)(w.row + M);
+    w.bm = w.bits + (size_t)M * WM;
+    w.hb = (uint8_t *)(w.bm + (size_t)a.nb * WM);
+    for (int t = threadIdx.x; t < a.nb * WM; t += C4_THREADS) w.bm[t] = 0u;
     w.next = &s_next;
     for (int t = threadIdx.x; t < (1 << tlog); t += C4_THREADS) w.key[t] = C4_EMPTY;
 
@@ -404,13 +413,26 @@ k_count4_large(C4Args a)
     }
 }
 
+// Bytes of one large-hub workspace slice (hubs of degree up to M), a multiple
+// of 256: spoke vectors, hash table, row, bit-matrix, bin masks, hub bins.
+static size_t c4_large_stride(int M, int nb)
+{
+    int tlog = 4;
+    while ((1 << tlog) < 2 * M) ++tlog;
+    const size_t WM = (size_t)(M + 31) / 32;
+    const size_t bytes = 16 * (size_t)M + sizeof(int32_t) * (2 * ((size_t)1 << tlog) + (size_t)M) +
+                         sizeof(unsigned) * ((size_t)M * WM + (size_t)nb * WM) + (size_t)M;
+    return (bytes + 255) & ~(size_t)255;
+}
+
 // Both kernels over the hubs [a.hub_begin, a.hub_end) (outputs accumulate).
 static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t st)
 {
     const int64_t hubs = a.hub_end - a.hub_begin;
     const int sms = gs_sm_count();
     const bool smem = a.ncfg <= C4_SMEM_HIST_MAX;
-    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * (size_t)a.ncfg : 0));
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)a.nb * C4_WORDS +
+                                           (smem ? 2 * (size_t)a.ncfg : 0));
     auto kern = windowed ? (smem ? k_count4_small<true, false, true> : k_count4_small<false, false, true>)
                          : (smem ? k_count4_small<true, false, false> : k_count4_small<false, false, false>);
     int per_sm = 0;
@@ -426,11 +448,7 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
 
     if (g->max_degree > C4_M) {
         const int M = g->max_degree;
-        int tlog = 4;
-        while ((1 << tlog) < 2 * M) ++tlog;
-        const size_t WM = (size_t)(M + 31) / 32;
-        size_t stride = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM + M;
-        stride = (stride + 255) & ~(size_t)255;
+        size_t stride = c4_large_stride(M, g->nb);
         const int gl = (int)std::min<int64_t>((int64_t)sms * 2, hubs);
         char *scratch = nullptr;
         GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
@@ -560,7 +578,8 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
 
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
-    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)g->nb * C4_WORDS +
+                                           (smem ? 2 * ncfg : 0));
     auto kern = smem ? k_count4_small<true, true, false> : k_count4_small<false, true, false>;
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
@@ -572,11 +591,7 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
     GS_TRY_CUDA(cudaGetLastError());
     if (g->max_degree > C4_M) {
         const int M = g->max_degree;
-        int tlog = 4;
-        while ((1 << tlog) < 2 * M) ++tlog;
-        const size_t WM = (size_t)(M + 31) / 32;
-        size_t stride = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM + M;
-        stride = (stride + 255) & ~(size_t)255;
+        size_t stride = c4_large_stride(M, g->nb);
         const int gl = (int)std::min<int64_t>((int64_t)sms * 2, count);
         char *scratch = nullptr;
         GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
@@ -653,11 +668,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     const int M = g->max_degree;
     size_t stride = 0;
     if (M > C4_M) {
-        int tlog = 4;
-        while ((1 << tlog) < 2 * M) ++tlog;
-        const size_t WM = (size_t)(M + 31) / 32;
-        stride = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM + M;
-        stride = (stride + 255) & ~(size_t)255;
+        stride = c4_large_stride(M, g->nb);
         if (stride > GS_C4_STATIC_BYTES - GS_C4_STATIC_HEAD)
             return gs_set_error(GS_ERR_CAPACITY,
                                 "a hub of degree %d needs %zu bytes of workspace; the static workspace holds %zu "
@@ -692,7 +703,8 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     const int64_t hubs = hub_end - hub_begin;
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
-    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (smem ? 2 * ncfg : 0));
+    const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)g->nb * C4_WORDS +
+                                           (smem ? 2 * ncfg : 0));
     auto kern = smem ? k_count4_small<true, false, false> : k_count4_small<false, false, false>;
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));

@@ -126,7 +126,7 @@ gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_de
  * cursors kept in the same array.
  *   Arguments, outputs and results are those of gs_count_4pcf_parity.
  *   Limit: one workspace slice must fit a hub of the graph's largest degree
- *   (about 16 MiB at degree ~11,800); otherwise GS_ERR_CAPACITY is returned
+ *   (16 MiB hold degree 11,392 at 8 bins); otherwise GS_ERR_CAPACITY is returned
  *   before anything is written.
  *   Set-up: the first call on each device looks up the workspace's device
  *   address (cudaGetSymbolAddress) with that device current and caches it;
