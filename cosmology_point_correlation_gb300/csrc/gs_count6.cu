@@ -88,7 +88,7 @@ struct C6Space {
     int32_t *pos;
     int32_t *row;      // [f] ids
     uint8_t *hb;       // [f] hub bins
-    int *vx, *vy, *vz; // [f] spoke vectors
+    int4 *v;           // [f] spoke vector x_s - x_i and hub bin (.w)
     unsigned *bits;    // [f][W]
     uint8_t *sbin;     // [f][f] spoke-spoke bins (valid where the bit is set)
     int16_t *ww;       // [f] spoke weights (weighted counts)
@@ -124,11 +124,11 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     for (int t = threadIdx.x; t < f; t += NT) {
         const int32_t k = F[t];
         w.row[t] = k;
-        w.hb[t] = FB[t];
+        const int b = FB[t];
+        w.hb[t] = (uint8_t)b;
         const int4 Q = a.pts[k];
-        w.vx[t] = gs_delta(P.x, Q.x, a.box, a.periodic);
-        w.vy[t] = gs_delta(P.y, Q.y, a.box, a.periodic);
-        w.vz[t] = gs_delta(P.z, Q.z, a.box, a.periodic);
+        w.v[t] = make_int4(gs_delta(P.x, Q.x, a.box, a.periodic), gs_delta(P.y, Q.y, a.box, a.periodic),
+                           gs_delta(P.z, Q.z, a.box, a.periodic), b);
         if (WEIGHTED) w.ww[t] = a.w[k];
         uint32_t h = gs_hash(k, shift);
         while (atomicCAS(&w.key[h], C6_EMPTY, k) != C6_EMPTY) h = (h + 1) & mask;
@@ -189,15 +189,17 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     };
     for (int s1 = next_row(-1); s1 < s1_end; s1 = next_row(s1)) {
         const unsigned *row1 = w.bits + (size_t)s1 * W;
-        const int b01 = w.hb[s1];
-        const long long x1 = w.vx[s1], y1 = w.vy[s1], z1 = w.vz[s1];
+        const int4 r1 = w.v[s1];
+        const int b01 = r1.w;
+        const long long x1 = r1.x, y1 = r1.y, z1 = r1.z;
         const long long w1 = WEIGHTED ? wi * w.ww[s1] : 0;
         auto make_pair = [&](int s2) {
             Pair p;
             p.s2 = s2;
-            p.b02 = w.hb[s2];
+            const int4 r2 = w.v[s2];
+            p.b02 = r2.w;
             p.b12 = w.sbin[(size_t)s1 * f + s2];
-            const long long x2 = w.vx[s2], y2 = w.vy[s2], z2 = w.vz[s2];
+            const long long x2 = r2.x, y2 = r2.y, z2 = r2.z;
             p.cx = y1 * z2 - z1 * y2;
             p.cy = z1 * x2 - x1 * z2;
             p.cz = x1 * y2 - y1 * x2;
@@ -206,12 +208,13 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
         };
         // one tetrahedron (i, s1, s2, s3)
         auto tetra = [&](const Pair &p, int s3) {
-            const int b03 = w.hb[s3];
+            const int4 r3 = w.v[s3];
+            const int b03 = r3.w;
             const int b13 = w.sbin[(size_t)s1 * f + s3], b23 = w.sbin[(size_t)p.s2 * f + s3];
             const int pk = ((((b01 * nb + p.b02) * nb + b03) * nb + p.b12) * nb + b13) * nb + b23;
             const int v = __ldg(a.cfg6 + pk);
             const int ci = v >> 2, par = (v & 3) - 1;
-            const long long d = p.cx * w.vx[s3] + p.cy * w.vy[s3] + p.cz * w.vz[s3];
+            const long long d = p.cx * r3.x + p.cy * r3.y + p.cz * r3.z;
             const int sg = par * ((d > 0) - (d < 0));
             if (WEIGHTED) {
                 const long long W4 = p.w12 * w.ww[s3];                    // |.| <= 2^60
@@ -308,7 +311,7 @@ k_count6_small(C6Args a)
     __shared__ int32_t s_pos[2 * M];
     __shared__ int32_t s_row[M];
     __shared__ uint8_t s_hb[M];
-    __shared__ int s_vx[M], s_vy[M], s_vz[M];
+    __shared__ int4 s_v[M];
     __shared__ int16_t s_ww[M];
     __shared__ long long s_hub;
     __shared__ int s_next;
@@ -328,7 +331,7 @@ k_count6_small(C6Args a)
         }
     for (int t = threadIdx.x; t < 2 * M; t += C6_THREADS) s_key[t] = C6_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
-    C6Space w{ s_key, s_pos, s_row, s_hb, s_vx, s_vy, s_vz, s_bits, s_sbin, s_ww, &s_next };
+    C6Space w{ s_key, s_pos, s_row, s_hb, s_v, s_bits, s_sbin, s_ww, &s_next };
 
     for (;;) {
         __syncthreads();
@@ -398,13 +401,11 @@ k_count6_large(C6Args a)
     const int WM = (M + 31) >> 5;
     char *base = a.scratch + (size_t)blockIdx.x * a.scratch_stride;
     C6Space w;
-    w.key = (int32_t *)base;
+    w.v = (int4 *)base;                                   // slices start 256-byte aligned
+    w.key = (int32_t *)(w.v + M);
     w.pos = w.key + (1 << tlog);
     w.row = w.pos + (1 << tlog);
-    w.vx = w.row + M;
-    w.vy = w.vx + M;
-    w.vz = w.vy + M;
-    w.bits = (unsigned *)(w.vz + M);
+    w.bits = (unsigned *)(w.row + M);
     w.hb = (uint8_t *)(w.bits + (size_t)M * WM);
     w.sbin = w.hb + M;
     w.ww = (int16_t *)(w.sbin + (size_t)M * M);          // M + M*M is even: 2-byte aligned
@@ -467,8 +468,8 @@ static size_t c6_large_stride(int M)
     int tlog = 4;
     while ((1 << tlog) < 2 * M) ++tlog;
     const size_t WM = (size_t)(M + 31) / 32;
-    const size_t bytes = sizeof(int32_t) * (2 * ((size_t)1 << tlog) + 4 * (size_t)M) + sizeof(unsigned) * M * WM +
-                         M + (size_t)M * M + sizeof(int16_t) * M;
+    const size_t bytes = 16 * (size_t)M + sizeof(int32_t) * (2 * ((size_t)1 << tlog) + (size_t)M) +
+                         sizeof(unsigned) * M * WM + M + (size_t)M * M + sizeof(int16_t) * M;
     return (bytes + 255) & ~(size_t)255;
 }
 
