@@ -9,19 +9,24 @@
 // m/32 word operations instead of a pointer walk.
 //
 // Per hub, one thread block:
-//   1. stages the hub row (ids, hub bins, minimum-image spoke vectors x_s - x_i)
-//      and a hash table id -> row position in shared memory;
+//   1. stages the hub row (ids; spoke vectors x_s - x_i, minimum image, with
+//      the hub bin, as one int4 per spoke), one bitset of positions per hub
+//      bin, and a hash table id -> row position in shared memory;
 //   2. builds the bit-matrix: each warp walks the forward part of N(j) for one
 //      spoke j (coalesced), probing the table;
-//   3. a warp per s1, its lanes over s2: for each pair with bit (s1, s2) set and
-//      distinct hub bins it ANDs the two rows, and for every s3 with a third distinct bin
-//      orders the spokes by hub bin, takes V = det[r_1; r_2; r_3] (Eq.(3)) in
-//      exact int64, and adds 1 to even and sign(V) to odd (V == 0 adds 0, the
-//      degenerate rule of §III.2).
-// Hubs of degree <= C4_M run entirely in shared memory with uint32 / int32
-// shared histograms; rarer hubs of higher degree run in a second kernel whose
-// per-block matrix lives in a global scratch slice and which adds straight
-// into the global histograms.
+//   3. clique search: warps take rows s1 from a counter, lanes take candidate
+//      spokes s2 with bit (s1, s2) set and a hub bin other than s1's. The
+//      third spokes of a pair are the AND of rows s1 and s2 above s2, less the
+//      bitsets of the two bins already used; the warp prefix-sums the lanes'
+//      counts word by word and deals the cliques out 32 at a time. A clique
+//      adds 1 to even and sign(V) to odd at its sorted bin triple, with
+//      V = det[r_1; r_2; r_3] of the bin-ordered spokes (Eq.(3)) obtained as
+//      (r_s1 x r_s2) . r_s3 times the sign of the sorting permutation, in
+//      exact int64 (V == 0 adds 0: the degenerate rule of §III.2).
+// Hubs of degree <= C4_M run entirely in shared memory; rarer hubs of higher
+// degree run in a second kernel whose per-block workspace lives in a global
+// scratch slice. Both keep uint32 / int32 histograms in shared memory (a hub
+// whose clique bound exceeds 2^31 adds straight to global memory).
 //
 // Windowed graphs (§III.5.3: tiles over pairs of search windows c1 <= c2):
 // a tile stages the hub window and windows c1, c2; the bit rows of spokes in

@@ -4,8 +4,8 @@
 //
 // Every tetrahedron {i, j1, j2, j3} with i < j1 < j2 < j3 (internal order) is
 // found once, at hub i, from its forward row F = {j in N(i) : j > i}:
-//   1. F is staged in shared memory (ids, hub bins, spoke vectors x_j - x_i)
-//      with a hash table id -> position;
+//   1. F is staged in shared memory (ids; spoke vectors x_j - x_i with the
+//      hub bin, one int4 per spoke) with a hash table id -> position;
 //   2. warps walk the forward part of each spoke's row N(j) and, for every
 //      entry that is also in F, set bit (s, t) of an adjacency bit-matrix and
 //      store the spoke-spoke bin in a byte matrix;
@@ -15,8 +15,12 @@
 //      turns this labelling into the configuration's smallest tuple (0 when
 //      orderings of both parities do: an achiral configuration); the odd
 //      channel adds that parity times sign(det[r_j1; r_j2; r_j3]).
-// Hubs with more than C6_M forward neighbours use a global scratch slice per
-// block instead of shared memory.
+// Hubs with up to 128 forward neighbours run in a 128-slot shared-memory
+// kernel (four blocks per SM), up to C6_M in a 256-slot one, larger hubs in a
+// kernel with a global workspace slice and 1024-thread blocks; all keep their
+// histograms in shared memory. In the weighted mode (several atomics per
+// tetrahedron) warps take rows s1 from a counter and deal the tetrahedra of
+// each word of the bit rows out 32 at a time, as the parity kernel does.
 //
 // Windowed graphs (§III.5.3): tiles (hub window, spoke windows c1 <= c2) as
 // for the parity count; only tetrahedra whose two lowest spokes lie in c1 and
