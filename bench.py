@@ -514,8 +514,20 @@ def run_ours(args, w):
                 rows.append({"window_edges": e_all // nwin + 1, "windows": g.windows()[0], "count_ms": t_w,
                              "count_ms_runs": ts_w, "overhead": t_w / t_res - 1.0,
                              "exact": bool(np.array_equal(h_w, h_res))})
+        # pinned host -> device copy rate in this process, which bounds the window staging
+        hbuf = torch.empty(1 << 28, dtype=torch.int32).pin_memory()
+        dbuf = torch.empty(1 << 28, dtype=torch.int32, device=dev)
+        dbuf.copy_(hbuf, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        h2d_gbs = hbuf.numel() * 4 / 1e9 / (e0.elapsed_time(e1) / 1e3)
+        del hbuf, dbuf
         windowed = {"config": wdesc, "resident_count_ms": t_res, "resident_count_ms_runs": ts_res,
-                    "n_edges": e_all, "tiles": rows}
+                    "n_edges": e_all, "tiles": rows, "pinned_h2d_gbs": h2d_gbs}
 
     # CPU oracle on a bounded sample (rank 0 only)
     cpu = None
