@@ -48,9 +48,9 @@ constexpr int C3_TABLE = 1 << C3_TABLE_LOG;
 constexpr int C3_CHUNK = C3_TABLE / 4;           // load factor <= 1/4: short probe chains
 constexpr int C3_SPOKES = 4096;                  // spokes grouped per pass
 constexpr int C3_SPAN_BITS = 1 << 18;            // bitmap mode: key span of a chunk
-constexpr int C3_SPAN_PAIRS = C3_SPAN_BITS / 64;
+constexpr int C3_SPAN_WORDS = C3_SPAN_BITS / 32;
 // bytes of the candidate-key region: the larger of the two modes
-constexpr int C3_REGION_BITMAP = C3_SPAN_PAIRS * (8 + 2) + C3_TABLE / 4;
+constexpr int C3_REGION_BITMAP = C3_SPAN_WORDS * (4 + 2) + C3_TABLE / 4;
 constexpr int C3_REGION_HASH = C3_TABLE * 5;
 constexpr int C3_REGION = ((C3_REGION_BITMAP > C3_REGION_HASH ? C3_REGION_BITMAP : C3_REGION_HASH) + 15) & ~15;
 // weighted: the chunk's weights follow the bins (int16 per key / per slot)
@@ -173,9 +173,9 @@ k_count3(C3Args a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nb = a.nb;
     // bitmap mode
-    uint2 *s_bm = (uint2 *)s_dyn;                                     // [C3_SPAN_PAIRS] bits
-    uint16_t *s_rank = (uint16_t *)(s_bm + C3_SPAN_PAIRS);            // [C3_SPAN_PAIRS] bits before the pair
-    uint8_t *s_cbin = (uint8_t *)(s_rank + C3_SPAN_PAIRS);            // [C3_CHUNK] bins in key order
+    unsigned *s_bm = (unsigned *)s_dyn;                               // [C3_SPAN_WORDS] bits
+    uint16_t *s_rank = (uint16_t *)(s_bm + C3_SPAN_WORDS);            // [C3_SPAN_WORDS] bits before the word
+    uint8_t *s_cbin = (uint8_t *)(s_rank + C3_SPAN_WORDS);            // [C3_CHUNK] bins in key order
     // hash mode
     int32_t *s_key = (int32_t *)s_dyn;
     uint8_t *s_bin = (uint8_t *)(s_key + C3_TABLE);
@@ -262,24 +262,24 @@ k_count3(C3Args a)
             if (bmode) {
                 // exact bitmap of the chunk's keys over [kfirst, kmax], the rank of
                 // every 64-bit pair, and the chunk's bins in key order
-                const int npairs = (span + 63) >> 6;
-                for (int t = threadIdx.x; t < npairs; t += C3_THREADS) s_bm[t] = make_uint2(0u, 0u);
+                const int nwords = (span + 31) >> 5;
+                for (int t = threadIdx.x; t < nwords; t += C3_THREADS) s_bm[t] = 0u;
                 __syncthreads();
                 for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
                     const int off = F[c0 + t] - kfirst;
-                    atomicOr(reinterpret_cast<unsigned *>(s_bm) + (off >> 5), 1u << (off & 31));
+                    atomicOr(s_bm + (off >> 5), 1u << (off & 31));
                     s_cbin[t] = FB[c0 + t];
                     if (WEIGHTED) s_cw[t] = a.w[off + kfirst];
                 }
                 __syncthreads();
-                const int per = (npairs + C3_THREADS - 1) / C3_THREADS;
+                const int per = (nwords + C3_THREADS - 1) / C3_THREADS;
                 const int q0 = threadIdx.x * per;
                 int cnt = 0;
-                for (int q = q0; q < min(npairs, q0 + per); ++q) cnt += __popc(s_bm[q].x) + __popc(s_bm[q].y);
+                for (int q = q0; q < min(nwords, q0 + per); ++q) cnt += __popc(s_bm[q]);
                 int run = c3_block_scan(cnt, s_warp);
-                for (int q = q0; q < min(npairs, q0 + per); ++q) {
+                for (int q = q0; q < min(nwords, q0 + per); ++q) {
                     s_rank[q] = (uint16_t)run;
-                    run += __popc(s_bm[q].x) + __popc(s_bm[q].y);
+                    run += __popc(s_bm[q]);
                 }
             } else {
                 for (int t = threadIdx.x; t < tsize; t += C3_THREADS) s_key[t] = C3_EMPTY;
@@ -400,11 +400,9 @@ k_count3(C3Args a)
                                 const unsigned off = (unsigned)(k[e] - kfirst);
                                 const bool in = off < (unsigned)span;
                                 const unsigned o = in ? off : 0u;
-                                const uint2 pr = s_bm[o >> 6];
-                                const unsigned w = (o & 32u) ? pr.y : pr.x;
+                                const unsigned w = s_bm[o >> 5];
                                 if (in && ((vmask >> e) & 1u) && ((w >> (o & 31u)) & 1u)) {
-                                    const int rank = s_rank[o >> 6] + ((o & 32u) ? __popc(pr.x) : 0) +
-                                                     __popc(w & ((1u << (o & 31u)) - 1u));
+                                    const int rank = s_rank[o >> 5] + __popc(w & ((1u << (o & 31u)) - 1u));
                                     hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
                                 }
                             }
