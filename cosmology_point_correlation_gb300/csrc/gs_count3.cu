@@ -49,8 +49,9 @@ constexpr int C3_CHUNK = C3_TABLE / 4;           // load factor <= 1/4: short pr
 constexpr int C3_SPOKES = 4096;                  // spokes grouped per pass
 constexpr int C3_SPAN_BITS = 1 << 18;            // bitmap mode: key span of a chunk
 constexpr int C3_SPAN_WORDS = C3_SPAN_BITS / 32;
+constexpr int C3_BM_WORDS = C3_SPAN_WORDS + 4;   // + a zero guard word that out-of-range probes read
 // bytes of the candidate-key region: the larger of the two modes
-constexpr int C3_REGION_BITMAP = C3_SPAN_WORDS * (4 + 2) + C3_TABLE / 4;
+constexpr int C3_REGION_BITMAP = C3_BM_WORDS * 4 + C3_SPAN_WORDS * 2 + C3_TABLE / 4;
 constexpr int C3_REGION_HASH = C3_TABLE * 5;
 constexpr int C3_REGION = ((C3_REGION_BITMAP > C3_REGION_HASH ? C3_REGION_BITMAP : C3_REGION_HASH) + 15) & ~15;
 // weighted: the chunk's weights follow the bins (int16 per key / per slot)
@@ -173,8 +174,8 @@ k_count3(C3Args a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nb = a.nb;
     // bitmap mode
-    unsigned *s_bm = (unsigned *)s_dyn;                               // [C3_SPAN_WORDS] bits
-    uint16_t *s_rank = (uint16_t *)(s_bm + C3_SPAN_WORDS);            // [C3_SPAN_WORDS] bits before the word
+    unsigned *s_bm = (unsigned *)s_dyn;                               // [C3_BM_WORDS] bits
+    uint16_t *s_rank = (uint16_t *)(s_bm + C3_BM_WORDS);              // [C3_SPAN_WORDS] bits before the word
     uint8_t *s_cbin = (uint8_t *)(s_rank + C3_SPAN_WORDS);            // [C3_CHUNK] bins in key order
     // hash mode
     int32_t *s_key = (int32_t *)s_dyn;
@@ -263,7 +264,8 @@ k_count3(C3Args a)
                 // exact bitmap of the chunk's keys over [kfirst, kmax], the rank of
                 // every 64-bit pair, and the chunk's bins in key order
                 const int nwords = (span + 31) >> 5;
-                for (int t = threadIdx.x; t < nwords; t += C3_THREADS) s_bm[t] = 0u;
+                // the word holding offset `span` stays zero: probes clamp to it
+                for (int t = threadIdx.x; t <= nwords; t += C3_THREADS) s_bm[t] = 0u;
                 __syncthreads();
                 for (int t = threadIdx.x; t < cn; t += C3_THREADS) {
                     const int off = F[c0 + t] - kfirst;
@@ -395,13 +397,19 @@ k_count3(C3Args a)
                         }
                         const int k[4] = { kk.x, kk.y, kk.z, kk.w };
                         if (bmode) {
+                            // entries outside [p0, pe) (first and last step) become kfirst - 1;
+                            // every offset outside [0, span) clamps to the zero guard bit at span
+                            int kv[4] = { k[0], k[1], k[2], k[3] };
+                            if (vmask != 0xfu) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (!((vmask >> e) & 1u)) kv[e] = kfirst - 1;
+                            }
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const unsigned off = (unsigned)(k[e] - kfirst);
-                                const bool in = off < (unsigned)span;
-                                const unsigned o = in ? off : 0u;
+                                const unsigned o = min((unsigned)(kv[e] - kfirst), (unsigned)span);
                                 const unsigned w = s_bm[o >> 5];
-                                if (in && ((vmask >> e) & 1u) && ((w >> (o & 31u)) & 1u)) {
+                                if ((w >> (o & 31u)) & 1u) {
                                     const int rank = s_rank[o >> 5] + __popc(w & ((1u << (o & 31u)) - 1u));
                                     hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
                                 }
