@@ -82,6 +82,10 @@ typedef enum {
  *   nbins       1..255
  *   out         receives the new graph handle (free with gs_graph_free)
  * The coordinates are copied; coords_dev may be freed after the call returns.
+ * The edge arrays normally live in device memory. When they would not fit in
+ * the free device memory, or when the environment variable GS_WINDOW_EDGES
+ * holds a positive edge count, the graph is built windowed instead (pinned
+ * host memory, see gs_build_graph_windowed); gs_graph_windows tells which.
  * Errors: GS_ERR_ARG for bad arguments or a coordinate outside [0, box_lu)
  * (checked on the device, reported at the call's one synchronisation),
  * GS_ERR_NOMEM, GS_ERR_CUDA. On error *out is set to NULL. */
