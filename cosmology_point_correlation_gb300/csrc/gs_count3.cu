@@ -22,14 +22,16 @@
 // chunk also holds each key's weight and a hit adds w_j w_k (|.| <= 2^30) to
 // the block's int64 sum T[config] of the current hub (two 32-bit words with
 // a carry, so that a hit costs one 32-bit shared atomic). A pass over at most
-// C3_SPOKES spokes of one chunk closes at most 2^23 triangles, so |T| stays
-// below 2^53; after each pass the block adds w_i T, an exact 128-bit product,
+// C3_SPOKES spokes of one chunk closes at most 2^24 triangles, so |T| stays
+// below 2^54; after each pass the block adds w_i T, an exact 128-bit product,
 // into its own 128-bit slice of a global scratch array (no atomics: each
 // configuration has one owner thread), and a second kernel sums the slices.
 //
-// Rows longer than the table are processed in chunks of the hub row: chunk
-// [c0, c1) holds the k candidates, every spoke at position s < c1 - 1 is
-// walked over keys in (max(j, F[c0] - 1), F[c1 - 1]].
+// Long rows are processed in chunks of the hub row: chunk [c0, c1) holds the
+// k candidates, every spoke at position s < c1 - 1 is walked over keys in
+// (max(j, F[c0] - 1), F[c1 - 1]]; a spoke of an earlier chunk first finds its
+// starting entry by binary search. A bitmap chunk holds up to C3_CHUNK_BM
+// keys (C3_CHUNK_BM_W weighted), a hash chunk C3_CHUNK.
 //
 // Hubs are handed out in increasing internal order from a global counter, so
 // the blocks resident at any moment work on neighbouring hubs whose spoke
@@ -45,17 +47,19 @@ constexpr int C3_THREADS = 512;
 constexpr int C3_WARPS = C3_THREADS / 32;
 constexpr int C3_TABLE_LOG = 13;                 // 8192 slots
 constexpr int C3_TABLE = 1 << C3_TABLE_LOG;
-constexpr int C3_CHUNK = C3_TABLE / 4;           // load factor <= 1/4: short probe chains
+constexpr int C3_CHUNK = C3_TABLE / 4;           // hash mode: keys per chunk (load factor <= 1/4)
+constexpr int C3_CHUNK_BM = 8192;                // bitmap mode: keys per chunk
+constexpr int C3_CHUNK_BM_W = 4096;              // bitmap mode, weighted (2 more bytes per key)
 constexpr int C3_SPOKES = 4096;                  // spokes grouped per pass
 constexpr int C3_SPAN_BITS = 1 << 18;            // bitmap mode: key span of a chunk
 constexpr int C3_SPAN_WORDS = C3_SPAN_BITS / 32;
 constexpr int C3_BM_WORDS = C3_SPAN_WORDS + 4;   // + a zero guard word that out-of-range probes read
 // bytes of the candidate-key region: the larger of the two modes
-constexpr int C3_REGION_BITMAP = C3_BM_WORDS * 4 + C3_SPAN_WORDS * 2 + C3_TABLE / 4;
+constexpr int C3_REGION_BITMAP = C3_BM_WORDS * 4 + C3_SPAN_WORDS * 2 + C3_CHUNK_BM;
 constexpr int C3_REGION_HASH = C3_TABLE * 5;
 constexpr int C3_REGION = ((C3_REGION_BITMAP > C3_REGION_HASH ? C3_REGION_BITMAP : C3_REGION_HASH) + 15) & ~15;
 // weighted: the chunk's weights follow the bins (int16 per key / per slot)
-constexpr int C3_REGION_BITMAP_W = C3_REGION_BITMAP + C3_CHUNK * 2;
+constexpr int C3_REGION_BITMAP_W = C3_BM_WORDS * 4 + C3_SPAN_WORDS * 2 + C3_CHUNK_BM_W * 3;
 constexpr int C3_REGION_HASH_W = C3_TABLE * 7;
 constexpr int C3_REGION_W = ((C3_REGION_BITMAP_W > C3_REGION_HASH_W ? C3_REGION_BITMAP_W : C3_REGION_HASH_W) + 15) & ~15;
 constexpr int C3_SMEM_HIST_MAX = 12288;          // configurations kept in shared memory (nbins <= 40)
@@ -158,7 +162,7 @@ k_count3(C3Args a)
     // per-pair ranks, chunk bins; hash mode: keys, bins), then (SMEM_HIST only)
     // the histogram [ncfg] u32 and one nb x nb u16 table per warp.
     // WEIGHTED: the region [C3_REGION_W bytes] also holds the weights (bitmap
-    // mode: [C3_CHUNK] after the bins; hash mode: [C3_TABLE] after the bins),
+    // mode: [C3_CHUNK_BM_W] after the bins; hash mode: [C3_TABLE] after the bins),
     // then the pass sums T [ncfg] int64
     extern __shared__ unsigned s_dyn[];
     __shared__ uint16_t s_order[C3_SPOKES];         // spoke positions grouped by b_ij
@@ -176,7 +180,8 @@ k_count3(C3Args a)
     // bitmap mode
     unsigned *s_bm = (unsigned *)s_dyn;                               // [C3_BM_WORDS] bits
     uint16_t *s_rank = (uint16_t *)(s_bm + C3_BM_WORDS);              // [C3_SPAN_WORDS] bits before the word
-    uint8_t *s_cbin = (uint8_t *)(s_rank + C3_SPAN_WORDS);            // [C3_CHUNK] bins in key order
+    constexpr int CHUNK_BM = WEIGHTED ? C3_CHUNK_BM_W : C3_CHUNK_BM;
+    uint8_t *s_cbin = (uint8_t *)(s_rank + C3_SPAN_WORDS);            // [CHUNK_BM] bins in key order
     // hash mode
     int32_t *s_key = (int32_t *)s_dyn;
     uint8_t *s_bin = (uint8_t *)(s_key + C3_TABLE);
@@ -184,7 +189,7 @@ k_count3(C3Args a)
     uint16_t *tab = (uint16_t *)(s_hist + ((a.ncfg + 3) & ~3)) + warp * nb * nb;
     int tab_z = -1;
     // weighted
-    int16_t *s_cw = (int16_t *)(s_cbin + C3_CHUNK);                   // [C3_CHUNK] weights in key order
+    int16_t *s_cw = (int16_t *)(s_cbin + CHUNK_BM);                   // [CHUNK_BM] weights in key order
     int16_t *s_hw = (int16_t *)(s_bin + C3_TABLE);                    // [C3_TABLE] weights per slot
     unsigned long long *s_T = (unsigned long long *)((char *)s_dyn + C3_REGION_W);
 
@@ -232,8 +237,15 @@ k_count3(C3Args a)
             q_lo = s_q[0];
             q_hi = s_q[1];
         }
-        for (int c0 = 0; c0 < f; c0 += C3_CHUNK) {           // chunks of candidate keys
-            const int c1 = min(f, c0 + C3_CHUNK);
+        for (int c0 = 0, c1 = 0; c0 < f; c0 = c1) {         // chunks of candidate keys
+            // a bitmap chunk of up to CHUNK_BM keys when their span fits, else a
+            // C3_CHUNK-key chunk (bitmap if its span fits, else hash); block-uniform
+            c1 = min(f, c0 + CHUNK_BM);
+            bool bmode = (int64_t)F[c1 - 1] - F[c0] + 1 <= C3_SPAN_BITS;
+            if (!bmode) {
+                c1 = min(f, c0 + C3_CHUNK);
+                bmode = (int64_t)F[c1 - 1] - F[c0] + 1 <= C3_SPAN_BITS;
+            }
             const int cn = c1 - c0;
             if (c1 < 2) break;                               // a lone key closes nothing
             const int s_end = min(c1 - 1, q_hi);             // spokes [q_lo, s_end) meet this chunk
@@ -241,7 +253,6 @@ k_count3(C3Args a)
             const int32_t kmax = F[c1 - 1];
             const int32_t kfirst = F[c0];
             const int64_t span64 = (int64_t)kmax - kfirst + 1;
-            const bool bmode = span64 <= C3_SPAN_BITS;       // block-uniform
             const int span = (int)(span64 < C3_SPAN_BITS ? span64 : C3_SPAN_BITS);
             int lg = 6;                                      // hash mode: 2^lg >= 4 cn slots
             while ((1 << lg) < 4 * cn) ++lg;
@@ -504,7 +515,7 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
     } else {
         // shared-memory histogram unless it is too large or a chunk's hit bound
         // (spokes x chunk) could overflow a 32-bit counter
-        smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK < (1ll << 31);
+        smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK_BM < (1ll << 31);
         dyn = C3_REGION + (smem ? sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * C3_WARPS * nb2 : 0);
         if (win)
             kern = smem ? k_count3<true, false, false, true> : k_count3<false, false, false, true>;
