@@ -157,3 +157,28 @@ def test_windowed_large_hubs_equal_resident():
         assert np.array_equal(e, pe) and np.array_equal(o, po)
         e, o = (t.cpu().numpy() for t in g.count_4pcf6())
         assert np.array_equal(e, se) and np.array_equal(o, so)
+
+
+@pytest.mark.slow
+def test_build_switches_to_windows_when_the_graph_does_not_fit():
+    # §III.5.3: chunked mode is selected at run time when the graph exceeds the
+    # free device memory. Hold all but 3 GB of it, then build the 2M-point
+    # uniform graph (5.4 GB of CSR): it must come out windowed and count the same.
+    torch, dev = torch_dev()
+    w = configs.LARGE_3PCF
+    xyz = w.points()
+    with _graph(xyz, w.box_lu, True, w.edges_lu) as g:
+        assert g.windows()[0] == 0
+        full = as_uint64(g.count_3pcf())
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info()
+    hold = torch.empty(max(free - (3 << 30), 0), dtype=torch.uint8, device=dev)
+    try:
+        with _graph(xyz, w.box_lu, True, w.edges_lu) as g:
+            nw, wmax = g.windows()
+            assert nw > 2 and wmax < g.n_edges
+            assert np.array_equal(as_uint64(g.count_3pcf()), full)
+    finally:
+        del hold
+        torch.cuda.empty_cache()
