@@ -38,6 +38,8 @@
 // rows overlap and stay in L2.
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <utility>
 #include <vector>
 
@@ -154,7 +156,126 @@ __device__ __forceinline__ int c3_block_scan(int v, int *s_warp)
     return r;
 }
 
-template <bool SMEM_HIST, bool HUB_LIST, bool WEIGHTED, bool WINDOWED>
+// Grouped walk, for graphs whose rows hold a few hundred entries: there a
+// spoke's walk is one or two steps, and its time is the latency of the loads
+// that start it (the spoke, its row bounds, its first step). So a warp walks
+// four spokes at a time, eight lanes each: lane l of a group reads entries
+// 4l .. 4l+3 of a 32-entry step, and four spokes' loads are in flight per warp.
+// The four spokes' bins b_ij differ, so configurations come from the whole
+// table [b_ij][b_ik][b_jk] in shared memory. Probes and hits are as in the
+// one-spoke-per-warp walk of k_count3.
+__device__ __forceinline__ void c3_walk_grouped(const C3Args &a, const int32_t *F, const uint8_t *FB, int sb,
+                                                int ns, int c0, int32_t kfirst, int32_t kmax, int span,
+                                                bool bmode, int shift, int mask, const unsigned *s_bm,
+                                                const uint16_t *s_rank, const uint8_t *s_cbin,
+                                                const int32_t *s_key, const uint8_t *s_bin, unsigned *s_hist,
+                                                const uint16_t *s_full, int *s_next)
+{
+    const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
+    const int nb = a.nb;
+    for (;;) {
+        int li = 0;
+        if (lane == 0) li = atomicAdd(s_next, 4);
+        li = __shfl_sync(0xffffffffu, li, 0);
+        if (li >= ns) break;
+        li += grp;
+        // this group's spoke j and the part [p0, pe) of N(j) it walks
+        int64_t p0 = 0, pe = 0;
+        int bij = 0;
+        if (li < ns) {
+            const int s = sb + li;
+            const int32_t j = F[s];
+            bij = FB[s];
+            pe = a.row_ptr[j + 1];
+            if (s + 1 >= c0) {
+                p0 = a.row_ptr[j] + a.fwd[j];                  // first entry > j
+            } else {
+                int64_t lo = a.row_ptr[j] + a.fwd[j], hi = pe;  // first entry >= kfirst
+                while (lo < hi) {
+                    const int64_t mid = (lo + hi) >> 1;
+                    if (a.snbr[mid] < kfirst) lo = mid + 1; else hi = mid;
+                }
+                p0 = lo;
+            }
+        }
+        const int64_t pa = p0 & ~(int64_t)3;
+        const int head = (int)(p0 - pa);
+        const int total = p0 < pe ? head + (int)(pe - p0) : 0;
+        const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + pa) + gl;
+        const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + pa) + gl;
+        const uint16_t *ztab = s_full + bij * nb * nb;
+        int4 kk = make_int4(0, 0, 0, 0);
+        uint32_t bb = 0;
+        bool go = total > 0;                                   // the same in the eight lanes of a group
+        if (go) {
+            kk = __ldg(vk);
+            bb = __ldg(vb);
+        }
+        for (int base = 0; __any_sync(0xffffffffu, go); base += 32) {
+            const bool more = go && base + 32 < total;
+            int4 kn = kk;
+            uint32_t bn = bb;
+            if (more) {                                        // next step in flight
+                vk += 8;
+                vb += 8;
+                kn = __ldg(vk);
+                bn = __ldg(vb);
+            }
+            if (go) {
+                unsigned vmask = 0xfu;
+                if (base == 0 || base + 32 > total) {
+                    const int r0 = base + 4 * gl;
+                    if (head > r0) vmask &= (0xfu << min(head - r0, 4)) & 0xfu;
+                    if (total - r0 < 4) vmask &= (1u << max(total - r0, 0)) - 1u;
+                }
+                const int k[4] = { kk.x, kk.y, kk.z, kk.w };
+                if (bmode) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int kv = ((vmask >> e) & 1u) ? k[e] : kfirst - 1;
+                        const unsigned o = min((unsigned)(kv - kfirst), (unsigned)span);
+                        const unsigned w = s_bm[o >> 5];
+                        if ((w >> (o & 31u)) & 1u) {
+                            const int rank = s_rank[o >> 5] + __popc(w & ((1u << (o & 31u)) - 1u));
+                            atomicAdd(&s_hist[ztab[s_cbin[rank] * nb + ((bb >> (8 * e)) & 0xffu)]], 1u);
+                        }
+                    }
+                } else {
+                    uint32_t h[4];
+                    int32_t key[4];
+                    unsigned pend = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        h[e] = gs_hash(k[e], shift);
+                        key[e] = s_key[h[e]];
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) pend |= (unsigned)(key[e] != k[e] && key[e] != C3_EMPTY) << e;
+                    while (pend) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if ((pend >> e) & 1u) {
+                                h[e] = (h[e] + 1) & mask;
+                                key[e] = s_key[h[e]];
+                                if (key[e] == k[e] || key[e] == C3_EMPTY) pend &= ~(1u << e);
+                            }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (((vmask >> e) & 1u) && key[e] == k[e])
+                            atomicAdd(&s_hist[ztab[s_bin[h[e]] * nb + ((bb >> (8 * e)) & 0xffu)]], 1u);
+                }
+            }
+            // rows are sorted: a group stops once its step's last key passes kmax
+            const int last = __shfl_sync(0xffffffffu, kk.w, lane | 7);
+            go = more && last <= kmax;
+            kk = kn;
+            bb = bn;
+        }
+    }
+}
+
+template <bool SMEM_HIST, bool HUB_LIST, bool WEIGHTED, bool WINDOWED, bool GROUPED = false>
 __global__ void __launch_bounds__(C3_THREADS, 2)
 k_count3(C3Args a)
 {
@@ -188,6 +309,8 @@ k_count3(C3Args a)
     unsigned *s_hist = (unsigned *)((char *)s_dyn + C3_REGION);
     uint16_t *tab = (uint16_t *)(s_hist + ((a.ncfg + 3) & ~3)) + warp * nb * nb;
     int tab_z = -1;
+    // GROUPED: the whole configuration table [nb][nb][nb] in place of the per-warp tables
+    uint16_t *s_full = (uint16_t *)(s_hist + ((a.ncfg + 3) & ~3));
     // weighted
     int16_t *s_cw = (int16_t *)(s_cbin + CHUNK_BM);                   // [CHUNK_BM] weights in key order
     int16_t *s_hw = (int16_t *)(s_bin + C3_TABLE);                    // [C3_TABLE] weights per slot
@@ -204,6 +327,8 @@ k_count3(C3Args a)
         for (int t = threadIdx.x; t < a.ncfg; t += C3_THREADS) s_T[t] = 0ull;
     } else if (SMEM_HIST) {
         for (int t = threadIdx.x; t < a.ncfg; t += C3_THREADS) s_hist[t] = 0;
+        if (GROUPED)
+            for (int t = threadIdx.x; t < nb * nb * nb; t += C3_THREADS) s_full[t] = __ldg(a.cfg3 + t);
     }
     if (threadIdx.x == 0) s_pending = 0;
     __syncthreads();
@@ -310,6 +435,14 @@ k_count3(C3Args a)
             for (int sb = q_lo; sb < s_end; sb += C3_SPOKES) {
                 const int se = min(s_end, sb + C3_SPOKES);
                 const int ns = se - sb;
+                if (GROUPED) {
+                    if (threadIdx.x == 0) s_next = 0;
+                    __syncthreads();
+                    c3_walk_grouped(a, F, FB, sb, ns, c0, kfirst, kmax, span, bmode, shift, mask,
+                                    s_bm, s_rank, s_cbin, s_key, s_bin, s_hist, s_full, &s_next);
+                    __syncthreads();
+                    continue;
+                }
                 // counting sort of the spokes by b_ij, so that a warp's spokes
                 // share their bin and its configuration table changes rarely
                 for (int t = threadIdx.x; t <= nb; t += C3_THREADS) s_bucket[t] = 0;
@@ -498,6 +631,21 @@ __global__ void k_sum128_slices(const unsigned long long *__restrict__ slices, i
     }
 }
 
+// Walk mode of the unweighted, device-resident count: one spoke per warp for
+// long rows, four spokes per warp (c3_walk_grouped) when the mean degree is at
+// most C3_GROUPED_MAX_DEGREE. The environment variable GS_COUNT3_WALK = "warp"
+// or "group" overrides the choice.
+constexpr int64_t C3_GROUPED_MAX_DEGREE = 1024;
+
+static int count3_walk_override()
+{
+    const char *env = getenv("GS_COUNT3_WALK");
+    if (!env) return -1;
+    if (!strcmp(env, "warp")) return 0;
+    if (!strcmp(env, "group")) return 1;
+    return -1;
+}
+
 static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_t st)
 {
     const int ncfg = a.ncfg;
@@ -522,6 +670,24 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
         else
             kern = smem ? (list ? k_count3<true, true, false, false> : k_count3<true, false, false, false>)
                         : (list ? k_count3<false, true, false, false> : k_count3<false, false, false, false>);
+        if (smem && !win && !list) {
+            // grouped walk: the whole configuration table in place of the per-warp
+            // tables; taken when chosen and two blocks still fit on an SM (or when forced)
+            const int mode = count3_walk_override();
+            const bool want = mode == 1 || (mode < 0 && g->n_edges <= C3_GROUPED_MAX_DEGREE * g->n);
+            if (want) {
+                const size_t dyn_g = C3_REGION + sizeof(unsigned) * ((ncfg + 3) & ~3) +
+                                     sizeof(uint16_t) * (size_t)nb2 * g->nb;
+                auto kg = k_count3<true, false, false, false, true>;
+                int per = 0;
+                GS_TRY_CUDA(cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_g));
+                GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kg, C3_THREADS, dyn_g));
+                if (per >= 2 || (mode == 1 && per >= 1)) {
+                    kern = kg;
+                    dyn = dyn_g;
+                }
+            }
+        }
     }
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));

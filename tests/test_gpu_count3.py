@@ -11,6 +11,14 @@ from tests.gpu_util import gpu_3pcf, gpu_graph, mirror
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["warp", "group"])
+def walk_mode(request, monkeypatch):
+    """Every test of this module runs with both spoke walks of the 3pCF count:
+    one spoke per warp and four spokes per warp (read at each launch)."""
+    monkeypatch.setenv("GS_COUNT3_WALK", request.param)
+    return request.param
+
+
 def test_tiny_config():
     w = configs.TINY_3PCF
     xyz = w.points()
@@ -62,6 +70,32 @@ def test_hub_rows_longer_than_the_table():
     with gpu_graph(xyz, 300000, 0, edges) as g:
         assert g.max_degree == 2299
         assert np.array_equal(as_uint64(g.count_3pcf()), ref)
+
+
+def test_two_cliques_rows_in_two_chunks():
+    # two tight balls of a = 5200 and b = 3300 points, 30000 apart: pairs inside a
+    # ball are closer than 9000 (bin 0), pairs across are 22000..38000 apart (bin 1).
+    # Every pair is an edge, so the first hubs' forward rows hold more than 8192
+    # keys and run in two chunks. Triangles: C(a,3) + C(b,3) of sides (0, 0, 0) and
+    # C(a,2) b + C(b,2) a of sides (0, 1, 1).
+    rng = np.random.default_rng(11)
+    a, b = 5200, 3300
+
+    def ball(m, centre):
+        v = rng.normal(size=(m, 3))
+        v *= 4000 * rng.uniform(0, 1, size=(m, 1)) ** (1 / 3) / np.linalg.norm(v, axis=1, keepdims=True)
+        return (v + centre).astype(np.int32)
+
+    xyz = np.concatenate([ball(a, 100000), ball(b, [130000, 100000, 100000])])
+    xyz = xyz[rng.permutation(len(xyz))]
+    edges = [0, 9000, 40000]
+    with gpu_graph(xyz, 300000, 0, edges) as g:
+        assert g.max_degree == a + b - 1
+        hist = as_uint64(g.count_3pcf())
+    c3 = lambda m: m * (m - 1) * (m - 2) // 6
+    expect = {(0, 0, 0): c3(a) + c3(b), (0, 1, 1): a * (a - 1) // 2 * b + b * (b - 1) // 2 * a}
+    cfg = fx.configs3(2)
+    assert {cfg[k]: int(v) for k, v in enumerate(hist) if v} == expect
 
 
 def test_many_bins_global_histogram():
