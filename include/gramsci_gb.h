@@ -101,6 +101,10 @@ gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_t box_lu, i
  *               Each triangle is counted at its lowest internal index, so the
  *               histograms of disjoint ranges that cover [0, n) sum exactly
  *               to the full one.
+ * A device-resident graph with mean degree <= 1024 is walked four spokes per
+ * warp, a longer-rowed or windowed one a spoke per warp; the environment
+ * variable GS_COUNT3_WALK = "warp" or "group" overrides the choice (read at
+ * each call). The histogram is the same either way.
  * Errors: GS_ERR_ARG (NULL pointers, range outside [0, n]), GS_ERR_CUDA. */
 gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int64_t hub_end,
                         void *cuda_stream);
