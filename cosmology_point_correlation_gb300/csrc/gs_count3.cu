@@ -440,153 +440,152 @@ k_count3(C3Args a)
                     __syncthreads();
                     c3_walk_grouped(a, F, FB, sb, ns, c0, kfirst, kmax, span, bmode, shift, mask,
                                     s_bm, s_rank, s_cbin, s_key, s_bin, s_hist, s_full, &s_next);
+                } else {
+                    // counting sort of the spokes by b_ij, so that a warp's spokes
+                    // share their bin and its configuration table changes rarely
+                    for (int t = threadIdx.x; t <= nb; t += C3_THREADS) s_bucket[t] = 0;
                     __syncthreads();
-                    continue;
-                }
-                // counting sort of the spokes by b_ij, so that a warp's spokes
-                // share their bin and its configuration table changes rarely
-                for (int t = threadIdx.x; t <= nb; t += C3_THREADS) s_bucket[t] = 0;
-                __syncthreads();
-                for (int t = threadIdx.x; t < ns; t += C3_THREADS) atomicAdd(&s_bucket[FB[sb + t] + 1], 1);
-                __syncthreads();
-                if (warp == 0) {
-                    int carry = 0;
-                    for (int b0 = 0; b0 <= nb; b0 += 32) {
-                        const int v = b0 + lane <= nb ? s_bucket[b0 + lane] : 0;
-                        int x = v;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const int y = __shfl_up_sync(0xffffffffu, x, o);
-                            if (lane >= o) x += y;
+                    for (int t = threadIdx.x; t < ns; t += C3_THREADS) atomicAdd(&s_bucket[FB[sb + t] + 1], 1);
+                    __syncthreads();
+                    if (warp == 0) {
+                        int carry = 0;
+                        for (int b0 = 0; b0 <= nb; b0 += 32) {
+                            const int v = b0 + lane <= nb ? s_bucket[b0 + lane] : 0;
+                            int x = v;
+    #pragma unroll
+                            for (int o = 1; o < 32; o <<= 1) {
+                                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                                if (lane >= o) x += y;
+                            }
+                            if (b0 + lane <= nb) s_bucket[b0 + lane] = carry + x;   // inclusive: bucket b starts at s_bucket[b]
+                            carry += __shfl_sync(0xffffffffu, x, 31);
                         }
-                        if (b0 + lane <= nb) s_bucket[b0 + lane] = carry + x;   // inclusive: bucket b starts at s_bucket[b]
-                        carry += __shfl_sync(0xffffffffu, x, 31);
                     }
-                }
-                __syncthreads();
-                for (int t = threadIdx.x; t < ns; t += C3_THREADS) {
-                    const int b = FB[sb + t];
-                    s_order[atomicAdd(&s_bucket[b], 1)] = (uint16_t)t;
-                }
-                if (threadIdx.x == 0) s_next = 0;
-                __syncthreads();
+                    __syncthreads();
+                    for (int t = threadIdx.x; t < ns; t += C3_THREADS) {
+                        const int b = FB[sb + t];
+                        s_order[atomicAdd(&s_bucket[b], 1)] = (uint16_t)t;
+                    }
+                    if (threadIdx.x == 0) s_next = 0;
+                    __syncthreads();
 
-                for (;;) {
-                    int li = 0;
-                    if (lane == 0) li = atomicAdd(&s_next, 1);
-                    li = __shfl_sync(0xffffffffu, li, 0);
-                    if (li >= ns) break;
-                    const int s = sb + s_order[li];
-                    const int32_t j = F[s];
-                    const int bij = FB[s];
-                    if (SMEM_HIST && !WEIGHTED && bij != tab_z) {
-                        c3_fill_tab(tab, a.cfg3, nb, bij);
-                        tab_z = bij;
-                    }
-                    const int64_t pe = a.row_ptr[j + 1];
-                    int64_t p0;
-                    if (s + 1 >= c0) {
-                        p0 = a.row_ptr[j] + a.fwd[j];                  // first entry > j
-                    } else {
-                        // first entry >= kfirst in N(j) (lower bound; only for later chunks)
-                        int64_t lo = a.row_ptr[j] + a.fwd[j], hi = pe;
-                        while (lo < hi) {
-                            const int64_t mid = (lo + hi) >> 1;
-                            if (a.snbr[mid - (WINDOWED ? a.soff : 0)] < kfirst) lo = mid + 1; else hi = mid;
+                    for (;;) {
+                        int li = 0;
+                        if (lane == 0) li = atomicAdd(&s_next, 1);
+                        li = __shfl_sync(0xffffffffu, li, 0);
+                        if (li >= ns) break;
+                        const int s = sb + s_order[li];
+                        const int32_t j = F[s];
+                        const int bij = FB[s];
+                        if (SMEM_HIST && !WEIGHTED && bij != tab_z) {
+                            c3_fill_tab(tab, a.cfg3, nb, bij);
+                            tab_z = bij;
                         }
-                        p0 = lo;
-                    }
-                    if (p0 >= pe) continue;
-                    const int wj = WEIGHTED ? (int)a.w[j] : 0;
-                    // one triangle with sides (b_ij, b_ik, b_jk) and third vertex weight wk
-                    auto hit = [&](int bik, int bjk, int wk) {
-                        if (WEIGHTED) {
-                            // T[c] += w_j w_k (|.| <= 2^30) as a 64-bit integer held in two
-                            // 32-bit words: add to the low word, then the carry out of it
-                            // plus the sign extension to the high word (zero, and skipped,
-                            // for most adds)
-                            unsigned *q = reinterpret_cast<unsigned *>(s_T + c3_index(bij, bik, bjk, s_lex_a, s_lex_b));
-                            const int p = wj * wk;
-                            const unsigned old = atomicAdd(q, (unsigned)p);
-                            const unsigned up = (old + (unsigned)p < old ? 1u : 0u) + (p < 0 ? ~0u : 0u);
-                            if (up) atomicAdd(q + 1, up);
-                        }
-                        else if (SMEM_HIST) atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
-                        else atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
-                    };
-                    // Walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
-                    // 4l .. 4l+3 of the step as one int4 and their bins as one word.
-                    const int64_t pa = p0 & ~(int64_t)3;
-                    const int head = (int)(p0 - pa);
-                    const int total = head + (int)(pe - p0);
-                    const int64_t soff = WINDOWED ? a.soff : 0;
-                    const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + lane;
-                    const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + lane;
-                    int4 kk = __ldg(vk);                            // step 0, then prefetch
-                    uint32_t bb = __ldg(vb);
-                    for (int base = 0; base < total; base += 128) {
-                        vk += 32;
-                        vb += 32;
-                        int4 kn = kk;
-                        uint32_t bn = bb;
-                        if (base + 128 < total) {                  // next step in flight
-                            kn = __ldg(vk);
-                            bn = __ldg(vb);
-                        }
-                        unsigned vmask = 0xfu;
-                        if (base == 0 || base + 128 > total) {     // first / last step only
-                            const int r0 = base + 4 * lane;
-                            if (head > r0) vmask &= (0xfu << min(head - r0, 4)) & 0xfu;
-                            if (total - r0 < 4) vmask &= (1u << max(total - r0, 0)) - 1u;
-                        }
-                        const int k[4] = { kk.x, kk.y, kk.z, kk.w };
-                        if (bmode) {
-                            // entries outside [p0, pe) (first and last step) become kfirst - 1;
-                            // every offset outside [0, span) clamps to the zero guard bit at span
-                            int kv[4] = { k[0], k[1], k[2], k[3] };
-                            if (vmask != 0xfu) {
-#pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    if (!((vmask >> e) & 1u)) kv[e] = kfirst - 1;
-                            }
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const unsigned o = min((unsigned)(kv[e] - kfirst), (unsigned)span);
-                                const unsigned w = s_bm[o >> 5];
-                                if ((w >> (o & 31u)) & 1u) {
-                                    const int rank = s_rank[o >> 5] + __popc(w & ((1u << (o & 31u)) - 1u));
-                                    hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
-                                }
-                            }
+                        const int64_t pe = a.row_ptr[j + 1];
+                        int64_t p0;
+                        if (s + 1 >= c0) {
+                            p0 = a.row_ptr[j] + a.fwd[j];                  // first entry > j
                         } else {
-                            uint32_t h[4];
-                            int32_t key[4];
-                            unsigned pend = 0;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {          // first probes, all in flight
-                                h[e] = gs_hash(k[e], shift);
-                                key[e] = s_key[h[e]];
+                            // first entry >= kfirst in N(j) (lower bound; only for later chunks)
+                            int64_t lo = a.row_ptr[j] + a.fwd[j], hi = pe;
+                            while (lo < hi) {
+                                const int64_t mid = (lo + hi) >> 1;
+                                if (a.snbr[mid - (WINDOWED ? a.soff : 0)] < kfirst) lo = mid + 1; else hi = mid;
                             }
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) pend |= (unsigned)(key[e] != k[e] && key[e] != C3_EMPTY) << e;
-                            while (pend) {                         // collisions
-#pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    if ((pend >> e) & 1u) {
-                                        h[e] = (h[e] + 1) & mask;
-                                        key[e] = s_key[h[e]];
-                                        if (key[e] == k[e] || key[e] == C3_EMPTY) pend &= ~(1u << e);
-                                    }
-                            }
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (((vmask >> e) & 1u) && key[e] == k[e])
-                                    hit(s_bin[h[e]], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_hw[h[e]] : 0);
+                            p0 = lo;
                         }
-                        // rows are sorted: stop once the step's last key passes kmax
-                        if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
-                        kk = kn;
-                        bb = bn;
+                        if (p0 >= pe) continue;
+                        const int wj = WEIGHTED ? (int)a.w[j] : 0;
+                        // one triangle with sides (b_ij, b_ik, b_jk) and third vertex weight wk
+                        auto hit = [&](int bik, int bjk, int wk) {
+                            if (WEIGHTED) {
+                                // T[c] += w_j w_k (|.| <= 2^30) as a 64-bit integer held in two
+                                // 32-bit words: add to the low word, then the carry out of it
+                                // plus the sign extension to the high word (zero, and skipped,
+                                // for most adds)
+                                unsigned *q = reinterpret_cast<unsigned *>(s_T + c3_index(bij, bik, bjk, s_lex_a, s_lex_b));
+                                const int p = wj * wk;
+                                const unsigned old = atomicAdd(q, (unsigned)p);
+                                const unsigned up = (old + (unsigned)p < old ? 1u : 0u) + (p < 0 ? ~0u : 0u);
+                                if (up) atomicAdd(q + 1, up);
+                            }
+                            else if (SMEM_HIST) atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
+                            else atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
+                        };
+                        // Walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
+                        // 4l .. 4l+3 of the step as one int4 and their bins as one word.
+                        const int64_t pa = p0 & ~(int64_t)3;
+                        const int head = (int)(p0 - pa);
+                        const int total = head + (int)(pe - p0);
+                        const int64_t soff = WINDOWED ? a.soff : 0;
+                        const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + lane;
+                        const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + lane;
+                        int4 kk = __ldg(vk);                            // step 0, then prefetch
+                        uint32_t bb = __ldg(vb);
+                        for (int base = 0; base < total; base += 128) {
+                            vk += 32;
+                            vb += 32;
+                            int4 kn = kk;
+                            uint32_t bn = bb;
+                            if (base + 128 < total) {                  // next step in flight
+                                kn = __ldg(vk);
+                                bn = __ldg(vb);
+                            }
+                            unsigned vmask = 0xfu;
+                            if (base == 0 || base + 128 > total) {     // first / last step only
+                                const int r0 = base + 4 * lane;
+                                if (head > r0) vmask &= (0xfu << min(head - r0, 4)) & 0xfu;
+                                if (total - r0 < 4) vmask &= (1u << max(total - r0, 0)) - 1u;
+                            }
+                            const int k[4] = { kk.x, kk.y, kk.z, kk.w };
+                            if (bmode) {
+                                // entries outside [p0, pe) (first and last step) become kfirst - 1;
+                                // every offset outside [0, span) clamps to the zero guard bit at span
+                                int kv[4] = { k[0], k[1], k[2], k[3] };
+                                if (vmask != 0xfu) {
+    #pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (!((vmask >> e) & 1u)) kv[e] = kfirst - 1;
+                                }
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const unsigned o = min((unsigned)(kv[e] - kfirst), (unsigned)span);
+                                    const unsigned w = s_bm[o >> 5];
+                                    if ((w >> (o & 31u)) & 1u) {
+                                        const int rank = s_rank[o >> 5] + __popc(w & ((1u << (o & 31u)) - 1u));
+                                        hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
+                                    }
+                                }
+                            } else {
+                                uint32_t h[4];
+                                int32_t key[4];
+                                unsigned pend = 0;
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) {          // first probes, all in flight
+                                    h[e] = gs_hash(k[e], shift);
+                                    key[e] = s_key[h[e]];
+                                }
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) pend |= (unsigned)(key[e] != k[e] && key[e] != C3_EMPTY) << e;
+                                while (pend) {                         // collisions
+    #pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if ((pend >> e) & 1u) {
+                                            h[e] = (h[e] + 1) & mask;
+                                            key[e] = s_key[h[e]];
+                                            if (key[e] == k[e] || key[e] == C3_EMPTY) pend &= ~(1u << e);
+                                        }
+                                }
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (((vmask >> e) & 1u) && key[e] == k[e])
+                                        hit(s_bin[h[e]], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_hw[h[e]] : 0);
+                            }
+                            // rows are sorted: stop once the step's last key passes kmax
+                            if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
+                            kk = kn;
+                            bb = bn;
+                        }
                     }
                 }
                 __syncthreads();
@@ -680,8 +679,14 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
                                      sizeof(uint16_t) * (size_t)nb2 * g->nb;
                 auto kg = k_count3<true, false, false, false, true>;
                 int per = 0;
-                GS_TRY_CUDA(cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_g));
-                GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kg, C3_THREADS, dyn_g));
+                // a table too large for one block (nb near 40) is refused here:
+                // then the one-spoke walk runs, and the refusal is cleared
+                cudaError_t ea = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_g);
+                if (ea == cudaSuccess) ea = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kg, C3_THREADS, dyn_g);
+                if (ea != cudaSuccess) {
+                    cudaGetLastError();
+                    per = 0;
+                }
                 if (per >= 2 || (mode == 1 && per >= 1)) {
                     kern = kg;
                     dyn = dyn_g;

@@ -98,6 +98,19 @@ def test_two_cliques_rows_in_two_chunks():
     assert {cfg[k]: int(v) for k, v in enumerate(hist) if v} == expect
 
 
+@pytest.mark.parametrize("nbins", [39, 40])
+def test_most_bins_with_a_shared_histogram(nbins):
+    # 39 and 40 bins: the largest histograms kept in shared memory. With short
+    # rows the four-spoke walk is chosen, but its nb^3 table fits one block
+    # only up to 39 bins; at 40 the count keeps the one-spoke walk
+    box = catalogues.box_lattice(60.0)
+    xyz = catalogues.uniform(3000, 60.0, 9)
+    edges = catalogues.linear_edges_lu(12.0, nbins)
+    ref = oracle.count_3pcf(xyz, box, 1, edges)
+    assert ref.sum() > 0
+    assert np.array_equal(gpu_3pcf(xyz, box, 1, edges), ref)
+
+
 def test_many_bins_global_histogram():
     # C(62,3) = 37820 configurations: histogram too large for shared memory
     box = catalogues.box_lattice(60.0)
