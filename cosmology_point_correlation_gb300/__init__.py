@@ -180,7 +180,11 @@ class Graph:
         return even, odd
 
     def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
-        """uint64 triangle histogram over sorted bin triples (int64 tensor on the device)."""
+        """uint64 triangle histogram over sorted bin triples (int64 tensor on the device).
+
+        The library walks one spoke per warp on long rows and four per warp on
+        short ones (mean degree <= 1024); the environment variable
+        GS_COUNT3_WALK = "warp" or "group" fixes the walk. Results are identical."""
         torch = _torch()
         hub_end = self.n if hub_end is None else hub_end
         m = config_count_3pcf(self.nbins)
