@@ -34,8 +34,11 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gs_oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+# GS_ORACLE_SRC / GS_ORACLE_LIB point the wrapper at another copy of the C
+# source and library. Only tests/test_oracle_mutants.py sets them, to run the
+# pins against copies with a planted mistake.
+_SRC = os.environ.get("GS_ORACLE_SRC") or os.path.join(_HERE, "gs_oracle.c")
+_LIB = os.environ.get("GS_ORACLE_LIB") or os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 _i64 = ctypes.c_int64
