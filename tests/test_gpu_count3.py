@@ -111,6 +111,37 @@ def test_most_bins_with_a_shared_histogram(nbins):
     assert np.array_equal(gpu_3pcf(xyz, box, 1, edges), ref)
 
 
+def test_hubs_whose_rows_wrap_the_box():
+    # 400k uniform points in a periodic box, the input put in the graph's own
+    # (cell) order, so that hub ranges mean the same to the oracle. The first
+    # hubs lie in the first slab of cells; their forward neighbours include
+    # points of the last slab across the periodic wrap, so their forward keys
+    # span more than 2^18 ids and run as hash-table chunks. Hubs [0, 1000) are
+    # counted against the oracle's hub loop over the same range (rows of those
+    # hubs only, by brute force).
+    import oracle as orc
+    box = catalogues.box_lattice(1000.0)
+    xyz = catalogues.uniform(400_000, 1000.0, 12)
+    edges = catalogues.linear_edges_lu(30.0, 10)
+    with gpu_graph(xyz, box, 1, edges) as g:
+        perm = g.export_perm().cpu().numpy()
+    xyz = np.ascontiguousarray(xyz[perm])
+    hubs = 1000
+    rows = [orc.row(xyz, box, 1, edges, i) for i in range(hubs)]
+    spans = [int(r[r > i].max() - r[r > i].min() + 1) for i, (r, _) in enumerate(rows) if (r > i).sum() > 1]
+    assert max(spans) > 1 << 18                       # hash-table chunks are exercised
+    row_ptr = np.zeros(len(xyz) + 1, dtype=np.int64)
+    row_ptr[1:hubs + 1] = np.cumsum([len(r) for r, _ in rows])
+    row_ptr[hubs + 1:] = row_ptr[hubs]
+    part = orc.Graph(row_ptr, np.concatenate([r for r, _ in rows]).astype(np.int32),
+                     np.concatenate([b for _, b in rows]).astype(np.uint8))
+    ref = orc.count_3pcf(xyz, box, 1, edges, g=part, hub_begin=0, hub_end=hubs)
+    assert ref.sum() > 0
+    with gpu_graph(xyz, box, 1, edges) as g:
+        assert np.array_equal(g.export_perm().cpu().numpy(), np.arange(len(xyz)))
+        assert np.array_equal(as_uint64(g.count_3pcf(0, hubs)), ref)
+
+
 def test_many_bins_global_histogram():
     # C(62,3) = 37820 configurations: histogram too large for shared memory
     box = catalogues.box_lattice(60.0)
