@@ -27,7 +27,8 @@ __all__ = ["Graph", "GramsciError", "build_graph", "count_3pcf_from_host",
            "count_4pcf_parity_from_host", "config_count_3pcf", "config_count_4pcf",
            "config_index_3pcf", "config_index_4pcf", "as_uint64", "library_path", "kernel_launches",
            "equilateral", "isosceles", "xi_natural", "config_tuples_4pcf6", "zeta4_disconnected",
-           "as_int128", "xi_signed", "zeta4_connected"]
+           "as_int128", "xi_signed", "zeta4_connected", "measure_smem_atomics",
+           "quantize_weights", "WEIGHT_SCALE"]
 
 
 def library_path() -> str:
@@ -37,6 +38,16 @@ def library_path() -> str:
 def kernel_launches() -> int:
     """Kernels the library has launched in this process."""
     return int(_lib.load().gs_kernel_launches())
+
+
+def measure_smem_atomics(ncfg: int, pattern: int = 0, lanes_active: int = 32, stream=None) -> float:
+    """Lane-adds per second the device retires when its SMs do nothing but
+    shared-memory atomic adds into a histogram of ncfg 32-bit counters
+    (pattern 0: random counters, 1: one bank per lane, 2: one counter)."""
+    v = ctypes.c_double()
+    _lib.check(_lib.load().gs_measure_smem_atomics(int(ncfg), int(pattern), int(lanes_active),
+                                                   ctypes.byref(v), _stream(stream)))
+    return v.value
 
 
 def _torch():
@@ -60,6 +71,22 @@ def _edges(edges_lu):
 def as_uint64(t) -> np.ndarray:
     """Host NumPy uint64 view of a histogram tensor."""
     return t.detach().cpu().numpy().view(np.uint64)
+
+
+WEIGHT_SCALE = 32767
+
+
+def quantize_weights(w) -> np.ndarray:
+    """int16 fixed-point weights for set_weights from real weights |w| <= 1:
+    q = round(WEIGHT_SCALE w). Each weight moves by at most 1/(2 WEIGHT_SCALE),
+    so a product of k weights (a pair, triangle or tetrahedron term) moves by
+    at most k/(2 WEIGHT_SCALE), and a weighted sum over n terms, divided by
+    WEIGHT_SCALE^k, is within n k/(2 WEIGHT_SCALE) of the sum of the real
+    weights' products. Weights of larger modulus must be rescaled first."""
+    w = np.asarray(w, dtype=np.float64)
+    if not np.all(np.isfinite(w)) or np.any(np.abs(w) > 1.0):
+        raise ValueError("weights must be finite with |w| <= 1 (rescale them first)")
+    return np.rint(w * WEIGHT_SCALE).astype(np.int16)
 
 
 def as_int128(t) -> list:
@@ -123,6 +150,18 @@ class Graph:
         _lib.check(_lib.load().gs_graph_stats(self._h, ctypes.byref(st), _stream(stream)))
         return {name: getattr(st, name) for name, _ in _lib.GraphStats._fields_ if name != "reserved"}
 
+    def hub_work(self, stream=None):
+        """(f int32 [n], w int64 [n]) per hub in internal order: the forward degree
+        and the spoke-row entries of the hub's 3pCF merge-walks (sum of f_j over
+        its forward spokes j)."""
+        torch = _torch()
+        n = self.n
+        f = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
+        w = torch.empty(max(n, 1), dtype=torch.int64, device=self.device)
+        _lib.check(_lib.load().gs_graph_hub_work(self._h, ctypes.c_void_p(f.data_ptr()),
+                                                 ctypes.c_void_p(w.data_ptr()), _stream(stream)))
+        return f[:n], w[:n]
+
     # -- counts
     def count_2pcf(self, out=None, stream=None):
         """Unordered pairs per radial bin (uint64 bits in an int64 tensor)."""
@@ -179,12 +218,17 @@ class Graph:
                                                        int(hub_end), _stream(stream)))
         return even, odd
 
+    @property
+    def count3_walk(self) -> str:
+        """The spoke walk count_3pcf takes on this graph: "map", "mapgroup", "group" or "warp"."""
+        return {3: "mapgroup", 2: "map", 1: "group", 0: "warp"}.get(_lib.load().gs_count3_walk(self._h), "?")
+
     def count_3pcf(self, hub_begin: int = 0, hub_end: int | None = None, out=None, stream=None):
         """uint64 triangle histogram over sorted bin triples (int64 tensor on the device).
 
-        The library walks one spoke per warp on long rows and four per warp on
-        short ones (mean degree <= 1024); the environment variable
-        GS_COUNT3_WALK = "warp" or "group" fixes the walk. Results are identical."""
+        The library picks the spoke walk from the graph (count3_walk); the
+        environment variable GS_COUNT3_WALK = "map", "mapgroup", "group" or
+        "warp" fixes it. Results are identical."""
         torch = _torch()
         hub_end = self.n if hub_end is None else hub_end
         m = config_count_3pcf(self.nbins)

@@ -24,6 +24,7 @@ SIGNATURES = {
     "gs_build_graph_windowed": (_int, [_p, _i64, _i64, _int, _i64, _p, _int, _i64, _p, ctypes.POINTER(_p)]),
     "gs_graph_windows": (_int, [_p, ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "gs_count_3pcf": (_int, [_p, _p, _i64, _i64, _p]),
+    "gs_count3_walk": (_int, [_p]),
     "gs_count_4pcf_parity": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_count_4pcf_parity_static": (_int, [_p, _p, _p, _i64, _i64, _p]),
     "gs_count_3pcf_hubs": (_int, [_p, _p, _i64, _p, _p]),
@@ -40,6 +41,7 @@ SIGNATURES = {
     "gs_graph_info": (_int, [_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i32)]),
     "gs_graph_export_csr": (_int, [_p, _p, _p, _p, _p]),
     "gs_graph_export_perm": (_int, [_p, _p, _p]),
+    "gs_graph_hub_work": (_int, [_p, _p, _p, _p]),
     "gs_config_count_3pcf": (_i64, [_int]),
     "gs_config_count_4pcf": (_i64, [_int]),
     "gs_config_index_3pcf": (_i64, [_int, _int, _int, _int]),
@@ -61,6 +63,8 @@ class GraphStats(ctypes.Structure):
 
 SIGNATURES["gs_graph_stats"] = (_int, [_p, ctypes.POINTER(GraphStats), _p])
 SIGNATURES["gs_kernel_launches"] = (ctypes.c_uint64, [])
+SIGNATURES["gs_alloc_calls"] = (ctypes.c_uint64, [])
+SIGNATURES["gs_measure_smem_atomics"] = (_int, [_int, _int, _int, ctypes.POINTER(ctypes.c_double), _p])
 
 _lib = None
 

@@ -38,7 +38,7 @@ static gs_status build_from_host(const int32_t *coords_host, int64_t n, int64_t 
     if (n > 0 && !coords_host) return gs_set_error(GS_ERR_ARG, "coords_host is NULL");
     int32_t *d = nullptr;
     if (n > 0) {
-        GS_TRY_CUDA(cudaMallocAsync(&d, sizeof(int32_t) * 3 * n, st));
+        GS_TRY_CUDA(gs_malloc_async(&d, sizeof(int32_t) * 3 * n, st));
         cudaError_t e = cudaMemcpyAsync(d, coords_host, sizeof(int32_t) * 3 * n, cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) {
             cudaFreeAsync(d, st);
@@ -54,7 +54,7 @@ extern "C" gs_status gs_3pcf_from_host(const int32_t *coords_host, int64_t n, in
                                        int64_t r_max_lu, const int64_t *edges_lu, int nbins,
                                        uint64_t *hist_host, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!hist_host) return gs_set_error(GS_ERR_ARG, "hist_host is NULL");
     cudaStream_t st = (cudaStream_t)cuda_stream;
     gs_graph_t g = nullptr;
@@ -62,7 +62,7 @@ extern "C" gs_status gs_3pcf_from_host(const int32_t *coords_host, int64_t n, in
     if (s != GS_OK) return s;
     const int64_t ncfg = gs_ncfg3(nbins);
     uint64_t *h = nullptr;
-    cudaError_t e = cudaMallocAsync(&h, sizeof(uint64_t) * ncfg, st);
+    cudaError_t e = gs_malloc_async(&h, sizeof(uint64_t) * ncfg, st);
     if (e != cudaSuccess) {
         gs_graph_free(g);
         return gs_set_error(GS_ERR_NOMEM, "histogram allocation failed: %s", cudaGetErrorString(e));
@@ -83,7 +83,7 @@ extern "C" gs_status gs_4pcf_parity_from_host(const int32_t *coords_host, int64_
                                               int nbins, uint64_t *even_host, int64_t *odd_host,
                                               void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     const int64_t ncfg = nbins >= 3 && nbins <= 255 ? gs_ncfg4(nbins) : 0;
     if (ncfg > 0 && (!even_host || !odd_host)) return gs_set_error(GS_ERR_ARG, "NULL histogram");
     cudaStream_t st = (cudaStream_t)cuda_stream;
@@ -96,8 +96,8 @@ extern "C" gs_status gs_4pcf_parity_from_host(const int32_t *coords_host, int64_
     }
     uint64_t *ev = nullptr;
     int64_t *od = nullptr;
-    cudaError_t e = cudaMallocAsync(&ev, sizeof(uint64_t) * ncfg, st);
-    if (e == cudaSuccess) e = cudaMallocAsync(&od, sizeof(int64_t) * ncfg, st);
+    cudaError_t e = gs_malloc_async(&ev, sizeof(uint64_t) * ncfg, st);
+    if (e == cudaSuccess) e = gs_malloc_async(&od, sizeof(int64_t) * ncfg, st);
     if (e != cudaSuccess) {
         if (ev) cudaFreeAsync(ev, st);
         gs_graph_free(g);

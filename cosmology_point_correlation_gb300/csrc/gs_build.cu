@@ -32,9 +32,32 @@ gs_status gs_set_error(gs_status s, const char *fmt, ...)
     return s;
 }
 
-void gs_clear_error() { g_msg[0] = 0; }
-
 extern "C" const char *gs_last_error(void) { return g_msg; }
+
+static thread_local int t_depth = 0;                 // public calls in progress on this thread
+static thread_local int64_t t_alloc_ordinal = 0;     // allocations since the outermost one began
+static std::atomic<uint64_t> g_allocs{ 0 };
+
+gs_call_scope::gs_call_scope()
+{
+    if (t_depth++ == 0) {
+        g_msg[0] = 0;
+        t_alloc_ordinal = 0;
+    }
+}
+
+gs_call_scope::~gs_call_scope() { --t_depth; }
+
+cudaError_t gs_alloc_gate()
+{
+    g_allocs.fetch_add(1, std::memory_order_relaxed);
+    const int64_t k = ++t_alloc_ordinal;
+    const char *env = getenv("GS_FAULT");
+    if (env && !strncmp(env, "alloc:", 6) && atoll(env + 6) == k) return cudaErrorMemoryAllocation;
+    return cudaSuccess;
+}
+
+extern "C" uint64_t gs_alloc_calls(void) { return g_allocs.load(); }
 
 static std::atomic<uint64_t> g_launches{ 0 };
 
@@ -163,7 +186,7 @@ static gs_status scan_impl(const int32_t *in, Tout *out, int64_t n, cudaStream_t
     }
     const int64_t ntiles = (n + SCAN_TILE - 1) / SCAN_TILE;
     Tout *sums = nullptr;
-    GS_TRY_CUDA(cudaMallocAsync(&sums, sizeof(Tout) * ntiles, st));
+    GS_TRY_CUDA(gs_malloc_async(&sums, sizeof(Tout) * ntiles, st));
     k_scan_tiles<Tout><<<(unsigned)ntiles, SCAN_THREADS, 0, st>>>(in, out, sums, n);
     gs_note_launch();
     k_scan_sums<Tout><<<1, SCAN_THREADS, 0, st>>>(sums, ntiles, out + n);
@@ -566,7 +589,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
                             int64_t r_max_lu, const int64_t *edges_lu, int nbins, int64_t window_edges,
                             void *cuda_stream, gs_graph_t *out)
 {
-    gs_clear_error();
+    GS_ENTRY();
     gs_status s = validate_build(coords_dev, n, box_lu, periodic, r_max_lu, edges_lu, nbins, out);
     if (s != GS_OK) return s;
     if (window_edges < 0) return gs_set_error(GS_ERR_ARG, "window_edges < 0");
@@ -604,12 +627,12 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
 
     {
         const size_t nn = (size_t)std::max<int64_t>(n, 1);
-        GS_BUILD_CUDA(cudaMalloc(&g->pts, sizeof(int4) * nn));
-        GS_BUILD_CUDA(cudaMalloc(&g->inv, sizeof(int32_t) * nn));
-        GS_BUILD_CUDA(cudaMalloc(&g->row_ptr, sizeof(int64_t) * (nn + 1)));
-        GS_BUILD_CUDA(cudaMalloc(&g->fwd, sizeof(int32_t) * nn));
-        GS_BUILD_CUDA(cudaMalloc(&g->work, sizeof(unsigned long long) * 4));
-        GS_BUILD_CUDA(cudaMalloc(&g->err, sizeof(int32_t)));
+        GS_BUILD_CUDA(gs_malloc(&g->pts, sizeof(int4) * nn));
+        GS_BUILD_CUDA(gs_malloc(&g->inv, sizeof(int32_t) * nn));
+        GS_BUILD_CUDA(gs_malloc(&g->row_ptr, sizeof(int64_t) * (nn + 1)));
+        GS_BUILD_CUDA(gs_malloc(&g->fwd, sizeof(int32_t) * nn));
+        GS_BUILD_CUDA(gs_malloc(&g->work, sizeof(unsigned long long) * 4));
+        GS_BUILD_CUDA(gs_malloc(&g->err, sizeof(int32_t)));
         if (nbins <= 40) {
             // configuration index of every (z, x, y) bin triple, for the 3pCF kernel
             std::vector<uint16_t> h((size_t)nbins * nbins * nbins);
@@ -620,18 +643,18 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
                         std::sort(v, v + 3);
                         h[((size_t)z * nbins + x) * nbins + y] = (uint16_t)gs_idx3(nbins, v[0], v[1], v[2]);
                     }
-            GS_BUILD_CUDA(cudaMalloc(&g->cfg3, sizeof(uint16_t) * h.size()));
+            GS_BUILD_CUDA(gs_malloc(&g->cfg3, sizeof(uint16_t) * h.size()));
             GS_BUILD_CUDA(cudaMemcpy(g->cfg3, h.data(), sizeof(uint16_t) * h.size(), cudaMemcpyHostToDevice));
         }
-        GS_BUILD_CUDA(cudaMallocAsync(&cell, sizeof(int32_t) * nn, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&slot, sizeof(int32_t) * nn, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&tmp, sizeof(int32_t) * nn, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&perm, sizeof(int32_t) * nn, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&deg, sizeof(int32_t) * nn, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&cell_count, sizeof(int32_t) * ncells, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&cell_start, sizeof(int32_t) * (ncells + 1), st));
-        GS_BUILD_CUDA(cudaMallocAsync(&esq, sizeof(long long) * 256, st));
-        GS_BUILD_CUDA(cudaMallocAsync(&maxd, 2 * sizeof(unsigned), st));
+        GS_BUILD_CUDA(gs_malloc_async(&cell, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(gs_malloc_async(&slot, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(gs_malloc_async(&tmp, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(gs_malloc_async(&perm, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(gs_malloc_async(&deg, sizeof(int32_t) * nn, st));
+        GS_BUILD_CUDA(gs_malloc_async(&cell_count, sizeof(int32_t) * ncells, st));
+        GS_BUILD_CUDA(gs_malloc_async(&cell_start, sizeof(int32_t) * (ncells + 1), st));
+        GS_BUILD_CUDA(gs_malloc_async(&esq, sizeof(long long) * 256, st));
+        GS_BUILD_CUDA(gs_malloc_async(&maxd, 2 * sizeof(unsigned), st));
 
         long long hesq[256];
         for (int k = 0; k <= nbins; ++k) hesq[k] = (long long)edges_lu[k] * edges_lu[k];
@@ -682,8 +705,8 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
         const size_t ne = (size_t)(g->n_edges + GS_EDGE_PAD);
         const int64_t wedges = choose_window_edges(window_edges, g->n_edges);
         if (wedges == 0) {
-            GS_BUILD_CUDA(cudaMalloc(&g->nbr, sizeof(int32_t) * ne));
-            GS_BUILD_CUDA(cudaMalloc(&g->bin, ne));
+            GS_BUILD_CUDA(gs_malloc(&g->nbr, sizeof(int32_t) * ne));
+            GS_BUILD_CUDA(gs_malloc(&g->bin, ne));
             GS_BUILD_CUDA(cudaMemsetAsync(g->nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD, st));
             GS_BUILD_CUDA(cudaMemsetAsync(g->bin + g->n_edges, 0, GS_EDGE_PAD, st));
             if (n > 0 && g->n_edges > 0) {
@@ -705,19 +728,19 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
                                           cudaMemcpyDeviceToHost, st));
             GS_BUILD_CUDA(cudaStreamSynchronize(st));
             const std::vector<int> wc = plan_windows(g, hcs, hrp, wedges);
-            GS_BUILD_CUDA(cudaMallocHost(&g->h_nbr, sizeof(int32_t) * ne));
-            GS_BUILD_CUDA(cudaMallocHost(&g->h_bin, ne));
+            GS_BUILD_CUDA(gs_malloc_host(&g->h_nbr, sizeof(int32_t) * ne));
+            GS_BUILD_CUDA(gs_malloc_host(&g->h_bin, ne));
             memset(g->h_nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD);
             memset(g->h_bin + g->n_edges, 0, GS_EDGE_PAD);
             for (int k = 0; k < GS_SLOTS; ++k) {
-                GS_BUILD_CUDA(cudaMalloc(&g->s_nbr[k], sizeof(int32_t) * (size_t)g->win_cap));
-                GS_BUILD_CUDA(cudaMalloc(&g->s_bin[k], (size_t)g->win_cap));
+                GS_BUILD_CUDA(gs_malloc(&g->s_nbr[k], sizeof(int32_t) * (size_t)g->win_cap));
+                GS_BUILD_CUDA(gs_malloc(&g->s_bin[k], (size_t)g->win_cap));
             }
             const int nw = g->n_win;
             g->win_pair = new uint8_t[(size_t)nw * nw]();
             std::vector<unsigned> hpair((size_t)nw * nw, 0u);
-            GS_BUILD_CUDA(cudaMallocAsync(&wrow_dev, sizeof(int64_t) * (nw + 1), st));
-            GS_BUILD_CUDA(cudaMallocAsync(&pair_dev, sizeof(unsigned) * (size_t)nw * nw, st));
+            GS_BUILD_CUDA(gs_malloc_async(&wrow_dev, sizeof(int64_t) * (nw + 1), st));
+            GS_BUILD_CUDA(gs_malloc_async(&pair_dev, sizeof(unsigned) * (size_t)nw * nw, st));
             GS_BUILD_CUDA(cudaMemcpyAsync(wrow_dev, g->win_row, sizeof(int64_t) * (nw + 1), cudaMemcpyHostToDevice, st));
             GS_BUILD_CUDA(cudaMemsetAsync(pair_dev, 0, sizeof(unsigned) * (size_t)nw * nw, st));
             for (int w = 0; w < g->n_win; ++w) {
@@ -866,7 +889,7 @@ static gs_status export_rows(gs_graph_t g, const int32_t *ids, int64_t count, in
         return GS_OK;
     }
     int32_t *deg_in = nullptr;
-    GS_TRY_CUDA(cudaMallocAsync(&deg_in, sizeof(int32_t) * count, st));
+    GS_TRY_CUDA(gs_malloc_async(&deg_in, sizeof(int32_t) * count, st));
     const int sms = gs_sm_count();
     const int grid = (int)std::min<int64_t>((count + 255) / 256, (int64_t)sms * 16);
     k_input_degrees<<<grid, 256, 0, st>>>(g->row_ptr, g->inv, ids, count, deg_in);
@@ -899,9 +922,10 @@ static gs_status export_rows(gs_graph_t g, const int32_t *ids, int64_t count, in
 extern "C" gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int32_t *nbr_dev,
                                          uint8_t *bin_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !row_ptr_dev || (g->n_edges > 0 && (!nbr_dev || !bin_dev)))
         return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     return export_rows(g, nullptr, g->n, row_ptr_dev, nbr_dev, bin_dev, (cudaStream_t)cuda_stream);
 }
 
@@ -909,9 +933,10 @@ extern "C" gs_status gs_graph_export_rows(gs_graph_t g, const int32_t *ids_dev, 
                                           int64_t *row_ptr_dev, int32_t *nbr_dev, uint8_t *bin_dev,
                                           void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !row_ptr_dev || (count > 0 && !ids_dev) || (nbr_dev && !bin_dev))
         return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (count < 0) return gs_set_error(GS_ERR_ARG, "negative row count");
     cudaStream_t st = (cudaStream_t)cuda_stream;
     gs_status s = gs_check_ids(g, ids_dev, count, st);
@@ -928,8 +953,9 @@ __global__ void k_perm(const int4 *__restrict__ pts, int64_t n, int32_t *__restr
 
 extern "C" gs_status gs_graph_export_perm(gs_graph_t g, int32_t *perm_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || (g->n > 0 && !perm_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (g->n == 0) return GS_OK;
     cudaStream_t st = (cudaStream_t)cuda_stream;
     const int grid = (int)std::min<int64_t>((g->n + 255) / 256, (int64_t)gs_sm_count() * 16);
@@ -967,11 +993,12 @@ __global__ void k_graph_stats(const int64_t *__restrict__ row_ptr, const int32_t
 
 extern "C" gs_status gs_graph_stats(gs_graph_t g, gs_graph_stats_t *out, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !out) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     cudaStream_t st = (cudaStream_t)cuda_stream;
     unsigned long long *acc = nullptr, h[3] = { 0, 0, 0 };
-    GS_TRY_CUDA(cudaMallocAsync(&acc, sizeof(h), st));
+    GS_TRY_CUDA(gs_malloc_async(&acc, sizeof(h), st));
     cudaError_t e = cudaMemsetAsync(acc, 0, sizeof(h), st);
     if (e == cudaSuccess && g->n > 0) {
         const int grid = (int)std::min<int64_t>((g->n + 255) / 256, (int64_t)gs_sm_count() * 8);
@@ -994,9 +1021,70 @@ extern "C" gs_status gs_graph_stats(gs_graph_t g, gs_graph_stats_t *out, void *c
     return GS_OK;
 }
 
+// Per-hub work of the 3pCF walk, one warp per hub of [r0, r1): f_i and
+// w_i = sum over the forward spokes j of i of f_j. Row entries are read at
+// e - off (the staged window of a windowed graph, else the device CSR).
+__global__ void k_hub_work(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd,
+                           const int32_t *__restrict__ nbr, int64_t off, int64_t r0, int64_t r1,
+                           int32_t *__restrict__ f_out, int64_t *__restrict__ w_out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t i = r0 + (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < r1; i += warps) {
+        const int64_t p0 = row_ptr[i] + fwd[i], pe = row_ptr[i + 1];
+        long long s = 0;
+        for (int64_t p = p0 + lane; p < pe; p += 32) {
+            const int32_t j = nbr[p - off];
+            s += (row_ptr[j + 1] - row_ptr[j]) - fwd[j];
+        }
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+        if (lane == 0) {
+            if (f_out) f_out[i] = (int32_t)(pe - p0);
+            w_out[i] = s;
+        }
+    }
+}
+
+extern "C" gs_status gs_graph_hub_work(gs_graph_t g, int32_t *fwd_dev, int64_t *walk_dev, void *cuda_stream)
+{
+    GS_ENTRY();
+    if (!g || (g->n > 0 && !walk_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    gs_status s = gs_check_device(g);
+    if (s != GS_OK || g->n == 0) return s;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const int grid = (int)std::min<int64_t>((g->n + 7) / 8, (int64_t)gs_sm_count() * 8);
+    if (g->n_win == 0) {
+        k_hub_work<<<grid, 256, 0, st>>>(g->row_ptr, g->fwd, g->nbr, 0, 0, g->n, fwd_dev, walk_dev);
+        gs_note_launch();
+        GS_TRY_CUDA(cudaGetLastError());
+        return GS_OK;
+    }
+    // windowed: stage each window's rows in turn; the spokes' degrees are on the device
+    for (int w = 0; w < g->n_win; ++w) {
+        if (g->win_row[w + 1] == g->win_row[w]) continue;
+        int64_t off = 0;
+        s = gs_stage_window(g, w, 0, st, &off);
+        if (s != GS_OK) return s;
+        k_hub_work<<<grid, 256, 0, st>>>(g->row_ptr, g->fwd, g->s_nbr[0], off, g->win_row[w], g->win_row[w + 1],
+                                         fwd_dev, walk_dev);
+        gs_note_launch();
+        GS_TRY_CUDA(cudaGetLastError());
+    }
+    return GS_OK;
+}
+
+gs_status gs_check_device(gs_graph_t g)
+{
+    int dev = -1;
+    GS_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev != g->device)
+        return gs_set_error(GS_ERR_ARG, "the graph lives on device %d but device %d is current", g->device, dev);
+    return GS_OK;
+}
+
 extern "C" gs_status gs_graph_info(gs_graph_t g, int64_t *n, int64_t *n_edges, int32_t *max_degree)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
     if (n) *n = g->n;
     if (n_edges) *n_edges = g->n_edges;
@@ -1015,14 +1103,14 @@ extern "C" gs_status gs_build_graph_windowed(const int32_t *coords_dev, int64_t 
                                              int64_t r_max_lu, const int64_t *edges_lu, int nbins,
                                              int64_t window_edges, void *cuda_stream, gs_graph_t *out)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (window_edges < 1) return gs_set_error(GS_ERR_ARG, "window_edges must be >= 1");
     return build_impl(coords_dev, n, box_lu, periodic, r_max_lu, edges_lu, nbins, window_edges, cuda_stream, out);
 }
 
 extern "C" gs_status gs_graph_windows(gs_graph_t g, int32_t *n_windows, int64_t *window_edges_max)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
     int64_t m = 0;
     for (int w = 0; w < g->n_win; ++w) m = std::max(m, g->win_e0[w + 1] - g->win_e0[w]);

@@ -75,8 +75,9 @@ static gs_status count2_bytes(const uint8_t *bin, int64_t n, int nb, unsigned lo
 
 extern "C" gs_status gs_count_2pcf(gs_graph_t g, uint64_t *hist_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !hist_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     cudaStream_t st = (cudaStream_t)cuda_stream;
     GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * g->nb, st));
     if (g->n_edges == 0) return GS_OK;

@@ -46,6 +46,7 @@
 #include "gs_internal.cuh"
 
 constexpr int C3_THREADS = 512;
+constexpr int C3_MAX_BLOCKS_PER_SM = 2;          // __launch_bounds__ of k_count3
 constexpr int C3_WARPS = C3_THREADS / 32;
 constexpr int C3_TABLE_LOG = 13;                 // 8192 slots
 constexpr int C3_TABLE = 1 << C3_TABLE_LOG;
@@ -94,6 +95,7 @@ struct C3Args {
     // [gridDim.x][ncfg][2] (low, high)
     const int16_t *w;
     unsigned long long *gsum;
+    unsigned long long *slices;   // weighted: the caller's scratch of c3_slice_bytes() bytes
 };
 
 // Flush the shared histogram into the global one and clear it.
@@ -276,7 +278,7 @@ __device__ __forceinline__ void c3_walk_grouped(const C3Args &a, const int32_t *
 }
 
 template <bool SMEM_HIST, bool HUB_LIST, bool WEIGHTED, bool WINDOWED, bool GROUPED = false>
-__global__ void __launch_bounds__(C3_THREADS, 2)
+__global__ void __launch_bounds__(C3_THREADS, C3_MAX_BLOCKS_PER_SM)
 k_count3(C3Args a)
 {
     // dynamic: the candidate-key region [C3_REGION bytes] (bitmap mode: bitmap,
@@ -613,6 +615,381 @@ k_count3(C3Args a)
     }
 }
 
+// ---------------------------------------------------------------- byte-map walk
+//
+// The walk for long rows, one spoke per warp, with fewer instructions per
+// triangle than the bitmap-and-rank lookup of k_count3. The count is bound by
+// instruction issue: there a closed triangle costs a membership probe, a rank,
+// a bin load, a configuration-table load and the atomic. Here:
+//
+//   * the chunk's keys are held as a byte map: the key span is cut into
+//     segments of C3M_SEG ids, a segment table gives each segment that holds
+//     a key a slot of C3M_SEG bytes, and byte k of a slot is b_ik (C3M_ABSENT
+//     when k is not a key). A probe is two dependent shared loads and yields
+//     the bin together with the membership;
+//   * hits go to an unsorted histogram H[b_ij][b_ik][b_jk] of nb^3 counters,
+//     addressed with two multiply-adds, so no configuration table is read per
+//     triangle and spokes need not be grouped by bin. The block folds the
+//     permutations of each sorted triple into the caller's histogram when a
+//     counter could overflow and when it exits.
+//
+// A chunk ends before the first key that would need more segment slots than
+// the block holds, or that lies C3M_SPAN_SEGS segments or more past the first
+// key's segment. So every chunk is a byte-map chunk (there is no hash mode):
+// a forward row that wraps a periodic box simply runs as two chunks.
+constexpr int C3M_SEG_LOG = 10;
+constexpr int C3M_SEG = 1 << C3M_SEG_LOG;        // ids per segment
+constexpr int C3M_SPAN_SEGS = 256;               // segments a chunk may span (2^18 ids)
+constexpr int C3M_SEG_TABLE = C3M_SPAN_SEGS + 16;  // + the guard entry (0: the absent slot), padded
+constexpr int C3M_KEYS_PER_THREAD = 8;           // chunk keys per thread
+constexpr int C3M_MIN_SLOTS = 24;                // fewest segment slots worth a launch
+constexpr int C3M_MAX_SLOTS = 255;               // slot numbers are bytes
+constexpr int C3M_MAX_BINS = 32;                 // nb^3 u32 counters must fit beside the map
+constexpr unsigned C3M_ABSENT = 0xffu;
+
+// Exclusive scan of one int per thread over a block of THREADS threads; *total
+// receives the sum.
+template <int THREADS>
+__device__ __forceinline__ int c3m_block_scan(int v, int *s_warp, int *total)
+{
+    constexpr int WARPS = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < WARPS ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < WARPS) s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int r = (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
+    *total = s_warp[WARPS - 1];
+    __syncthreads();
+    return r;
+}
+
+// Fold the unsorted counters into the caller's sorted-triple histogram and
+// clear them: the thread that meets the sorted triple x <= y <= z sums its
+// distinct permutations (cfg3 at (x, y, z) is its packed index).
+template <int THREADS>
+__device__ __forceinline__ void c3m_flush(unsigned *h, int nb, const uint16_t *cfg3, unsigned long long *gh)
+{
+    const int nb2 = nb * nb, n3 = nb2 * nb;
+    for (int u = threadIdx.x; u < n3; u += THREADS) {
+        const int x = u / nb2, y = (u / nb) % nb, z = u % nb;
+        if (x > y || y > z) continue;
+        const int p[6] = { (x * nb + y) * nb + z, (x * nb + z) * nb + y, (y * nb + x) * nb + z,
+                           (y * nb + z) * nb + x, (z * nb + x) * nb + y, (z * nb + y) * nb + x };
+        unsigned long long v = 0;
+#pragma unroll
+        for (int q = 0; q < 6; ++q) {
+            bool dup = false;
+#pragma unroll
+            for (int r = 0; r < q; ++r) dup |= p[r] == p[q];
+            if (!dup) {
+                v += h[p[q]];
+                h[p[q]] = 0;
+            }
+        }
+        if (v) atomicAdd(gh + __ldg(cfg3 + u), v);
+    }
+}
+
+// The part [*p0, *pe) of N(j) that spoke s (j = F[s]) walks against the chunk
+// starting at c0 (first key kfirst): from the first entry beyond j, or, for a
+// spoke of an earlier chunk, from the first entry >= kfirst (binary search).
+// Spoke rows are read at e - soff (a staged window of a windowed graph, else 0).
+__device__ __forceinline__ void c3m_spoke_range(const C3Args &a, int64_t soff, int32_t j, int s, int c0,
+                                                int32_t kfirst, int64_t *p0, int64_t *pe)
+{
+    *pe = a.row_ptr[j + 1];
+    if (s + 1 >= c0) {
+        *p0 = a.row_ptr[j] + a.fwd[j];
+    } else {
+        int64_t lo = a.row_ptr[j] + a.fwd[j], hi = *pe;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (a.snbr[mid - soff] < kfirst) lo = mid + 1; else hi = mid;
+        }
+        *p0 = lo;
+    }
+}
+
+// Probe four row entries against the chunk's byte map and count the hits
+// into H[b_ij][b_ik][b_jk] (hb = b_ij nb^2; bins of the four entries in bb).
+__device__ __forceinline__ void c3m_probe4(const int k[4], uint32_t bb, int32_t kbase, unsigned guard,
+                                           const uint8_t *s_seg, const uint8_t *s_map, unsigned *s_h, int hb,
+                                           int nb)
+{
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const unsigned o = min((unsigned)(k[e] - kbase), guard);
+        const unsigned sl = s_seg[o >> C3M_SEG_LOG];
+        const unsigned b = s_map[(sl << C3M_SEG_LOG) | (o & (C3M_SEG - 1))];
+        if (b != C3M_ABSENT) atomicAdd(&s_h[hb + (int)b * nb + (int)((bb >> (8 * e)) & 0xffu)], 1u);
+    }
+}
+
+// Four spokes per warp, eight lanes each (for rows of a few hundred entries,
+// where a spoke's walk is one or two steps and its time is the latency of the
+// loads that start it): lane l of a group reads entries 4l .. 4l+3 of a
+// 32-entry step of its spoke's row. Each group stops once its step passes kmax.
+__device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, const int32_t *F, const uint8_t *FB,
+                                                 int s_lo, int s_end, int c0, int32_t kfirst, int32_t kbase,
+                                                 int32_t kmax, unsigned guard, const uint8_t *s_seg,
+                                                 const uint8_t *s_map, unsigned *s_h, int *s_next)
+{
+    const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
+    const int nb = a.nb, nb2 = nb * nb;
+    for (;;) {
+        int li = 0;
+        if (lane == 0) li = s_lo + atomicAdd(s_next, 4);
+        li = __shfl_sync(0xffffffffu, li, 0);
+        if (li >= s_end) break;
+        const int s = li + grp;
+        int64_t p0 = 0, pe = 0;
+        int hb = 0;
+        if (s < s_end) {
+            c3m_spoke_range(a, soff, F[s], s, c0, kfirst, &p0, &pe);
+            hb = FB[s] * nb2;
+        }
+        const int64_t pa = p0 & ~(int64_t)3;
+        const int head = (int)(p0 - pa);
+        const int total = p0 < pe ? head + (int)(pe - p0) : 0;
+        const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + gl;
+        const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + gl;
+        int4 kk = make_int4(0, 0, 0, 0);
+        uint32_t bb = 0;
+        bool go = total > 0;                                 // the same in the eight lanes of a group
+        if (go) {
+            kk = __ldg(vk);
+            bb = __ldg(vb);
+        }
+        for (int base = 0; __any_sync(0xffffffffu, go); base += 32) {
+            const bool more = go && base + 32 < total;
+            int4 kn = kk;
+            uint32_t bn = bb;
+            if (more) {                                      // next step in flight
+                vk += 8;
+                vb += 8;
+                kn = __ldg(vk);
+                bn = __ldg(vb);
+            }
+            if (go) {
+                int k[4] = { kk.x, kk.y, kk.z, kk.w };
+                if (base == 0 || base + 32 > total) {
+                    const int r0 = base + 4 * gl;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (r0 + e < head || r0 + e >= total) k[e] = kbase - 1;
+                }
+                c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb);
+            }
+            // rows are sorted: a group stops once its step's last key passes kmax
+            const int last = __shfl_sync(0xffffffffu, kk.w, lane | 7);
+            go = more && last <= kmax;
+            kk = kn;
+            bb = bn;
+        }
+    }
+}
+
+template <int THREADS, bool GROUPED, bool WINDOWED>
+__global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 1 : 2)
+k_count3m(C3Args a, int nslots)
+{
+    constexpr int WARPS = THREADS / 32;
+    constexpr int KPT = C3M_KEYS_PER_THREAD;
+    constexpr int MAX_KEYS = THREADS * KPT;
+    // dynamic: histogram [nb^3] u32, segment table [C3M_SEG_TABLE] u8,
+    // map [(nslots + 1) * C3M_SEG] u8 (slot 0: the all-absent segment)
+    extern __shared__ unsigned s_dyn[];
+    __shared__ int s_next;
+    __shared__ int s_cut;
+    __shared__ int s_warp[WARPS];
+    __shared__ long long s_hub;
+    __shared__ unsigned long long s_pending;        // bound on the counts added since the last flush
+    __shared__ int s_q[2];                          // windowed: spoke positions [q_lo, q_hi) of F
+
+    const int lane = threadIdx.x & 31;
+    const int nb = a.nb, nb2 = nb * nb, n3 = nb2 * nb;
+    const int64_t soff = WINDOWED ? a.soff : 0;
+    unsigned *s_h = s_dyn;
+    uint8_t *s_seg = reinterpret_cast<uint8_t *>(s_dyn + ((n3 + 3) & ~3));
+    uint8_t *s_map = s_seg + C3M_SEG_TABLE;
+
+    for (int t = threadIdx.x; t < n3; t += THREADS) s_h[t] = 0;
+    for (int t = threadIdx.x; t < C3M_SEG / 16; t += THREADS)
+        reinterpret_cast<uint4 *>(s_map)[t] = make_uint4(~0u, ~0u, ~0u, ~0u);
+    if (threadIdx.x == 0) s_pending = 0;
+
+    for (;;) {
+        __syncthreads();                                     // everyone has read the last s_hub
+        if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
+        __syncthreads();
+        if (s_hub >= a.hub_end) break;
+        const long long i = s_hub;
+        const int64_t f0 = a.row_ptr[i] + a.fwd[i];
+        const int f = (int)(a.row_ptr[i + 1] - f0);
+        if (f < 2) continue;                                 // fewer than two forward keys close nothing
+        const int64_t hoff = WINDOWED ? a.hoff : 0;
+        const int32_t *F = a.hnbr + (f0 - hoff);             // the hub's forward row and its bins
+        const uint8_t *FB = a.hbin + (f0 - hoff);
+        // spokes whose rows are walked: positions [q_lo, q_hi) of F (all of F
+        // unless the graph is windowed; rows are sorted, so a window is a range)
+        int q_lo = 0, q_hi = f;
+        if (WINDOWED) {
+            if (threadIdx.x == 0) {
+                int lo = 0, hi = f;
+                while (lo < hi) { const int m = (lo + hi) >> 1; if (F[m] < a.s_lo) lo = m + 1; else hi = m; }
+                s_q[0] = lo;
+                hi = f;
+                while (lo < hi) { const int m = (lo + hi) >> 1; if (F[m] < a.s_hi) lo = m + 1; else hi = m; }
+                s_q[1] = lo;
+            }
+            __syncthreads();
+            q_lo = s_q[0];
+            q_hi = s_q[1];
+            if (q_lo >= q_hi || q_lo >= f - 1) continue;     // no spoke of this tile (block-uniform)
+        }
+        for (int c0 = 0, c1 = 0; c0 < f; c0 = c1) {
+            // ---- the chunk [c0, c1); thread t owns keys c0 + KPT t .. + KPT - 1
+            const int32_t kbase = F[c0] & ~(C3M_SEG - 1);
+            const int cap = min(f, c0 + MAX_KEYS);
+            const int t0 = c0 + threadIdx.x * KPT;
+            int32_t key[KPT];
+            unsigned starts = 0;                             // bit q: key q opens a segment
+            int32_t prev = (t0 > c0 && t0 < cap) ? (F[t0 - 1] - kbase) >> C3M_SEG_LOG : -1;
+#pragma unroll
+            for (int q = 0; q < KPT; ++q) {
+                key[q] = t0 + q < cap ? F[t0 + q] : 0;
+                const int32_t sg = (key[q] - kbase) >> C3M_SEG_LOG;
+                if (t0 + q < cap && sg != prev) starts |= 1u << q;
+                prev = sg;
+            }
+            if (threadIdx.x == 0) s_cut = cap;
+            int total = 0;
+            // slot of a key = the number of segments opened from c0 through it
+            const int sbase = c3m_block_scan<THREADS>(__popc(starts), s_warp, &total);
+            {
+                int slot = sbase;
+#pragma unroll
+                for (int q = 0; q < KPT; ++q) {
+                    if (t0 + q >= cap) break;
+                    slot += (starts >> q) & 1u;
+                    if (slot > nslots || ((key[q] - kbase) >> C3M_SEG_LOG) >= C3M_SPAN_SEGS) {
+                        atomicMin(&s_cut, t0 + q);           // slots and segments grow with q
+                        break;
+                    }
+                }
+            }
+            // clear the segment table and the slots the chunk can use
+            for (int t = threadIdx.x; t < C3M_SEG_TABLE; t += THREADS) s_seg[t] = 0;
+            {
+                const int nclear = min(nslots, total);
+                uint4 *m = reinterpret_cast<uint4 *>(s_map + C3M_SEG);
+                for (int t = threadIdx.x; t < nclear * (C3M_SEG / 16); t += THREADS)
+                    m[t] = make_uint4(~0u, ~0u, ~0u, ~0u);
+            }
+            __syncthreads();
+            c1 = s_cut;
+            {
+                int slot = sbase;
+#pragma unroll
+                for (int q = 0; q < KPT; ++q) {
+                    if (t0 + q >= c1) break;
+                    slot += (starts >> q) & 1u;
+                    const int off = key[q] - kbase;
+                    if ((starts >> q) & 1u) s_seg[off >> C3M_SEG_LOG] = (uint8_t)slot;
+                    s_map[(slot << C3M_SEG_LOG) | (off & (C3M_SEG - 1))] = FB[t0 + q];
+                }
+            }
+            const int s_end = min(c1 - 1, q_hi);             // spokes [q_lo, s_end) meet this chunk
+            const int cn = c1 - c0;
+            // bound on the counts of this chunk: every spoke before c1 closes at
+            // most cn triangles; flush first if a counter could pass 2^32 - 1
+            const unsigned long long bound = (unsigned long long)c1 * cn;
+            const bool flush = s_pending + bound > 0xffffffffull;   // the same in every thread
+            __syncthreads();                                 // s_pending read; the map is written
+            if (flush) {
+                c3m_flush<THREADS>(s_h, nb, a.cfg3, a.ghist);
+                __syncthreads();
+            }
+            if (threadIdx.x == 0) {
+                s_pending = (flush ? 0ull : s_pending) + bound;
+                s_next = 0;
+            }
+            __syncthreads();
+            if (s_end <= q_lo) continue;
+            const int32_t kmax = F[c1 - 1];
+            const int32_t kfirst = F[c0];
+            const unsigned guard = (unsigned)C3M_SPAN_SEGS << C3M_SEG_LOG;
+
+            if (GROUPED) {
+                c3m_walk_grouped(a, soff, F, FB, q_lo, s_end, c0, kfirst, kbase, kmax, guard, s_seg, s_map, s_h,
+                                 &s_next);
+            } else {
+                // ---- spokes, one per warp, handed out in row order
+                for (;;) {
+                    int s = 0;
+                    if (lane == 0) s = q_lo + atomicAdd(&s_next, 1);
+                    s = __shfl_sync(0xffffffffu, s, 0);
+                    if (s >= s_end) break;
+                    int64_t p0, pe;
+                    c3m_spoke_range(a, soff, F[s], s, c0, kfirst, &p0, &pe);
+                    const int hb = FB[s] * nb2;
+                    if (p0 >= pe) continue;
+                    // walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
+                    // 4l .. 4l+3 of a step as one int4 and their bins as one word
+                    const int64_t pa = p0 & ~(int64_t)3;
+                    const int head = (int)(p0 - pa);
+                    const int total_e = head + (int)(pe - p0);
+                    const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + lane;
+                    const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + lane;
+                    int4 kk = __ldg(vk);
+                    uint32_t bb = __ldg(vb);
+                    for (int base = 0; base < total_e; base += 128) {
+                        vk += 32;
+                        vb += 32;
+                        int4 kn = kk;
+                        uint32_t bn = bb;
+                        if (base + 128 < total_e) {                // next step in flight
+                            kn = __ldg(vk);
+                            bn = __ldg(vb);
+                        }
+                        int k[4] = { kk.x, kk.y, kk.z, kk.w };
+                        if (base == 0 || base + 128 > total_e) {   // first / last step only
+                            // entries outside [p0, pe) become kbase - 1, whose offset clamps to the guard
+                            const int r0 = base + 4 * lane;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (r0 + e < head || r0 + e >= total_e) k[e] = kbase - 1;
+                        }
+                        c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb);
+                        // rows are sorted: stop once the step's last key passes kmax
+                        if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
+                        kk = kn;
+                        bb = bn;
+                    }
+                }
+            }
+            __syncthreads();                                 // the chunk's map is no longer read
+        }
+    }
+    __syncthreads();
+    c3m_flush<THREADS>(s_h, nb, a.cfg3, a.ghist);
+}
+
 // out[c] += sum over the slices of slice[c], 128-bit (low, high) words.
 __global__ void k_sum128_slices(const unsigned long long *__restrict__ slices, int nslices, int ncfg,
                                 unsigned long long *__restrict__ out)
@@ -642,7 +1019,115 @@ static int count3_walk_override()
     if (!env) return -1;
     if (!strcmp(env, "warp")) return 0;
     if (!strcmp(env, "group")) return 1;
+    if (!strcmp(env, "map")) return 2;
+    if (!strcmp(env, "mapgroup")) return 3;
     return -1;
+}
+
+// Shape of a byte-map walk launch: 512-thread blocks two per SM when the
+// histogram leaves room for C3M_MIN_SLOTS segment slots each, else one
+// 1024-thread block per SM; as many slots as fit. False when neither fits
+// (e.g. nb > C3M_MAX_BINS).
+template <bool W>
+static decltype(&k_count3m<512, false, false>) c3m_kernel(int threads, bool grouped)
+{
+    return threads == 512 ? (grouped ? k_count3m<512, true, W> : k_count3m<512, false, W>)
+                          : (grouped ? k_count3m<1024, true, W> : k_count3m<1024, false, W>);
+}
+
+static decltype(&k_count3m<512, false, false>) c3m_kernel(int threads, bool grouped, bool windowed)
+{
+    return windowed ? c3m_kernel<true>(threads, grouped) : c3m_kernel<false>(threads, grouped);
+}
+
+static bool plan_count3m(gs_graph_t g, bool grouped, bool windowed, int *threads, int *slots, size_t *dyn)
+{
+    if (g->nb > C3M_MAX_BINS || !g->cfg3) return false;
+    const int n3 = g->nb * g->nb * g->nb;
+    const size_t fixed = sizeof(unsigned) * (size_t)((n3 + 3) & ~3) + C3M_SEG_TABLE;
+    int dev = 0, smem_sm = 0, smem_block = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    for (int variant = 0; variant < 2; ++variant) {
+        const int t = variant == 0 ? 512 : 1024;
+        const int want = variant == 0 ? 2 : 1;                   // resident blocks per SM
+        auto kern = c3m_kernel(t, grouped, windowed);
+        // per block: the SM's shared memory split, less 1 KB reserved and 2 KB of static data
+        const long long room = std::min<long long>(smem_block, smem_sm / want - 1024) - 2048;
+        int sl = (int)std::min<long long>(C3M_MAX_SLOTS, (room - (long long)fixed) / C3M_SEG - 1);
+        while (sl >= C3M_MIN_SLOTS) {
+            const size_t d = fixed + (size_t)(sl + 1) * C3M_SEG;
+            int per = 0;
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d);
+            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, t, d);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                per = 0;
+            }
+            if (per >= want) {
+                *threads = t;
+                *slots = sl;
+                *dyn = d;
+                return true;
+            }
+            sl -= 4;
+        }
+    }
+    return false;
+}
+
+// Shared-memory size of the four-spokes-per-warp walk (the whole nb^3
+// configuration table replaces the per-warp tables); false unless two blocks
+// fit on an SM (one when the walk is forced) or the histogram is global.
+static bool plan_count3g(gs_graph_t g, bool forced, size_t *dyn)
+{
+    const int ncfg = (int)gs_ncfg3(g->nb);
+    const bool smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK_BM < (1ll << 31);
+    if (!smem) return false;
+    const size_t d = C3_REGION + sizeof(unsigned) * ((ncfg + 3) & ~3) + sizeof(uint16_t) * (size_t)g->nb * g->nb * g->nb;
+    auto kg = k_count3<true, false, false, false, true>;
+    int per = 0;
+    // a table too large for one block (nb near 40) is refused here: the
+    // one-spoke walk runs instead, and the refusal is cleared
+    cudaError_t e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kg, C3_THREADS, d);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        per = 0;
+    }
+    *dyn = d;
+    return per >= 2 || (forced && per >= 1);
+}
+
+// The walk an unweighted count takes: 2 = byte map, one spoke per warp (long
+// rows of a device-resident graph: mean degree above C3_GROUPED_MAX_DEGREE,
+// at most C3M_MAX_BINS bins); 1 = bitmap, four spokes per warp (short rows);
+// 0 = bitmap, one spoke per warp (windowed graphs, and when neither fits).
+// GS_COUNT3_WALK overrides the choice; 3 = byte map, four spokes per warp, is
+// taken only on request.
+static int count3_walk(gs_graph_t g)
+{
+    int mode = count3_walk_override();
+    const bool long_rows = g->n_edges > C3_GROUPED_MAX_DEGREE * g->n;
+    int t, sl;
+    size_t d;
+    if (mode < 0) mode = (long_rows && !g->n_win) ? 2 : 1;
+    if (mode >= 2 && plan_count3m(g, mode == 3, g->n_win > 0, &t, &sl, &d)) return mode;
+    if (g->n_win) return 0;                                  // the bitmap walk of windowed tiles
+    if (mode == 1 || mode == 3 || (mode == 2 && !long_rows)) return plan_count3g(g, mode == 1, &d) ? 1 : 0;
+    return 0;
+}
+
+extern "C" int gs_count3_walk(gs_graph_t g)
+{
+    GS_ENTRY();
+    if (!g) return -1;
+    if (gs_check_device(g) != GS_OK) return -1;
+    return count3_walk(g);
 }
 
 static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_t st)
@@ -660,6 +1145,20 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
         dyn = C3_REGION_W + sizeof(unsigned long long) * (size_t)ncfg;
         kern = win ? k_count3<true, false, true, true> : k_count3<true, false, true, false>;
     } else {
+        const int walk = !list ? count3_walk(g) : 0;
+        if (walk >= 2) {
+            const bool grouped = walk == 3;
+            int threads = 0, slots = 0;
+            size_t dm = 0;
+            if (!plan_count3m(g, grouped, win, &threads, &slots, &dm))
+                return gs_set_error(GS_ERR_INTERNAL, "byte-map walk plan");
+            const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * (threads == 512 ? 2 : 1), hubs);
+            GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
+            c3m_kernel(threads, grouped, win)<<<grid, threads, dm, st>>>(a, slots);
+            gs_note_launch();
+            GS_TRY_CUDA(cudaGetLastError());
+            return GS_OK;
+        }
         // shared-memory histogram unless it is too large or a chunk's hit bound
         // (spokes x chunk) could overflow a 32-bit counter
         smem = ncfg <= C3_SMEM_HIST_MAX && g->cfg3 && (int64_t)g->max_degree * C3_CHUNK_BM < (1ll << 31);
@@ -669,36 +1168,18 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
         else
             kern = smem ? (list ? k_count3<true, true, false, false> : k_count3<true, false, false, false>)
                         : (list ? k_count3<false, true, false, false> : k_count3<false, false, false, false>);
-        if (smem && !win && !list) {
-            // grouped walk: the whole configuration table in place of the per-warp
-            // tables; taken when chosen and two blocks still fit on an SM (or when forced)
-            const int mode = count3_walk_override();
-            const bool want = mode == 1 || (mode < 0 && g->n_edges <= C3_GROUPED_MAX_DEGREE * g->n);
-            if (want) {
-                const size_t dyn_g = C3_REGION + sizeof(unsigned) * ((ncfg + 3) & ~3) +
-                                     sizeof(uint16_t) * (size_t)nb2 * g->nb;
-                auto kg = k_count3<true, false, false, false, true>;
-                int per = 0;
-                // a table too large for one block (nb near 40) is refused here:
-                // then the one-spoke walk runs, and the refusal is cleared
-                cudaError_t ea = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_g);
-                if (ea == cudaSuccess) ea = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kg, C3_THREADS, dyn_g);
-                if (ea != cudaSuccess) {
-                    cudaGetLastError();
-                    per = 0;
-                }
-                if (per >= 2 || (mode == 1 && per >= 1)) {
-                    kern = kg;
-                    dyn = dyn_g;
-                }
-            }
+        if (walk == 1) {
+            size_t dg = 0;
+            plan_count3g(g, true, &dg);
+            kern = k_count3<true, false, false, false, true>;
+            dyn = dg;
         }
     }
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C3_THREADS, dyn));
     if (per_sm < 1) return gs_set_error(GS_ERR_CAPACITY, "3pCF workspace of %zu bytes does not fit in shared memory", dyn);
-    const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * per_sm, hubs);
+    const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * std::min(per_sm, C3_MAX_BLOCKS_PER_SM), hubs);
     GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
     if (!weighted) {
         kern<<<grid, C3_THREADS, dyn, st>>>(a);
@@ -706,25 +1187,27 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
         GS_TRY_CUDA(cudaGetLastError());
         return GS_OK;
     }
-    // weighted: one 128-bit slice per block, then their sum added to the output
-    unsigned long long *out = a.gsum, *slices = nullptr;
+    // weighted: one 128-bit slice per block (in the caller's scratch, which
+    // holds C3_MAX_BLOCKS_PER_SM slices per SM), then their sum added to the output
+    unsigned long long *out = a.gsum, *slices = a.slices;
     const size_t bytes = 16 * (size_t)ncfg * grid;
-    GS_TRY_CUDA(cudaMallocAsync(&slices, bytes, st));
-    cudaError_t e = cudaMemsetAsync(slices, 0, bytes, st);
-    if (e == cudaSuccess) {
-        a.gsum = slices;
-        kern<<<grid, C3_THREADS, dyn, st>>>(a);
-        gs_note_launch();
-        e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) {
-        k_sum128_slices<<<(ncfg + 255) / 256, 256, 0, st>>>(slices, grid, ncfg, out);
-        gs_note_launch();
-        e = cudaGetLastError();
-    }
-    cudaFreeAsync(slices, st);
-    GS_TRY_CUDA(e);
+    GS_TRY_CUDA(cudaMemsetAsync(slices, 0, bytes, st));
+    a.gsum = slices;
+    kern<<<grid, C3_THREADS, dyn, st>>>(a);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
+    k_sum128_slices<<<(ncfg + 255) / 256, 256, 0, st>>>(slices, grid, ncfg, out);
+    gs_note_launch();
+    GS_TRY_CUDA(cudaGetLastError());
     return GS_OK;
+}
+
+// Scratch of the weighted count: a 128-bit slice per configuration for every
+// block that can be resident (k_count3 is launched with at most
+// C3_MAX_BLOCKS_PER_SM blocks per SM).
+static size_t c3_slice_bytes(gs_graph_t g)
+{
+    return 16 * (size_t)gs_ncfg3(g->nb) * (size_t)gs_sm_count() * C3_MAX_BLOCKS_PER_SM;
 }
 
 // The hubs [hub_begin, hub_end): one launch on a device-resident graph; on a
@@ -869,8 +1352,9 @@ static C3Args count3_args(gs_graph_t g, uint64_t *hist_dev)
 extern "C" gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int64_t hub_end,
                                    void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !hist_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
         return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
                             (long long)hub_end, (long long)g->n);
@@ -906,8 +1390,9 @@ gs_status gs_check_ids(gs_graph_t g, const int32_t *ids, int64_t count, cudaStre
 extern "C" gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
                                         uint64_t *hist_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !hist_dev || (count > 0 && !hubs_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (count < 0) return gs_set_error(GS_ERR_ARG, "negative hub count");
     if (g->n_win) return gs_set_error(GS_ERR_ARG, "hub lists need a device-resident graph (this one is windowed)");
     cudaStream_t st = (cudaStream_t)cuda_stream;
@@ -926,8 +1411,9 @@ extern "C" gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, i
 extern "C" gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int64_t hub_begin, int64_t hub_end,
                                             void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !sums_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (!g->w) return gs_set_error(GS_ERR_ARG, "no weights: call gs_graph_set_weights first");
     if (g->nb > C3_WEIGHTED_MAX_BINS)
         return gs_set_error(GS_ERR_ARG, "the weighted 3pCF supports at most %d bins", C3_WEIGHTED_MAX_BINS);
@@ -936,10 +1422,20 @@ extern "C" gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int
                             (long long)hub_end, (long long)g->n);
     cudaStream_t st = (cudaStream_t)cuda_stream;
     const int ncfg = (int)gs_ncfg3(g->nb);
-    GS_TRY_CUDA(cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
-    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
-    C3Args a = count3_args(g, nullptr);
-    a.w = g->w;
-    a.gsum = (unsigned long long *)sums_dev;
-    return run_count3(g, a, hub_begin, hub_end, st);
+    const bool work = hub_end > hub_begin && g->n_edges > 0;
+    // the per-block slices are allocated before any output is written
+    unsigned long long *slices = nullptr;
+    if (work) GS_TRY_CUDA(gs_malloc_async(&slices, c3_slice_bytes(g), st));
+    gs_status s = GS_OK;
+    const cudaError_t e = cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * ncfg, st);
+    if (e != cudaSuccess) s = gs_set_error(GS_ERR_CUDA, "clearing the sums failed: %s", cudaGetErrorString(e));
+    if (s == GS_OK && work) {
+        C3Args a = count3_args(g, nullptr);
+        a.w = g->w;
+        a.gsum = (unsigned long long *)sums_dev;
+        a.slices = slices;
+        s = run_count3(g, a, hub_begin, hub_end, st);
+    }
+    if (slices) cudaFreeAsync(slices, st);
+    return s;
 }

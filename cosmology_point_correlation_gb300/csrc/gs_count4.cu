@@ -452,33 +452,40 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
     GS_TRY_CUDA(cudaGetLastError());
 
     if (g->max_degree > C4_M) {
+        // a.scratch: the caller's workspace of c4_scratch_bytes(g, hubs) bytes
         const int M = g->max_degree;
-        size_t stride = c4_large_stride(M, g->nb);
-        const int gl = (int)std::min<int64_t>((int64_t)sms * 2, hubs);
-        char *scratch = nullptr;
-        GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
         a.cursor = g->work + 2;
         a.big_m = M;
-        a.scratch = scratch;
-        a.scratch_stride = stride;
+        a.scratch_stride = c4_large_stride(M, g->nb);
+        const int gl = (int)std::min<int64_t>((int64_t)sms * 2, hubs);
         const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)a.ncfg : 0;
         auto big = windowed ? (smem ? k_count4_large<true, false, true> : k_count4_large<false, false, true>)
                             : (smem ? k_count4_large<true, false, false> : k_count4_large<false, false, false>);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
-        cudaError_t e = cudaGetLastError();
-        cudaFreeAsync(scratch, st);
-        if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        GS_TRY_CUDA(cudaGetLastError());
     }
     return GS_OK;
 }
 
+// Workspace of the large-hub kernel for a launch over at most `hubs` hubs
+// (0 when no hub has more than C4_M neighbours).
+static size_t c4_scratch_bytes(gs_graph_t g, int64_t hubs)
+{
+    if (g->max_degree <= C4_M || hubs <= 0) return 0;
+    return c4_large_stride(g->max_degree, g->nb) * (size_t)std::min<int64_t>((int64_t)gs_sm_count() * 2, hubs);
+}
+
+static gs_status c4_count(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
+                          int64_t hub_end, char *scratch, cudaStream_t st);
+
 extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
                                           int64_t hub_begin, int64_t hub_end, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    GS_TRY_DEVICE(g);
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
         return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,
                             (long long)hub_end, (long long)g->n);
@@ -488,6 +495,21 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
     if (ncfg <= 0) return GS_OK;
     if (!even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL histogram");
     cudaStream_t st = (cudaStream_t)cuda_stream;
+    // the large-hub workspace is allocated before any output is written
+    char *scratch = nullptr;
+    const size_t sbytes = g->n_edges > 0 ? c4_scratch_bytes(g, hub_end - hub_begin) : 0;
+    if (sbytes) GS_TRY_CUDA(gs_malloc_async(&scratch, sbytes, st));
+    gs_status s = c4_count(g, (uint64_t *)even_dev, odd_dev, hub_begin, hub_end, scratch, st);
+    if (scratch) cudaFreeAsync(scratch, st);
+    return s;
+}
+
+// The parity count once its workspace is in hand: clear the outputs, then
+// one launch (device-resident graph) or one per window tile.
+static gs_status c4_count(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
+                          int64_t hub_end, char *scratch, cudaStream_t st)
+{
+    const int64_t ncfg = gs_ncfg4(g->nb);
     GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
     GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
     if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
@@ -506,6 +528,7 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
     a.ncfg = (int)ncfg;
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
+    a.scratch = scratch;
     if (!g->n_win) return c4_launch(g, a, false, st);
 
     // windowed: tiles (hub window h, spoke windows c1 <= c2), both adjacent to h
@@ -544,11 +567,15 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
     return GS_OK;
 }
 
+static gs_status c4_count_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count, uint64_t *even_dev,
+                               int64_t *odd_dev, char *scratch, cudaStream_t st);
+
 extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count,
                                                uint64_t *even_dev, int64_t *odd_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || (count > 0 && !hubs_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (count < 0) return gs_set_error(GS_ERR_ARG, "negative hub count");
     if (g->n_win) return gs_set_error(GS_ERR_ARG, "the parity 4pCF needs a device-resident graph (this one is windowed)");
     if (g->edges[g->nb] >= (1ll << 20))
@@ -559,6 +586,19 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
     cudaStream_t st = (cudaStream_t)cuda_stream;
     gs_status s = gs_check_ids(g, hubs_dev, count, st);
     if (s != GS_OK) return s;
+    // the large-hub workspace is allocated before any output is written
+    char *scratch = nullptr;
+    const size_t sbytes = g->n_edges > 0 ? c4_scratch_bytes(g, count) : 0;
+    if (sbytes) GS_TRY_CUDA(gs_malloc_async(&scratch, sbytes, st));
+    s = c4_count_hubs(g, hubs_dev, count, (uint64_t *)even_dev, odd_dev, scratch, st);
+    if (scratch) cudaFreeAsync(scratch, st);
+    return s;
+}
+
+static gs_status c4_count_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t count, uint64_t *even_dev,
+                               int64_t *odd_dev, char *scratch, cudaStream_t st)
+{
+    const int64_t ncfg = gs_ncfg4(g->nb);
     GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
     GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
     if (count == 0 || g->n_edges == 0) return GS_OK;
@@ -580,6 +620,7 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
     a.ncfg = (int)ncfg;
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
+    a.scratch = scratch;
 
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
@@ -598,20 +639,15 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
         const int M = g->max_degree;
         size_t stride = c4_large_stride(M, g->nb);
         const int gl = (int)std::min<int64_t>((int64_t)sms * 2, count);
-        char *scratch = nullptr;
-        GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
         a.cursor = g->work + 2;
         a.big_m = M;
-        a.scratch = scratch;
         a.scratch_stride = stride;
         const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
         auto big = smem ? k_count4_large<true, true, false> : k_count4_large<false, true, false>;
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
-        cudaError_t e = cudaGetLastError();
-        cudaFreeAsync(scratch, st);
-        if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        GS_TRY_CUDA(cudaGetLastError());
     }
     return GS_OK;
 }
@@ -657,8 +693,9 @@ static gs_status c4_static_base(char **out)
 extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev,
                                                  int64_t hub_begin, int64_t hub_end, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g) return gs_set_error(GS_ERR_ARG, "graph is NULL");
+    GS_TRY_DEVICE(g);
     if (g->n_win) return gs_set_error(GS_ERR_ARG, "the parity 4pCF needs a device-resident graph (this one is windowed)");
     if (hub_begin < 0 || hub_end > g->n || hub_begin > hub_end)
         return gs_set_error(GS_ERR_ARG, "hub range [%lld, %lld) outside [0, %lld]", (long long)hub_begin,

@@ -551,7 +551,7 @@ static gs_status c6_prepare(gs_graph_t g)
     int n = 0;
     std::vector<int32_t> t = c6_table(g->nb, &n);
     int32_t *d = nullptr;
-    GS_TRY_CUDA(cudaMalloc(&d, sizeof(int32_t) * t.size()));
+    GS_TRY_CUDA(gs_malloc(&d, sizeof(int32_t) * t.size()));
     cudaError_t e = cudaMemcpy(d, t.data(), sizeof(int32_t) * t.size(), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaFree(d);
@@ -564,7 +564,7 @@ static gs_status c6_prepare(gs_graph_t g)
 
 extern "C" gs_status gs_config_tuple_4pcf6(int nbins, int64_t config, int32_t *tuple_host)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (nbins < 1 || nbins > C6_MAX_BINS || !tuple_host) return gs_set_error(GS_ERR_ARG, "bad argument");
     int n = 0;
     static thread_local int cached_nb = 0;
@@ -598,6 +598,22 @@ extern "C" int64_t gs_config_count_4pcf6(int nbins)
     if (nbins < 1 || nbins > C6_MAX_BINS) return -1;
     const int64_t b = nbins;
     return (b * b * b * b * b * b + 9 * b * b * b * b + 14 * b * b) / 24;
+}
+
+// Blocks of the large-hub kernel for a launch over `hubs` hubs (its
+// workspace is capped at 2 GiB), and the workspace they need (0 when no hub
+// has more than C6_M forward neighbours).
+static int c6_large_blocks(gs_graph_t g, int64_t hubs)
+{
+    const size_t budget = (size_t)2 << 30;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>((int64_t)gs_sm_count() * 2, hubs),
+                                                       (int64_t)(budget / c6_large_stride(g->max_forward))));
+}
+
+static size_t c6_scratch_bytes(gs_graph_t g, int64_t hubs)
+{
+    if (g->max_forward <= C6_M || hubs <= 0 || g->n_edges == 0) return 0;
+    return c6_large_stride(g->max_forward) * (size_t)c6_large_blocks(g, hubs);
 }
 
 // Launch the small-hub and large-hub kernels over [hub_begin, hub_end) of a
@@ -638,15 +654,11 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
 
     const int M = g->max_forward;              // bounds the large path's slices
     if (M > C6_M) {
+        // a.scratch: the caller's workspace of c6_scratch_bytes(g, hubs) bytes
         const size_t stride = c6_large_stride(M);
-        const size_t budget = (size_t)2 << 30;
-        const int gl = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>((int64_t)sms * 2, hubs),
-                                                                   (int64_t)(budget / stride)));
-        char *scratch = nullptr;
-        GS_TRY_CUDA(cudaMallocAsync(&scratch, stride * gl, st));
+        const int gl = c6_large_blocks(g, hubs);
         GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
         a.big_m = M;
-        a.scratch = scratch;
         a.scratch_stride = stride;
         const size_t bdyn = smem ? acc : 0;
         decltype(&k_count6_large<true, true, true>) big;
@@ -659,9 +671,7 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bdyn));
         big<<<gl, C6_LARGE_THREADS, bdyn, st>>>(a);
         gs_note_launch();
-        cudaError_t e = cudaGetLastError();
-        cudaFreeAsync(scratch, st);
-        if (e != cudaSuccess) return gs_set_error(GS_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        GS_TRY_CUDA(cudaGetLastError());
     }
     return GS_OK;
 }
@@ -744,40 +754,54 @@ static C6Args c6_args(gs_graph_t g, int64_t hub_begin, int64_t hub_end)
     return a;
 }
 
+// A count with its workspace allocated before any output is written: then
+// the outputs (out_bytes each) are cleared and the tiles run.
+static gs_status c6_count(gs_graph_t g, C6Args a, void *even_dev, void *odd_dev, size_t out_bytes,
+                          int64_t hub_begin, int64_t hub_end, cudaStream_t st)
+{
+    char *scratch = nullptr;
+    const size_t sbytes = c6_scratch_bytes(g, hub_end - hub_begin);
+    if (sbytes) GS_TRY_CUDA(gs_malloc_async(&scratch, sbytes, st));
+    gs_status s = GS_OK;
+    cudaError_t e = cudaMemsetAsync(even_dev, 0, out_bytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(odd_dev, 0, out_bytes, st);
+    if (e != cudaSuccess) s = gs_set_error(GS_ERR_CUDA, "clearing the histograms failed: %s", cudaGetErrorString(e));
+    if (s == GS_OK && hub_end > hub_begin && g->n_edges > 0) {
+        a.scratch = scratch;
+        s = c6_run(g, a, hub_begin, hub_end, st);
+    }
+    if (scratch) cudaFreeAsync(scratch, st);
+    return s;
+}
+
 extern "C" gs_status gs_count_4pcf6(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
                                     int64_t hub_end, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     gs_status s = c6_check(g, hub_begin, hub_end);
     if (s != GS_OK) return s;
-    const int ncfg = g->ncfg6;
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(uint64_t) * ncfg, st));
-    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * ncfg, st));
-    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
     C6Args a = c6_args(g, hub_begin, hub_end);
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
-    return c6_run(g, a, hub_begin, hub_end, st);
+    return c6_count(g, a, even_dev, odd_dev, sizeof(uint64_t) * g->ncfg6, hub_begin, hub_end, st);
 }
 
 extern "C" gs_status gs_count_4pcf6_weighted(gs_graph_t g, int64_t *even_dev, int64_t *odd_dev, int64_t hub_begin,
                                              int64_t hub_end, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !even_dev || !odd_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (!g->w) return gs_set_error(GS_ERR_ARG, "no weights: call gs_graph_set_weights first");
     gs_status s = c6_check(g, hub_begin, hub_end);
     if (s != GS_OK) return s;
-    const int ncfg = g->ncfg6;
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    GS_TRY_CUDA(cudaMemsetAsync(even_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
-    GS_TRY_CUDA(cudaMemsetAsync(odd_dev, 0, sizeof(int64_t) * 2 * ncfg, st));
-    if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
     C6Args a = c6_args(g, hub_begin, hub_end);
     a.w = g->w;
     a.weven = (unsigned long long *)even_dev;
     a.wodd = (unsigned long long *)odd_dev;
-    return c6_run(g, a, hub_begin, hub_end, st);
+    return c6_count(g, a, even_dev, odd_dev, sizeof(int64_t) * 2 * g->ncfg6, hub_begin, hub_end, st);
 }

@@ -88,7 +88,43 @@ inline bool gs_windows_adjacent(gs_graph_t g, int h, int c)
 // ---------------------------------------------------------------- errors
 
 gs_status gs_set_error(gs_status s, const char *fmt, ...);
-void gs_clear_error();
+
+// A public entry point in progress on this thread. The outermost one (calls
+// nest: gs_3pcf_from_host calls gs_build_graph) clears the thread's error
+// message and restarts the allocation ordinal that fault injection counts.
+struct gs_call_scope {
+    gs_call_scope();
+    ~gs_call_scope();
+};
+#define GS_ENTRY() gs_call_scope gs_scope_
+
+// Every device and pinned-host allocation of the library passes this gate
+// first. It counts the allocation (gs_alloc_calls) and, when the environment
+// variable GS_FAULT holds "alloc:N", fails the N-th allocation of the current
+// outermost call with cudaErrorMemoryAllocation without allocating anything,
+// so that the NOMEM path of every allocation site can be exercised on the host.
+cudaError_t gs_alloc_gate();
+
+template <typename T>
+inline cudaError_t gs_malloc(T **p, size_t bytes)
+{
+    const cudaError_t e = gs_alloc_gate();
+    return e != cudaSuccess ? e : cudaMalloc((void **)p, bytes);
+}
+
+template <typename T>
+inline cudaError_t gs_malloc_async(T **p, size_t bytes, cudaStream_t st)
+{
+    const cudaError_t e = gs_alloc_gate();
+    return e != cudaSuccess ? e : cudaMallocAsync((void **)p, bytes, st);
+}
+
+template <typename T>
+inline cudaError_t gs_malloc_host(T **p, size_t bytes)
+{
+    const cudaError_t e = gs_alloc_gate();
+    return e != cudaSuccess ? e : cudaMallocHost((void **)p, bytes);
+}
 
 #define GS_TRY_CUDA(call)                                                              \
     do {                                                                               \
@@ -107,6 +143,16 @@ void gs_note_launch();
 // 16-byte vectors up to 128 entries past a row's end without leaving the
 // allocation.
 constexpr int64_t GS_EDGE_PAD = 128;
+
+// GS_ERR_ARG unless the current device is the one the graph was built on
+// (every pointer a count passes to its kernels belongs to that device).
+gs_status gs_check_device(gs_graph_t g);
+
+#define GS_TRY_DEVICE(g)                                                               \
+    do {                                                                               \
+        gs_status s_ = gs_check_device(g);                                             \
+        if (s_ != GS_OK) return s_;                                                    \
+    } while (0)
 
 // GS_ERR_ARG unless every one of `count` device input indices lies in [0, n);
 // synchronises st.

@@ -22,10 +22,11 @@ __global__ void k_gather_weights(const int4 *__restrict__ pts, const int16_t *__
 
 extern "C" gs_status gs_graph_set_weights(gs_graph_t g, const int16_t *w_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || (g->n > 0 && !w_dev)) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    if (!g->w) GS_TRY_CUDA(cudaMalloc(&g->w, sizeof(int16_t) * (size_t)std::max<int64_t>(g->n, 1)));
+    if (!g->w) GS_TRY_CUDA(gs_malloc(&g->w, sizeof(int16_t) * (size_t)std::max<int64_t>(g->n, 1)));
     if (g->n == 0) return GS_OK;
     const int grid = (int)std::min<int64_t>((g->n + 255) / 256, (int64_t)gs_sm_count() * 16);
     k_gather_weights<<<grid, 256, 0, st>>>(g->pts, w_dev, g->n, g->w);
@@ -102,8 +103,9 @@ k_count2w(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd, 
 
 extern "C" gs_status gs_count_2pcf_weighted(gs_graph_t g, int64_t *sums_dev, void *cuda_stream)
 {
-    gs_clear_error();
+    GS_ENTRY();
     if (!g || !sums_dev) return gs_set_error(GS_ERR_ARG, "NULL argument");
+    GS_TRY_DEVICE(g);
     if (!g->w) return gs_set_error(GS_ERR_ARG, "no weights: call gs_graph_set_weights first");
     cudaStream_t st = (cudaStream_t)cuda_stream;
     GS_TRY_CUDA(cudaMemsetAsync(sums_dev, 0, sizeof(int64_t) * 2 * g->nb, st));

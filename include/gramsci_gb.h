@@ -101,13 +101,28 @@ gs_status gs_build_graph(const int32_t *coords_dev, int64_t n, int64_t box_lu, i
  *               Each triangle is counted at its lowest internal index, so the
  *               histograms of disjoint ranges that cover [0, n) sum exactly
  *               to the full one.
- * A device-resident graph with mean degree <= 1024 is walked four spokes per
- * warp, a longer-rowed or windowed one a spoke per warp; the environment
- * variable GS_COUNT3_WALK = "warp" or "group" overrides the choice (read at
- * each call). The histogram is the same either way.
+ * The spoke walk depends on the graph (gs_count3_walk); the environment
+ * variable GS_COUNT3_WALK = "map", "mapgroup", "group" or "warp" overrides the choice
+ * (read at each call). The histogram is the same for every walk.
  * Errors: GS_ERR_ARG (NULL pointers, range outside [0, n]), GS_ERR_CUDA. */
 gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int64_t hub_end,
                         void *cuda_stream);
+
+/* The spoke walk gs_count_3pcf takes on this graph (host query, no device
+ * work). The hub's keys and their bins are held in shared memory either as a
+ * byte map (a bin byte per id of the key span, in 1024-id segments; hits go
+ * to an unsorted nb^3 histogram) or as a bitmap with ranks (hits go to the
+ * sorted-triple histogram through a configuration table):
+ *   2 = byte map, one spoke per warp (device-resident graphs with long rows,
+ *       mean degree above 1024, and at most 32 bins)
+ *   1 = bitmap, four spokes per warp (device-resident graphs with short rows)
+ *   0 = bitmap, one spoke per warp (windowed graphs, and when the others do
+ *       not fit in shared memory)
+ *   3 = byte map, four spokes per warp (on request only)
+ * GS_COUNT3_WALK = "map", "mapgroup", "warp" or "group" overrides the choice,
+ * as for the count (the byte-map walks also run on windowed graphs). -1 for a
+ * NULL graph or one of another device. */
+int gs_count3_walk(gs_graph_t g);
 
 /* Parity-decomposed 4pCF histograms (§III.1.1 three-way intersection,
  * §III.2 Eq.(3), degenerate volumes add 0 to odd).
@@ -271,6 +286,18 @@ typedef struct {
 
 gs_status gs_graph_stats(gs_graph_t g, gs_graph_stats_t *out, void *cuda_stream);
 
+/* Per-hub work of the 3pCF count, in the graph's internal (hub) order: the
+ * forward degree f_i and the spoke-row length of hub i's merge-walks,
+ * w_i = sum over the forward spokes j of i of f_j (§III.1: the entries of
+ * N(j) beyond j that the intersections of hub i read). The prefix sum of
+ * w_i splits [0, n) into contiguous hub ranges of equal work, the partition
+ * of the counts across devices (§IV.7: hub windows, no communication).
+ *   fwd_dev   int32 [n] or NULL, device, overwritten
+ *   walk_dev  int64 [n], device, overwritten
+ * Asynchronous (a windowed graph stages its windows one at a time).
+ * Errors: GS_ERR_ARG (NULL, graph of another device), GS_ERR_CUDA. */
+gs_status gs_graph_hub_work(gs_graph_t g, int32_t *fwd_dev, int64_t *walk_dev, void *cuda_stream);
+
 /* The graph of gs_build_graph with its edge arrays in pinned HOST memory,
  * split into row windows of at most window_edges directed edges (whole cells;
  * a larger cell gets a window of its own). This is the out-of-core mode of
@@ -298,6 +325,16 @@ gs_status gs_graph_windows(gs_graph_t g, int32_t *n_windows, int64_t *window_edg
 /* Number of CUDA kernels this library has launched in this process so far
  * (all threads, all devices). */
 uint64_t gs_kernel_launches(void);
+
+/* Number of device and pinned-host allocations this library has attempted in
+ * this process so far (all threads). A call that allocates nothing leaves it
+ * unchanged.
+ * Fault injection for tests: when the environment variable GS_FAULT holds
+ * "alloc:N" (N >= 1), the N-th allocation inside each public call (counted
+ * from the start of the outermost call on the calling thread) fails without
+ * allocating, and the call returns GS_ERR_NOMEM having freed what it had
+ * allocated. The variable is read at every allocation. */
+uint64_t gs_alloc_calls(void);
 
 /* The graph as CSR in INPUT numbering, rows sorted by neighbour id (Eq.(1)).
  *   row_ptr_dev int64 [n+1], device
@@ -345,6 +382,21 @@ gs_status gs_4pcf_parity_from_host(const int32_t *coords_host, int64_t n, int64_
                                    int periodic, int64_t r_max_lu, const int64_t *edges_lu,
                                    int nbins, uint64_t *even_host, int64_t *odd_host,
                                    void *cuda_stream);
+
+/* Measured ceiling of the counts' histogram adds (a measurement aid for the
+ * roofline of the triangle count, whose every closed triangle is one
+ * shared-memory atomic add of 1 into a histogram; §III.5.2 accumulates into
+ * per-gang histograms the same way). Launches two 512-thread blocks per SM
+ * that do nothing but such adds into a histogram of ncfg 32-bit counters in
+ * shared memory, lanes_active lanes of each warp taking part, and returns
+ * the lane-adds retired per second on the whole device.
+ *   pattern  0: pseudo-random counters (the count's pattern), 1: one bank
+ *            per lane (no conflicts), 2: one counter for all lanes
+ * Synchronises cuda_stream; runs for about 20 ms. Errors: GS_ERR_ARG
+ * (ncfg outside [32, 27648], pattern, lanes_active outside 1..32),
+ * GS_ERR_NOMEM, GS_ERR_CUDA. */
+gs_status gs_measure_smem_atomics(int ncfg, int pattern, int lanes_active, double *lane_adds_per_s,
+                                  void *cuda_stream);
 
 /* Release a graph and its device memory (NULL is a no-op). Synchronises the
  * device before freeing. */

@@ -11,10 +11,12 @@ from tests.gpu_util import gpu_3pcf, gpu_graph, mirror
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["warp", "group"])
+@pytest.fixture(autouse=True, params=["warp", "group", "map", "mapgroup"])
 def walk_mode(request, monkeypatch):
-    """Every test of this module runs with both spoke walks of the 3pCF count:
-    one spoke per warp and four spokes per warp (read at each launch)."""
+    """Every test of this module runs with each spoke walk of the 3pCF count:
+    one or four spokes per warp over a bitmap of the hub's keys, and one or
+    four spokes per warp over a byte map of the keys' bins (read at each
+    launch)."""
     monkeypatch.setenv("GS_COUNT3_WALK", request.param)
     return request.param
 

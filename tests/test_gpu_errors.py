@@ -76,3 +76,28 @@ def test_parity_needs_exact_volume_range():
         with pytest.raises(GramsciError, match="2\\^20"):
             g.count_4pcf_parity()
         g.count_3pcf()                         # the 3pCF has no such limit
+
+
+def test_graph_of_another_device_is_refused():
+    # every count and export checks that the current device is the graph's own
+    # (a graph's pointers are meaningless on another device). With one GPU the
+    # test makes the recorded device differ instead of switching devices.
+    torch, dev = torch_dev()
+    xyz = catalogues.uniform(300, 10000 / 1024, 4)
+    lib = _lib.load()
+    with gpu_graph(xyz, 10000, 1, [0, 1000, 2000, 3000]) as g:
+        rec = ctypes.cast(g._h, ctypes.POINTER(ctypes.c_int))   # the handle's first field is its device
+        own = rec[0]
+        hist = torch.zeros(20, dtype=torch.int64, device=dev)
+        rec[0] = own + 1
+        try:
+            for call in (lambda: lib.gs_count_3pcf(g._h, ctypes.c_void_p(hist.data_ptr()), 0, 300, None),
+                         lambda: lib.gs_count_4pcf_parity(g._h, ctypes.c_void_p(hist.data_ptr()),
+                                                          ctypes.c_void_p(hist.data_ptr()), 0, 300, None),
+                         lambda: lib.gs_count_2pcf(g._h, ctypes.c_void_p(hist.data_ptr()), None),
+                         lambda: lib.gs_graph_hub_work(g._h, None, ctypes.c_void_p(hist.data_ptr()), None)):
+                assert call() == _lib.GS_ERR_ARG
+                assert b"device" in lib.gs_last_error()
+        finally:
+            rec[0] = own
+        assert lib.gs_count_3pcf(g._h, ctypes.c_void_p(hist.data_ptr()), 0, 300, None) == _lib.GS_OK

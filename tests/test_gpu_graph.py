@@ -75,3 +75,27 @@ def test_rows_sorted_and_symmetric_on_clustered_open_box():
     pos = np.searchsorted(key[order], rkey)
     assert np.array_equal(key[order][pos], rkey)
     assert np.array_equal(b[order][pos], b)
+
+
+@pytest.mark.parametrize("periodic", [0, 1])
+def test_hub_work_matches_the_oracle_graph(periodic):
+    # f_i = |{j in N(i): j > i}| and w_i = sum of f_j over those j, in the
+    # graph's internal order (the input put in that order first)
+    import oracle
+    from tests.gpu_util import gpu_graph
+    box = catalogues.box_lattice(100.0)
+    xyz = catalogues.neyman_scott(8000, 100.0, 160, 50.0, 3.0, 31 + periodic)
+    edges = catalogues.linear_edges_lu(10.0, 6)
+    with gpu_graph(xyz, box, periodic, edges) as g:
+        perm = g.export_perm().cpu().numpy()
+    xg = np.ascontiguousarray(xyz[perm])
+    ref = oracle.graph(xg, box, periodic, edges)
+    n = len(xg)
+    f = np.array([(ref.nbr[ref.row_ptr[i]:ref.row_ptr[i + 1]] > i).sum() for i in range(n)])
+    w = np.array([f[ref.nbr[ref.row_ptr[i]:ref.row_ptr[i + 1]][ref.nbr[ref.row_ptr[i]:ref.row_ptr[i + 1]] > i]].sum()
+                  for i in range(n)])
+    with gpu_graph(xg, box, periodic, edges) as g:
+        gf, gw = (t.cpu().numpy() for t in g.hub_work())
+        st = g.stats()
+    assert np.array_equal(gf, f) and np.array_equal(gw, w)
+    assert gw.sum() == st["spoke_walk"] and gf.max() == st["max_forward"]

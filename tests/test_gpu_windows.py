@@ -27,10 +27,13 @@ def _clustered(n, seed, periodic):
     return xyz, box, catalogues.linear_edges_lu(10.0, 15)
 
 
+@pytest.mark.parametrize("walk", ["map", "mapgroup", "warp"])
 @pytest.mark.parametrize("periodic", [0, 1])
 @pytest.mark.parametrize("frac", [1.0, 0.3, 0.05, 0.0])
-def test_windowed_graph_and_3pcf_match_oracle(periodic, frac):
-    # frac of the edges per window; 0 -> one cell per window
+def test_windowed_graph_and_3pcf_match_oracle(periodic, frac, walk, monkeypatch):
+    # frac of the edges per window; 0 -> one cell per window. Window tiles run
+    # the byte-map walks (one or four spokes per warp) or the bitmap walk.
+    monkeypatch.setenv("GS_COUNT3_WALK", walk)
     xyz, box, edges = _clustered(20_011, 5, periodic)
     ref = oracle.graph(xyz, box, periodic, edges)
     hist_ref = oracle.count_3pcf(xyz, box, periodic, edges, ref)

@@ -1,6 +1,8 @@
-"""The multi-process path on CPU (gloo, world size 2): hub ranges split one
-count across ranks and the integer histograms all-reduce to the full one; the
-benchmark's cross-rank reduction takes the max of times and the sum of counts."""
+"""The multi-process path on CPU (gloo, world size 2): hub ranges balanced on
+the per-hub merge-walk work split one count across ranks, and the integer
+histograms all-reduce (with the reduction bench.py --strong uses) to the full
+one; the benchmark's cross-rank reduction of timings takes the max of times
+and the sum of counts."""
 import os
 import socket
 
@@ -12,7 +14,7 @@ import torch.multiprocessing as mp
 
 import oracle
 from cosmology_point_correlation_gb300 import catalogues
-from cosmology_point_correlation_gb300.sharding import hub_ranges
+from cosmology_point_correlation_gb300.sharding import balanced_ranges, hub_ranges, reduce_histograms
 
 
 def _free_port():
@@ -29,13 +31,17 @@ def _worker(rank, world, port, result):
         xyz = catalogues.neyman_scott(600, box / 1024, 12, 50.0, 1.5, 17)
         edges = catalogues.linear_edges_lu(5.0, 5)
         g = oracle.graph(xyz, box, 1, edges)
-        deg = np.diff(g.row_ptr)
-        b, e = hub_ranges(len(xyz), world, weights=deg.astype(np.float64) ** 2)[rank]
+        # the per-hub work the library's hub_work export gives: forward degree
+        # f_i and the spoke-row entries w_i = sum of f_j over forward spokes j
+        n = len(xyz)
+        fwd = np.array([(g.nbr[g.row_ptr[i]:g.row_ptr[i + 1]] > i).sum() for i in range(n)])
+        walk = np.array([fwd[[j for j in g.nbr[g.row_ptr[i]:g.row_ptr[i + 1]] if j > i]].sum()
+                         for i in range(n)])
+        b, e = balanced_ranges(fwd, walk, world)[rank]
         h3 = torch.from_numpy(oracle.count_3pcf(xyz, box, 1, edges, g, b, e).astype(np.int64))
         ev, od = oracle.count_4pcf_parity(xyz, box, 1, edges, g, b, e)
         h4 = torch.from_numpy(np.concatenate([ev.astype(np.int64), od]))
-        dist.all_reduce(h3)
-        dist.all_reduce(h4)
+        reduce_histograms(h3, h4)                 # the reduction bench.py --strong uses
         import bench
         mx, sm = bench.reduce_max_sum(world, [float(rank + 1), 10.0 * rank], [float(rank + 1)])
         if rank == 0:
@@ -68,3 +74,11 @@ def test_hub_ranges_cover_and_balance():
     assert r[0] == (0, 1)
     with pytest.raises(ValueError):
         hub_ranges(5, 0)
+
+
+def test_balanced_ranges_follow_the_walk_work():
+    fwd = np.array([0, 5, 5, 0, 0, 0, 0, 0])
+    walk = np.array([0, 1000, 1000, 0, 0, 0, 0, 0])
+    r = balanced_ranges(fwd, walk, 2)
+    assert r[0][0] == 0 and r[-1][1] == 8 and r[0][1] == r[1][0]
+    assert r[0][1] == 2                      # the two heavy hubs go to different ranks

@@ -6,7 +6,9 @@ device-wide synchronisation of cudaMalloc / cudaFree, or a service that
 reserves all of its memory up front. It takes its scratch space from a 16 MiB
 array compiled into the library instead of allocating it. These tests call it
 through the C ABI twice in a row on the same graph and require results
-identical (bit for bit: the counts are integers) to gs_count_4pcf_parity.
+identical (bit for bit: the counts are integers) to gs_count_4pcf_parity and
+to the oracle's count over the same input, and they check that the calls
+allocate nothing (the library's allocation counter does not move).
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
 """
@@ -15,6 +17,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from cosmology_point_correlation_gb300 import _lib, catalogues
 from tests.gpu_util import gpu_graph, torch_dev
 
@@ -59,9 +62,15 @@ def test_static_workspace_matches_allocating_entry_point(make):
         ref_even, ref_odd = _count(lib.gs_count_4pcf_parity, g, torch, dev, m)
         assert ref_even.sum() > 0
         for _ in range(2):                                        # the workspace is reused
+            before = lib.gs_alloc_calls()
             even, odd = _count(lib.gs_count_4pcf_parity_static, g, torch, dev, m)
+            assert lib.gs_alloc_calls() == before, "the fixed-workspace call allocated memory"
             assert np.array_equal(even, ref_even)
             assert np.array_equal(odd, ref_odd)
+    # the oracle over the same points (the counts do not depend on input order)
+    o_even, o_odd = oracle.count_4pcf_parity(xyz, box, periodic, edges)
+    assert np.array_equal(even.view(np.uint64), o_even)
+    assert np.array_equal(odd, o_odd)
 
 
 def test_static_workspace_refuses_hubs_too_large():
