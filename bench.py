@@ -573,24 +573,13 @@ def run_ours(args, w):
         with build_graph(wc, wbox, ww.periodic, ww.edges_lu) as g:
             t_res, h_res, ts_res = _count_ms(g)
             e_all = g.n_edges
-            # a windowed count walks one spoke per warp; the resident count of a
-            # graph with short rows walks four (GS_COUNT3_WALK selects the walk), so
-            # the overhead of windows is taken against the resident one-spoke walk
-            walk_env = os.environ.get("GS_COUNT3_WALK")
-            os.environ["GS_COUNT3_WALK"] = "warp"
-            try:
-                t_res_warp, h_res_warp, ts_res_warp = _count_ms(g)
-            finally:
-                if walk_env is None:
-                    del os.environ["GS_COUNT3_WALK"]
-                else:
-                    os.environ["GS_COUNT3_WALK"] = walk_env
+            res_walk = g.count3_walk
         rows = []
         for nwin in (2, 4, 8):
             with build_graph(wc, wbox, ww.periodic, ww.edges_lu, window_edges=e_all // nwin + 1) as g:
                 t_w, h_w, ts_w = _count_ms(g)
-                rows.append({"window_edges": e_all // nwin + 1, "windows": g.windows()[0], "count_ms": t_w,
-                             "count_ms_runs": ts_w, "overhead": t_w / t_res_warp - 1.0,
+                rows.append({"window_edges": e_all // nwin + 1, "windows": g.windows()[0], "walk": g.count3_walk,
+                             "count_ms": t_w, "count_ms_runs": ts_w, "overhead": t_w / t_res - 1.0,
                              "exact": bool(np.array_equal(h_w, h_res))})
         # pinned host -> device copy rate in this process, which bounds the window staging
         hbuf = torch.empty(1 << 28, dtype=torch.int32).pin_memory()
@@ -605,10 +594,8 @@ def run_ours(args, w):
         h2d_gbs = hbuf.numel() * 4 / 1e9 / (e0.elapsed_time(e1) / 1e3)
         del hbuf, dbuf
         windowed = {"config": wdesc, "resident_count_ms": t_res, "resident_count_ms_runs": ts_res,
-                    "resident_count_ms_one_spoke_walk": t_res_warp,
-                    "resident_count_ms_one_spoke_walk_runs": ts_res_warp,
-                    "walks_agree": bool(np.array_equal(h_res, h_res_warp)),
-                    "overhead_against": "resident_count_ms_one_spoke_walk (the walk the windowed count uses)",
+                    "resident_walk": res_walk,
+                    "overhead_against": "resident_count_ms (the tiles run the same walk)",
                     "n_edges": e_all, "tiles": rows, "pinned_h2d_gbs": h2d_gbs}
 
     # CPU oracle on a bounded hub sample of the same catalogue (rank 0 only)

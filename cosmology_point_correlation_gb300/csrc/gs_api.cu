@@ -27,7 +27,10 @@ extern "C" int64_t gs_config_index_4pcf(int nbins, int b1, int b2, int b3)
     return gs_idx4(nbins, b1, b2, b3);
 }
 
-extern "C" const char *gs_version(void) { return "gramsci_gb 0.1 (sm_103a)"; }
+extern "C" const char *gs_version(void)
+{
+    return GS_CHECKED_BUILD ? "gramsci_gb 0.2 (sm_103a, checked)" : "gramsci_gb 0.2 (sm_103a)";
+}
 
 // Copy host coordinates to the device and build the graph.
 static gs_status build_from_host(const int32_t *coords_host, int64_t n, int64_t box_lu, int periodic,

@@ -17,6 +17,8 @@
 #include <cstring>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gs_internal.cuh"
 
 // ---------------------------------------------------------------- errors
@@ -38,15 +40,20 @@ static thread_local int t_depth = 0;                 // public calls in progress
 static thread_local int64_t t_alloc_ordinal = 0;     // allocations since the outermost one began
 static std::atomic<uint64_t> g_allocs{ 0 };
 
-gs_call_scope::gs_call_scope()
+gs_call_scope::gs_call_scope(const char *name)
 {
+    nvtxRangePushA(name);
     if (t_depth++ == 0) {
         g_msg[0] = 0;
         t_alloc_ordinal = 0;
     }
 }
 
-gs_call_scope::~gs_call_scope() { --t_depth; }
+gs_call_scope::~gs_call_scope()
+{
+    --t_depth;
+    nvtxRangePop();
+}
 
 cudaError_t gs_alloc_gate()
 {
@@ -58,6 +65,32 @@ cudaError_t gs_alloc_gate()
 }
 
 extern "C" uint64_t gs_alloc_calls(void) { return g_allocs.load(); }
+
+gs_status gs_checked_begin(gs_graph_t g, cudaStream_t st)
+{
+#ifdef GS_CHECKED
+    GS_TRY_CUDA(cudaMemsetAsync(g->chk, 0, sizeof(unsigned), st));
+#else
+    (void)g;
+    (void)st;
+#endif
+    return GS_OK;
+}
+
+gs_status gs_checked_end(gs_graph_t g, cudaStream_t st, const char *what)
+{
+#ifdef GS_CHECKED
+    unsigned h = 0;
+    GS_TRY_CUDA(cudaMemcpyAsync(&h, g->chk, sizeof(unsigned), cudaMemcpyDeviceToHost, st));
+    GS_TRY_CUDA(cudaStreamSynchronize(st));
+    if (h) return gs_set_error(GS_ERR_INTERNAL, "%s: device bounds checks failed at sites 0x%x", what, h);
+#else
+    (void)g;
+    (void)st;
+    (void)what;
+#endif
+    return GS_OK;
+}
 
 static std::atomic<uint64_t> g_launches{ 0 };
 
@@ -294,7 +327,8 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
             const long long *__restrict__ esq, int nb,
             int32_t *__restrict__ deg, int32_t *__restrict__ fwd,
             const int64_t *__restrict__ row_ptr, int32_t *__restrict__ nbr,
-            uint8_t *__restrict__ bin, unsigned *__restrict__ max_deg, int cell0, int64_t woff)
+            uint8_t *__restrict__ bin, unsigned *__restrict__ max_deg, int cell0, int64_t woff,
+            unsigned *__restrict__ chk, int64_t cap)
 {
     __shared__ int4 s_home[NB_HOME];
     __shared__ int s_cnt[NB_HOME];
@@ -391,8 +425,11 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
                                 const int mid = (lo_b + hi_b) >> 1;
                                 if (s_esq[mid] <= d2) lo_b = mid; else hi_b = mid;
                             }
-                            nbr[pos] = cb + t;
-                            bin[pos] = (uint8_t)lo_b;
+                            // checked builds: the edge lies in its own row and in the array
+                            if (GS_DCHECK(pos >= 0 && pos < cap && pos + woff < row_ptr[p + 1], chk, GS_SITE_NB_ROW)) {
+                                nbr[pos] = cb + t;
+                                bin[pos] = (uint8_t)lo_b;
+                            }
                         }
                         cnt += __popc(m);
                         if (!FILL) lo += __popc(__ballot_sync(0xffffffffu, hit && cb + t < p));
@@ -439,6 +476,7 @@ static void free_graph_arrays(gs_graph *g)
     cudaFree(g->bin);
     cudaFree(g->work);
     cudaFree(g->err);
+    cudaFree(g->chk);
     cudaFree(g->cfg3);
     cudaFree(g->cfg6);
     cudaFree(g->w);
@@ -452,6 +490,7 @@ static void free_graph_arrays(gs_graph *g)
     delete[] g->win_e0;
     delete[] g->win_maxnbr;
     delete[] g->win_pair;
+    delete[] g->win_first;
 }
 
 extern "C" void gs_graph_free(gs_graph_t g)
@@ -512,11 +551,12 @@ static std::vector<int> plan_windows(gs_graph *g, const std::vector<int32_t> &cs
     return wc;
 }
 
-// pair[w] = 1 for every window w that holds a forward neighbour of a row in
-// [r0, r1) (edges staged at nbr - off; win_row on the device, nw + 1 entries).
+// first[w] = the smallest i - r0 over the rows i in [r0, r1) that have a
+// forward neighbour in window w (0xffffffff: none); edges staged at
+// nbr - off; win_row on the device, nw + 1 entries.
 __global__ void k_window_pairs(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ fwd,
                                const int32_t *__restrict__ nbr, int64_t off, int64_t r0, int64_t r1,
-                               const int64_t *__restrict__ win_row, int nw, unsigned *__restrict__ pair)
+                               const int64_t *__restrict__ win_row, int nw, unsigned *__restrict__ first)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -529,7 +569,8 @@ __global__ void k_window_pairs(const int64_t *__restrict__ row_ptr, const int32_
                 const int m = (lo + hi) >> 1;
                 if (win_row[m] <= k) lo = m; else hi = m;
             }
-            if (!pair[lo]) atomicOr(pair + lo, 1u);
+            const unsigned r = (unsigned)(i - r0);
+            if (r < first[lo]) atomicMin(first + lo, r);
         }
 }
 
@@ -633,6 +674,8 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
         GS_BUILD_CUDA(gs_malloc(&g->fwd, sizeof(int32_t) * nn));
         GS_BUILD_CUDA(gs_malloc(&g->work, sizeof(unsigned long long) * 4));
         GS_BUILD_CUDA(gs_malloc(&g->err, sizeof(int32_t)));
+        GS_BUILD_CUDA(gs_malloc(&g->chk, sizeof(unsigned)));
+        GS_BUILD_CUDA(cudaMemset(g->chk, 0, sizeof(unsigned)));
         if (nbins <= 40) {
             // configuration index of every (z, x, y) bin triple, for the 3pCF kernel
             std::vector<uint16_t> h((size_t)nbins * nbins * nbins);
@@ -682,7 +725,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
             k_neighbors<false><<<ncells, NB_THREADS, 0, st>>>(
                 g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                 (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
-                deg, g->fwd, nullptr, nullptr, nullptr, maxd, 0, 0);
+                deg, g->fwd, nullptr, nullptr, nullptr, maxd, 0, 0, g->chk, 0);
             gs_note_launch();
             GS_BUILD_CUDA(cudaGetLastError());
         }
@@ -704,6 +747,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
 
         const size_t ne = (size_t)(g->n_edges + GS_EDGE_PAD);
         const int64_t wedges = choose_window_edges(window_edges, g->n_edges);
+        g->nbr_len = (int64_t)ne;
         if (wedges == 0) {
             GS_BUILD_CUDA(gs_malloc(&g->nbr, sizeof(int32_t) * ne));
             GS_BUILD_CUDA(gs_malloc(&g->bin, ne));
@@ -713,7 +757,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
                 k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
                     g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                     (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
-                    nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr, 0, 0);
+                    nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr, 0, 0, g->chk, (int64_t)ne);
                 gs_note_launch();
                 GS_BUILD_CUDA(cudaGetLastError());
             }
@@ -732,17 +776,19 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
             GS_BUILD_CUDA(gs_malloc_host(&g->h_bin, ne));
             memset(g->h_nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD);
             memset(g->h_bin + g->n_edges, 0, GS_EDGE_PAD);
+            g->nbr_len = g->win_cap;
             for (int k = 0; k < GS_SLOTS; ++k) {
                 GS_BUILD_CUDA(gs_malloc(&g->s_nbr[k], sizeof(int32_t) * (size_t)g->win_cap));
                 GS_BUILD_CUDA(gs_malloc(&g->s_bin[k], (size_t)g->win_cap));
             }
             const int nw = g->n_win;
             g->win_pair = new uint8_t[(size_t)nw * nw]();
+            g->win_first = new int64_t[(size_t)nw * nw]();
             std::vector<unsigned> hpair((size_t)nw * nw, 0u);
             GS_BUILD_CUDA(gs_malloc_async(&wrow_dev, sizeof(int64_t) * (nw + 1), st));
             GS_BUILD_CUDA(gs_malloc_async(&pair_dev, sizeof(unsigned) * (size_t)nw * nw, st));
             GS_BUILD_CUDA(cudaMemcpyAsync(wrow_dev, g->win_row, sizeof(int64_t) * (nw + 1), cudaMemcpyHostToDevice, st));
-            GS_BUILD_CUDA(cudaMemsetAsync(pair_dev, 0, sizeof(unsigned) * (size_t)nw * nw, st));
+            GS_BUILD_CUDA(cudaMemsetAsync(pair_dev, 0xff, sizeof(unsigned) * (size_t)nw * nw, st));
             for (int w = 0; w < g->n_win; ++w) {
                 const int cell0 = wc[w], cell1 = wc[w + 1];
                 const int64_t e0 = g->win_e0[w], e1 = g->win_e0[w + 1];
@@ -751,7 +797,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
                     k_neighbors<true><<<cell1 - cell0, NB_THREADS, 0, st>>>(
                         g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                         (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
-                        nullptr, nullptr, g->row_ptr, g->s_nbr[0], g->s_bin[0], nullptr, cell0, a);
+                        nullptr, nullptr, g->row_ptr, g->s_nbr[0], g->s_bin[0], nullptr, cell0, a, g->chk, g->win_cap);
                     gs_note_launch();
                     GS_BUILD_CUDA(cudaGetLastError());
                     GS_BUILD_CUDA(cudaMemcpyAsync(g->h_nbr + e0, g->s_nbr[0] + (e0 - a), sizeof(int32_t) * (e1 - e0),
@@ -769,11 +815,18 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
             GS_BUILD_CUDA(cudaMemcpyAsync(hpair.data(), pair_dev, sizeof(unsigned) * hpair.size(),
                                           cudaMemcpyDeviceToHost, st));
             GS_BUILD_CUDA(cudaStreamSynchronize(st));
-            for (size_t q = 0; q < hpair.size(); ++q) g->win_pair[q] = hpair[q] ? 1 : 0;
+            for (size_t q = 0; q < hpair.size(); ++q) {
+                g->win_pair[q] = hpair[q] != 0xffffffffu ? 1 : 0;
+                g->win_first[q] = g->win_row[q / nw] + (g->win_pair[q] ? (int64_t)hpair[q] : 0);
+            }
             for (int w = 0; w < g->n_win; ++w)        // rows are sorted: the last entry is the row's largest
                 for (int64_t i = g->win_row[w]; i < g->win_row[w + 1]; ++i)
                     if (hrp[i + 1] > hrp[i]) g->win_maxnbr[w] = std::max(g->win_maxnbr[w], g->h_nbr[hrp[i + 1] - 1]);
         }
+    }
+    if (GS_CHECKED_BUILD) {                                   // the fill kernels' bounds checks
+        s = gs_checked_end(g, st, "graph build");
+        if (s != GS_OK) goto fail;
     }
     cudaFreeAsync(cell, st);
     cudaFreeAsync(slot, st);

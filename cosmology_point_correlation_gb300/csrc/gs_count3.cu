@@ -96,6 +96,8 @@ struct C3Args {
     const int16_t *w;
     unsigned long long *gsum;
     unsigned long long *slices;   // weighted: the caller's scratch of c3_slice_bytes() bytes
+    unsigned *chk;                // checked builds: the graph's check word
+    int64_t nbr_len;              // entries readable at snbr / sbin (checked builds)
 };
 
 // Flush the shared histogram into the global one and clear it.
@@ -511,7 +513,11 @@ k_count3(C3Args a)
                                 const unsigned up = (old + (unsigned)p < old ? 1u : 0u) + (p < 0 ? ~0u : 0u);
                                 if (up) atomicAdd(q + 1, up);
                             }
-                            else if (SMEM_HIST) atomicAdd(&s_hist[tab[bik * nb + bjk]], 1u);
+                            else if (SMEM_HIST) {
+                                const int c = tab[bik * nb + bjk];
+                                if (GS_DCHECK(bik < nb && bjk < nb && c < a.ncfg, a.chk, GS_SITE_C3_HIST))
+                                    atomicAdd(&s_hist[c], 1u);
+                            }
                             else atomicAdd(a.ghist + c3_index(bij, bik, bjk, s_lex_a, s_lex_b), 1ull);
                         };
                         // Walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
@@ -555,7 +561,8 @@ k_count3(C3Args a)
                                     const unsigned w = s_bm[o >> 5];
                                     if ((w >> (o & 31u)) & 1u) {
                                         const int rank = s_rank[o >> 5] + __popc(w & ((1u << (o & 31u)) - 1u));
-                                        hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
+                                        if (GS_DCHECK(rank < cn, a.chk, GS_SITE_C3_BITMAP))
+                                            hit(s_cbin[rank], (bb >> (8 * e)) & 0xffu, WEIGHTED ? s_cw[rank] : 0);
                                     }
                                 }
                             } else {
@@ -708,6 +715,25 @@ __device__ __forceinline__ void c3m_flush(unsigned *h, int nb, const uint16_t *c
 // The part [*p0, *pe) of N(j) that spoke s (j = F[s]) walks against the chunk
 // starting at c0 (first key kfirst): from the first entry beyond j, or, for a
 // spoke of an earlier chunk, from the first entry >= kfirst (binary search).
+// First position of the sorted row F[0, f) whose id is >= key, found by the 32
+// lanes of a warp together: each round probes 32 evenly spaced positions, so
+// a row of up to 32^r entries takes r + 1 dependent loads.
+__device__ __forceinline__ int c3m_warp_lower_bound(const int32_t *F, int f, int32_t key)
+{
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = f;                                      // the answer lies in [lo, hi]
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) >> 5;
+        const int p = lo + lane * step;
+        const int c = __popc(__ballot_sync(0xffffffffu, p < hi && F[p] < key));   // probes below key
+        const int nlo = c > 0 ? lo + (c - 1) * step + 1 : lo;
+        hi = min(hi, lo + c * step);
+        lo = nlo;
+    }
+    const int p = lo + lane;
+    return lo + __popc(__ballot_sync(0xffffffffu, p < hi && F[p] < key));
+}
+
 // Spoke rows are read at e - soff (a staged window of a windowed graph, else 0).
 __device__ __forceinline__ void c3m_spoke_range(const C3Args &a, int64_t soff, int32_t j, int s, int c0,
                                                 int32_t kfirst, int64_t *p0, int64_t *pe)
@@ -729,15 +755,36 @@ __device__ __forceinline__ void c3m_spoke_range(const C3Args &a, int64_t soff, i
 // into H[b_ij][b_ik][b_jk] (hb = b_ij nb^2; bins of the four entries in bb).
 __device__ __forceinline__ void c3m_probe4(const int k[4], uint32_t bb, int32_t kbase, unsigned guard,
                                            const uint8_t *s_seg, const uint8_t *s_map, unsigned *s_h, int hb,
-                                           int nb)
+                                           int nb, const C3Args &a, int nslots)
 {
+#ifdef GS_CHECKED
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const unsigned o = min((unsigned)(k[e] - kbase), guard);
         const unsigned sl = s_seg[o >> C3M_SEG_LOG];
+        if (!GS_DCHECK(sl <= (unsigned)nslots, a.chk, GS_SITE_C3M_MAP_R)) continue;
         const unsigned b = s_map[(sl << C3M_SEG_LOG) | (o & (C3M_SEG - 1))];
-        if (b != C3M_ABSENT) atomicAdd(&s_h[hb + (int)b * nb + (int)((bb >> (8 * e)) & 0xffu)], 1u);
+        if (b == C3M_ABSENT) continue;
+        const int idx = hb + (int)b * nb + (int)((bb >> (8 * e)) & 0xffu);
+        if (GS_DCHECK(b < (unsigned)nb && idx >= 0 && idx < nb * nb * nb, a.chk, GS_SITE_C3M_HIST))
+            atomicAdd(s_h + idx, 1u);
     }
+#else
+    (void)a;
+    (void)nslots;
+    const unsigned h0 = (unsigned)__cvta_generic_to_shared(s_h) + 4u * (unsigned)hb;
+    const unsigned nb4 = 4u * (unsigned)nb;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const unsigned o = min((unsigned)(k[e] - kbase), guard);
+        const unsigned sl = s_seg[o >> C3M_SEG_LOG];
+        const unsigned b = s_map[sl * C3M_SEG + (o & (C3M_SEG - 1))];
+        // a predicated reduction, no branch: a lane whose entry is absent adds nothing
+        const unsigned addr = h0 + b * nb4 + 4u * __byte_perm(bb, 0u, 0x4440u + (unsigned)e);
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 255;\n\t@p red.shared.add.u32 [%1], 1;\n\t}"
+                     :: "r"(b), "r"(addr) : "memory");
+    }
+#endif
 }
 
 // Four spokes per warp, eight lanes each (for rows of a few hundred entries,
@@ -747,7 +794,7 @@ __device__ __forceinline__ void c3m_probe4(const int k[4], uint32_t bb, int32_t 
 __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, const int32_t *F, const uint8_t *FB,
                                                  int s_lo, int s_end, int c0, int32_t kfirst, int32_t kbase,
                                                  int32_t kmax, unsigned guard, const uint8_t *s_seg,
-                                                 const uint8_t *s_map, unsigned *s_h, int *s_next)
+                                                 const uint8_t *s_map, unsigned *s_h, int *s_next, int nslots)
 {
     const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
     const int nb = a.nb, nb2 = nb * nb;
@@ -770,7 +817,8 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
         const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + gl;
         int4 kk = make_int4(0, 0, 0, 0);
         uint32_t bb = 0;
-        bool go = total > 0;                                 // the same in the eight lanes of a group
+        // checked builds: the group's last vector of the row lies in the readable array
+        bool go = total > 0 && GS_DCHECK((pa - soff) + (((total + 31) >> 5) << 5) <= a.nbr_len, a.chk, GS_SITE_C3M_ROW);
         if (go) {
             kk = __ldg(vk);
             bb = __ldg(vb);
@@ -788,12 +836,11 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
             if (go) {
                 int k[4] = { kk.x, kk.y, kk.z, kk.w };
                 if (base == 0 || base + 32 > total) {
-                    const int r0 = base + 4 * gl;
+                    const unsigned r0 = (unsigned)(base + 4 * gl - head), len = (unsigned)(total - head);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (r0 + e < head || r0 + e >= total) k[e] = kbase - 1;
+                    for (int e = 0; e < 4; ++e) k[e] = r0 + e < len ? k[e] : kbase - 1;
                 }
-                c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb);
+                c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
             }
             // rows are sorted: a group stops once its step's last key passes kmax
             const int last = __shfl_sync(0xffffffffu, kk.w, lane | 7);
@@ -811,8 +858,8 @@ k_count3m(C3Args a, int nslots)
     constexpr int WARPS = THREADS / 32;
     constexpr int KPT = C3M_KEYS_PER_THREAD;
     constexpr int MAX_KEYS = THREADS * KPT;
-    // dynamic: histogram [nb^3] u32, segment table [C3M_SEG_TABLE] u8,
-    // map [(nslots + 1) * C3M_SEG] u8 (slot 0: the all-absent segment)
+    // dynamic: segment table [C3M_SEG_TABLE] u8, map [(nslots + 1) * C3M_SEG] u8
+    // (slot 0: the all-absent segment), histogram [nb^3] u32
     extern __shared__ unsigned s_dyn[];
     __shared__ int s_next;
     __shared__ int s_cut;
@@ -824,9 +871,11 @@ k_count3m(C3Args a, int nslots)
     const int lane = threadIdx.x & 31;
     const int nb = a.nb, nb2 = nb * nb, n3 = nb2 * nb;
     const int64_t soff = WINDOWED ? a.soff : 0;
-    unsigned *s_h = s_dyn;
-    uint8_t *s_seg = reinterpret_cast<uint8_t *>(s_dyn + ((n3 + 3) & ~3));
+    // the segment table and the map first, at fixed offsets (their probes need
+    // no base register), then the histogram
+    uint8_t *s_seg = reinterpret_cast<uint8_t *>(s_dyn);
     uint8_t *s_map = s_seg + C3M_SEG_TABLE;
+    unsigned *s_h = reinterpret_cast<unsigned *>(s_map + (size_t)(nslots + 1) * C3M_SEG);
 
     for (int t = threadIdx.x; t < n3; t += THREADS) s_h[t] = 0;
     for (int t = threadIdx.x; t < C3M_SEG / 16; t += THREADS)
@@ -849,13 +898,14 @@ k_count3m(C3Args a, int nslots)
         // unless the graph is windowed; rows are sorted, so a window is a range)
         int q_lo = 0, q_hi = f;
         if (WINDOWED) {
-            if (threadIdx.x == 0) {
-                int lo = 0, hi = f;
-                while (lo < hi) { const int m = (lo + hi) >> 1; if (F[m] < a.s_lo) lo = m + 1; else hi = m; }
-                s_q[0] = lo;
-                hi = f;
-                while (lo < hi) { const int m = (lo + hi) >> 1; if (F[m] < a.s_hi) lo = m + 1; else hi = m; }
-                s_q[1] = lo;
+            if (threadIdx.x < 32) {
+                // rows are sorted: the tile's spokes [s_lo, s_hi) are one range of F
+                const int lo = F[f - 1] < a.s_lo ? f : c3m_warp_lower_bound(F, f, a.s_lo);
+                const int hi = lo >= f ? f : c3m_warp_lower_bound(F, f, a.s_hi);
+                if (threadIdx.x == 0) {
+                    s_q[0] = lo;
+                    s_q[1] = hi;
+                }
             }
             __syncthreads();
             q_lo = s_q[0];
@@ -910,6 +960,9 @@ k_count3m(C3Args a, int nslots)
                     if (t0 + q >= c1) break;
                     slot += (starts >> q) & 1u;
                     const int off = key[q] - kbase;
+                    if (!GS_DCHECK(slot >= 1 && slot <= nslots && off >= 0 && (off >> C3M_SEG_LOG) < C3M_SPAN_SEGS,
+                                   a.chk, GS_SITE_C3M_MAP_W))
+                        continue;
                     if ((starts >> q) & 1u) s_seg[off >> C3M_SEG_LOG] = (uint8_t)slot;
                     s_map[(slot << C3M_SEG_LOG) | (off & (C3M_SEG - 1))] = FB[t0 + q];
                 }
@@ -937,7 +990,7 @@ k_count3m(C3Args a, int nslots)
 
             if (GROUPED) {
                 c3m_walk_grouped(a, soff, F, FB, q_lo, s_end, c0, kfirst, kbase, kmax, guard, s_seg, s_map, s_h,
-                                 &s_next);
+                                 &s_next, nslots);
             } else {
                 // ---- spokes, one per warp, handed out in row order
                 for (;;) {
@@ -949,37 +1002,57 @@ k_count3m(C3Args a, int nslots)
                     c3m_spoke_range(a, soff, F[s], s, c0, kfirst, &p0, &pe);
                     const int hb = FB[s] * nb2;
                     if (p0 >= pe) continue;
-                    // walk nbr[p0, pe) in aligned 128-entry steps: lane l reads entries
-                    // 4l .. 4l+3 of a step as one int4 and their bins as one word
+                    // walk nbr[p0, pe) in aligned 256-entry steps: lane l reads entries
+                    // 4l .. 4l+3 and 128+4l .. 128+4l+3 of a step as two int4 and their
+                    // bins as two words
                     const int64_t pa = p0 & ~(int64_t)3;
                     const int head = (int)(p0 - pa);
                     const int total_e = head + (int)(pe - p0);
+                    // checked builds: the walk's last loaded half step lies in the readable array
+                    if (!GS_DCHECK((pa - soff) + (((total_e + 127) >> 7) << 7) <= a.nbr_len, a.chk, GS_SITE_C3M_ROW))
+                        continue;
                     const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + lane;
                     const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + lane;
-                    int4 kk = __ldg(vk);
-                    uint32_t bb = __ldg(vb);
-                    for (int base = 0; base < total_e; base += 128) {
-                        vk += 32;
-                        vb += 32;
-                        int4 kn = kk;
-                        uint32_t bn = bb;
-                        if (base + 128 < total_e) {                // next step in flight
+                    // a half step is loaded only when it starts before the row's end:
+                    // the arrays hold GS_EDGE_PAD (128) entries past the last row
+                    int4 kk = __ldg(vk), kk2 = make_int4(0, 0, 0, 0);
+                    uint32_t bb = __ldg(vb), bb2 = 0;
+                    if (128 < total_e) {
+                        kk2 = __ldg(vk + 32);
+                        bb2 = __ldg(vb + 32);
+                    }
+                    for (int base = 0; base < total_e; base += 256) {
+                        vk += 64;
+                        vb += 64;
+                        int4 kn = kk, kn2 = kk2;
+                        uint32_t bn = bb, bn2 = bb2;
+                        if (base + 256 < total_e) {                // next step in flight
                             kn = __ldg(vk);
                             bn = __ldg(vb);
+                            if (base + 384 < total_e) {
+                                kn2 = __ldg(vk + 32);
+                                bn2 = __ldg(vb + 32);
+                            }
                         }
                         int k[4] = { kk.x, kk.y, kk.z, kk.w };
-                        if (base == 0 || base + 128 > total_e) {   // first / last step only
+                        int k2[4] = { kk2.x, kk2.y, kk2.z, kk2.w };
+                        if (base == 0 || base + 256 > total_e) {   // first / last step only
                             // entries outside [p0, pe) become kbase - 1, whose offset clamps to the guard
-                            const int r0 = base + 4 * lane;
+                            const unsigned r0 = (unsigned)(base + 4 * lane - head), len = (unsigned)(total_e - head);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (r0 + e < head || r0 + e >= total_e) k[e] = kbase - 1;
+                            for (int e = 0; e < 4; ++e) {
+                                k[e] = r0 + e < len ? k[e] : kbase - 1;
+                                k2[e] = r0 + 128 + e < len ? k2[e] : kbase - 1;
+                            }
                         }
-                        c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb);
+                        c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
+                        c3m_probe4(k2, bb2, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
                         // rows are sorted: stop once the step's last key passes kmax
-                        if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) break;
+                        if (__shfl_sync(0xffffffffu, kk2.w, 31) > kmax) break;
                         kk = kn;
+                        kk2 = kn2;
                         bb = bn;
+                        bb2 = bn2;
                     }
                 }
             }
@@ -1104,18 +1177,18 @@ static bool plan_count3g(gs_graph_t g, bool forced, size_t *dyn)
 }
 
 // The walk an unweighted count takes: 2 = byte map, one spoke per warp (long
-// rows of a device-resident graph: mean degree above C3_GROUPED_MAX_DEGREE,
-// at most C3M_MAX_BINS bins); 1 = bitmap, four spokes per warp (short rows);
-// 0 = bitmap, one spoke per warp (windowed graphs, and when neither fits).
-// GS_COUNT3_WALK overrides the choice; 3 = byte map, four spokes per warp, is
-// taken only on request.
+// rows: mean degree above C3_GROUPED_MAX_DEGREE); 3 = byte map, four spokes
+// per warp (short rows); when the byte map does not fit (more than
+// C3M_MAX_BINS bins) 1 = bitmap, four spokes per warp (device-resident
+// graphs) or 0 = bitmap, one spoke per warp. GS_COUNT3_WALK overrides the
+// choice.
 static int count3_walk(gs_graph_t g)
 {
     int mode = count3_walk_override();
     const bool long_rows = g->n_edges > C3_GROUPED_MAX_DEGREE * g->n;
     int t, sl;
     size_t d;
-    if (mode < 0) mode = (long_rows && !g->n_win) ? 2 : 1;
+    if (mode < 0) mode = long_rows ? 2 : 3;
     if (mode >= 2 && plan_count3m(g, mode == 3, g->n_win > 0, &t, &sl, &d)) return mode;
     if (g->n_win) return 0;                                  // the bitmap walk of windowed tiles
     if (mode == 1 || mode == 3 || (mode == 2 && !long_rows)) return plan_count3g(g, mode == 1, &d) ? 1 : 0;
@@ -1295,8 +1368,14 @@ static gs_status run_count3(gs_graph_t g, C3Args a, int64_t hub_begin, int64_t h
         a.soff = off[sw];
         a.s_lo = (int32_t)g->win_row[w];
         a.s_hi = (int32_t)g->win_row[w + 1];
-        a.hub_begin = std::max(hub_begin, g->win_row[h]);
+        // hubs of window h before the first one with a forward neighbour in w hold no work
+        a.hub_begin = std::max(hub_begin, g->win_first[(size_t)h * g->n_win + w]);
         a.hub_end = std::min(hub_end, g->win_row[h + 1]);
+        if (a.hub_begin >= a.hub_end) {
+            e = cudaEventRecord(done[sh], st);
+            if (e == cudaSuccess) e = cudaEventRecord(done[sw], st);
+            continue;
+        }
         s = launch_count3(g, a, a.hub_end - a.hub_begin, st);
         if (s != GS_OK) break;
         e = cudaEventRecord(done[sh], st);
@@ -1346,6 +1425,8 @@ static C3Args count3_args(gs_graph_t g, uint64_t *hist_dev)
     a.cursor = g->work;
     a.cfg3 = g->cfg3;
     a.inv = g->inv;
+    a.chk = g->chk;
+    a.nbr_len = g->nbr_len;
     return a;
 }
 
@@ -1362,7 +1443,10 @@ extern "C" gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub
     const int ncfg = (int)gs_ncfg3(g->nb);
     GS_TRY_CUDA(cudaMemsetAsync(hist_dev, 0, sizeof(uint64_t) * ncfg, st));
     if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
-    return run_count3(g, count3_args(g, hist_dev), hub_begin, hub_end, st);
+    gs_status s = gs_checked_begin(g, st);
+    if (s == GS_OK) s = run_count3(g, count3_args(g, hist_dev), hub_begin, hub_end, st);
+    if (s == GS_OK) s = gs_checked_end(g, st, "3pCF count");
+    return s;
 }
 
 // Range check of a device list of input indices, one flag word for the host.
@@ -1405,7 +1489,10 @@ extern "C" gs_status gs_count_3pcf_hubs(gs_graph_t g, const int32_t *hubs_dev, i
     a.hub_begin = 0;
     a.hub_end = count;
     a.hubs = hubs_dev;
-    return launch_count3(g, a, count, st);
+    s = gs_checked_begin(g, st);
+    if (s == GS_OK) s = launch_count3(g, a, count, st);
+    if (s == GS_OK) s = gs_checked_end(g, st, "3pCF hub-list count");
+    return s;
 }
 
 extern "C" gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int64_t hub_begin, int64_t hub_end,
@@ -1434,7 +1521,9 @@ extern "C" gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int
         a.w = g->w;
         a.gsum = (unsigned long long *)sums_dev;
         a.slices = slices;
-        s = run_count3(g, a, hub_begin, hub_end, st);
+        s = gs_checked_begin(g, st);
+        if (s == GS_OK) s = run_count3(g, a, hub_begin, hub_end, st);
+        if (s == GS_OK) s = gs_checked_end(g, st, "weighted 3pCF count");
     }
     if (slices) cudaFreeAsync(slices, st);
     return s;

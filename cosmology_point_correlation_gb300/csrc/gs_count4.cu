@@ -36,6 +36,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "gs_internal.cuh"
@@ -74,7 +75,16 @@ struct C4Args {
     const uint8_t *hbin;
     int64_t hoff, aoff, boff;
     int32_t a_lo, a_hi, b_lo, b_hi;
+    unsigned *chk;                // checked builds: the graph's check word
 };
+
+// Bins up to which the clique's packed index and bin-sorting parity come from
+// one table of nb^3 entries (in the shared memory of the per-bin index tables).
+constexpr int C4_TAB_BINS = 10;
+// r_max (lattice units) up to which a spoke-pair cross product fits in int32:
+// components |r| <= 32767, so |y1 z2 - z1 y2| <= 2 * 32767^2 < 2^31
+constexpr int64_t C4_SMALL_R = 32768;
+static_assert(C4_TAB_BINS * C4_TAB_BINS * C4_TAB_BINS * 2 <= 512 * 4, "the u16 table must fit the index tables' space");
 
 // First position of a sorted row whose id is >= key.
 __device__ __forceinline__ int c4_lower(const int32_t *row, int m, int32_t key)
@@ -99,9 +109,9 @@ struct HubSpace {
     int *next;         // shared counter handing out the rows s1 of the clique search
 };
 
-template <bool SMEM_HIST, bool WINDOWED>
+template <bool SMEM_HIST, bool WINDOWED, bool SMALLR>
 __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long long i, int m,
-                                       int tlog, unsigned *s_even, int *s_odd,
+                                       int tlog, unsigned long long *s_eo,
                                        const int *lex_a, const int *lex_b)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -165,7 +175,8 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
                 while ((key = w.key[h]) != k && key != C4_EMPTY) h = (h + 1) & mask;
                 if (key == k) {
                     const int t = w.pos[h];
-                    atomicOr(&w.bits[(size_t)s * W + (t >> 5)], 1u << (t & 31));
+                    if (GS_DCHECK(t > s && t < m, a.chk, GS_SITE_C4_BITS))
+                        atomicOr(&w.bits[(size_t)s * W + (t >> 5)], 1u << (t & 31));
                 }
             }
             if (__shfl_sync(0xffffffffu, k, 31) > kmax) break;
@@ -192,18 +203,32 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
         const int b1 = r1.w, x1 = r1.x, y1 = r1.y, z1 = r1.z;
         const unsigned *bm1 = w.bm + b1 * W;
         const unsigned *row1 = w.bits + (size_t)s1 * W;
+        // cross products in int32 when r_max < C4_SMALL_R, else int64
+        using CT = typename std::conditional<SMALLR, int, long long>::type;
         // s3's hub bin differs from b1 and b2 (the common bits were masked)
-        auto clique = [&](int b2, long long cx, long long cy, long long cz, int s3) {
+        auto clique = [&](int b2, CT cx, CT cy, CT cz, int s3) {
+            if (!GS_DCHECK(s3 > s1 && s3 < m, a.chk, GS_SITE_C4_BITS)) return;
             const int4 r3 = w.v[s3];
             const int b3 = r3.w;
-            const long long d = cx * r3.x + cy * r3.y + cz * r3.z;                // |d| < 3 * 2^60
+            const long long d = (long long)cx * r3.x + (long long)cy * r3.y + (long long)cz * r3.z;   // |d| < 3 * 2^60
             int sg = (d > 0) - (d < 0);
-            if (((b1 > b2) + (b1 > b3) + (b2 > b3)) & 1) sg = -sg;
-            const int lo = min(b1, min(b2, b3)), hi = max(b1, max(b2, b3));
-            const int idx = lex_a[lo] + lex_b[b1 + b2 + b3 - lo - hi] + hi;
+            int idx;
+            if (a.nb <= C4_TAB_BINS) {                             // block-uniform
+                // lex_a holds the table: (idx4 << 1) | parity of the sorting permutation
+                const int e = reinterpret_cast<const uint16_t *>(lex_a)[(b1 * a.nb + b2) * a.nb + b3];
+                idx = e >> 1;
+                if (e & 1) sg = -sg;
+            } else {
+                if (((b1 > b2) + (b1 > b3) + (b2 > b3)) & 1) sg = -sg;
+                const int lo = min(b1, min(b2, b3)), hi = max(b1, max(b2, b3));
+                idx = lex_a[lo] + lex_b[b1 + b2 + b3 - lo - hi] + hi;
+            }
+            if (!GS_DCHECK(idx >= 0 && idx < a.ncfg, a.chk, GS_SITE_C4_HIST)) return;
             if (SMEM_HIST) {
-                atomicAdd(&s_even[idx], 1u);
-                if (sg) atomicAdd(&s_odd[idx], sg);
+                // even count in the low word, odd sum in the high word of one 64-bit
+                // counter: one shared add per clique (the flush bound keeps the low
+                // word below 2^31, so no carry reaches the high word)
+                atomicAdd(&s_eo[idx], (unsigned long long)(((long long)sg << 32) + 1));
             } else {
                 atomicAdd(a.even + idx, 1ull);
                 if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
@@ -213,15 +238,15 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
             const int s2 = c2 + lane;
             bool valid = s2 < s2_end && ((row1[s2 >> 5] >> (s2 & 31)) & 1u);
             int b2 = 0;
-            long long cx = 0, cy = 0, cz = 0;
+            CT cx = 0, cy = 0, cz = 0;
             if (valid) {
                 const int4 r2 = w.v[s2];
                 b2 = r2.w;
                 valid = b2 != b1;
                 const int x2 = r2.x, y2 = r2.y, z2 = r2.z;                       // r_s1 x r_s2, |.| < 2^41
-                cx = (long long)y1 * z2 - (long long)z1 * y2;
-                cy = (long long)z1 * x2 - (long long)x1 * z2;
-                cz = (long long)x1 * y2 - (long long)y1 * x2;
+                cx = (CT)y1 * z2 - (CT)z1 * y2;
+                cy = (CT)z1 * x2 - (CT)x1 * z2;
+                cz = (CT)x1 * y2 - (CT)y1 * x2;
             }
             if (!__any_sync(0xffffffffu, valid)) continue;
             const unsigned *row2 = w.bits + (size_t)(valid ? s2 : s1) * W;
@@ -232,6 +257,7 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
                     common = row1[wd] & row2[wd] & ~(bm1[wd] | bm2[wd]);
                     if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // keep s3 > s2
                 }
+                if (!__ballot_sync(0xffffffffu, common != 0u)) continue;   // no clique in this word
                 const int cnt = __popc(common);
                 int inc = cnt;                                     // inclusive prefix over lanes
 #pragma unroll
@@ -249,10 +275,10 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
                     const unsigned cm = __shfl_sync(0xffffffffu, common, owner);
                     const int first = __shfl_sync(0xffffffffu, inc - cnt, owner);
                     const int o_b2 = __shfl_sync(0xffffffffu, b2, owner);
-                    const long long ocx = __shfl_sync(0xffffffffu, cx, owner);
-                    const long long ocy = __shfl_sync(0xffffffffu, cy, owner);
-                    const long long ocz = __shfl_sync(0xffffffffu, cz, owner);
-                    if (q < total) clique(o_b2, ocx, ocy, ocz, (wd << 5) + (int)__fns(cm, 0, q - first + 1));
+                    const CT ocx = __shfl_sync(0xffffffffu, cx, owner);
+                    const CT ocy = __shfl_sync(0xffffffffu, cy, owner);
+                    const CT ocz = __shfl_sync(0xffffffffu, cz, owner);
+                    if (q < total) clique(o_b2, ocx, ocy, ocz, (wd << 5) + gs_nth_bit(cm, q - first));
                 }
             }
         }
@@ -264,9 +290,22 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
 
 // gs_idx4(a, b, c) = F4(a) - H(a + 1) + H(b) + c - b - 1 with
 // H(t) = t (nb - 1) - t (t - 1) / 2 and F4(a) = gs_idx4(a, a + 1, a + 2),
-// split into two per-bin tables: idx4 = lex_a[a] + lex_b[b] + c.
+// split into two per-bin tables: idx4 = lex_a[a] + lex_b[b] + c. For
+// nb <= C4_TAB_BINS the space of both (contiguous) holds instead one u16 per
+// ordered triple (b1, b2, b3) of distinct bins: (idx4 of the sorted triple
+// << 1) | the parity of the permutation that sorts it.
 __device__ __forceinline__ void c4_lex_tables(int nb, int *lex_a, int *lex_b)
 {
+    if (nb <= C4_TAB_BINS) {
+        uint16_t *tab = reinterpret_cast<uint16_t *>(lex_a);
+        for (int t = threadIdx.x; t < nb * nb * nb; t += C4_THREADS) {
+            const int x = t / (nb * nb), y = (t / nb) % nb, z = t % nb;
+            if (x == y || x == z || y == z) continue;
+            const int lo = min(x, min(y, z)), hi = max(x, max(y, z)), mid = x + y + z - lo - hi;
+            tab[t] = (uint16_t)((gs_idx4(nb, lo, mid, hi) << 1) | (((x > y) + (x > z) + (y > z)) & 1));
+        }
+        return;
+    }
     for (int t = threadIdx.x; t < nb; t += C4_THREADS) {
         const int64_t h1 = (int64_t)(t + 1) * (nb - 1) - (int64_t)(t + 1) * t / 2;
         const int64_t h0 = (int64_t)t * (nb - 1) - (int64_t)t * (t - 1) / 2;
@@ -275,45 +314,44 @@ __device__ __forceinline__ void c4_lex_tables(int nb, int *lex_a, int *lex_b)
     }
 }
 
-__device__ __forceinline__ void c4_flush(unsigned *se, int *so, int ncfg, unsigned long long *ge, long long *go)
+// Add the shared counters (even count in the low word, odd sum as a signed
+// high word) into the caller's histograms and clear them.
+__device__ __forceinline__ void c4_flush(unsigned long long *seo, int ncfg, unsigned long long *ge, long long *go)
 {
     for (int t = threadIdx.x; t < ncfg; t += C4_THREADS) {
-        const unsigned e = se[t];
-        const int o = so[t];
+        const unsigned long long v = seo[t];
+        const unsigned e = (unsigned)v;
+        const int o = (int)(unsigned)(v >> 32);
         if (e) atomicAdd(ge + t, (unsigned long long)e);
         if (o) atomicAdd((unsigned long long *)(go + t), (unsigned long long)(long long)o);
-        se[t] = 0;
-        so[t] = 0;
+        seo[t] = 0ull;
     }
 }
 
 // Hubs of degree 3..C4_M, workspace in shared memory; histograms in shared
 // memory too unless there are too many configurations.
-template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
+template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED, bool SMALLR>
 __global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_small(C4Args a)
 {
-    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], bin masks [nb * C4_WORDS], even, odd [ncfg]
+    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], bin masks [nb * C4_WORDS], even/odd [ncfg] u64
     __shared__ int32_t s_key[C4_TABLE];
     __shared__ int32_t s_pos[C4_TABLE];
     __shared__ int32_t s_row[C4_M];
     __shared__ uint8_t s_hb[C4_M];
     __shared__ int4 s_v[C4_M];
-    __shared__ int s_lex_a[256], s_lex_b[256];
+    __shared__ int s_lex[512];                  // lex_a, lex_b (or the u16 table; see c4_lex_tables)
+    int *s_lex_a = s_lex, *s_lex_b = s_lex + 256;
     __shared__ long long s_hub;
     __shared__ unsigned long long s_pending;
     __shared__ int s_next;
 
     unsigned *s_bits = s_dyn;
     unsigned *s_bm = s_dyn + C4_M * C4_WORDS;                 // [nb][C4_WORDS]
-    unsigned *s_even = s_bm + a.nb * C4_WORDS;
-    int *s_odd = (int *)(s_even + a.ncfg);
+    unsigned long long *s_eo = reinterpret_cast<unsigned long long *>(s_bm + a.nb * C4_WORDS);   // 8-byte aligned
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
     if (SMEM_HIST)
-        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) {
-            s_even[t] = 0;
-            s_odd[t] = 0;
-        }
+        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) s_eo[t] = 0ull;
     for (int t = threadIdx.x; t < C4_TABLE; t += C4_THREADS) s_key[t] = C4_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
     HubSpace w{ s_key, s_pos, s_row, s_hb, s_v, s_bits, s_bm, &s_next };
@@ -331,7 +369,7 @@ k_count4_small(C4Args a)
             // C(m, 3) bounds the cliques of this hub
             const unsigned long long bound = (unsigned long long)m * (m - 1) * (m - 2) / 6;
             if (s_pending + bound > 0x7fffffffull) {
-                c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+                c4_flush(s_eo, a.ncfg, a.even, a.odd);
                 __syncthreads();
                 if (threadIdx.x == 0) s_pending = 0;
             }
@@ -340,11 +378,11 @@ k_count4_small(C4Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * m) ++tlog;
-        c4_hub<SMEM_HIST, WINDOWED>(a, w, i, m, tlog, s_even, s_odd, s_lex_a, s_lex_b);
+        c4_hub<SMEM_HIST, WINDOWED, SMALLR>(a, w, i, m, tlog, s_eo, s_lex_a, s_lex_b);
     }
     if (SMEM_HIST) {
         __syncthreads();
-        c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+        c4_flush(s_eo, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -352,23 +390,20 @@ k_count4_small(C4Args a)
 // histograms in shared memory (SMEM_HIST) as in the small kernel, except for
 // a hub whose clique bound could overflow the 32-bit counters, which adds
 // straight to global memory.
-template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED>
+template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED, bool SMALLR>
 __global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_large(C4Args a)
 {
-    extern __shared__ unsigned s_dyn[];             // (SMEM_HIST) even, odd [ncfg]
-    __shared__ int s_lex_a[256], s_lex_b[256];
+    extern __shared__ unsigned s_dyn[];             // (SMEM_HIST) even/odd [ncfg] u64
+    __shared__ int s_lex[512];                  // lex_a, lex_b (or the u16 table; see c4_lex_tables)
+    int *s_lex_a = s_lex, *s_lex_b = s_lex + 256;
     __shared__ long long s_hub;
     __shared__ int s_next;
     __shared__ unsigned long long s_pending;
-    unsigned *s_even = s_dyn;
-    int *s_odd = (int *)(s_even + a.ncfg);
+    unsigned long long *s_eo = reinterpret_cast<unsigned long long *>(s_dyn);
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
     if (SMEM_HIST)
-        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) {
-            s_even[t] = 0;
-            s_odd[t] = 0;
-        }
+        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) s_eo[t] = 0ull;
     if (threadIdx.x == 0) s_pending = 0;
 
     const int M = a.big_m;
@@ -400,21 +435,21 @@ k_count4_large(C4Args a)
         while ((1 << tl) < 2 * m) ++tl;
         const unsigned long long bound = (unsigned long long)m * (m - 1) * (m - 2) / 6;
         if (!SMEM_HIST || bound > 0x7fffffffull) {
-            c4_hub<false, WINDOWED>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
+            c4_hub<false, WINDOWED, SMALLR>(a, w, i, m, tl, nullptr, s_lex_a, s_lex_b);
             continue;
         }
         if (s_pending + bound > 0x7fffffffull) {
-            c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+            c4_flush(s_eo, a.ncfg, a.even, a.odd);
             __syncthreads();
             if (threadIdx.x == 0) s_pending = 0;
         }
         __syncthreads();
         if (threadIdx.x == 0) s_pending += bound;
-        c4_hub<SMEM_HIST, WINDOWED>(a, w, i, m, tl, s_even, s_odd, s_lex_a, s_lex_b);
+        c4_hub<SMEM_HIST, WINDOWED, SMALLR>(a, w, i, m, tl, s_eo, s_lex_a, s_lex_b);
     }
     if (SMEM_HIST) {
         __syncthreads();
-        c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+        c4_flush(s_eo, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -430,6 +465,28 @@ static size_t c4_large_stride(int M, int nb)
     return (bytes + 255) & ~(size_t)255;
 }
 
+// The kernel instantiations by shared histogram, hub list, windows and the
+// width of the cross products.
+using C4Kernel = void (*)(C4Args);
+
+template <bool S, bool L, bool W>
+static C4Kernel c4_pick(bool large, bool sr)
+{
+    if (large) return sr ? k_count4_large<S, L, W, true> : k_count4_large<S, L, W, false>;
+    return sr ? k_count4_small<S, L, W, true> : k_count4_small<S, L, W, false>;
+}
+
+static C4Kernel c4_kernel(bool large, bool smem, bool list, bool win, gs_graph_t g)
+{
+    const bool sr = g->edges[g->nb] <= C4_SMALL_R;
+    if (smem) {
+        if (list) return win ? c4_pick<true, true, true>(large, sr) : c4_pick<true, true, false>(large, sr);
+        return win ? c4_pick<true, false, true>(large, sr) : c4_pick<true, false, false>(large, sr);
+    }
+    if (list) return win ? c4_pick<false, true, true>(large, sr) : c4_pick<false, true, false>(large, sr);
+    return win ? c4_pick<false, false, true>(large, sr) : c4_pick<false, false, false>(large, sr);
+}
+
 // Both kernels over the hubs [a.hub_begin, a.hub_end) (outputs accumulate).
 static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t st)
 {
@@ -438,8 +495,7 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
     const bool smem = a.ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)a.nb * C4_WORDS +
                                            (smem ? 2 * (size_t)a.ncfg : 0));
-    auto kern = windowed ? (smem ? k_count4_small<true, false, true> : k_count4_small<false, false, true>)
-                         : (smem ? k_count4_small<true, false, false> : k_count4_small<false, false, false>);
+    const C4Kernel kern = c4_kernel(false, smem, false, windowed, g);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -459,8 +515,7 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
         a.scratch_stride = c4_large_stride(M, g->nb);
         const int gl = (int)std::min<int64_t>((int64_t)sms * 2, hubs);
         const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)a.ncfg : 0;
-        auto big = windowed ? (smem ? k_count4_large<true, false, true> : k_count4_large<false, false, true>)
-                            : (smem ? k_count4_large<true, false, false> : k_count4_large<false, false, false>);
+        const C4Kernel big = c4_kernel(true, smem, false, windowed, g);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
@@ -499,7 +554,9 @@ extern "C" gs_status gs_count_4pcf_parity(gs_graph_t g, uint64_t *even_dev, int6
     char *scratch = nullptr;
     const size_t sbytes = g->n_edges > 0 ? c4_scratch_bytes(g, hub_end - hub_begin) : 0;
     if (sbytes) GS_TRY_CUDA(gs_malloc_async(&scratch, sbytes, st));
-    gs_status s = c4_count(g, (uint64_t *)even_dev, odd_dev, hub_begin, hub_end, scratch, st);
+    gs_status s = gs_checked_begin(g, st);
+    if (s == GS_OK) s = c4_count(g, (uint64_t *)even_dev, odd_dev, hub_begin, hub_end, scratch, st);
+    if (s == GS_OK) s = gs_checked_end(g, st, "parity 4pCF count");
     if (scratch) cudaFreeAsync(scratch, st);
     return s;
 }
@@ -528,6 +585,7 @@ static gs_status c4_count(gs_graph_t g, uint64_t *even_dev, int64_t *odd_dev, in
     a.ncfg = (int)ncfg;
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
+    a.chk = g->chk;
     a.scratch = scratch;
     if (!g->n_win) return c4_launch(g, a, false, st);
 
@@ -590,7 +648,9 @@ extern "C" gs_status gs_count_4pcf_parity_hubs(gs_graph_t g, const int32_t *hubs
     char *scratch = nullptr;
     const size_t sbytes = g->n_edges > 0 ? c4_scratch_bytes(g, count) : 0;
     if (sbytes) GS_TRY_CUDA(gs_malloc_async(&scratch, sbytes, st));
-    s = c4_count_hubs(g, hubs_dev, count, (uint64_t *)even_dev, odd_dev, scratch, st);
+    s = gs_checked_begin(g, st);
+    if (s == GS_OK) s = c4_count_hubs(g, hubs_dev, count, (uint64_t *)even_dev, odd_dev, scratch, st);
+    if (s == GS_OK) s = gs_checked_end(g, st, "parity 4pCF hub-list count");
     if (scratch) cudaFreeAsync(scratch, st);
     return s;
 }
@@ -620,13 +680,14 @@ static gs_status c4_count_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t co
     a.ncfg = (int)ncfg;
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
+    a.chk = g->chk;
     a.scratch = scratch;
 
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)g->nb * C4_WORDS +
                                            (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true, true, false> : k_count4_small<false, true, false>;
+    const C4Kernel kern = c4_kernel(false, smem, true, false, g);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -643,7 +704,7 @@ static gs_status c4_count_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t co
         a.big_m = M;
         a.scratch_stride = stride;
         const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
-        auto big = smem ? k_count4_large<true, true, false> : k_count4_large<false, true, false>;
+        const C4Kernel big = c4_kernel(true, smem, true, false, g);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
@@ -726,6 +787,8 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     if (hub_end == hub_begin || g->n_edges == 0) return GS_OK;
     unsigned long long *cursors = (unsigned long long *)base;
     GS_TRY_CUDA(cudaMemsetAsync(cursors, 0, 2 * sizeof(unsigned long long), st));   // left over from the last call
+    s = gs_checked_begin(g, st);
+    if (s != GS_OK) return s;
 
     C4Args a{};
     a.pts = g->pts;
@@ -741,13 +804,14 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     a.ncfg = (int)ncfg;
     a.even = (unsigned long long *)even_dev;
     a.odd = (long long *)odd_dev;
+    a.chk = g->chk;
 
     const int64_t hubs = hub_end - hub_begin;
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)g->nb * C4_WORDS +
                                            (smem ? 2 * ncfg : 0));
-    auto kern = smem ? k_count4_small<true, false, false> : k_count4_small<false, false, false>;
+    const C4Kernel kern = c4_kernel(false, smem, false, false, g);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
     GS_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C4_THREADS, dyn));
@@ -766,11 +830,11 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
         a.scratch = base + GS_C4_STATIC_HEAD;
         a.scratch_stride = stride;
         const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
-        auto big = smem ? k_count4_large<true, false, false> : k_count4_large<false, false, false>;
+        const C4Kernel big = c4_kernel(true, smem, false, false, g);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
         gs_note_launch();
         GS_TRY_CUDA(cudaGetLastError());
     }
-    return GS_OK;
+    return gs_checked_end(g, st, "parity 4pCF count (fixed workspace)");
 }

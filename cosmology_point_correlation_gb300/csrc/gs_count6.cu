@@ -265,6 +265,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                     common = row1[wd] & row2[wd];
                     if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
                 }
+                if (!__ballot_sync(0xffffffffu, common != 0u)) continue;   // no tetrahedron in this word
                 const int cnt = __popc(common);
                 int inc = cnt;                                     // inclusive prefix over lanes
 #pragma unroll
@@ -282,7 +283,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                     const unsigned cm = __shfl_sync(0xffffffffu, common, owner);
                     const int first = __shfl_sync(0xffffffffu, inc - cnt, owner);
                     const int o_s2 = __shfl_sync(0xffffffffu, s2, owner);
-                    if (q < total) tetra(make_pair(o_s2), (wd << 5) + (int)__fns(cm, 0, q - first + 1));
+                    if (q < total) tetra(make_pair(o_s2), (wd << 5) + gs_nth_bit(cm, q - first));
                 }
             }
         }

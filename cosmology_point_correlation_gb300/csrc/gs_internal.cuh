@@ -41,6 +41,8 @@ struct gs_graph {
     uint8_t *bin;
     unsigned long long *work;  // 4 device counters used by the count kernels
     int32_t *err;              // device error word of the build kernels
+    unsigned *chk;             // device check word of checked builds (see GS_DCHECK)
+    int64_t nbr_len;           // entries of nbr / bin (E + GS_EDGE_PAD), or of a staging slot when windowed
     uint16_t *cfg3;            // [nb][nb][nb] idx3(sort(x, y, z)) at (z, x, y), nb <= 40; or NULL
     int32_t *cfg6;             // [nb^6] six-bin 4pCF configuration and orientation (built on first use)
     int ncfg6;
@@ -59,6 +61,7 @@ struct gs_graph {
     int64_t *win_e0;           // host [n_win + 1]
     int32_t *win_maxnbr;       // host [n_win]
     uint8_t *win_pair;         // host [n_win][n_win]: 1 if a row of window h has a forward neighbour in window w
+    int64_t *win_first;        // host [n_win][n_win]: the first such row of window h (when win_pair is 1)
     int32_t *h_nbr;
     uint8_t *h_bin;
     int64_t win_cap;           // edges a staging slot holds
@@ -92,11 +95,14 @@ gs_status gs_set_error(gs_status s, const char *fmt, ...);
 // A public entry point in progress on this thread. The outermost one (calls
 // nest: gs_3pcf_from_host calls gs_build_graph) clears the thread's error
 // message and restarts the allocation ordinal that fault injection counts.
+// Every one opens an NVTX range named after the call, so a profiler's
+// timeline shows the graph build and each count as a phase (NVTX is
+// header-only and costs nothing when no tool is attached).
 struct gs_call_scope {
-    gs_call_scope();
+    explicit gs_call_scope(const char *name);
     ~gs_call_scope();
 };
-#define GS_ENTRY() gs_call_scope gs_scope_
+#define GS_ENTRY() gs_call_scope gs_scope_(__func__)
 
 // Every device and pinned-host allocation of the library passes this gate
 // first. It counts the allocation (gs_alloc_calls) and, when the environment
@@ -165,6 +171,45 @@ int gs_sm_count();
 gs_status gs_scan_i32_to_i64(const int32_t *in, int64_t *out, int64_t n, cudaStream_t st);
 gs_status gs_scan_i32_to_i32(const int32_t *in, int32_t *out, int64_t n, cudaStream_t st);
 
+// ---------------------------------------------------------------- checked builds
+//
+// A build compiled with -DGS_CHECKED (libgramsci_gb_checked.so) tests the
+// indices of the hot kernels' shared-memory and global accesses. A failed
+// test sets bit `site` of the graph's check word and the access is skipped;
+// the entry point reads the word after its kernels (synchronising its
+// stream) and returns GS_ERR_INTERNAL naming the sites. In the regular build
+// every test is the constant true and the word is never read.
+#ifdef GS_CHECKED
+constexpr bool GS_CHECKED_BUILD = true;
+__device__ __forceinline__ bool gs_dcheck(bool ok, unsigned *word, int site)
+{
+    if (!ok) atomicOr(word, 1u << site);
+    return ok;
+}
+#define GS_DCHECK(ok, word, site) gs_dcheck((ok), (word), (site))
+#else
+constexpr bool GS_CHECKED_BUILD = false;
+#define GS_DCHECK(ok, word, site) true
+#endif
+
+// Check sites (bits of the check word).
+enum {
+    GS_SITE_NB_ROW = 0,        // k_neighbors: an edge written outside its row
+    GS_SITE_C3M_MAP_W = 1,     // k_count3m: byte-map or segment-table write
+    GS_SITE_C3M_MAP_R = 2,     // k_count3m: byte-map read
+    GS_SITE_C3M_HIST = 3,      // k_count3m: histogram counter
+    GS_SITE_C3M_ROW = 4,       // k_count3m: spoke-row read
+    GS_SITE_C3_BITMAP = 5,     // k_count3: bitmap, rank or bin read
+    GS_SITE_C3_HIST = 6,       // k_count3: histogram counter
+    GS_SITE_C4_BITS = 7,       // k_count4_*: adjacency bits or spoke vector
+    GS_SITE_C4_HIST = 8        // k_count4_*: histogram counter
+};
+
+// Clear the check word before a count's kernels, and read it after them
+// (checked builds only; both are no-ops otherwise).
+gs_status gs_checked_begin(gs_graph_t g, cudaStream_t st);
+gs_status gs_checked_end(gs_graph_t g, cudaStream_t st, const char *what);
+
 // ---------------------------------------------------------------- device helpers
 
 // Minimum-image (periodic) or raw displacement component b - a; |b - a| < 2^30.
@@ -207,6 +252,22 @@ __host__ __device__ __forceinline__ int64_t gs_ncfg4(int nb) { return (int64_t)n
 __device__ __forceinline__ uint32_t gs_hash(int32_t key, int shift)
 {
     return ((uint32_t)key * 0x9E3779B1u) >> shift;
+}
+
+// Position of the n-th set bit (n from 0) of x, which has more than n set
+// bits: a binary search on the popcounts of the lower halves.
+__device__ __forceinline__ int gs_nth_bit(unsigned x, int n)
+{
+    int pos = 0, c;
+    c = __popc(x & 0xffffu);
+    if (n >= c) { n -= c; pos += 16; x >>= 16; }
+    c = __popc(x & 0xffu);
+    if (n >= c) { n -= c; pos += 8; x >>= 8; }
+    c = __popc(x & 0xfu);
+    if (n >= c) { n -= c; pos += 4; x >>= 4; }
+    c = __popc(x & 0x3u);
+    if (n >= c) { n -= c; pos += 2; x >>= 2; }
+    return pos + (n >= (int)(x & 1u));
 }
 
 __device__ __forceinline__ unsigned gs_lanemask_lt()

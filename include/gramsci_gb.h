@@ -113,15 +113,14 @@ gs_status gs_count_3pcf(gs_graph_t g, uint64_t *hist_dev, int64_t hub_begin, int
  * byte map (a bin byte per id of the key span, in 1024-id segments; hits go
  * to an unsorted nb^3 histogram) or as a bitmap with ranks (hits go to the
  * sorted-triple histogram through a configuration table):
- *   2 = byte map, one spoke per warp (device-resident graphs with long rows,
- *       mean degree above 1024, and at most 32 bins)
- *   1 = bitmap, four spokes per warp (device-resident graphs with short rows)
- *   0 = bitmap, one spoke per warp (windowed graphs, and when the others do
- *       not fit in shared memory)
- *   3 = byte map, four spokes per warp (on request only)
- * GS_COUNT3_WALK = "map", "mapgroup", "warp" or "group" overrides the choice,
- * as for the count (the byte-map walks also run on windowed graphs). -1 for a
- * NULL graph or one of another device. */
+ *   2 = byte map, one spoke per warp (long rows: mean degree above 1024)
+ *   3 = byte map, four spokes per warp (short rows)
+ *   1 = bitmap, four spokes per warp, and 0 = bitmap, one spoke per warp,
+ *       when the byte map does not fit (more than 32 bins; windowed graphs
+ *       then take 0)
+ * Windowed graphs run the same walks on their tiles. GS_COUNT3_WALK = "map",
+ * "mapgroup", "warp" or "group" overrides the choice, as for the count. -1
+ * for a NULL graph or one of another device. */
 int gs_count3_walk(gs_graph_t g);
 
 /* Parity-decomposed 4pCF histograms (§III.1.1 three-way intersection,
@@ -405,7 +404,12 @@ void gs_graph_free(gs_graph_t g);
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char *gs_last_error(void);
 
-/* Library version string. */
+/* Library version string; it ends in ", checked)" for the checked build
+ * (libgramsci_gb_checked.so: the same sources compiled with GS_CHECKED, whose
+ * graph build, 3pCF and parity-4pCF kernels test the indices of their memory
+ * accesses, skip an access that fails, and make the call return
+ * GS_ERR_INTERNAL naming the failed check sites; its calls synchronise their
+ * stream to read the check word). */
 const char *gs_version(void);
 
 #ifdef __cplusplus
