@@ -648,6 +648,11 @@ constexpr int C3M_SEG_LOG = 10;
 constexpr int C3M_SEG = 1 << C3M_SEG_LOG;        // ids per segment
 constexpr int C3M_SPAN_SEGS = 256;               // segments a chunk may span (2^18 ids)
 constexpr int C3M_SEG_TABLE = C3M_SPAN_SEGS + 16;  // + the guard entry (0: the absent slot), padded
+// Catalogues of at most C3M_ABS_SEGS segments of ids index the segment table by
+// the absolute segment k >> C3M_SEG_LOG: no subtraction and no clamp per probe
+// (an entry outside its row is replaced by the guard id, whose segment is absent).
+constexpr int C3M_ABS_SEGS = 2048;               // ids below 2^21
+constexpr int C3M_SEG_TABLE_ABS = C3M_ABS_SEGS + 16;
 constexpr int C3M_KEYS_PER_THREAD = 8;           // chunk keys per thread
 constexpr int C3M_MIN_SLOTS = 24;                // fewest segment slots worth a launch
 constexpr int C3M_MAX_SLOTS = 255;               // slot numbers are bytes
@@ -751,38 +756,50 @@ __device__ __forceinline__ void c3m_spoke_range(const C3Args &a, int64_t soff, i
     }
 }
 
-// Probe four row entries against the chunk's byte map and count the hits
-// into H[b_ij][b_ik][b_jk] (hb = b_ij nb^2; bins of the four entries in bb).
-__device__ __forceinline__ void c3m_probe4(const int k[4], uint32_t bb, int32_t kbase, unsigned guard,
-                                           const uint8_t *s_seg, const uint8_t *s_map, unsigned *s_h, int hb,
-                                           int nb, const C3Args &a, int nslots)
+// Probe N row entries against the chunk's byte map and count the hits into
+// H[b_ij][b_ik][b_jk] (hb = b_ij nb^2; bins of entries 4q .. 4q+3 in bb[q]).
+// ABS: the segment table is indexed by the absolute segment of k (kbase 0,
+// every k below the guard id), so the offset needs no clamp.
+// The segment slots of all N entries are loaded first, then their bin bytes,
+// then the adds are issued: the two dependent shared loads of one entry
+// overlap those of the others. The adds touch only the histogram, which
+// nothing in the walk reads (it is read after a block barrier), so they carry
+// no memory clobber and the loads may be scheduled around them.
+template <bool ABS, int N>
+__device__ __forceinline__ void c3m_probe(const int *k, const uint32_t *bb, int32_t kbase, unsigned guard,
+                                          const uint8_t *s_seg, const uint8_t *s_map, unsigned *s_h, int hb,
+                                          int nb, const C3Args &a, int nslots)
 {
 #ifdef GS_CHECKED
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const unsigned o = min((unsigned)(k[e] - kbase), guard);
+    for (int e = 0; e < N; ++e) {
+        const unsigned o = ABS ? (unsigned)k[e] : min((unsigned)(k[e] - kbase), guard);
         const unsigned sl = s_seg[o >> C3M_SEG_LOG];
         if (!GS_DCHECK(sl <= (unsigned)nslots, a.chk, GS_SITE_C3M_MAP_R)) continue;
         const unsigned b = s_map[(sl << C3M_SEG_LOG) | (o & (C3M_SEG - 1))];
         if (b == C3M_ABSENT) continue;
-        const int idx = hb + (int)b * nb + (int)((bb >> (8 * e)) & 0xffu);
+        const int idx = hb + (int)b * nb + (int)((bb[e >> 2] >> (8 * (e & 3))) & 0xffu);
         if (GS_DCHECK(b < (unsigned)nb && idx >= 0 && idx < nb * nb * nb, a.chk, GS_SITE_C3M_HIST))
             atomicAdd(s_h + idx, 1u);
     }
 #else
     (void)a;
     (void)nslots;
+    unsigned o[N], v[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) o[e] = ABS ? (unsigned)k[e] : min((unsigned)(k[e] - kbase), guard);
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = s_seg[o[e] >> C3M_SEG_LOG];
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = s_map[v[e] * C3M_SEG + (o[e] & (C3M_SEG - 1))];
     const unsigned h0 = (unsigned)__cvta_generic_to_shared(s_h) + 4u * (unsigned)hb;
     const unsigned nb4 = 4u * (unsigned)nb;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const unsigned o = min((unsigned)(k[e] - kbase), guard);
-        const unsigned sl = s_seg[o >> C3M_SEG_LOG];
-        const unsigned b = s_map[sl * C3M_SEG + (o & (C3M_SEG - 1))];
+    for (int e = 0; e < N; ++e) {
         // a predicated reduction, no branch: a lane whose entry is absent adds nothing
-        const unsigned addr = h0 + b * nb4 + 4u * __byte_perm(bb, 0u, 0x4440u + (unsigned)e);
+        const unsigned addr = h0 + v[e] * nb4 + 4u * __byte_perm(bb[e >> 2], 0u, 0x4440u + (unsigned)(e & 3));
         asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %0, 255;\n\t@p red.shared.add.u32 [%1], 1;\n\t}"
-                     :: "r"(b), "r"(addr) : "memory");
+                     :: "r"(v[e]), "r"(addr));
     }
 #endif
 }
@@ -791,6 +808,7 @@ __device__ __forceinline__ void c3m_probe4(const int k[4], uint32_t bb, int32_t 
 // where a spoke's walk is one or two steps and its time is the latency of the
 // loads that start it): lane l of a group reads entries 4l .. 4l+3 of a
 // 32-entry step of its spoke's row. Each group stops once its step passes kmax.
+template <bool ABS>
 __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, const int32_t *F, const uint8_t *FB,
                                                  int s_lo, int s_end, int c0, int32_t kfirst, int32_t kbase,
                                                  int32_t kmax, unsigned guard, const uint8_t *s_seg,
@@ -798,6 +816,7 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
 {
     const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
     const int nb = a.nb, nb2 = nb * nb;
+    const int32_t kout = ABS ? (int32_t)guard : kbase - 1;   // an id whose segment is absent
     for (;;) {
         int li = 0;
         if (lane == 0) li = s_lo + atomicAdd(s_next, 4);
@@ -838,9 +857,9 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
                 if (base == 0 || base + 32 > total) {
                     const unsigned r0 = (unsigned)(base + 4 * gl - head), len = (unsigned)(total - head);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) k[e] = r0 + e < len ? k[e] : kbase - 1;
+                    for (int e = 0; e < 4; ++e) k[e] = r0 + e < len ? k[e] : kout;
                 }
-                c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
+                c3m_probe<ABS, 4>(k, &bb, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
             }
             // rows are sorted: a group stops once its step's last key passes kmax
             const int last = __shfl_sync(0xffffffffu, kk.w, lane | 7);
@@ -851,7 +870,7 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
     }
 }
 
-template <int THREADS, bool GROUPED, bool WINDOWED>
+template <int THREADS, bool GROUPED, bool WINDOWED, bool ABS>
 __global__ void __launch_bounds__(THREADS, THREADS >= 1024 ? 1 : 2)
 k_count3m(C3Args a, int nslots)
 {
@@ -873,8 +892,10 @@ k_count3m(C3Args a, int nslots)
     const int64_t soff = WINDOWED ? a.soff : 0;
     // the segment table and the map first, at fixed offsets (their probes need
     // no base register), then the histogram
+    constexpr int SEG_TABLE = ABS ? C3M_SEG_TABLE_ABS : C3M_SEG_TABLE;
+    constexpr int SPAN_SEGS = ABS ? C3M_ABS_SEGS : C3M_SPAN_SEGS;
     uint8_t *s_seg = reinterpret_cast<uint8_t *>(s_dyn);
-    uint8_t *s_map = s_seg + C3M_SEG_TABLE;
+    uint8_t *s_map = s_seg + SEG_TABLE;
     unsigned *s_h = reinterpret_cast<unsigned *>(s_map + (size_t)(nslots + 1) * C3M_SEG);
 
     for (int t = threadIdx.x; t < n3; t += THREADS) s_h[t] = 0;
@@ -914,7 +935,7 @@ k_count3m(C3Args a, int nslots)
         }
         for (int c0 = 0, c1 = 0; c0 < f; c0 = c1) {
             // ---- the chunk [c0, c1); thread t owns keys c0 + KPT t .. + KPT - 1
-            const int32_t kbase = F[c0] & ~(C3M_SEG - 1);
+            const int32_t kbase = ABS ? 0 : F[c0] & ~(C3M_SEG - 1);
             const int cap = min(f, c0 + MAX_KEYS);
             const int t0 = c0 + threadIdx.x * KPT;
             int32_t key[KPT];
@@ -937,14 +958,14 @@ k_count3m(C3Args a, int nslots)
                 for (int q = 0; q < KPT; ++q) {
                     if (t0 + q >= cap) break;
                     slot += (starts >> q) & 1u;
-                    if (slot > nslots || ((key[q] - kbase) >> C3M_SEG_LOG) >= C3M_SPAN_SEGS) {
+                    if (slot > nslots || ((key[q] - kbase) >> C3M_SEG_LOG) >= SPAN_SEGS) {
                         atomicMin(&s_cut, t0 + q);           // slots and segments grow with q
                         break;
                     }
                 }
             }
             // clear the segment table and the slots the chunk can use
-            for (int t = threadIdx.x; t < C3M_SEG_TABLE; t += THREADS) s_seg[t] = 0;
+            for (int t = threadIdx.x; t < SEG_TABLE; t += THREADS) s_seg[t] = 0;
             {
                 const int nclear = min(nslots, total);
                 uint4 *m = reinterpret_cast<uint4 *>(s_map + C3M_SEG);
@@ -960,7 +981,7 @@ k_count3m(C3Args a, int nslots)
                     if (t0 + q >= c1) break;
                     slot += (starts >> q) & 1u;
                     const int off = key[q] - kbase;
-                    if (!GS_DCHECK(slot >= 1 && slot <= nslots && off >= 0 && (off >> C3M_SEG_LOG) < C3M_SPAN_SEGS,
+                    if (!GS_DCHECK(slot >= 1 && slot <= nslots && off >= 0 && (off >> C3M_SEG_LOG) < SPAN_SEGS,
                                    a.chk, GS_SITE_C3M_MAP_W))
                         continue;
                     if ((starts >> q) & 1u) s_seg[off >> C3M_SEG_LOG] = (uint8_t)slot;
@@ -986,11 +1007,12 @@ k_count3m(C3Args a, int nslots)
             if (s_end <= q_lo) continue;
             const int32_t kmax = F[c1 - 1];
             const int32_t kfirst = F[c0];
-            const unsigned guard = (unsigned)C3M_SPAN_SEGS << C3M_SEG_LOG;
+            const unsigned guard = (unsigned)SPAN_SEGS << C3M_SEG_LOG;   // an id of the absent guard segment
+            const int32_t kout = ABS ? (int32_t)guard : kbase - 1;      // what entries outside the row become
 
             if (GROUPED) {
-                c3m_walk_grouped(a, soff, F, FB, q_lo, s_end, c0, kfirst, kbase, kmax, guard, s_seg, s_map, s_h,
-                                 &s_next, nslots);
+                c3m_walk_grouped<ABS>(a, soff, F, FB, q_lo, s_end, c0, kfirst, kbase, kmax, guard, s_seg, s_map,
+                                      s_h, &s_next, nslots);
             } else {
                 // ---- spokes, one per warp, handed out in row order
                 for (;;) {
@@ -1034,20 +1056,24 @@ k_count3m(C3Args a, int nslots)
                                 bn2 = __ldg(vb + 32);
                             }
                         }
-                        int k[4] = { kk.x, kk.y, kk.z, kk.w };
-                        int k2[4] = { kk2.x, kk2.y, kk2.z, kk2.w };
+                        int k[8] = { kk.x, kk.y, kk.z, kk.w, kk2.x, kk2.y, kk2.z, kk2.w };
+                        const uint32_t b2[2] = { bb, bb2 };
                         if (base == 0 || base + 256 > total_e) {   // first / last step only
-                            // entries outside [p0, pe) become kbase - 1, whose offset clamps to the guard
+                            // entries outside [p0, pe) become an id of an absent segment
                             const unsigned r0 = (unsigned)(base + 4 * lane - head), len = (unsigned)(total_e - head);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                k[e] = r0 + e < len ? k[e] : kbase - 1;
-                                k2[e] = r0 + 128 + e < len ? k2[e] : kbase - 1;
+                                k[e] = r0 + e < len ? k[e] : kout;
+                                k[4 + e] = r0 + 128 + e < len ? k[4 + e] : kout;
                             }
                         }
-                        c3m_probe4(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
-                        c3m_probe4(k2, bb2, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
-                        // rows are sorted: stop once the step's last key passes kmax
+                        // rows are sorted: once the first half's last key passes kmax, the
+                        // second half holds no key of the chunk, and the walk ends here
+                        if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) {
+                            c3m_probe<ABS, 4>(k, b2, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
+                            break;
+                        }
+                        c3m_probe<ABS, 8>(k, b2, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
                         if (__shfl_sync(0xffffffffu, kk2.w, 31) > kmax) break;
                         kk = kn;
                         kk2 = kn2;
@@ -1101,23 +1127,30 @@ static int count3_walk_override()
 // histogram leaves room for C3M_MIN_SLOTS segment slots each, else one
 // 1024-thread block per SM; as many slots as fit. False when neither fits
 // (e.g. nb > C3M_MAX_BINS).
-template <bool W>
-static decltype(&k_count3m<512, false, false>) c3m_kernel(int threads, bool grouped)
+using C3MKernel = void (*)(C3Args, int);
+
+template <bool W, bool A>
+static C3MKernel c3m_kernel(int threads, bool grouped)
 {
-    return threads == 512 ? (grouped ? k_count3m<512, true, W> : k_count3m<512, false, W>)
-                          : (grouped ? k_count3m<1024, true, W> : k_count3m<1024, false, W>);
+    return threads == 512 ? (grouped ? k_count3m<512, true, W, A> : k_count3m<512, false, W, A>)
+                          : (grouped ? k_count3m<1024, true, W, A> : k_count3m<1024, false, W, A>);
 }
 
-static decltype(&k_count3m<512, false, false>) c3m_kernel(int threads, bool grouped, bool windowed)
+// The absolute segment table serves graphs whose ids lie below 2^21.
+static bool c3m_abs(gs_graph_t g) { return g->n <= (int64_t)C3M_ABS_SEGS * C3M_SEG; }
+
+static C3MKernel c3m_kernel(gs_graph_t g, int threads, bool grouped, bool windowed)
 {
-    return windowed ? c3m_kernel<true>(threads, grouped) : c3m_kernel<false>(threads, grouped);
+    if (c3m_abs(g))
+        return windowed ? c3m_kernel<true, true>(threads, grouped) : c3m_kernel<false, true>(threads, grouped);
+    return windowed ? c3m_kernel<true, false>(threads, grouped) : c3m_kernel<false, false>(threads, grouped);
 }
 
 static bool plan_count3m(gs_graph_t g, bool grouped, bool windowed, int *threads, int *slots, size_t *dyn)
 {
     if (g->nb > C3M_MAX_BINS || !g->cfg3) return false;
     const int n3 = g->nb * g->nb * g->nb;
-    const size_t fixed = sizeof(unsigned) * (size_t)((n3 + 3) & ~3) + C3M_SEG_TABLE;
+    const size_t fixed = sizeof(unsigned) * (size_t)((n3 + 3) & ~3) + (c3m_abs(g) ? C3M_SEG_TABLE_ABS : C3M_SEG_TABLE);
     int dev = 0, smem_sm = 0, smem_block = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
@@ -1128,7 +1161,7 @@ static bool plan_count3m(gs_graph_t g, bool grouped, bool windowed, int *threads
     for (int variant = 0; variant < 2; ++variant) {
         const int t = variant == 0 ? 512 : 1024;
         const int want = variant == 0 ? 2 : 1;                   // resident blocks per SM
-        auto kern = c3m_kernel(t, grouped, windowed);
+        const C3MKernel kern = c3m_kernel(g, t, grouped, windowed);
         // per block: the SM's shared memory split, less 1 KB reserved and 2 KB of static data
         const long long room = std::min<long long>(smem_block, smem_sm / want - 1024) - 2048;
         int sl = (int)std::min<long long>(C3M_MAX_SLOTS, (room - (long long)fixed) / C3M_SEG - 1);
@@ -1227,7 +1260,7 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
                 return gs_set_error(GS_ERR_INTERNAL, "byte-map walk plan");
             const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * (threads == 512 ? 2 : 1), hubs);
             GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
-            c3m_kernel(threads, grouped, win)<<<grid, threads, dm, st>>>(a, slots);
+            c3m_kernel(g, threads, grouped, win)<<<grid, threads, dm, st>>>(a, slots);
             gs_note_launch();
             GS_TRY_CUDA(cudaGetLastError());
             return GS_OK;
