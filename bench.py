@@ -603,9 +603,14 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = oracle_line(xyz, box_lu, w, oracle_sample_size(xyz, box_lu, w))
 
-    # roofline of the count kernel: the merge-walk re-reads its rows from L2
-    # (profiles/), so HBM is not its ceiling; each closed triangle is one
-    # shared-memory histogram add, and the kernel is bound by instruction issue.
+    # roofline of the count kernel. The merge-walk re-reads its rows from L2
+    # (profiles/), so HBM is not its ceiling. Every probe of a spoke-row entry
+    # is two shared-memory loads and every closed triangle a shared-memory add,
+    # and the rows come in through L1 as well: the binding unit is the L1 data
+    # pipe, one 128-byte wavefront per SM per cycle. Its use per triangle comes
+    # from the ncu capture of the same kernel source (scaled by triangles), the
+    # time from this run; the atomic, issue, DRAM and walk ceilings are given
+    # beside it.
     from cosmology_point_correlation_gb300 import measure_smem_atomics
     count_s = count_ms / 1e3
     n3 = w.nbins ** 3
@@ -617,16 +622,20 @@ def run_ours(args, w):
     sm_mhz = clocks.get("sm_mhz") or 2070.0
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     walk_gbs = alg_bytes / count_s / 1e9
+    l1_peak = sms * sm_mhz * 1e6                                  # wavefronts per second
+    l1_rate = prof["l1_wavefronts_per_full_launch"] / count_s if prof and "l1_wavefronts_per_full_launch" in prof \
+        else None
     roofline = {
         "bound": "alu", "kernel": kernel_name,
-        "ceiling": ("instruction issue of the merge-walk: a probe per spoke-row entry read and, per closed "
-                    "triangle, a bin lookup and one shared-memory histogram add; the rows are re-read from "
-                    "L2, so HBM is not the ceiling"),
-        "achieved": tri_rate / 1e9, "peak": atom_rate / 1e9, "unit": "G lane-adds/s", "frac": tri_rate / atom_rate,
-        "per_unit": "one shared-memory histogram add (a lane-add) per closed triangle",
-        "peak_kind": (f"measured in this run: gs_measure_smem_atomics, two 512-thread blocks per SM doing only "
-                      f"shared-memory atomic adds of 1 into {probe_cfg} random 32-bit counters, 20 of 32 lanes "
-                      "active (the count's lanes per add)"),
+        "ceiling": ("the L1 / shared-memory data pipe (one 128-byte wavefront per SM per cycle): per spoke-row "
+                    "entry two shared-memory loads (segment slot, bin byte), per closed triangle one shared-memory "
+                    "add, and the row loads; the rows are re-read from L2, so HBM is not the ceiling"),
+        "achieved": l1_rate / 1e9 if l1_rate else None, "peak": l1_peak / 1e9, "unit": "G wavefronts/s",
+        "frac": l1_rate / l1_peak if l1_rate else None,
+        "per_unit": ("L1 data-pipe wavefronts per closed triangle, from the ncu capture of this kernel source "
+                     "(profiles/k_count3m_bao_3pcf.json), times the triangles per second of this run"),
+        "peak_kind": f"derived: {sms} SMs x 1 wavefront per cycle x the sampled SM clock ({sm_mhz:.0f} MHz)",
+        "wavefronts_per_triangle": (prof["l1_wavefronts_per_full_launch"] / tris) if l1_rate else None,
         "traffic": traffic,
         "dram_gbs": traffic / count_s / 1e9 if traffic else None,
         "dram_frac": traffic / count_s / 1e9 / peak if traffic else None,
@@ -637,6 +646,10 @@ def run_ours(args, w):
                       "forward edge of hub rows, divided by the count time, against the measured HBM copy peak; "
                       "almost all of it is served from L2, so it is not DRAM traffic"),
         "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+        "atomic_adds_per_s": tri_rate, "atomic_peak_per_s": atom_rate, "atomic_frac": tri_rate / atom_rate,
+        "atomic_peak_kind": (f"measured in this run: gs_measure_smem_atomics, two 512-thread blocks per SM doing "
+                             f"only shared-memory atomic adds of 1 into {probe_cfg} random 32-bit counters, 20 of 32 "
+                             "lanes active (one add per closed triangle)"),
         "issue_frac": (prof["warp_inst_per_full_launch"] / (count_s * sms * 4 * sm_mhz * 1e6)) if prof else None,
         "lane_adds_per_triangle": (prof["shared_atom_lane_ops_per_full_launch"] / tris) if prof else None,
         "counters": ("profiles/k_count3m_bao_3pcf.json (ncu, kernel source hash checked)" if prof else

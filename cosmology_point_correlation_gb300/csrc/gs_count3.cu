@@ -84,6 +84,7 @@ struct C3Args {
     int64_t hub_begin, hub_end;
     int nb;
     int ncfg;
+    int hs;                       // byte-map walk: row stride of the b_ik index of its histogram (>= nb)
     unsigned long long *ghist;
     unsigned long long *cursor;   // next hub to hand out
     const uint16_t *cfg3;         // [nb][nb][nb] configuration index of (z, x, y) (SMEM_HIST)
@@ -694,14 +695,14 @@ __device__ __forceinline__ int c3m_block_scan(int v, int *s_warp, int *total)
 // clear them: the thread that meets the sorted triple x <= y <= z sums its
 // distinct permutations (cfg3 at (x, y, z) is its packed index).
 template <int THREADS>
-__device__ __forceinline__ void c3m_flush(unsigned *h, int nb, const uint16_t *cfg3, unsigned long long *gh)
+__device__ __forceinline__ void c3m_flush(unsigned *h, int nb, int hs, const uint16_t *cfg3, unsigned long long *gh)
 {
     const int nb2 = nb * nb, n3 = nb2 * nb;
     for (int u = threadIdx.x; u < n3; u += THREADS) {
         const int x = u / nb2, y = (u / nb) % nb, z = u % nb;
         if (x > y || y > z) continue;
-        const int p[6] = { (x * nb + y) * nb + z, (x * nb + z) * nb + y, (y * nb + x) * nb + z,
-                           (y * nb + z) * nb + x, (z * nb + x) * nb + y, (z * nb + y) * nb + x };
+        const int p[6] = { (x * nb + y) * hs + z, (x * nb + z) * hs + y, (y * nb + x) * hs + z,
+                           (y * nb + z) * hs + x, (z * nb + x) * hs + y, (z * nb + y) * hs + x };
         unsigned long long v = 0;
 #pragma unroll
         for (int q = 0; q < 6; ++q) {
@@ -757,7 +758,8 @@ __device__ __forceinline__ void c3m_spoke_range(const C3Args &a, int64_t soff, i
 }
 
 // Probe N row entries against the chunk's byte map and count the hits into
-// H[b_ij][b_ik][b_jk] (hb = b_ij nb^2; bins of entries 4q .. 4q+3 in bb[q]).
+// H[b_ij][b_ik][b_jk] at (b_ij nb + b_ik) hs + b_jk (hb = b_ij nb hs; bins of
+// entries 4q .. 4q+3 in bb[q]).
 // ABS: the segment table is indexed by the absolute segment of k (kbase 0,
 // every k below the guard id), so the offset needs no clamp.
 // The segment slots of all N entries are loaded first, then their bin bytes,
@@ -768,7 +770,7 @@ __device__ __forceinline__ void c3m_spoke_range(const C3Args &a, int64_t soff, i
 template <bool ABS, int N>
 __device__ __forceinline__ void c3m_probe(const int *k, const uint32_t *bb, int32_t kbase, unsigned guard,
                                           const uint8_t *s_seg, const uint8_t *s_map, unsigned *s_h, int hb,
-                                          int nb, const C3Args &a, int nslots)
+                                          int nb, int hs, const C3Args &a, int nslots)
 {
 #ifdef GS_CHECKED
 #pragma unroll
@@ -778,13 +780,14 @@ __device__ __forceinline__ void c3m_probe(const int *k, const uint32_t *bb, int3
         if (!GS_DCHECK(sl <= (unsigned)nslots, a.chk, GS_SITE_C3M_MAP_R)) continue;
         const unsigned b = s_map[(sl << C3M_SEG_LOG) | (o & (C3M_SEG - 1))];
         if (b == C3M_ABSENT) continue;
-        const int idx = hb + (int)b * nb + (int)((bb[e >> 2] >> (8 * (e & 3))) & 0xffu);
-        if (GS_DCHECK(b < (unsigned)nb && idx >= 0 && idx < nb * nb * nb, a.chk, GS_SITE_C3M_HIST))
+        const int idx = hb + (int)b * hs + (int)((bb[e >> 2] >> (8 * (e & 3))) & 0xffu);
+        if (GS_DCHECK(b < (unsigned)nb && idx >= 0 && idx < nb * nb * hs, a.chk, GS_SITE_C3M_HIST))
             atomicAdd(s_h + idx, 1u);
     }
 #else
     (void)a;
     (void)nslots;
+    (void)nb;
     unsigned o[N], v[N];
 #pragma unroll
     for (int e = 0; e < N; ++e) o[e] = ABS ? (unsigned)k[e] : min((unsigned)(k[e] - kbase), guard);
@@ -793,7 +796,7 @@ __device__ __forceinline__ void c3m_probe(const int *k, const uint32_t *bb, int3
 #pragma unroll
     for (int e = 0; e < N; ++e) v[e] = s_map[v[e] * C3M_SEG + (o[e] & (C3M_SEG - 1))];
     const unsigned h0 = (unsigned)__cvta_generic_to_shared(s_h) + 4u * (unsigned)hb;
-    const unsigned nb4 = 4u * (unsigned)nb;
+    const unsigned nb4 = 4u * (unsigned)hs;
 #pragma unroll
     for (int e = 0; e < N; ++e) {
         // a predicated reduction, no branch: a lane whose entry is absent adds nothing
@@ -802,6 +805,52 @@ __device__ __forceinline__ void c3m_probe(const int *k, const uint32_t *bb, int3
                      :: "r"(v[e]), "r"(addr));
     }
 #endif
+}
+
+// One 256-entry step of a spoke's walk in the one-spoke-per-warp form: cur
+// holds the step's entries (lane l: 4l .. 4l+3 in k0/b0, 128+4l .. in k1/b1);
+// the next step, when it starts before the row's end, is loaded into nxt.
+// Entries outside the row (the first step's head, the last step's tail)
+// become kout, an id of an absent segment. True when the spoke's walk ends:
+// at the row's end, or once a loaded key passes kmax (rows are sorted, so no
+// later entry is a key of the chunk).
+struct C3MStep {
+    int4 k0, k1;
+    uint32_t b0, b1;
+};
+
+template <bool ABS>
+__device__ __forceinline__ bool c3m_step(const C3MStep &cur, C3MStep &nxt, const int4 *&vk, const uint32_t *&vb,
+                                         int base, int total_e, int head, int lane, int32_t kmax, int32_t kout,
+                                         int32_t kbase, unsigned guard, const uint8_t *s_seg, const uint8_t *s_map,
+                                         unsigned *s_h, int hb, int nb, int hs, const C3Args &a, int nslots)
+{
+    const bool more = base + 256 < total_e;                  // the same in every lane
+    if (more) {
+        vk += 64;
+        vb += 64;
+        nxt.k0 = __ldg(vk);
+        nxt.b0 = __ldg(vb);
+        nxt.k1 = __ldg(vk + 32);
+        nxt.b1 = __ldg(vb + 32);
+    }
+    int k[8] = { cur.k0.x, cur.k0.y, cur.k0.z, cur.k0.w, cur.k1.x, cur.k1.y, cur.k1.z, cur.k1.w };
+    const uint32_t bb[2] = { cur.b0, cur.b1 };
+    if (base == 0 || !more) {
+        const unsigned r0 = (unsigned)(base + 4 * lane - head), len = (unsigned)(total_e - head);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            k[e] = r0 + e < len ? k[e] : kout;
+            k[4 + e] = r0 + 128 + e < len ? k[4 + e] : kout;
+        }
+    }
+    // once the first half's last key passes kmax, the second half holds no key
+    if (__shfl_sync(0xffffffffu, cur.k0.w, 31) > kmax) {
+        c3m_probe<ABS, 4>(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, hs, a, nslots);
+        return true;
+    }
+    c3m_probe<ABS, 8>(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, hs, a, nslots);
+    return !more || __shfl_sync(0xffffffffu, cur.k1.w, 31) > kmax;
 }
 
 // Four spokes per warp, eight lanes each (for rows of a few hundred entries,
@@ -815,7 +864,7 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
                                                  const uint8_t *s_map, unsigned *s_h, int *s_next, int nslots)
 {
     const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
-    const int nb = a.nb, nb2 = nb * nb;
+    const int nb = a.nb, hs = a.hs, nbhs = nb * hs;
     const int32_t kout = ABS ? (int32_t)guard : kbase - 1;   // an id whose segment is absent
     for (;;) {
         int li = 0;
@@ -827,7 +876,7 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
         int hb = 0;
         if (s < s_end) {
             c3m_spoke_range(a, soff, F[s], s, c0, kfirst, &p0, &pe);
-            hb = FB[s] * nb2;
+            hb = FB[s] * nbhs;
         }
         const int64_t pa = p0 & ~(int64_t)3;
         const int head = (int)(p0 - pa);
@@ -859,7 +908,7 @@ __device__ __forceinline__ void c3m_walk_grouped(const C3Args &a, int64_t soff, 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) k[e] = r0 + e < len ? k[e] : kout;
                 }
-                c3m_probe<ABS, 4>(k, &bb, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
+                c3m_probe<ABS, 4>(k, &bb, kbase, guard, s_seg, s_map, s_h, hb, nb, hs, a, nslots);
             }
             // rows are sorted: a group stops once its step's last key passes kmax
             const int last = __shfl_sync(0xffffffffu, kk.w, lane | 7);
@@ -878,7 +927,7 @@ k_count3m(C3Args a, int nslots)
     constexpr int KPT = C3M_KEYS_PER_THREAD;
     constexpr int MAX_KEYS = THREADS * KPT;
     // dynamic: segment table [C3M_SEG_TABLE] u8, map [(nslots + 1) * C3M_SEG] u8
-    // (slot 0: the all-absent segment), histogram [nb^3] u32
+    // (slot 0: the all-absent segment), histogram [nb][nb][hs] u32
     extern __shared__ unsigned s_dyn[];
     __shared__ int s_next;
     __shared__ int s_cut;
@@ -888,7 +937,7 @@ k_count3m(C3Args a, int nslots)
     __shared__ int s_q[2];                          // windowed: spoke positions [q_lo, q_hi) of F
 
     const int lane = threadIdx.x & 31;
-    const int nb = a.nb, nb2 = nb * nb, n3 = nb2 * nb;
+    const int nb = a.nb, hs = a.hs, nbhs = nb * hs, nh = nb * nbhs;
     const int64_t soff = WINDOWED ? a.soff : 0;
     // the segment table and the map first, at fixed offsets (their probes need
     // no base register), then the histogram
@@ -898,7 +947,7 @@ k_count3m(C3Args a, int nslots)
     uint8_t *s_map = s_seg + SEG_TABLE;
     unsigned *s_h = reinterpret_cast<unsigned *>(s_map + (size_t)(nslots + 1) * C3M_SEG);
 
-    for (int t = threadIdx.x; t < n3; t += THREADS) s_h[t] = 0;
+    for (int t = threadIdx.x; t < nh; t += THREADS) s_h[t] = 0;
     for (int t = threadIdx.x; t < C3M_SEG / 16; t += THREADS)
         reinterpret_cast<uint4 *>(s_map)[t] = make_uint4(~0u, ~0u, ~0u, ~0u);
     if (threadIdx.x == 0) s_pending = 0;
@@ -996,7 +1045,7 @@ k_count3m(C3Args a, int nslots)
             const bool flush = s_pending + bound > 0xffffffffull;   // the same in every thread
             __syncthreads();                                 // s_pending read; the map is written
             if (flush) {
-                c3m_flush<THREADS>(s_h, nb, a.cfg3, a.ghist);
+                c3m_flush<THREADS>(s_h, nb, hs, a.cfg3, a.ghist);
                 __syncthreads();
             }
             if (threadIdx.x == 0) {
@@ -1022,63 +1071,33 @@ k_count3m(C3Args a, int nslots)
                     if (s >= s_end) break;
                     int64_t p0, pe;
                     c3m_spoke_range(a, soff, F[s], s, c0, kfirst, &p0, &pe);
-                    const int hb = FB[s] * nb2;
+                    const int hb = FB[s] * nbhs;
                     if (p0 >= pe) continue;
                     // walk nbr[p0, pe) in aligned 256-entry steps: lane l reads entries
                     // 4l .. 4l+3 and 128+4l .. 128+4l+3 of a step as two int4 and their
-                    // bins as two words
+                    // bins as two words (the arrays hold GS_EDGE_PAD = 256 entries past
+                    // the last row, so a step that starts before the row's end is read
+                    // whole); two step buffers take turns, the next step in flight
                     const int64_t pa = p0 & ~(int64_t)3;
                     const int head = (int)(p0 - pa);
                     const int total_e = head + (int)(pe - p0);
-                    // checked builds: the walk's last loaded half step lies in the readable array
-                    if (!GS_DCHECK((pa - soff) + (((total_e + 127) >> 7) << 7) <= a.nbr_len, a.chk, GS_SITE_C3M_ROW))
+                    // checked builds: the walk's last loaded step lies in the readable array
+                    if (!GS_DCHECK((pa - soff) + (((total_e + 255) >> 8) << 8) <= a.nbr_len, a.chk, GS_SITE_C3M_ROW))
                         continue;
                     const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + (pa - soff)) + lane;
                     const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + (pa - soff)) + lane;
-                    // a half step is loaded only when it starts before the row's end:
-                    // the arrays hold GS_EDGE_PAD (128) entries past the last row
-                    int4 kk = __ldg(vk), kk2 = make_int4(0, 0, 0, 0);
-                    uint32_t bb = __ldg(vb), bb2 = 0;
-                    if (128 < total_e) {
-                        kk2 = __ldg(vk + 32);
-                        bb2 = __ldg(vb + 32);
-                    }
-                    for (int base = 0; base < total_e; base += 256) {
-                        vk += 64;
-                        vb += 64;
-                        int4 kn = kk, kn2 = kk2;
-                        uint32_t bn = bb, bn2 = bb2;
-                        if (base + 256 < total_e) {                // next step in flight
-                            kn = __ldg(vk);
-                            bn = __ldg(vb);
-                            if (base + 384 < total_e) {
-                                kn2 = __ldg(vk + 32);
-                                bn2 = __ldg(vb + 32);
-                            }
-                        }
-                        int k[8] = { kk.x, kk.y, kk.z, kk.w, kk2.x, kk2.y, kk2.z, kk2.w };
-                        const uint32_t b2[2] = { bb, bb2 };
-                        if (base == 0 || base + 256 > total_e) {   // first / last step only
-                            // entries outside [p0, pe) become an id of an absent segment
-                            const unsigned r0 = (unsigned)(base + 4 * lane - head), len = (unsigned)(total_e - head);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                k[e] = r0 + e < len ? k[e] : kout;
-                                k[4 + e] = r0 + 128 + e < len ? k[4 + e] : kout;
-                            }
-                        }
-                        // rows are sorted: once the first half's last key passes kmax, the
-                        // second half holds no key of the chunk, and the walk ends here
-                        if (__shfl_sync(0xffffffffu, kk.w, 31) > kmax) {
-                            c3m_probe<ABS, 4>(k, b2, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
+                    C3MStep A, B;
+                    A.k0 = __ldg(vk);
+                    A.b0 = __ldg(vb);
+                    A.k1 = __ldg(vk + 32);
+                    A.b1 = __ldg(vb + 32);
+                    for (int base = 0;; base += 512) {
+                        if (c3m_step<ABS>(A, B, vk, vb, base, total_e, head, lane, kmax, kout, kbase, guard, s_seg,
+                                          s_map, s_h, hb, nb, hs, a, nslots))
                             break;
-                        }
-                        c3m_probe<ABS, 8>(k, b2, kbase, guard, s_seg, s_map, s_h, hb, nb, a, nslots);
-                        if (__shfl_sync(0xffffffffu, kk2.w, 31) > kmax) break;
-                        kk = kn;
-                        kk2 = kn2;
-                        bb = bn;
-                        bb2 = bn2;
+                        if (c3m_step<ABS>(B, A, vk, vb, base + 256, total_e, head, lane, kmax, kout, kbase, guard,
+                                          s_seg, s_map, s_h, hb, nb, hs, a, nslots))
+                            break;
                     }
                 }
             }
@@ -1086,7 +1105,7 @@ k_count3m(C3Args a, int nslots)
         }
     }
     __syncthreads();
-    c3m_flush<THREADS>(s_h, nb, a.cfg3, a.ghist);
+    c3m_flush<THREADS>(s_h, nb, hs, a.cfg3, a.ghist);
 }
 
 // out[c] += sum over the slices of slice[c], 128-bit (low, high) words.
@@ -1146,11 +1165,12 @@ static C3MKernel c3m_kernel(gs_graph_t g, int threads, bool grouped, bool window
     return windowed ? c3m_kernel<true, false>(threads, grouped) : c3m_kernel<false, false>(threads, grouped);
 }
 
-static bool plan_count3m(gs_graph_t g, bool grouped, bool windowed, int *threads, int *slots, size_t *dyn)
+// Threads, map slots and dynamic shared memory of a byte-map launch whose
+// histogram and segment table take `fixed` bytes; false when fewer than
+// C3M_MIN_SLOTS slots fit.
+static bool plan_count3m_slots(gs_graph_t g, bool grouped, bool windowed, size_t fixed, int *threads, int *slots,
+                               size_t *dyn)
 {
-    if (g->nb > C3M_MAX_BINS || !g->cfg3) return false;
-    const int n3 = g->nb * g->nb * g->nb;
-    const size_t fixed = sizeof(unsigned) * (size_t)((n3 + 3) & ~3) + (c3m_abs(g) ? C3M_SEG_TABLE_ABS : C3M_SEG_TABLE);
     int dev = 0, smem_sm = 0, smem_block = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
@@ -1181,6 +1201,34 @@ static bool plan_count3m(gs_graph_t g, bool grouped, bool windowed, int *threads
                 return true;
             }
             sl -= 4;
+        }
+    }
+    return false;
+}
+
+// Row stride of the b_ik index of the byte-map walk's histogram. A warp's
+// adds share b_ij and spread over (b_ik, b_jk); the counter's bank is
+// (hs b_ik + b_jk) mod 32. With hs = nb = 30 (the BAO-scale bins) many pairs
+// collide (30 = -2 mod 32); a stride of 5 mod 32 spreads them. Modelled on
+// the one-spoke walk's adds over a scaled BAO-scale catalogue (15 of 32 lanes
+// hit): 1.58 wavefronts per add instruction with hs = 30, 1.07 with hs = 37;
+// on a uniform catalogue (8.5 hitting lanes) the stride made no difference.
+// So the one-spoke walk (dense rows) takes the padded stride while its
+// histogram leaves room for enough map slots; the four-spokes-per-warp walk
+// keeps hs = nb.
+static int c3m_padded_stride(int nb) { return nb + ((5 - nb) & 31); }
+
+static bool plan_count3m(gs_graph_t g, bool grouped, bool windowed, int *threads, int *slots, size_t *dyn, int *hs)
+{
+    if (g->nb > C3M_MAX_BINS || !g->cfg3) return false;
+    for (int pad = grouped ? 1 : 0; pad < 2; ++pad) {
+        const int h = pad == 0 ? c3m_padded_stride(g->nb) : g->nb;
+        const int nh = g->nb * g->nb * h;
+        const size_t fixed =
+            sizeof(unsigned) * (size_t)((nh + 3) & ~3) + (c3m_abs(g) ? C3M_SEG_TABLE_ABS : C3M_SEG_TABLE);
+        if (plan_count3m_slots(g, grouped, windowed, fixed, threads, slots, dyn)) {
+            *hs = h;
+            return true;
         }
     }
     return false;
@@ -1219,10 +1267,10 @@ static int count3_walk(gs_graph_t g)
 {
     int mode = count3_walk_override();
     const bool long_rows = g->n_edges > C3_GROUPED_MAX_DEGREE * g->n;
-    int t, sl;
+    int t, sl, hs;
     size_t d;
     if (mode < 0) mode = long_rows ? 2 : 3;
-    if (mode >= 2 && plan_count3m(g, mode == 3, g->n_win > 0, &t, &sl, &d)) return mode;
+    if (mode >= 2 && plan_count3m(g, mode == 3, g->n_win > 0, &t, &sl, &d, &hs)) return mode;
     if (g->n_win) return 0;                                  // the bitmap walk of windowed tiles
     if (mode == 1 || mode == 3 || (mode == 2 && !long_rows)) return plan_count3g(g, mode == 1, &d) ? 1 : 0;
     return 0;
@@ -1256,7 +1304,7 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
             const bool grouped = walk == 3;
             int threads = 0, slots = 0;
             size_t dm = 0;
-            if (!plan_count3m(g, grouped, win, &threads, &slots, &dm))
+            if (!plan_count3m(g, grouped, win, &threads, &slots, &dm, &a.hs))
                 return gs_set_error(GS_ERR_INTERNAL, "byte-map walk plan");
             const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count() * (threads == 512 ? 2 : 1), hubs);
             GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));

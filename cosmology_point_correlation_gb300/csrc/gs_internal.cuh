@@ -146,9 +146,10 @@ inline cudaError_t gs_malloc_host(T **p, size_t bytes)
 void gs_note_launch();
 
 // Entries of padding after the last edge of nbr / bin: a warp may read whole
-// 16-byte vectors up to 128 entries past a row's end without leaving the
-// allocation.
-constexpr int64_t GS_EDGE_PAD = 128;
+// 16-byte vectors up to 256 entries past a row's end without leaving the
+// allocation (the 3pCF walk reads every 256-entry step that starts in a row
+// whole).
+constexpr int64_t GS_EDGE_PAD = 256;
 
 // GS_ERR_ARG unless the current device is the one the graph was built on
 // (every pointer a count passes to its kernels belongs to that device).
