@@ -47,6 +47,10 @@ constexpr int C4_M = 512;                   // largest hub degree kept in shared
 constexpr int C4_WORDS = C4_M / 32;
 constexpr int C4_TABLE = 2 * C4_M;
 constexpr int C4_SMEM_HIST_MAX = 8192;
+// Shared-memory histogram: three u32 counters per configuration, the cliques
+// of negative, zero and positive volume, so that a clique is one add (the
+// even count is their sum, the odd sum positive minus negative).
+constexpr int C4_HIST_WORDS = 3;
 constexpr int C4_EMPTY = -1;
 
 struct C4Args {
@@ -111,7 +115,7 @@ struct HubSpace {
 
 template <bool SMEM_HIST, bool WINDOWED, bool SMALLR>
 __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long long i, int m,
-                                       int tlog, unsigned *s_even, int *s_odd,
+                                       int tlog, unsigned *s_cnt,
                                        const int *lex_a, const int *lex_b)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -225,10 +229,8 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
             }
             if (!GS_DCHECK(idx >= 0 && idx < a.ncfg, a.chk, GS_SITE_C4_HIST)) return;
             if (SMEM_HIST) {
-                // two 32-bit adds: a 64-bit shared-memory add (even and odd packed in
-                // one word) measured three times slower on 56 contended counters
-                atomicAdd(&s_even[idx], 1u);
-                if (sg) atomicAdd(&s_odd[idx], sg);
+                // one add, into the counter of the volume's sign
+                atomicAdd(&s_cnt[(sg + 1) * a.ncfg + idx], 1u);
             } else {
                 atomicAdd(a.even + idx, 1ull);
                 if (sg) atomicAdd((unsigned long long *)(a.odd + idx), (unsigned long long)(long long)sg);
@@ -314,16 +316,19 @@ __device__ __forceinline__ void c4_lex_tables(int nb, int *lex_a, int *lex_b)
     }
 }
 
-// Add the shared counters into the caller's histograms and clear them.
-__device__ __forceinline__ void c4_flush(unsigned *se, int *so, int ncfg, unsigned long long *ge, long long *go)
+// Add the shared counters into the caller's histograms and clear them: even =
+// negative + zero + positive volume, odd = positive - negative.
+__device__ __forceinline__ void c4_flush(unsigned *sc, int ncfg, unsigned long long *ge, long long *go)
 {
     for (int t = threadIdx.x; t < ncfg; t += C4_THREADS) {
-        const unsigned e = se[t];
-        const int o = so[t];
+        const unsigned neg = sc[t], zero = sc[ncfg + t], pos = sc[2 * ncfg + t];
+        const unsigned long long e = (unsigned long long)neg + zero + pos;
+        const long long o = (long long)pos - (long long)neg;
         if (e) atomicAdd(ge + t, (unsigned long long)e);
-        if (o) atomicAdd((unsigned long long *)(go + t), (unsigned long long)(long long)o);
-        se[t] = 0u;
-        so[t] = 0;
+        if (o) atomicAdd((unsigned long long *)(go + t), (unsigned long long)o);
+        sc[t] = 0u;
+        sc[ncfg + t] = 0u;
+        sc[2 * ncfg + t] = 0u;
     }
 }
 
@@ -333,7 +338,7 @@ template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED, bool SMALLR>
 __global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_small(C4Args a)
 {
-    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], bin masks [nb * C4_WORDS], even, odd [ncfg]
+    extern __shared__ unsigned s_dyn[];         // bits [C4_M * C4_WORDS], bin masks [nb * C4_WORDS], counters [3][ncfg]
     __shared__ int32_t s_key[C4_TABLE];
     __shared__ int32_t s_pos[C4_TABLE];
     __shared__ int32_t s_row[C4_M];
@@ -347,14 +352,10 @@ k_count4_small(C4Args a)
 
     unsigned *s_bits = s_dyn;
     unsigned *s_bm = s_dyn + C4_M * C4_WORDS;                 // [nb][C4_WORDS]
-    unsigned *s_even = s_bm + a.nb * C4_WORDS;
-    int *s_odd = reinterpret_cast<int *>(s_even + a.ncfg);
+    unsigned *s_cnt = s_bm + a.nb * C4_WORDS;
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
     if (SMEM_HIST)
-        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) {
-            s_even[t] = 0u;
-            s_odd[t] = 0;
-        }
+        for (int t = threadIdx.x; t < C4_HIST_WORDS * a.ncfg; t += C4_THREADS) s_cnt[t] = 0u;
     for (int t = threadIdx.x; t < C4_TABLE; t += C4_THREADS) s_key[t] = C4_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
     HubSpace w{ s_key, s_pos, s_row, s_hb, s_v, s_bits, s_bm, &s_next };
@@ -372,7 +373,7 @@ k_count4_small(C4Args a)
             // C(m, 3) bounds the cliques of this hub
             const unsigned long long bound = (unsigned long long)m * (m - 1) * (m - 2) / 6;
             if (s_pending + bound > 0x7fffffffull) {
-                c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+                c4_flush(s_cnt, a.ncfg, a.even, a.odd);
                 __syncthreads();
                 if (threadIdx.x == 0) s_pending = 0;
             }
@@ -381,11 +382,11 @@ k_count4_small(C4Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * m) ++tlog;
-        c4_hub<SMEM_HIST, WINDOWED, SMALLR>(a, w, i, m, tlog, s_even, s_odd, s_lex_a, s_lex_b);
+        c4_hub<SMEM_HIST, WINDOWED, SMALLR>(a, w, i, m, tlog, s_cnt, s_lex_a, s_lex_b);
     }
     if (SMEM_HIST) {
         __syncthreads();
-        c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+        c4_flush(s_cnt, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -397,20 +398,16 @@ template <bool SMEM_HIST, bool HUB_LIST, bool WINDOWED, bool SMALLR>
 __global__ void __launch_bounds__(C4_THREADS, 4)
 k_count4_large(C4Args a)
 {
-    extern __shared__ unsigned s_dyn[];             // (SMEM_HIST) even, odd [ncfg]
+    extern __shared__ unsigned s_dyn[];             // (SMEM_HIST) counters [3][ncfg]
     __shared__ int s_lex[512];                  // lex_a, lex_b (or the u16 table; see c4_lex_tables)
     int *s_lex_a = s_lex, *s_lex_b = s_lex + 256;
     __shared__ long long s_hub;
     __shared__ int s_next;
     __shared__ unsigned long long s_pending;
-    unsigned *s_even = s_dyn;
-    int *s_odd = reinterpret_cast<int *>(s_even + a.ncfg);
+    unsigned *s_cnt = s_dyn;
     c4_lex_tables(a.nb, s_lex_a, s_lex_b);
     if (SMEM_HIST)
-        for (int t = threadIdx.x; t < a.ncfg; t += C4_THREADS) {
-            s_even[t] = 0u;
-            s_odd[t] = 0;
-        }
+        for (int t = threadIdx.x; t < C4_HIST_WORDS * a.ncfg; t += C4_THREADS) s_cnt[t] = 0u;
     if (threadIdx.x == 0) s_pending = 0;
 
     const int M = a.big_m;
@@ -442,21 +439,21 @@ k_count4_large(C4Args a)
         while ((1 << tl) < 2 * m) ++tl;
         const unsigned long long bound = (unsigned long long)m * (m - 1) * (m - 2) / 6;
         if (!SMEM_HIST || bound > 0x7fffffffull) {
-            c4_hub<false, WINDOWED, SMALLR>(a, w, i, m, tl, nullptr, nullptr, s_lex_a, s_lex_b);
+            c4_hub<false, WINDOWED, SMALLR>(a, w, i, m, tl, nullptr, s_lex_a, s_lex_b);
             continue;
         }
         if (s_pending + bound > 0x7fffffffull) {
-            c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+            c4_flush(s_cnt, a.ncfg, a.even, a.odd);
             __syncthreads();
             if (threadIdx.x == 0) s_pending = 0;
         }
         __syncthreads();
         if (threadIdx.x == 0) s_pending += bound;
-        c4_hub<SMEM_HIST, WINDOWED, SMALLR>(a, w, i, m, tl, s_even, s_odd, s_lex_a, s_lex_b);
+        c4_hub<SMEM_HIST, WINDOWED, SMALLR>(a, w, i, m, tl, s_cnt, s_lex_a, s_lex_b);
     }
     if (SMEM_HIST) {
         __syncthreads();
-        c4_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+        c4_flush(s_cnt, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -501,7 +498,7 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
     const int sms = gs_sm_count();
     const bool smem = a.ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)a.nb * C4_WORDS +
-                                           (smem ? 2 * (size_t)a.ncfg : 0));
+                                           (smem ? C4_HIST_WORDS * (size_t)a.ncfg : 0));
     const C4Kernel kern = c4_kernel(false, smem, false, windowed, g);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
@@ -521,7 +518,7 @@ static gs_status c4_launch(gs_graph_t g, C4Args a, bool windowed, cudaStream_t s
         a.big_m = M;
         a.scratch_stride = c4_large_stride(M, g->nb);
         const int gl = (int)std::min<int64_t>((int64_t)sms * 2, hubs);
-        const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)a.ncfg : 0;
+        const size_t ldyn = smem ? sizeof(unsigned) * C4_HIST_WORDS * (size_t)a.ncfg : 0;
         const C4Kernel big = c4_kernel(true, smem, false, windowed, g);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
@@ -693,7 +690,7 @@ static gs_status c4_count_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t co
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)g->nb * C4_WORDS +
-                                           (smem ? 2 * ncfg : 0));
+                                           (smem ? C4_HIST_WORDS * ncfg : 0));
     const C4Kernel kern = c4_kernel(false, smem, true, false, g);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
@@ -710,7 +707,7 @@ static gs_status c4_count_hubs(gs_graph_t g, const int32_t *hubs_dev, int64_t co
         a.cursor = g->work + 2;
         a.big_m = M;
         a.scratch_stride = stride;
-        const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
+        const size_t ldyn = smem ? sizeof(unsigned) * C4_HIST_WORDS * (size_t)ncfg : 0;
         const C4Kernel big = c4_kernel(true, smem, true, false, g);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
@@ -817,7 +814,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
     const int sms = gs_sm_count();
     const bool smem = ncfg <= C4_SMEM_HIST_MAX;
     const size_t dyn = sizeof(unsigned) * ((size_t)C4_M * C4_WORDS + (size_t)g->nb * C4_WORDS +
-                                           (smem ? 2 * ncfg : 0));
+                                           (smem ? C4_HIST_WORDS * ncfg : 0));
     const C4Kernel kern = c4_kernel(false, smem, false, false, g);
     int per_sm = 0;
     GS_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
@@ -836,7 +833,7 @@ extern "C" gs_status gs_count_4pcf_parity_static(gs_graph_t g, uint64_t *even_de
         a.big_m = M;
         a.scratch = base + GS_C4_STATIC_HEAD;
         a.scratch_stride = stride;
-        const size_t ldyn = smem ? sizeof(unsigned) * 2 * (size_t)ncfg : 0;
+        const size_t ldyn = smem ? sizeof(unsigned) * C4_HIST_WORDS * (size_t)ncfg : 0;
         const C4Kernel big = c4_kernel(true, smem, false, false, g);
         GS_TRY_CUDA(cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ldyn));
         big<<<gl, C4_THREADS, ldyn, st>>>(a);
