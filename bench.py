@@ -45,6 +45,7 @@ METRIC = "3pCF triangles/s and edges/s on 1 GB300; achieved HBM GB/s vs peak"
 FALLBACK_HBM_GBS = 6800.0
 BYTES_PER_EDGE = 5                      # int32 neighbour id + uint8 bin
 PROFILE_COUNTERS = os.path.join(ROOT, "profiles", "k_count3m_bao_3pcf.json")
+PARITY_COUNTERS = os.path.join(ROOT, "profiles", "k_count4_small_parity_4pcf.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "cosmology_point_correlation_gb300", "csrc", f)
                   for f in ("gs_count3.cu", "gs_internal.cuh")]
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
@@ -279,6 +280,36 @@ def profiled_counters(workload: str):
     return d
 
 
+def parity_roofline(workload: str, cliques: int, count_s: float, dev, sm_mhz: float):
+    """The parity count's on-chip ceilings: L1 data-pipe wavefronts and warp
+    instructions per clique from the ncu capture of the same kernel source
+    (profiles/k_count4_small_parity_4pcf.json), times the clique rate of this
+    run, against one wavefront and four instruction issues per SM per cycle."""
+    import torch
+    try:
+        with open(PARITY_COUNTERS) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for p in d.get("sources", []):
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    if d.get("workload") != workload or d.get("kernel_source_sha256") != h.hexdigest() or \
+            d.get("cliques_per_launch") != cliques:
+        return None
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk = sm_mhz * 1e6
+    l1_rate = d["l1_wavefronts_per_launch"] / count_s
+    return {"bound": "alu", "kernel": "k_count4_small",
+            "ceiling": "the L1 / shared-memory data pipe and instruction issue of the clique search",
+            "achieved": l1_rate / 1e9, "peak": sms * clk / 1e9, "unit": "G wavefronts/s",
+            "frac": l1_rate / (sms * clk),
+            "peak_kind": f"derived: {sms} SMs x 1 wavefront per cycle x the sampled SM clock ({sm_mhz:.0f} MHz)",
+            "issue_frac": d["warp_inst_per_launch"] / count_s / (sms * 4 * clk),
+            "counters": "profiles/k_count4_small_parity_4pcf.json (ncu, kernel source hash checked)"}
+
+
 # ------------------------------------------------------------------ distributed
 
 def dist_init(n_gpus: int):
@@ -503,7 +534,9 @@ def run_ours(args, w):
                                                              [float(cliques), float(pres[-1][3])])
         parity = {"config": pdesc, "ms_per_step": p_step, "count_ms": p_count,
                   "cliques_per_s": cl_all / (p_step / 1e3), "edges_per_s": pe_all / (p_step / 1e3),
-                  "cliques": cliques, "odd_sum": int(odd.sum().item()), "n_edges": pres[-1][3]}
+                  "cliques": cliques, "odd_sum": int(odd.sum().item()), "n_edges": pres[-1][3],
+                  "roofline": (parity_roofline(pw.name, cliques, p_count / 1e3, dev, clocks.get("sm_mhz") or 2070.0)
+                               if args.scale == 1.0 else None)}
 
     # six-edge-bin 4pCF (276 configurations) on the parity catalogue with 4 bins
     fourpcf6 = None

@@ -47,6 +47,10 @@ constexpr int C6_SMEM_HIST_MAX = 4096;
 constexpr int C6_SMEM_W_MAX = 2500;         // weighted: configurations with shared 128-bit sums (nb <= 6)
 constexpr int C6_EMPTY = -1;
 constexpr int C6_MAX_BINS = 10;             // the tuple table holds nb^6 entries
+// Unweighted shared-memory histogram: three u32 counters per configuration,
+// the tetrahedra of negative, zero and positive signed volume, so that a
+// tetrahedron is one add (even = their sum, odd = positive - negative).
+constexpr int C6_HIST_WORDS = 3;
 
 struct C6Args {
     const int4 *pts;
@@ -101,7 +105,7 @@ struct C6Space {
 
 template <int NT, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
 __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long long i, int64_t f0, int f,
-                                       int tlog, unsigned *s_even, int *s_odd, unsigned *s_w128)
+                                       int tlog, unsigned *s_cnt, unsigned *s_w128)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t *F = WINDOWED ? a.hnbr + (f0 - a.hoff) : a.nbr + f0;       // forward row and its bins
@@ -230,8 +234,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                     if (sg) gs_add128(a.wodd + 2 * ci, sg * W4);
                 }
             } else if (SMEM_HIST) {
-                atomicAdd(&s_even[ci], 1u);
-                if (sg) atomicAdd(&s_odd[ci], sg);
+                atomicAdd(&s_cnt[(sg + 1) * a.ncfg + ci], 1u);       // the counter of the volume's sign
             } else {
                 atomicAdd(a.even + ci, 1ull);
                 if (sg) atomicAdd((unsigned long long *)(a.odd + ci), (unsigned long long)(long long)sg);
@@ -292,13 +295,20 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     for (int t = threadIdx.x; t < tsize; t += NT) w.key[t] = C6_EMPTY;
 }
 
-__device__ __forceinline__ void c6_flush(unsigned *se, int *so, int ncfg, unsigned long long *ge, long long *go)
+// Add the unweighted shared counters into the caller's histograms (even =
+// negative + zero + positive volume, odd = positive - negative) and clear them.
+template <int NT>
+__device__ __forceinline__ void c6_flush(unsigned *sc, int ncfg, unsigned long long *ge, long long *go)
 {
-    for (int t = threadIdx.x; t < ncfg; t += C6_THREADS) {
-        if (se[t]) atomicAdd(ge + t, (unsigned long long)se[t]);
-        if (so[t]) atomicAdd((unsigned long long *)(go + t), (unsigned long long)(long long)so[t]);
-        se[t] = 0;
-        so[t] = 0;
+    for (int t = threadIdx.x; t < ncfg; t += NT) {
+        const unsigned neg = sc[t], zero = sc[ncfg + t], pos = sc[2 * ncfg + t];
+        const unsigned long long e = (unsigned long long)neg + zero + pos;
+        const long long o = (long long)pos - (long long)neg;
+        if (e) atomicAdd(ge + t, e);
+        if (o) atomicAdd((unsigned long long *)(go + t), (unsigned long long)o);
+        sc[t] = 0u;
+        sc[ncfg + t] = 0u;
+        sc[2 * ncfg + t] = 0u;
     }
 }
 
@@ -309,8 +319,8 @@ template <int M, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
 __global__ void __launch_bounds__(C6_THREADS, M <= C6_M_SMALL ? 4 : 2)
 k_count6_small(C6Args a)
 {
-    // dynamic: bits [M*M/32], sbin [M*M], then (SMEM_HIST) even, odd [ncfg]
-    // each, or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
+    // dynamic: bits [M*M/32], sbin [M*M], then (SMEM_HIST) the counters
+    // [3][ncfg], or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
     extern __shared__ unsigned s_dyn[];
     __shared__ int32_t s_key[2 * M];
     __shared__ int32_t s_pos[2 * M];
@@ -324,16 +334,12 @@ k_count6_small(C6Args a)
 
     unsigned *s_bits = s_dyn;
     uint8_t *s_sbin = (uint8_t *)(s_bits + M * (M / 32));
-    unsigned *s_even = (unsigned *)(s_sbin + M * M);
-    int *s_odd = (int *)(s_even + a.ncfg);
-    unsigned *s_w128 = s_even;
+    unsigned *s_cnt = (unsigned *)(s_sbin + M * M);
+    unsigned *s_w128 = s_cnt;
     if (SMEM_HIST && WEIGHTED)
         for (int t = threadIdx.x; t < 8 * a.ncfg; t += C6_THREADS) s_w128[t] = 0;
     else if (SMEM_HIST)
-        for (int t = threadIdx.x; t < a.ncfg; t += C6_THREADS) {
-            s_even[t] = 0;
-            s_odd[t] = 0;
-        }
+        for (int t = threadIdx.x; t < C6_HIST_WORDS * a.ncfg; t += C6_THREADS) s_cnt[t] = 0u;
     for (int t = threadIdx.x; t < 2 * M; t += C6_THREADS) s_key[t] = C6_EMPTY;
     if (threadIdx.x == 0) s_pending = 0;
     C6Space w{ s_key, s_pos, s_row, s_hb, s_v, s_bits, s_sbin, s_ww, &s_next };
@@ -350,7 +356,7 @@ k_count6_small(C6Args a)
         if (SMEM_HIST && !WEIGHTED) {
             const unsigned long long bound = (unsigned long long)f * (f - 1) * (f - 2) / 6;
             if (s_pending + bound > 0x7fffffffull) {
-                c6_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+                c6_flush<C6_THREADS>(s_cnt, a.ncfg, a.even, a.odd);
                 __syncthreads();
                 if (threadIdx.x == 0) s_pending = 0;
             }
@@ -359,7 +365,7 @@ k_count6_small(C6Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * f) ++tlog;
-        c6_hub<C6_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tlog, s_even, s_odd, s_w128);
+        c6_hub<C6_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tlog, s_cnt, s_w128);
     }
     if (SMEM_HIST && WEIGHTED) {
         __syncthreads();
@@ -372,7 +378,7 @@ k_count6_small(C6Args a)
         }
     } else if (SMEM_HIST) {
         __syncthreads();
-        c6_flush(s_even, s_odd, a.ncfg, a.even, a.odd);
+        c6_flush<C6_THREADS>(s_cnt, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -384,21 +390,17 @@ template <bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
 __global__ void __launch_bounds__(C6_LARGE_THREADS, 1)
 k_count6_large(C6Args a)
 {
-    // dynamic (SMEM_HIST): even, odd [ncfg] each, or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
+    // dynamic (SMEM_HIST): the counters [3][ncfg], or (WEIGHTED) the 128-bit sums [ncfg][2][4] u32
     extern __shared__ unsigned s_dyn[];
     __shared__ long long s_hub;
     __shared__ int s_next;
     __shared__ unsigned long long s_pending;
-    unsigned *s_even = s_dyn;
-    int *s_odd = (int *)(s_even + a.ncfg);
+    unsigned *s_cnt = s_dyn;
     unsigned *s_w128 = s_dyn;
     if (SMEM_HIST && WEIGHTED)
         for (int t = threadIdx.x; t < 8 * a.ncfg; t += C6_LARGE_THREADS) s_w128[t] = 0;
     else if (SMEM_HIST)
-        for (int t = threadIdx.x; t < a.ncfg; t += C6_LARGE_THREADS) {
-            s_even[t] = 0;
-            s_odd[t] = 0;
-        }
+        for (int t = threadIdx.x; t < C6_HIST_WORDS * a.ncfg; t += C6_LARGE_THREADS) s_cnt[t] = 0u;
     if (threadIdx.x == 0) s_pending = 0;
     const int M = a.big_m;
     int tlog = 4;
@@ -431,24 +433,19 @@ k_count6_large(C6Args a)
         const unsigned long long bound = (unsigned long long)f * (f - 1) * (f - 2) / 6;
         if (SMEM_HIST && !WEIGHTED && bound > 0x7fffffffull) {
             // one hub could overflow the 32-bit shared counters: global atomics
-            c6_hub<C6_LARGE_THREADS, false, false, WINDOWED>(a, w, i, f0, f, tl, nullptr, nullptr, nullptr);
+            c6_hub<C6_LARGE_THREADS, false, false, WINDOWED>(a, w, i, f0, f, tl, nullptr, nullptr);
             continue;
         }
         if (SMEM_HIST && !WEIGHTED) {
             if (s_pending + bound > 0x7fffffffull) {
-                for (int t = threadIdx.x; t < a.ncfg; t += C6_LARGE_THREADS) {
-                    if (s_even[t]) atomicAdd(a.even + t, (unsigned long long)s_even[t]);
-                    if (s_odd[t]) atomicAdd((unsigned long long *)(a.odd + t), (unsigned long long)(long long)s_odd[t]);
-                    s_even[t] = 0;
-                    s_odd[t] = 0;
-                }
+                c6_flush<C6_LARGE_THREADS>(s_cnt, a.ncfg, a.even, a.odd);
                 __syncthreads();
                 if (threadIdx.x == 0) s_pending = 0;
             }
             __syncthreads();
             if (threadIdx.x == 0) s_pending += bound;
         }
-        c6_hub<C6_LARGE_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tl, s_even, s_odd, s_w128);
+        c6_hub<C6_LARGE_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tl, s_cnt, s_w128);
     }
     if (SMEM_HIST && WEIGHTED) {
         __syncthreads();
@@ -461,10 +458,7 @@ k_count6_large(C6Args a)
         }
     } else if (SMEM_HIST) {
         __syncthreads();
-        for (int t = threadIdx.x; t < a.ncfg; t += C6_LARGE_THREADS) {
-            if (s_even[t]) atomicAdd(a.even + t, (unsigned long long)s_even[t]);
-            if (s_odd[t]) atomicAdd((unsigned long long *)(a.odd + t), (unsigned long long)(long long)s_odd[t]);
-        }
+        c6_flush<C6_LARGE_THREADS>(s_cnt, a.ncfg, a.even, a.odd);
     }
 }
 
@@ -626,7 +620,7 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
     const int ncfg = a.ncfg;
     const bool weighted = a.w != nullptr;
     const bool smem = weighted ? ncfg <= C6_SMEM_W_MAX : ncfg <= C6_SMEM_HIST_MAX;
-    const size_t acc = weighted ? 32 * (size_t)ncfg : 8 * (size_t)ncfg;
+    const size_t acc = weighted ? 32 * (size_t)ncfg : sizeof(unsigned) * C6_HIST_WORDS * (size_t)ncfg;
     // the two shared-memory kernels: hubs of forward degree 3..128, then 129..256
     for (int pass = 0; pass < 2; ++pass) {
         const int m = pass ? C6_M : C6_M_SMALL;
