@@ -845,12 +845,14 @@ __device__ __forceinline__ bool c3m_step(const C3MStep &cur, C3MStep &nxt, const
         }
     }
     // once the first half's last key passes kmax, the second half holds no key
-    if (__shfl_sync(0xffffffffu, cur.k0.w, 31) > kmax) {
+    // (lane 31 holds it; a vote, not a shuffle: shuffles take slots of the
+    // shared-memory pipe that the probes use)
+    if (__any_sync(0xffffffffu, lane == 31 && cur.k0.w > kmax)) {
         c3m_probe<ABS, 4>(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, hs, a, nslots);
         return true;
     }
     c3m_probe<ABS, 8>(k, bb, kbase, guard, s_seg, s_map, s_h, hb, nb, hs, a, nslots);
-    return !more || __shfl_sync(0xffffffffu, cur.k1.w, 31) > kmax;
+    return !more || __any_sync(0xffffffffu, lane == 31 && cur.k1.w > kmax);
 }
 
 // Four spokes per warp, eight lanes each (for rows of a few hundred entries,
