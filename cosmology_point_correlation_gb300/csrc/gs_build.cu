@@ -309,18 +309,24 @@ __global__ void k_gather_points(const int32_t *__restrict__ xyz, const int32_t *
 
 // ---------------------------------------------------------------- neighbour search
 //
-// One block per home cell. The block stages up to NB_HOME home points and,
-// range by range, up to NB_CAND candidate points in shared memory; each warp
-// tests its home points against the staged tile, 32 candidates per step, and
-// (FILL pass) writes hits in candidate order with a ballot prefix count.
-// Neighbour cells are visited in increasing id, merged into contiguous index
-// ranges (a z-run of three cells is one range unless it wraps).
+// NB_SPLIT blocks per home cell (blockIdx.y), each taking every NB_SPLIT-th
+// batch of NB_HOME home points, so that the grid holds several waves of
+// blocks and the cells of a clustered catalogue, which differ widely in size,
+// leave no long tail. A block stages its home points and, range by range, up
+// to NB_CAND candidate points in shared memory; each warp tests its home
+// points against the staged tile, 32 candidates per step, and (FILL pass)
+// writes hits in candidate order with a ballot prefix count. Neighbour cells
+// are visited in increasing id, merged into contiguous index ranges (a z-run
+// of three cells is one range unless it wraps). PERIODIC and LOWER (a lower
+// edge e_0 > 0) are compile-time, so the common open or periodic box with
+// e_0 = 0 pays for neither test it does not need.
 
 constexpr int NB_THREADS = 256;
-constexpr int NB_HOME = 512;
+constexpr int NB_HOME = 256;
+constexpr int NB_SPLIT = 4;
 constexpr int NB_CAND = 1024;
 
-template <bool FILL>
+template <bool FILL, bool PERIODIC, bool LOWER>
 __global__ void __launch_bounds__(NB_THREADS)
 k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start, int ncell,
             int box, int periodic, long long e0sq, long long rsq,
@@ -341,7 +347,7 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
     // cells [cell0, cell0 + gridDim.x); FILL writes edge e at nbr[e - woff]
     const int c = cell0 + blockIdx.x;
     const int h0 = cell_start[c], h1 = cell_start[c + 1];
-    if (h0 >= h1) return;
+    if (h0 + (int)blockIdx.y * NB_HOME >= h1) return;        // no batch of this cell for this block
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = NB_THREADS / 32;
 
     if (FILL)
@@ -386,7 +392,7 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
     __syncthreads();
     const int nr = s_nr;
 
-    for (int hb = h0; hb < h1; hb += NB_HOME) {
+    for (int hb = h0 + (int)blockIdx.y * NB_HOME; hb < h1; hb += NB_SPLIT * NB_HOME) {
         const int hn = min(NB_HOME, h1 - hb);
         for (int t = threadIdx.x; t < hn; t += NB_THREADS) {
             s_home[t] = pts[hb + t];
@@ -411,11 +417,11 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
                         long long d2 = 0;
                         if (t < cn) {
                             const int4 Q = s_cand[t];
-                            const int dx = gs_delta(P.x, Q.x, box, periodic);
-                            const int dy = gs_delta(P.y, Q.y, box, periodic);
-                            const int dz = gs_delta(P.z, Q.z, box, periodic);
+                            const int dx = gs_delta(P.x, Q.x, box, PERIODIC);
+                            const int dy = gs_delta(P.y, Q.y, box, PERIODIC);
+                            const int dz = gs_delta(P.z, Q.z, box, PERIODIC);
                             d2 = gs_norm2(dx, dy, dz);
-                            hit = (cb + t != p) && d2 >= e0sq && d2 < rsq;
+                            hit = (cb + t != p) && (!LOWER || d2 >= e0sq) && d2 < rsq;
                         }
                         const unsigned m = __ballot_sync(0xffffffffu, hit);
                         if (FILL && hit) {
@@ -432,7 +438,12 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
                             }
                         }
                         cnt += __popc(m);
-                        if (!FILL) lo += __popc(__ballot_sync(0xffffffffu, hit && cb + t < p));
+                        if (!FILL) {
+                            // neighbours below p: the step lies below p, above it, or
+                            // straddles it (lanes below p - cb - t0 < 32)
+                            if (cb + t0 + 31 < p) lo += __popc(m);
+                            else if (cb + t0 < p) lo += __popc(m & ((1u << (p - cb - t0)) - 1u));
+                        }
                     }
                     if (lane == 0) {
                         s_cnt[hp] = cnt;
@@ -452,6 +463,18 @@ k_neighbors(const int4 *__restrict__ pts, const int32_t *__restrict__ cell_start
         }
         __syncthreads();
     }
+}
+
+// The neighbour kernel of a pass (count or fill), box type and lower edge.
+using NeighborsKernel = decltype(&k_neighbors<false, false, false>);
+
+static NeighborsKernel neighbors_kernel(bool fill, bool periodic, bool lower)
+{
+    if (fill)
+        return periodic ? (lower ? k_neighbors<true, true, true> : k_neighbors<true, true, false>)
+                        : (lower ? k_neighbors<true, false, true> : k_neighbors<true, false, false>);
+    return periodic ? (lower ? k_neighbors<false, true, true> : k_neighbors<false, true, false>)
+                    : (lower ? k_neighbors<false, false, true> : k_neighbors<false, false, false>);
 }
 
 // ---------------------------------------------------------------- build
@@ -722,7 +745,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
             gs_note_launch();
             k_gather_points<<<grid1, 256, 0, st>>>(coords_dev, perm, n, g->pts, g->inv);
             gs_note_launch();
-            k_neighbors<false><<<ncells, NB_THREADS, 0, st>>>(
+            neighbors_kernel(false, g->periodic, edges_lu[0] > 0)<<<dim3(ncells, NB_SPLIT), NB_THREADS, 0, st>>>(
                 g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                 (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
                 deg, g->fwd, nullptr, nullptr, nullptr, maxd, 0, 0, g->chk, 0);
@@ -754,7 +777,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
             GS_BUILD_CUDA(cudaMemsetAsync(g->nbr + g->n_edges, 0xff, sizeof(int32_t) * GS_EDGE_PAD, st));
             GS_BUILD_CUDA(cudaMemsetAsync(g->bin + g->n_edges, 0, GS_EDGE_PAD, st));
             if (n > 0 && g->n_edges > 0) {
-                k_neighbors<true><<<ncells, NB_THREADS, 0, st>>>(
+                neighbors_kernel(true, g->periodic, edges_lu[0] > 0)<<<dim3(ncells, NB_SPLIT), NB_THREADS, 0, st>>>(
                     g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                     (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
                     nullptr, nullptr, g->row_ptr, g->nbr, g->bin, nullptr, 0, 0, g->chk, (int64_t)ne);
@@ -794,7 +817,7 @@ static gs_status build_impl(const int32_t *coords_dev, int64_t n, int64_t box_lu
                 const int64_t e0 = g->win_e0[w], e1 = g->win_e0[w + 1];
                 if (e1 > e0) {
                     const int64_t a = e0 & ~(int64_t)3;
-                    k_neighbors<true><<<cell1 - cell0, NB_THREADS, 0, st>>>(
+                    neighbors_kernel(true, g->periodic, edges_lu[0] > 0)<<<dim3(cell1 - cell0, NB_SPLIT), NB_THREADS, 0, st>>>(
                         g->pts, cell_start, g->ncell, (int)box_lu, g->periodic,
                         (long long)edges_lu[0] * edges_lu[0], (long long)r_max_lu * r_max_lu, esq, nbins,
                         nullptr, nullptr, g->row_ptr, g->s_nbr[0], g->s_bin[0], nullptr, cell0, a, g->chk, g->win_cap);
