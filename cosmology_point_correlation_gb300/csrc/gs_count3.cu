@@ -1110,6 +1110,237 @@ k_count3m(C3Args a, int nslots)
     c3m_flush<THREADS>(s_h, nb, hs, a.cfg3, a.ghist);
 }
 
+// ---------------------------------------------------------------- weighted byte-map walk
+//
+// The weighted 3pCF (for every configuration the exact sum of w_i w_j w_k over
+// its triangles, §II.1) on the byte-map walk, for device-resident graphs with
+// at most C3M_MAX_BINS bins; k_count3<..., WEIGHTED> (bitmap walk) serves the
+// rest. The chunk's keys are held as in k_count3m (a byte map of their bins)
+// and, in a parallel map with the same slots, as their int16 weights. A hit
+// adds w_j w_k (|.| <= 2^30) to the hub's sum T[c], c read from the nb^3
+// configuration table in shared memory; T[c] is an int64 held as two 32-bit
+// words, one shared add on the low word and a second, on the high word, only
+// on a carry or borrow. A hub closes at most f (f - 1) / 2 triangles, and
+// the kernel serves graphs whose forward rows hold fewer than 2^16 keys, so
+// |T| < 2^61. After the hub's last chunk the block adds w_i T[c], an exact
+// 128-bit product, into its own slice (each configuration has one owner
+// thread, no atomics) and clears T; k_sum128_slices adds the slices. Spokes
+// are walked one per warp in 256-entry steps.
+
+// T[c] += p for the (low, high) word pair q of an int64 sum.
+__device__ __forceinline__ void c3w_add64(unsigned *q, int p)
+{
+    const unsigned pu = (unsigned)p;
+    const unsigned old = atomicAdd(q, pu);
+    const unsigned up = (old + pu < old ? 1u : 0u) + (p < 0 ? ~0u : 0u);   // carry, plus the sign extension
+    if (up) atomicAdd(q + 1, up);
+}
+
+// Probe the eight entries of a step (lane l: 4l .. 4l+3 in k[0..3], 128+4l ..
+// in k[4..7], their bins in bb[0], bb[1]); a hit adds w_j w_k to T.
+template <bool ABS>
+__device__ __forceinline__ void c3w_probe8(const int *k, const uint32_t *bb, int32_t kbase, unsigned guard,
+                                           const uint8_t *s_seg, const uint8_t *s_map, const int16_t *s_wmap,
+                                           const uint16_t *s_cfg, unsigned *s_T, int hb, int nb, int wj,
+                                           const C3Args &a, int nslots)
+{
+    unsigned o[8], sl[8], v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = ABS ? (unsigned)k[e] : min((unsigned)(k[e] - kbase), guard);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sl[e] = s_seg[o[e] >> C3M_SEG_LOG];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (!GS_DCHECK(sl[e] <= (unsigned)nslots, a.chk, GS_SITE_C3M_MAP_R)) sl[e] = 0;
+        v[e] = s_map[sl[e] * C3M_SEG + (o[e] & (C3M_SEG - 1))];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (v[e] == C3M_ABSENT) continue;
+        const int bjk = (int)((bb[e >> 2] >> (8 * (e & 3))) & 0xffu);
+        const int u = hb + (int)v[e] * nb + bjk;
+        if (!GS_DCHECK(v[e] < (unsigned)nb && u >= 0 && u < nb * nb * nb, a.chk, GS_SITE_C3M_HIST)) continue;
+        const int c = s_cfg[u];
+        const int wk = s_wmap[sl[e] * C3M_SEG + (o[e] & (C3M_SEG - 1))];
+        if (GS_DCHECK(c < a.ncfg, a.chk, GS_SITE_C3M_HIST)) c3w_add64(s_T + 2 * c, wj * wk);
+    }
+}
+
+template <int THREADS, bool ABS>
+__global__ void __launch_bounds__(THREADS, 1)
+k_count3mw(C3Args a, int nslots)
+{
+    constexpr int WARPS = THREADS / 32;
+    constexpr int KPT = C3M_KEYS_PER_THREAD;
+    constexpr int MAX_KEYS = THREADS * KPT;
+    constexpr int SEG_TABLE = ABS ? C3M_SEG_TABLE_ABS : C3M_SEG_TABLE;
+    constexpr int SPAN_SEGS = ABS ? C3M_ABS_SEGS : C3M_SPAN_SEGS;
+    // dynamic: pass sums T [ncfg rounded up to even] x (low, high) u32, weight
+    // map [(nslots + 1) * C3M_SEG] i16, configuration table [nb^3 rounded up
+    // to a multiple of 8] u16, segment table [SEG_TABLE] u8, bin map
+    // [(nslots + 1) * C3M_SEG] u8 (slot 0: the all-absent segment)
+    extern __shared__ unsigned s_dyn[];
+    __shared__ int s_next;
+    __shared__ int s_cut;
+    __shared__ int s_warp[WARPS];
+    __shared__ long long s_hub;
+
+    const int lane = threadIdx.x & 31;
+    const int nb = a.nb, nb2 = nb * nb, n3 = nb2 * nb, ncfg = a.ncfg;
+    unsigned *s_T = s_dyn;
+    int16_t *s_wmap = reinterpret_cast<int16_t *>(s_T + 2 * ((ncfg + 1) & ~1));
+    uint16_t *s_cfg = reinterpret_cast<uint16_t *>(s_wmap + (size_t)(nslots + 1) * C3M_SEG);
+    uint8_t *s_seg = reinterpret_cast<uint8_t *>(s_cfg + ((n3 + 7) & ~7));
+    uint8_t *s_map = s_seg + SEG_TABLE;
+    unsigned long long *slice = a.gsum + 2 * (size_t)ncfg * blockIdx.x;
+
+    for (int t = threadIdx.x; t < 2 * ncfg; t += THREADS) s_T[t] = 0u;
+    for (int t = threadIdx.x; t < n3; t += THREADS) s_cfg[t] = __ldg(a.cfg3 + t);
+    for (int t = threadIdx.x; t < C3M_SEG / 16; t += THREADS)
+        reinterpret_cast<uint4 *>(s_map)[t] = make_uint4(~0u, ~0u, ~0u, ~0u);
+
+    for (;;) {
+        __syncthreads();                                     // everyone has read the last s_hub; T is folded
+        if (threadIdx.x == 0) s_hub = (long long)atomicAdd(a.cursor, 1ull) + a.hub_begin;
+        __syncthreads();
+        if (s_hub >= a.hub_end) break;
+        const long long i = s_hub;
+        const int64_t f0 = a.row_ptr[i] + a.fwd[i];
+        const int f = (int)(a.row_ptr[i + 1] - f0);
+        if (f < 2) continue;                                 // fewer than two forward keys close nothing
+        const int32_t *F = a.hnbr + f0;                      // the hub's forward row and its bins
+        const uint8_t *FB = a.hbin + f0;
+        for (int c0 = 0, c1 = 0; c0 < f; c0 = c1) {
+            // ---- the chunk [c0, c1): keys, segment slots and the two maps, as in k_count3m
+            const int32_t kbase = ABS ? 0 : F[c0] & ~(C3M_SEG - 1);
+            const int cap = min(f, c0 + MAX_KEYS);
+            const int t0 = c0 + threadIdx.x * KPT;
+            int32_t key[KPT];
+            unsigned starts = 0;
+            int32_t prev = (t0 > c0 && t0 < cap) ? (F[t0 - 1] - kbase) >> C3M_SEG_LOG : -1;
+#pragma unroll
+            for (int q = 0; q < KPT; ++q) {
+                key[q] = t0 + q < cap ? F[t0 + q] : 0;
+                const int32_t sg = (key[q] - kbase) >> C3M_SEG_LOG;
+                if (t0 + q < cap && sg != prev) starts |= 1u << q;
+                prev = sg;
+            }
+            if (threadIdx.x == 0) s_cut = cap;
+            int total = 0;
+            const int sbase = c3m_block_scan<THREADS>(__popc(starts), s_warp, &total);
+            {
+                int slot = sbase;
+#pragma unroll
+                for (int q = 0; q < KPT; ++q) {
+                    if (t0 + q >= cap) break;
+                    slot += (starts >> q) & 1u;
+                    if (slot > nslots || ((key[q] - kbase) >> C3M_SEG_LOG) >= SPAN_SEGS) {
+                        atomicMin(&s_cut, t0 + q);
+                        break;
+                    }
+                }
+            }
+            for (int t = threadIdx.x; t < SEG_TABLE; t += THREADS) s_seg[t] = 0;
+            {
+                const int nclear = min(nslots, total);
+                uint4 *m = reinterpret_cast<uint4 *>(s_map + C3M_SEG);
+                for (int t = threadIdx.x; t < nclear * (C3M_SEG / 16); t += THREADS)
+                    m[t] = make_uint4(~0u, ~0u, ~0u, ~0u);
+            }
+            __syncthreads();
+            c1 = s_cut;
+            {
+                int slot = sbase;
+#pragma unroll
+                for (int q = 0; q < KPT; ++q) {
+                    if (t0 + q >= c1) break;
+                    slot += (starts >> q) & 1u;
+                    const int off = key[q] - kbase;
+                    if (!GS_DCHECK(slot >= 1 && slot <= nslots && off >= 0 && (off >> C3M_SEG_LOG) < SPAN_SEGS,
+                                   a.chk, GS_SITE_C3M_MAP_W))
+                        continue;
+                    if ((starts >> q) & 1u) s_seg[off >> C3M_SEG_LOG] = (uint8_t)slot;
+                    const int at = (slot << C3M_SEG_LOG) | (off & (C3M_SEG - 1));
+                    s_map[at] = FB[t0 + q];
+                    s_wmap[at] = a.w[key[q]];
+                }
+            }
+            if (threadIdx.x == 0) s_next = 0;
+            __syncthreads();                                 // the maps are written
+            const int s_end = c1 - 1;                        // spokes [0, s_end) meet this chunk
+            const int32_t kmax = F[c1 - 1];
+            const int32_t kfirst = F[c0];
+            const unsigned guard = (unsigned)SPAN_SEGS << C3M_SEG_LOG;
+            const int32_t kout = ABS ? (int32_t)guard : kbase - 1;
+            for (;;) {
+                int s = 0;
+                if (lane == 0) s = atomicAdd(&s_next, 1);
+                s = __shfl_sync(0xffffffffu, s, 0);
+                if (s >= s_end) break;
+                const int32_t j = F[s];
+                int64_t p0, pe;
+                c3m_spoke_range(a, 0, j, s, c0, kfirst, &p0, &pe);
+                if (p0 >= pe) continue;
+                const int hb = FB[s] * nb2;
+                const int wj = a.w[j];
+                const int64_t pa = p0 & ~(int64_t)3;
+                const int head = (int)(p0 - pa);
+                const int total_e = head + (int)(pe - p0);
+                if (!GS_DCHECK(pa + (((total_e + 255) >> 8) << 8) <= a.nbr_len, a.chk, GS_SITE_C3M_ROW)) continue;
+                const int4 *vk = reinterpret_cast<const int4 *>(a.snbr + pa) + lane;
+                const uint32_t *vb = reinterpret_cast<const uint32_t *>(a.sbin + pa) + lane;
+                int4 k0 = __ldg(vk), k1 = __ldg(vk + 32);
+                uint32_t b0 = __ldg(vb), b1 = __ldg(vb + 32);
+                for (int base = 0;; base += 256) {
+                    const bool more = base + 256 < total_e;
+                    int4 n0 = k0, n1 = k1;
+                    uint32_t nb0 = b0, nb1 = b1;
+                    if (more) {                              // the next step in flight
+                        vk += 64;
+                        vb += 64;
+                        n0 = __ldg(vk);
+                        n1 = __ldg(vk + 32);
+                        nb0 = __ldg(vb);
+                        nb1 = __ldg(vb + 32);
+                    }
+                    int k[8] = { k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w };
+                    const uint32_t bb[2] = { b0, b1 };
+                    if (base == 0 || !more) {                // entries outside the row: an absent segment
+                        const unsigned r0 = (unsigned)(base + 4 * lane - head), len = (unsigned)(total_e - head);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            k[e] = r0 + e < len ? k[e] : kout;
+                            k[4 + e] = r0 + 128 + e < len ? k[4 + e] : kout;
+                        }
+                    }
+                    c3w_probe8<ABS>(k, bb, kbase, guard, s_seg, s_map, s_wmap, s_cfg, s_T, hb, nb, wj, a, nslots);
+                    // rows are sorted: stop once the step's last key passes kmax
+                    if (!more || __any_sync(0xffffffffu, lane == 31 && k1.w > kmax)) break;
+                    k0 = n0;
+                    k1 = n1;
+                    b0 = nb0;
+                    b1 = nb1;
+                }
+            }
+            __syncthreads();                                 // the chunk's maps are no longer read
+        }
+        // slice[c] += w_i T[c] (128-bit); thread t owns configurations t, t + THREADS, ...
+        const long long wi = a.w[i];
+        for (int t = threadIdx.x; t < ncfg; t += THREADS) {
+            const long long v = (long long)(((unsigned long long)s_T[2 * t + 1] << 32) | s_T[2 * t]);
+            if (v) {
+                s_T[2 * t] = 0u;
+                s_T[2 * t + 1] = 0u;
+                const unsigned long long lo = (unsigned long long)(wi * v);
+                const unsigned long long hi = (unsigned long long)__mul64hi(wi, v);
+                const unsigned long long l0 = slice[2 * t];
+                slice[2 * t] = l0 + lo;
+                slice[2 * t + 1] += hi + (l0 + lo < l0 ? 1ull : 0ull);
+            }
+        }
+    }
+}
+
 // out[c] += sum over the slices of slice[c], 128-bit (low, high) words.
 __global__ void k_sum128_slices(const unsigned long long *__restrict__ slices, int nslices, int ncfg,
                                 unsigned long long *__restrict__ out)
@@ -1286,6 +1517,47 @@ extern "C" int gs_count3_walk(gs_graph_t g)
     return count3_walk(g);
 }
 
+// Shared memory of the weighted byte-map walk (1024-thread blocks, one per
+// SM): false when it does not apply (more than C3M_MAX_BINS bins, forward rows
+// of 2^16 keys or more, GS_COUNT3_WALK naming a bitmap walk) or fewer than
+// C3M_MIN_SLOTS segment slots fit beside the sums and the configuration table.
+static bool plan_count3mw(gs_graph_t g, int *slots, size_t *dyn)
+{
+    const int mode = count3_walk_override();
+    if (mode == 0 || mode == 1) return false;
+    if (g->nb > C3M_MAX_BINS || !g->cfg3 || g->max_forward >= 65536) return false;
+    const int n3 = g->nb * g->nb * g->nb, ncfg = (int)gs_ncfg3(g->nb);
+    const size_t fixed = 8 * (size_t)((ncfg + 1) & ~1) + 2 * (size_t)((n3 + 7) & ~7) +
+                         (c3m_abs(g) ? C3M_SEG_TABLE_ABS : C3M_SEG_TABLE);
+    int dev = 0, smem_sm = 0, smem_block = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const auto kern = c3m_abs(g) ? k_count3mw<1024, true> : k_count3mw<1024, false>;
+    // the SM's shared memory, less 1 KB reserved and 2 KB of static data; 3 bytes per id of a slot
+    const long long room = std::min<long long>(smem_block, smem_sm - 1024) - 2048;
+    for (int sl = (int)std::min<long long>(C3M_MAX_SLOTS, (room - (long long)fixed) / (3 * C3M_SEG) - 1);
+         sl >= C3M_MIN_SLOTS; sl -= 4) {
+        const size_t d = fixed + 3 * (size_t)(sl + 1) * C3M_SEG;
+        int per = 0;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, 1024, d);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            per = 0;
+        }
+        if (per >= 1) {
+            *slots = sl;
+            *dyn = d;
+            return true;
+        }
+    }
+    return false;
+}
+
 static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_t st)
 {
     const int ncfg = a.ncfg;
@@ -1296,6 +1568,25 @@ static gs_status launch_count3(gs_graph_t g, C3Args a, int64_t hubs, cudaStream_
     size_t dyn;
     const bool win = a.windowed != 0;
     decltype(&k_count3<true, true, false, false>) kern;
+    if (weighted && !win && !list) {
+        int slots = 0;
+        size_t dm = 0;
+        if (plan_count3mw(g, &slots, &dm)) {
+            // one 128-bit slice per block, then their sum added to the output
+            unsigned long long *out = a.gsum, *slices = a.slices;
+            const int grid = (int)std::min<int64_t>((int64_t)gs_sm_count(), hubs);
+            GS_TRY_CUDA(cudaMemsetAsync(slices, 0, 16 * (size_t)ncfg * grid, st));
+            GS_TRY_CUDA(cudaMemsetAsync(a.cursor, 0, sizeof(unsigned long long), st));
+            a.gsum = slices;
+            (c3m_abs(g) ? k_count3mw<1024, true> : k_count3mw<1024, false>)<<<grid, 1024, dm, st>>>(a, slots);
+            gs_note_launch();
+            GS_TRY_CUDA(cudaGetLastError());
+            k_sum128_slices<<<(ncfg + 255) / 256, 256, 0, st>>>(slices, grid, ncfg, out);
+            gs_note_launch();
+            GS_TRY_CUDA(cudaGetLastError());
+            return GS_OK;
+        }
+    }
     if (weighted) {
         smem = true;
         dyn = C3_REGION_W + sizeof(unsigned long long) * (size_t)ncfg;

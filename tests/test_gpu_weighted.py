@@ -36,9 +36,12 @@ def test_unit_weights_equal_the_counts():
         assert as_int128(g.count_2pcf_weighted()) == [int(v) for v in as_uint64(g.count_2pcf())]
 
 
+@pytest.mark.parametrize("walk", ["map", "warp"])
 @pytest.mark.parametrize("periodic", [0, 1])
 @pytest.mark.parametrize("n", [5_000, 20_011])
-def test_random_weights_clustered(periodic, n):
+def test_random_weights_clustered(periodic, n, walk, monkeypatch):
+    # the byte-map walk (default) and the bitmap walk of the weighted count
+    monkeypatch.setenv("GS_COUNT3_WALK", walk)
     xyz, box, edges = _clustered(n, n, periodic)
     wt = _weights(n, n + 7)
     with gpu_graph(xyz, box, periodic, edges) as g:
@@ -93,6 +96,41 @@ def test_hub_rows_longer_than_the_table():
     ref = [-int(v) * 32767 ** 3 for v in oracle.count_3pcf(xyz, 300000, 0, edges)]
     assert min(ref) < -(1 << 63)
     assert h3 == ref
+
+
+@pytest.mark.parametrize("walk", ["map", "warp"])
+def test_two_cliques_rows_in_two_chunks(walk, monkeypatch):
+    # Two tight balls of a = 5200 and b = 3300 points 30000 apart, every pair an
+    # edge (bin 0 inside a ball, bin 1 across): the first hubs' forward rows
+    # hold more than 8192 keys and run in two chunks. With weights w, the sums
+    # are elementary symmetric polynomials of each ball's weights, computed
+    # exactly from power sums (Newton's identities): (0, 0, 0) gets
+    # e3(A) + e3(B), (0, 1, 1) gets e2(A) e1(B) + e2(B) e1(A).
+    monkeypatch.setenv("GS_COUNT3_WALK", walk)
+    rng = np.random.default_rng(11)
+    a, b = 5200, 3300
+
+    def ball(m, centre):
+        v = rng.normal(size=(m, 3))
+        v *= 4000 * rng.uniform(0, 1, size=(m, 1)) ** (1 / 3) / np.linalg.norm(v, axis=1, keepdims=True)
+        return (v + centre).astype(np.int32)
+
+    xyz = np.concatenate([ball(a, 100000), ball(b, [130000, 100000, 100000])])
+    wt = _weights(a + b, 12)
+    order = rng.permutation(a + b)
+    edges = [0, 9000, 40000]
+
+    def e123(w):
+        p1, p2, p3 = (sum(int(x) ** k for x in w) for k in (1, 2, 3))
+        return p1, (p1 * p1 - p2) // 2, (p1 ** 3 - 3 * p1 * p2 + 2 * p3) // 6
+
+    ea, eb = e123(wt[:a]), e123(wt[a:])
+    with gpu_graph(xyz[order], 300000, 0, edges) as g:
+        assert g.max_degree == a + b - 1
+        _set(g, wt[order])
+        sums = as_int128(g.count_3pcf_weighted())
+    # configurations of 2 bins in lexicographic order: (0,0,0) (0,0,1) (0,1,1) (1,1,1)
+    assert sums == [ea[2] + eb[2], 0, ea[1] * eb[0] + eb[1] * ea[0], 0]
 
 
 @pytest.mark.parametrize("nb", [1, 32, 33, 40])
