@@ -193,3 +193,51 @@ def test_tiny_inputs(n):
     assert int(h.sum()) == (1 if n == 3 else 0)
     if n == 3:
         assert h[0] == 1
+
+
+_ABOVE_2_21 = {}
+
+
+def _above_2_21_reference():
+    """A uniform catalogue of 2,200,000 points (above 2^21, so the byte-map
+    walks index their segment table relative to each chunk's first key, not by
+    absolute segment) in a periodic box, in the graph's own order, with the
+    oracle's unweighted and weighted counts over hubs [0, 500): rows of those
+    hubs by brute force. The first hubs lie in the first cells, and their
+    forward rows wrap the box, so they span more than 2^18 ids and run in
+    several chunks."""
+    if not _ABOVE_2_21:
+        import oracle as orc
+        box = catalogues.box_lattice(1000.0)
+        xyz = catalogues.uniform(2_200_000, 1000.0, 31)
+        edges = catalogues.linear_edges_lu(12.0, 5)
+        with gpu_graph(xyz, box, 1, edges) as g:
+            perm = g.export_perm().cpu().numpy()
+        xyz = np.ascontiguousarray(xyz[perm])
+        hubs = 500
+        rows = [orc.row(xyz, box, 1, edges, i) for i in range(hubs)]
+        spans = [int(r[r > i].max() - r[r > i].min() + 1) for i, (r, _) in enumerate(rows) if (r > i).sum() > 1]
+        assert max(spans) > 1 << 18
+        row_ptr = np.zeros(len(xyz) + 1, dtype=np.int64)
+        row_ptr[1:hubs + 1] = np.cumsum([len(r) for r, _ in rows])
+        row_ptr[hubs + 1:] = row_ptr[hubs]
+        part = orc.Graph(row_ptr, np.concatenate([r for r, _ in rows]).astype(np.int32),
+                         np.concatenate([b for _, b in rows]).astype(np.uint8))
+        wt = np.random.default_rng(32).integers(-32767, 32768, size=len(xyz)).astype(np.int16)
+        _ABOVE_2_21.update(xyz=xyz, box=box, edges=edges, hubs=hubs, wt=wt,
+                           ref=orc.count_3pcf(xyz, box, 1, edges, g=part, hub_begin=0, hub_end=hubs),
+                           ref_w=orc.count_3pcf_weighted(xyz, box, 1, edges, wt, g=part))
+    return _ABOVE_2_21
+
+
+def test_catalogue_above_2_21_points():
+    import torch
+    from cosmology_point_correlation_gb300 import as_int128
+    r = _above_2_21_reference()
+    assert r["ref"].sum() > 0
+    with gpu_graph(r["xyz"], r["box"], 1, r["edges"]) as g:
+        assert g.n > 1 << 21
+        assert np.array_equal(g.export_perm().cpu().numpy(), np.arange(g.n))
+        assert np.array_equal(as_uint64(g.count_3pcf(0, r["hubs"])), r["ref"])
+        g.set_weights(torch.from_numpy(r["wt"]).cuda())
+        assert as_int128(g.count_3pcf_weighted(0, r["hubs"])) == r["ref_w"]
