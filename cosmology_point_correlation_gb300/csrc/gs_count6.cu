@@ -47,6 +47,7 @@ constexpr int C6_SMEM_HIST_MAX = 4096;
 constexpr int C6_SMEM_W_MAX = 2500;         // weighted: configurations with shared 128-bit sums (nb <= 6)
 constexpr int C6_EMPTY = -1;
 constexpr int C6_MAX_BINS = 10;             // the tuple table holds nb^6 entries
+constexpr int64_t C6_SMALL_R = 32768;       // r_max (lattice units) below which cross products fit in int32
 // Unweighted shared-memory histogram: three u32 counters per configuration,
 // the tetrahedra of negative, zero and positive signed volume, so that a
 // tetrahedron is one add (even = their sum, odd = positive - negative).
@@ -103,7 +104,10 @@ struct C6Space {
     int *next;         // shared counter handing out the rows s1 of the tetrahedron search
 };
 
-template <int NT, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
+// SMALLR: r_max below C6_SMALL_R lattice units, so a spoke-pair cross product
+// fits in int32 (components |r| <= 32767: |y1 z2 - z1 y2| < 2^31) and the
+// volume is three 32 x 32 -> 64-bit products instead of 64-bit arithmetic.
+template <int NT, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED, bool SMALLR = false>
 __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long long i, int64_t f0, int f,
                                        int tlog, unsigned *s_cnt, unsigned *s_w128)
 {
@@ -183,9 +187,11 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
     // each word of the bit rows, prefix-sums the lanes' common-bit counts and
     // hands the tetrahedra out 32 at a time, so that all lanes stay busy however
     // unevenly the tetrahedra are spread over the pairs.
+    using CT = typename std::conditional<SMALLR, int, long long>::type;
     struct Pair {
         int s2, b02, b12;
-        long long cx, cy, cz, w12;
+        CT cx, cy, cz;
+        long long w12;
     };
     // rows s1: weighted, from the shared counter (low rows, with the most
     // candidates, first); unweighted, where rows are cheap, strided by warp
@@ -199,7 +205,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
         const unsigned *row1 = w.bits + (size_t)s1 * W;
         const int4 r1 = w.v[s1];
         const int b01 = r1.w;
-        const long long x1 = r1.x, y1 = r1.y, z1 = r1.z;
+        const CT x1 = r1.x, y1 = r1.y, z1 = r1.z;
         const long long w1 = WEIGHTED ? wi * w.ww[s1] : 0;
         auto make_pair = [&](int s2) {
             Pair p;
@@ -207,7 +213,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
             const int4 r2 = w.v[s2];
             p.b02 = r2.w;
             p.b12 = w.sbin[(size_t)s1 * f + s2];
-            const long long x2 = r2.x, y2 = r2.y, z2 = r2.z;
+            const CT x2 = r2.x, y2 = r2.y, z2 = r2.z;
             p.cx = y1 * z2 - z1 * y2;
             p.cy = z1 * x2 - x1 * z2;
             p.cz = x1 * y2 - y1 * x2;
@@ -222,7 +228,7 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
             const int pk = ((((b01 * nb + p.b02) * nb + b03) * nb + p.b12) * nb + b13) * nb + b23;
             const int v = __ldg(a.cfg6 + pk);
             const int ci = v >> 2, par = (v & 3) - 1;
-            const long long d = p.cx * r3.x + p.cy * r3.y + p.cz * r3.z;
+            const long long d = (long long)p.cx * r3.x + (long long)p.cy * r3.y + (long long)p.cz * r3.z;
             const int sg = par * ((d > 0) - (d < 0));
             if (WEIGHTED) {
                 const long long W4 = p.w12 * w.ww[s3];                    // |.| <= 2^60
@@ -315,7 +321,7 @@ __device__ __forceinline__ void c6_flush(unsigned *sc, int ncfg, unsigned long l
 // Hubs with max(3, a.f_lo + 1) .. M forward neighbours, workspace in shared
 // memory. M = 128 keeps the per-block footprint near 25 KB (about four
 // resident blocks per SM); M = 256 takes the rarer hubs up to C6_M.
-template <int M, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED>
+template <int M, bool SMEM_HIST, bool WEIGHTED, bool WINDOWED, bool SMALLR = false>
 __global__ void __launch_bounds__(C6_THREADS, M <= C6_M_SMALL ? 4 : 2)
 k_count6_small(C6Args a)
 {
@@ -365,7 +371,7 @@ k_count6_small(C6Args a)
         }
         int tlog = 4;
         while ((1 << tlog) < 2 * f) ++tlog;
-        c6_hub<C6_THREADS, SMEM_HIST, WEIGHTED, WINDOWED>(a, w, i, f0, f, tlog, s_cnt, s_w128);
+        c6_hub<C6_THREADS, SMEM_HIST, WEIGHTED, WINDOWED, SMALLR>(a, w, i, f0, f, tlog, s_cnt, s_w128);
     }
     if (SMEM_HIST && WEIGHTED) {
         __syncthreads();
@@ -621,6 +627,7 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
     const bool weighted = a.w != nullptr;
     const bool smem = weighted ? ncfg <= C6_SMEM_W_MAX : ncfg <= C6_SMEM_HIST_MAX;
     const size_t acc = weighted ? 32 * (size_t)ncfg : sizeof(unsigned) * C6_HIST_WORDS * (size_t)ncfg;
+    const bool small_r = g->edges[g->nb] < C6_SMALL_R;    // int32 cross products (the resident shared-memory kernels)
     // the two shared-memory kernels: hubs of forward degree 3..128, then 129..256
     for (int pass = 0; pass < 2; ++pass) {
         const int m = pass ? C6_M : C6_M_SMALL;
@@ -632,6 +639,8 @@ static gs_status c6_launch(gs_graph_t g, C6Args a, bool windowed, cudaStream_t s
             if (windowed)
                 return weighted ? (smem ? k_count6_small<MM, true, true, true> : k_count6_small<MM, false, true, true>)
                                 : (smem ? k_count6_small<MM, true, false, true> : k_count6_small<MM, false, false, true>);
+            if (smem && small_r)
+                return weighted ? k_count6_small<MM, true, true, false, true> : k_count6_small<MM, true, false, false, true>;
             return weighted ? (smem ? k_count6_small<MM, true, true, false> : k_count6_small<MM, false, true, false>)
                             : (smem ? k_count6_small<MM, true, false, false> : k_count6_small<MM, false, false, false>);
         };
