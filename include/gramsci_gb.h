@@ -252,8 +252,13 @@ gs_status gs_count_2pcf_weighted(gs_graph_t g, int64_t *sums_dev, void *cuda_str
  *   sums_dev  int64 [2 * gs_config_count_3pcf(nbins)], device, overwritten,
  *             128-bit sums as (low, high) word pairs
  *   hub_begin, hub_end  internal-order hub range, as for gs_count_3pcf
+ * Device-resident graphs with at most 32 bins take the byte-map walk (the
+ * hub's keys as a byte map of their bins and a parallel map of their
+ * weights), others the bitmap walk; GS_COUNT3_WALK = "warp" or "group" asks
+ * for the bitmap walk. The call allocates 32 bytes per configuration and SM
+ * of scratch (per-block 128-bit slices) before writing sums_dev.
  * Limits: nbins <= 40. Errors: GS_ERR_ARG (NULL, no weights set, nbins,
- * range), GS_ERR_CAPACITY, GS_ERR_CUDA. */
+ * range), GS_ERR_NOMEM, GS_ERR_CAPACITY, GS_ERR_CUDA. */
 gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int64_t hub_begin, int64_t hub_end,
                                  void *cuda_stream);
 
