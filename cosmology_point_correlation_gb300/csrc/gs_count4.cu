@@ -261,6 +261,16 @@ __device__ __forceinline__ void c4_hub(const C4Args &a, const HubSpace &w, long 
                 }
                 if (!__ballot_sync(0xffffffffu, common != 0u)) continue;   // no clique in this word
                 const int cnt = __popc(common);
+                // When the lanes' cliques in this word are even enough (the largest
+                // count at most twice the rounds that dealing them out would take),
+                // each lane takes its own, with its pair data in its registers;
+                // else they are dealt out 32 at a time
+                const int all = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+                const int most = (int)__reduce_max_sync(0xffffffffu, (unsigned)cnt);
+                if (most <= 2 * ((all + 31) >> 5)) {
+                    for (unsigned cm = common; cm; cm &= cm - 1) clique(b2, cx, cy, cz, (wd << 5) + __ffs(cm) - 1);
+                    continue;
+                }
                 int inc = cnt;                                     // inclusive prefix over lanes
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
