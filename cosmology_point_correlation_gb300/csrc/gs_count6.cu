@@ -181,12 +181,17 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
 
     const long long wi = WEIGHTED ? (long long)a.w[i] : 0;
     const int s1_end = min(pa1, f - 2), s2_end = min(q2_hi, f - 1);
-    // A warp per s1, its lanes over the spokes s2. Unweighted, each lane walks
-    // the common bits of its own pairs (s1, s2). Weighted, where a tetrahedron
-    // costs several atomics, the warp takes 32 candidates s2 at a time and, for
-    // each word of the bit rows, prefix-sums the lanes' common-bit counts and
-    // hands the tetrahedra out 32 at a time, so that all lanes stay busy however
-    // unevenly the tetrahedra are spread over the pairs.
+    // A warp per s1, its lanes over 32 candidate spokes s2 at a time, one pair
+    // (s1, s2) per lane with its cross product in registers. For each word of
+    // the bit rows: when the lanes' tetrahedra are even enough (the largest
+    // count at most C6_WALK_ROUNDS times the rounds that dealing them out would
+    // take) each lane walks the common bits of its own pair; else the counts are
+    // prefix-summed and the tetrahedra handed out 32 at a time with the owner's
+    // pair data, so that all lanes stay busy however unevenly the tetrahedra are
+    // spread over the pairs. Dealing costs a prefix sum, an owner search and the
+    // pair's shuffles per round; a weighted tetrahedron costs two 128-bit
+    // atomics, so dealing pays off sooner there.
+    constexpr int C6_WALK_ROUNDS = WEIGHTED ? 2 : 3;
     using CT = typename std::conditional<SMALLR, int, long long>::type;
     struct Pair {
         int s2, b02, b12;
@@ -246,44 +251,33 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                 if (sg) atomicAdd((unsigned long long *)(a.odd + ci), (unsigned long long)(long long)sg);
             }
         };
-        if (!WEIGHTED) {
-            for (int s2 = max(s1 + 1, q2_lo) + lane; s2 < s2_end; s2 += 32) {
-                if (!((row1[s2 >> 5] >> (s2 & 31)) & 1u)) continue;
-                const unsigned *row2 = w.bits + (size_t)s2 * W;
-                const Pair p = make_pair(s2);
-                for (int wd = s2 >> 5; wd < W; ++wd) {
-                    unsigned common = row1[wd] & row2[wd];
-                    if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
-                    while (common) {
-                        const int s3 = (wd << 5) + __ffs(common) - 1;
-                        common &= common - 1;
-                        tetra(p, s3);
-                    }
-                }
-            }
-            continue;
-        }
         for (int c2 = max(s1 + 1, q2_lo); c2 < s2_end; c2 += 32) {        // warp-uniform
             const int s2 = c2 + lane;
             const bool valid = s2 < s2_end && ((row1[s2 >> 5] >> (s2 & 31)) & 1u);
             if (!__any_sync(0xffffffffu, valid)) continue;
             const unsigned *row2 = w.bits + (size_t)(valid ? s2 : s1) * W;
+            const Pair p = make_pair(valid ? s2 : s1);                 // an idle lane's pair is never used
             for (int wd = c2 >> 5; wd < W; ++wd) {
                 unsigned common = 0u;
                 if (valid && wd >= (s2 >> 5)) {
                     common = row1[wd] & row2[wd];
                     if (wd == (s2 >> 5)) common &= ~((2u << (s2 & 31)) - 1u);   // s3 > s2
                 }
-                if (!__ballot_sync(0xffffffffu, common != 0u)) continue;   // no tetrahedron in this word
                 const int cnt = __popc(common);
+                const int all = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+                if (all == 0) continue;                            // no tetrahedron in this word
+                const int most = (int)__reduce_max_sync(0xffffffffu, (unsigned)cnt);
+                if (most <= C6_WALK_ROUNDS * ((all + 31) >> 5)) {
+                    for (unsigned cm = common; cm; cm &= cm - 1) tetra(p, (wd << 5) + __ffs(cm) - 1);
+                    continue;
+                }
                 int inc = cnt;                                     // inclusive prefix over lanes
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const int y = __shfl_up_sync(0xffffffffu, inc, o);
                     if (lane >= o) inc += y;
                 }
-                const int total = __shfl_sync(0xffffffffu, inc, 31);
-                for (int k = 0; k < total; k += 32) {
+                for (int k = 0; k < all; k += 32) {
                     const int q = k + lane;
                     int owner = 0;                                 // first lane whose prefix exceeds q
 #pragma unroll
@@ -291,8 +285,15 @@ __device__ __forceinline__ void c6_hub(const C6Args &a, const C6Space &w, long l
                         if (__shfl_sync(0xffffffffu, inc, owner + step - 1) <= q) owner += step;
                     const unsigned cm = __shfl_sync(0xffffffffu, common, owner);
                     const int first = __shfl_sync(0xffffffffu, inc - cnt, owner);
-                    const int o_s2 = __shfl_sync(0xffffffffu, s2, owner);
-                    if (q < total) tetra(make_pair(o_s2), (wd << 5) + gs_nth_bit(cm, q - first));
+                    Pair o;                                        // the owner's pair
+                    o.s2 = __shfl_sync(0xffffffffu, p.s2, owner);
+                    o.b02 = __shfl_sync(0xffffffffu, p.b02, owner);
+                    o.b12 = __shfl_sync(0xffffffffu, p.b12, owner);
+                    o.cx = __shfl_sync(0xffffffffu, p.cx, owner);
+                    o.cy = __shfl_sync(0xffffffffu, p.cy, owner);
+                    o.cz = __shfl_sync(0xffffffffu, p.cz, owner);
+                    o.w12 = WEIGHTED ? __shfl_sync(0xffffffffu, p.w12, owner) : 0;
+                    if (q < all) tetra(o, (wd << 5) + gs_nth_bit(cm, q - first));
                 }
             }
         }
