@@ -18,9 +18,11 @@
 // Hubs with up to 128 forward neighbours run in a 128-slot shared-memory
 // kernel (four blocks per SM), up to C6_M in a 256-slot one, larger hubs in a
 // kernel with a global workspace slice and 1024-thread blocks; all keep their
-// histograms in shared memory. In the weighted mode (several atomics per
-// tetrahedron) warps take rows s1 from a counter and deal the tetrahedra of
-// each word of the bit rows out 32 at a time, as the parity kernel does.
+// histograms in shared memory. A warp takes a row s1 and its lanes one pair
+// (s1, s2) each; per word of the bit rows the lanes either walk their own
+// pairs' tetrahedra or, when those are uneven, deal them out 32 at a time, as
+// the parity kernel does. In the weighted mode (several atomics per
+// tetrahedron) warps take rows s1 from a counter and deal sooner.
 //
 // Windowed graphs (§III.5.3): tiles (hub window, spoke windows c1 <= c2) as
 // for the parity count; only tetrahedra whose two lowest spokes lie in c1 and
