@@ -15,9 +15,12 @@ memory in row windows ("windowed"), all outside the headline step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle (oracle/, plain C) on a bounded
-sub-cube sample of the same workload. Under torchrun every rank counts its
-own realisation of the workload (weak scaling, no collective on the data
-path); rank 0 prints the line.
+random sample of the workload's hubs, each with its full row found by brute
+force over all points, as the "cpu_baseline" object of the default line does.
+Under torchrun every rank counts its own realisation of the workload (weak
+scaling, no collective on the data path); with --strong the ranks split one
+catalogue's hubs into ranges of equal work and sum their histograms. Rank 0
+prints the line.
 """
 from __future__ import annotations
 
