@@ -265,18 +265,22 @@ gs_status gs_count_3pcf_weighted(gs_graph_t g, int64_t *sums_dev, int64_t hub_be
 /* Sizes of a built graph (host outputs; any pointer may be NULL).
  *   n           number of points
  *   n_edges     directed edges, sum of degrees (= 2 x pairs)
- *   max_degree  largest |N(i)| */
+ *   max_degree  largest |N(i)|
+ * Host data only, no device work. Errors: GS_ERR_ARG (NULL graph). */
 gs_status gs_graph_info(gs_graph_t g, int64_t *n, int64_t *n_edges, int32_t *max_degree);
 
-/* Work statistics of a built graph, in the graph's internal order, where
- * f_i = |{j in N(i): j > i}| (forward degree) and b_i = deg_i - f_i:
+/* Work statistics of a built graph (the merge-walk work of §III.1), in the
+ * graph's internal order, where f_i = |{j in N(i): j > i}| (forward degree)
+ * and b_i = deg_i - f_i:
  *   hub_tail    sum_i C(f_i, 2): hub-tail entries the merge-walk of §III.1
  *               reads over all forward spokes (also the number of candidate
  *               third vertices)
  *   spoke_walk  sum over forward edges (i, j) of f_j = sum_j b_j f_j: spoke-row
  *               entries the merge-walk reads
  *   max_forward largest f_i
- * Computed on the device; the call synchronises cuda_stream. */
+ * Computed on the device; the call synchronises cuda_stream. Errors:
+ * GS_ERR_ARG (NULL, graph of another device), GS_ERR_NOMEM (24 bytes
+ * of scratch), GS_ERR_CUDA. */
 typedef struct {
     int64_t n;
     int64_t n_edges;
@@ -310,9 +314,10 @@ gs_status gs_graph_hub_work(gs_graph_t g, int32_t *fwd_dev, int64_t *walk_dev, v
  * window) and runs one tile per (hub window, spoke window >= it) pair; the
  * 4pCF counts run one tile per (hub window, spoke windows c1 <= c2) triple
  * (three slots). Every triangle and clique lands in exactly one tile, so
- * results equal those of the resident graph bit for bit. gs_build_graph itself switches to this mode when the CSR
- * does not fit in free device memory, or when the environment variable
- * GS_WINDOW_EDGES holds a positive edge count.
+ * results equal those of the resident graph bit for bit. gs_build_graph
+ * itself switches to this mode when the CSR does not fit in free device
+ * memory, or when the environment variable GS_WINDOW_EDGES holds a positive
+ * edge count.
  *   window_edges  >= 1
  * Windowed graphs support every count (plain and weighted), the exports,
  * stats and info; the hub-list counts and gs_count_4pcf_parity_static return
@@ -321,9 +326,10 @@ gs_status gs_build_graph_windowed(const int32_t *coords_dev, int64_t n, int64_t 
                                   int64_t r_max_lu, const int64_t *edges_lu, int nbins,
                                   int64_t window_edges, void *cuda_stream, gs_graph_t *out);
 
-/* Row windows of a graph (host outputs; either pointer may be NULL):
- * n_windows = 0 for a device-resident graph; window_edges_max = the largest
- * window's edge count (all edges when resident). */
+/* Row windows of a graph (§III.5.3; host outputs, either pointer may be
+ * NULL): n_windows = 0 for a device-resident graph; window_edges_max = the
+ * largest window's edge count (all edges when resident). Host data only.
+ * Errors: GS_ERR_ARG (NULL graph). */
 gs_status gs_graph_windows(gs_graph_t g, int32_t *n_windows, int64_t *window_edges_max);
 
 /* Number of CUDA kernels this library has launched in this process so far
@@ -348,19 +354,24 @@ uint64_t gs_alloc_calls(void);
 gs_status gs_graph_export_csr(gs_graph_t g, int64_t *row_ptr_dev, int32_t *nbr_dev,
                               uint8_t *bin_dev, void *cuda_stream);
 
-/* Selected rows in INPUT numbering, each sorted (Eq.(1)).
+/* Selected rows N(i) of the graph (§II.1, Eq.(1)) in INPUT numbering, each
+ * sorted.
  *   ids_dev     int32 [count], device, input indices in [0, n)
  *   row_ptr_dev int64 [count+1], device: offsets of the output rows
  *   nbr_dev     int32 [row_ptr_dev[count]] or NULL, device
  *   bin_dev     uint8 [row_ptr_dev[count]], device (needed when nbr_dev is set)
  * With nbr_dev NULL only row_ptr_dev is written, so a caller can size the
- * row arrays first. Synchronises cuda_stream once (index check). */
+ * row arrays first. Synchronises cuda_stream once (index check). Errors:
+ * GS_ERR_ARG (NULL, negative count, an index outside [0, n), graph of another
+ * device), GS_ERR_NOMEM, GS_ERR_CUDA. */
 gs_status gs_graph_export_rows(gs_graph_t g, const int32_t *ids_dev, int64_t count,
                                int64_t *row_ptr_dev, int32_t *nbr_dev, uint8_t *bin_dev,
                                void *cuda_stream);
 
-/* Internal order: perm_dev int32 [n], device; perm_dev[p] = input index of
- * the point the graph numbers p (the hub order of the count calls). */
+/* Internal order (the cell order of the §II.1 neighbour search):
+ * perm_dev int32 [n], device; perm_dev[p] = input index of the point the
+ * graph numbers p (the hub order of the count calls). Asynchronous. Errors:
+ * GS_ERR_ARG (NULL, graph of another device), GS_ERR_CUDA. */
 gs_status gs_graph_export_perm(gs_graph_t g, int32_t *perm_dev, void *cuda_stream);
 
 /* Number of histogram entries: C(nbins+2, 3) and C(nbins, 3); -1 if nbins is
@@ -378,7 +389,10 @@ int64_t gs_config_index_4pcf(int nbins, int b1, int b2, int b3);
  * device, builds the graph, counts, copies the result back and frees
  * everything, all on cuda_stream; returns once the result is in host memory.
  * Arguments as for gs_build_graph; hist_host / even_host / odd_host are host
- * arrays of the sizes above (pinned memory makes the copies faster). */
+ * arrays of the sizes above (pinned memory makes the copies faster).
+ * Errors: those of gs_build_graph and of the count, GS_ERR_ARG for a NULL
+ * histogram, GS_ERR_NOMEM, GS_ERR_CUDA; the host outputs are written only
+ * after the count succeeded. */
 gs_status gs_3pcf_from_host(const int32_t *coords_host, int64_t n, int64_t box_lu, int periodic,
                             int64_t r_max_lu, const int64_t *edges_lu, int nbins,
                             uint64_t *hist_host, void *cuda_stream);
