@@ -309,11 +309,13 @@ gs_status gs_graph_hub_work(gs_graph_t g, int32_t *fwd_dev, int64_t *walk_dev, v
 /* The graph of gs_build_graph with its edge arrays in pinned HOST memory,
  * split into row windows of at most window_edges directed edges (whole cells;
  * a larger cell gets a window of its own). This is the out-of-core mode of
- * §III.5.3 for graphs larger than device memory: a query stages one hub
- * window and one spoke window at a time (two device slots of the largest
- * window) and runs one tile per (hub window, spoke window >= it) pair; the
- * 4pCF counts run one tile per (hub window, spoke windows c1 <= c2) triple
- * (three slots). Every triangle and clique lands in exactly one tile, so
+ * §III.5.3 for graphs larger than device memory. The graph holds three
+ * device slots of the largest window's size. A 3pCF query runs one tile per
+ * (hub window, spoke window >= it) pair that holds work, with the two windows
+ * staged in slots; a window already in a slot is not copied again, and the
+ * next tile's missing window is copied on a second stream while the current
+ * tile runs. The 4pCF counts run one tile per (hub window, spoke windows
+ * c1 <= c2) triple. Every triangle and clique lands in exactly one tile, so
  * results equal those of the resident graph bit for bit. gs_build_graph
  * itself switches to this mode when the CSR does not fit in free device
  * memory, or when the environment variable GS_WINDOW_EDGES holds a positive
