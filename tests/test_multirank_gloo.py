@@ -82,3 +82,37 @@ def test_balanced_ranges_follow_the_walk_work():
     r = balanced_ranges(fwd, walk, 2)
     assert r[0][0] == 0 and r[-1][1] == 8 and r[0][1] == r[1][0]
     assert r[0][1] == 2                      # the two heavy hubs go to different ranks
+
+
+def test_hub_ranges_properties_on_random_work():
+    # Every cut is the nearer of the two prefix sums around its target, so it
+    # lies within half the largest hub weight of the target, and each range's
+    # work within one largest weight of total / world; the ranges are
+    # contiguous, ordered and cover [0, n) for any world size.
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        n = int(rng.integers(0, 60))
+        world = int(rng.integers(1, 12))
+        kind = trial % 3
+        if kind == 0:
+            w = rng.integers(0, 1000, size=n).astype(float)
+        elif kind == 1:                                 # heavy tail, many empty hubs
+            w = np.where(rng.random(n) < 0.5, 0.0, rng.pareto(1.2, size=n) * 100).round()
+        else:                                           # one dominant hub
+            w = np.ones(n)
+            if n:
+                w[int(rng.integers(0, n))] = 10_000.0
+        r = hub_ranges(n, world, w)
+        assert len(r) == world
+        assert r[0][0] == 0 and r[-1][1] == n
+        for (b0, e0), (b1, e1) in zip(r, r[1:]):
+            assert e0 == b1
+        assert all(b <= e for b, e in r)
+        if n == 0:
+            continue
+        share, wmax = w.sum() / world, w.max()
+        for b, e in r:
+            assert abs(w[b:e].sum() - share) <= wmax + 1e-9 * max(1.0, w.sum())
+        # without weights the sizes differ by at most one hub
+        sizes = [e - b for b, e in hub_ranges(n, world)]
+        assert max(sizes) - min(sizes) <= 1 and sum(sizes) == n
